@@ -1,0 +1,377 @@
+#!/usr/bin/env python
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic inputs:
+  * prefill forward, B=4, H=16, Sq=Skv=2048, d=128, bf16, non-causal, then causal
+    (tcgen05 kernel: Q tile load, K/V streaming, S = Q K^T, masks, online
+    softmax, O += P V, epilogue, tile scheduling);
+  * paged split-KV decode, B=64, Hq=32, Hkv=8, d=128, 16-token pages, lengths
+    uniform in [1024, 8192], 8 splits (split kernel + LSE merge).
+The headline ``value`` is the prefill forward throughput in TFLOP/s with the
+FLOP convention 4*B*H*Sq*Skv*d, halved for causal; decode is reported as
+algorithmic KV bytes per second next to it.  L2 is flushed (256 MB write)
+before every step.  Kernel times come from CUDA events recorded on the stream
+the kernels run on.
+
+``--impl reference`` times the fp64 CPU oracle (the slow, obviously correct
+program the kernels are checked against) on a bounded sample of the same
+prefill workload, on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOP/s & % BF16 tensor peak; decode KV GB/s & % HBM peak"
+UNIT = "TFLOP/s"
+WORKLOAD = ("prefill MHA B=4 H=16 Sq=Skv=2048 d=128 bf16 (non-causal + causal) + paged decode "
+            "B=64 Hq=32 Hkv=8 d=128 L~U[1024,8192] page=16 splits=8")
+L2_FLUSH_BYTES = 256 << 20
+PREFILL_SHAPE = dict(B=4, H=16, S=2048, d=128)
+
+
+def prefill_flops(B, H, Sq, Skv, d, causal):
+    f = 4.0 * B * H * Sq * Skv * d
+    return f / 2 if causal else f
+
+
+def decode_kv_bytes(seqlens, Hkv, d):
+    """Algorithmic bytes of one decode call: every visible key and value once."""
+    return int(sum(int(L) for L in seqlens)) * Hkv * d * 2 * 2
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash(name):
+    with open(os.path.join(ROOT, "exact_attention_08_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_file, summary):
+    """DRAM bytes per launch recorded from an ncu capture of the same kernel
+    source (profiles/traffic.json); None when absent or the kernel changed."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    e = t.get(summary)
+    if not e or e.get("source_sha256_16") != kernel_source_hash(kernel_file):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        with open(self.out.name) as f:
+            lines = [l.strip() for l in f if l.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in lines:
+            c = [x.strip() for x in l.split(",")]
+            if len(c) < 9:
+                continue
+            try:
+                sm.append(float(c[1]))
+                smax.append(float(c[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, c[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    """The oracle (fp64, CPU) as the reference arm: bounded sample per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import workloads
+    x = workloads.prefill_mha(False)
+    heads, rows = 2, 256
+    q = x.q[:1, :rows, :heads].double().numpy()
+    k = x.k[:1, :, :heads].double().numpy()
+    v = x.v[:1, :, :heads].double().numpy()
+    flops = prefill_flops(1, heads, rows, 2048, 128, False)
+    for _ in range(args.warmup):
+        oracle.attn_fwd(q, k, v, x.scale)
+    t = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v, x.scale)
+        t.append(time.perf_counter() - t0)
+    sec = statistics.median(t)
+    val = flops / sec / 1e12
+    sample = f"prefill non-causal, batch 0, heads 0-{heads - 1}, rows 0-{rows - 1} of 2048"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def cpu_baseline():
+    """The oracle as it stands on this host: a bounded sample (~10 s) of the
+    prefill workload, reported in the same unit."""
+    import oracle
+    import workloads
+    x = workloads.prefill_mha(False)
+    heads, rows = 16, 2048
+    q = x.q[:1, :rows].double().numpy()
+    k = x.k[:1].double().numpy()
+    v = x.v[:1].double().numpy()
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, x.scale)
+    sec = time.perf_counter() - t0
+    flops = prefill_flops(1, heads, rows, 2048, 128, False)
+    return {"value": flops / sec / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": sec,
+            "sample": "prefill non-causal, batch element 0 of 4 (16 heads x 2048 rows)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import exact_attention_08_gb300 as ea
+    import workloads
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---------------------------------------------------------------- inputs (resident)
+    xs = [workloads.prefill_mha(False), workloads.prefill_mha(True)]
+    pre = []
+    for x in xs:
+        q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[0], q.shape[2], q.shape[1], dtype=torch.float32, device=dev)
+        pre.append((x, q, k, v, o, lse))
+    dx = workloads.paged_decode()
+    dq, dkp, dvp = dx.q.to(dev), dx.k_pages.to(dev), dx.v_pages.to(dev)
+    dpt, dsl = dx.page_table.to(dev), dx.seqlens.to(dev)
+    do = torch.empty_like(dq)
+    dlse = torch.empty(dq.shape[0], dq.shape[1], dtype=torch.float32, device=dev)
+    dws = torch.empty(ea.attn_decode_workspace_size(64, 32, 128, 8), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    B, H, S, d = (PREFILL_SHAPE[k] for k in ("B", "H", "S", "d"))
+    f_nc = prefill_flops(B, H, S, S, d, False)
+    f_c = prefill_flops(B, H, S, S, d, True)
+    kv_bytes = decode_kv_bytes(dx.seqlens.tolist(), 8, 128)
+    launches_per_step = 1 + 1 + 2
+
+    def step(ev):
+        with torch.cuda.stream(stream):
+            flush.fill_(1)
+            ev[0].record(stream)
+            for i, (x, q, k, v, o, lse) in enumerate(pre):
+                ea.attn_fwd(q, k, v, o, lse, causal=x.causal, scale=x.scale, stream=stream)
+                ev[1 + i].record(stream)
+            ea.attn_decode_paged(dq, dkp, dvp, dpt, dsl, do, dlse, num_splits=8, scale=dx.scale,
+                                 workspace=dws, stream=stream)
+            ev[3].record(stream)
+
+    def mk():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    for _ in range(args.warmup):
+        step(mk())
+    torch.cuda.synchronize(dev)
+    if ea.attn_device_status(stream) != ea.ATTN_OK:
+        raise RuntimeError("device status reported an error during warm-up")
+
+    sampler = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [mk() for _ in range(args.steps)]
+    wall0 = time.perf_counter()
+    for ev in evs:
+        step(ev)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    barrier()
+    clocks = sampler.stop()
+    status = ea.attn_device_status(stream)
+    if status != ea.ATTN_OK:
+        raise RuntimeError(f"device status {ea.attn_status_string(status)}")
+
+    t_nc = [e[0].elapsed_time(e[1]) for e in evs]
+    t_c = [e[1].elapsed_time(e[2]) for e in evs]
+    t_dec = [e[2].elapsed_time(e[3]) for e in evs]
+    tot_pre = sum(t_nc) + sum(t_c)
+    tot_step = sum(t_nc) + sum(t_c) + sum(t_dec)
+    if world > 1:
+        tt = torch.tensor([tot_pre, tot_step, sum(t_dec)], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        tot_pre, tot_step, tot_dec = tt.tolist()
+    else:
+        tot_dec = sum(t_dec)
+    K = args.steps
+    value = world * K * (f_nc + f_c) / (tot_pre / 1e3) / 1e12
+    dec_gbs = world * K * kv_bytes / (tot_dec / 1e3) / 1e9
+    hbm, bf16, src = peaks()
+
+    # ---------------------------------------------------------------- end to end (host buffers)
+    x0 = pre[0][0]
+    e2e_steps = max(3, min(20, K))
+    hq = [x.q.pin_memory() for x in xs]
+    hk = [x.k.pin_memory() for x in xs]
+    hv = [x.v.pin_memory() for x in xs]
+    ho = [torch.empty(x.q.shape, dtype=torch.bfloat16).pin_memory() for x in xs]
+    hl = [torch.empty(x.q.shape[0], x.q.shape[2], x.q.shape[1], dtype=torch.float32).pin_memory()
+          for x in xs]
+    dbuf = [(torch.empty_like(p[1]), torch.empty_like(p[2]), torch.empty_like(p[3])) for p in pre]
+    h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv)
+    d2h = sum(t.numel() * t.element_size() for t in ho + hl)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for i, x in enumerate(xs):
+                q, k, v = dbuf[i]
+                q.copy_(hq[i], non_blocking=True)
+                k.copy_(hk[i], non_blocking=True)
+                v.copy_(hv[i], non_blocking=True)
+                o, lse = ea.attn_fwd(q, k, v, pre[i][4], pre[i][5], causal=x.causal,
+                                     scale=x.scale, stream=stream)
+                ho[i].copy_(o, non_blocking=True)
+                hl[i].copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = tt.item()
+    e2e_val = world * e2e_steps * (f_nc + f_c) / (e2e_ms / 1e3) / 1e12
+
+    if rank == 0:
+        achieved = (f_nc + f_c) * K / (tot_pre / 1e3) / 1e12
+        dec_achieved = kv_bytes * K / (tot_dec / 1e3) / 1e9
+        tr = profiled_traffic("attn_fwd_sm103.cu", "attn_fwd_prefill_b4h16s2048d128")
+        dtr = profiled_traffic("attn_decode_sm103.cu", "attn_decode_split_b64hq32hkv8d128")
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": tot_step / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "prefill_flops_per_step": f_nc + f_c,
+                       "decode_kv_bytes_per_step": kv_bytes,
+                       "l2": "flushed before every step (256 MB write)",
+                       "parallelism": f"replicas x{world} (each rank its own batch)"},
+            "prefill_ms": {"noncausal": statistics.median(t_nc), "causal": statistics.median(t_c)},
+            "decode": {"value": dec_gbs, "unit": "GB/s", "ms": statistics.median(t_dec),
+                       "roofline": {"bound": "hbm", "achieved": dec_achieved, "peak": hbm,
+                                    "unit": "GB/s", "frac": dec_achieved / hbm,
+                                    "peak_source": src, "traffic": dtr}},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16,
+                         "unit": "TFLOP/s", "frac": achieved / bf16, "peak_source": src,
+                         "traffic": tr},
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clocks,
+            "wall_s_timed": wall,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

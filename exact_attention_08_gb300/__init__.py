@@ -1,0 +1,231 @@
+"""Exact attention on GB300 (sm_103a): thin Python binding of libattn_gb300.so.
+
+Every function here only marshals arguments (device pointers, sizes, the
+current CUDA stream) and calls the C ABI declared in include/attn.h of the
+same name; all attention arithmetic runs in the library's CUDA kernels.
+PyTorch is used for device memory and streams only.  There is no fallback:
+importing this package fails if the library cannot be built or loaded, and a
+call fails if the library reports an error.
+
+    o, lse = attn_fwd(q, k, v, causal=True)          # q [B,Sq,Hq,d], k/v [B,Skv,Hkv,d]
+    o, lse = attn_fwd_ex(q, k, v, cu_q, cu_k, max_seqlen_q=..., causal=True)
+    o, lse = attn_decode_paged(q, k_pages, v_pages, page_table, seqlens, num_splits=8)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from . import _build
+
+__all__ = [
+    "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT",
+    "ATTN_ERR_BAD_INPUT", "AttnError", "attn_fwd", "attn_fwd_ex", "attn_decode_workspace_size",
+    "attn_decode_paged", "attn_device_status", "attn_check_wait_timeout", "attn_status_string",
+    "attn_last_error", "library_path", "lib",
+]
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+ATTN_ERR_BAD_INPUT = 5
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB
+    if _build.needs_build():
+        try:
+            path = _build.build()
+        except Exception as e:  # no silent fallback: the package is unusable without it
+            raise ImportError(f"exact_attention_08_gb300: cannot build {_build.LIB}: {e}") from e
+    if not os.path.exists(path):
+        raise ImportError(f"exact_attention_08_gb300: {path} is missing")
+    L = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
+    L.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, i, i, vp]
+    L.attn_decode_workspace_size.argtypes = [i, i, i, i]
+    L.attn_decode_workspace_size.restype = sz
+    L.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, sz,
+                                    vp]
+    L.attn_device_status.argtypes = [vp]
+    L.attn_check_wait_timeout.argtypes = [i, vp]
+    L.attn_status_string.argtypes = [i]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_last_error.argtypes = []
+    L.attn_last_error.restype = ctypes.c_char_p
+    for fn in ("attn_fwd", "attn_fwd_ex", "attn_decode_paged", "attn_device_status",
+               "attn_check_wait_timeout"):
+        getattr(L, fn).restype = ctypes.c_int
+    return L
+
+
+lib = _load()
+library_path = _build.LIB
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        detail = lib.attn_last_error().decode()
+        msg = f"{what}: {lib.attn_status_string(status).decode()}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
+
+
+def attn_status_string(status: int) -> str:
+    return lib.attn_status_string(int(status)).decode()
+
+
+def attn_last_error() -> str:
+    return lib.attn_last_error().decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != ATTN_OK:
+        raise AttnError(rc, what)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    if stream is None:
+        return _torch().cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, name, dtype, device=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def attn_fwd(q, k, v, o=None, lse=None, *, causal=False, window=0, scale=None, stream=None,
+             want_lse=True):
+    """Dense BSHD forward.  q [B,Sq,Hq,d], k/v [B,Skv,Hkv,d] bf16 -> o [B,Sq,Hq,d] bf16,
+    lse [B,Hq,Sq] fp32 (None when want_lse is False and lse is not given)."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, q.device)
+    B, Sq, Hq, d = q.shape
+    Bk, Skv, Hkv, dk = k.shape
+    if Bk != B or dk != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q/k/v shapes disagree")
+    if o is None:
+        o = torch.empty_like(q)
+    _need(o, "o", torch.bfloat16, q.device)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, d,
+                      scale, int(bool(causal)), int(window), _stream(stream))
+    _check(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_ex(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, *, max_seqlen_q=None,
+                max_seqlen_k=None, o=None, lse=None, causal=False, window=0, n_sink=0, scale=None,
+                stream=None, want_lse=True):
+    """Forward with sink keys and optional packing.  With cu_seqlens (int32 CUDA
+    tensors [nseq+1]): q [Tq,Hq,d], k/v [Tk,Hkv,d], o [Tq,Hq,d], lse [Hq,Tq].
+    Without: the dense layout of attn_fwd."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, q.device)
+    varlen = cu_seqlens_q is not None
+    if varlen:
+        _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, q.device)
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, q.device)
+        Tq, Hq, d = q.shape
+        Tk, Hkv, _ = k.shape
+        nseq = cu_seqlens_q.numel() - 1
+        if max_seqlen_q is None or max_seqlen_k is None:
+            raise ValueError("max_seqlen_q and max_seqlen_k are required with cu_seqlens")
+        B, sq, sk = nseq, int(max_seqlen_q), int(max_seqlen_k)
+        lse_shape = (Hq, Tq)
+    else:
+        B, sq, Hq, d = q.shape
+        _, sk, Hkv, _ = k.shape
+        Tq = Tk = 0
+        lse_shape = (B, Hq, sq)
+    if o is None:
+        o = torch.empty_like(q)
+    _need(o, "o", torch.bfloat16, q.device)
+    if lse is None and want_lse:
+        lse = torch.empty(*lse_shape, dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib.attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
+                         _ptr(cu_seqlens_k), B, Hq, Hkv, sq, sk, Tq, Tk, d, scale,
+                         int(bool(causal)), int(window), int(n_sink), _stream(stream))
+    _check(rc, "attn_fwd_ex")
+    return o, lse
+
+
+def attn_decode_workspace_size(B: int, Hq: int, d: int, num_splits: int) -> int:
+    return int(lib.attn_decode_workspace_size(int(B), int(Hq), int(d), int(num_splits)))
+
+
+def attn_decode_paged(q, k_pages, v_pages, page_table, seqlens, o=None, lse=None, *,
+                      num_splits=8, scale=None, workspace=None, stream=None, want_lse=True):
+    """One-token decode.  q [B,Hq,d] bf16, k/v_pages [P,16,Hkv,d] bf16, page_table
+    [B,maxP] int32, seqlens [B] int32 -> o [B,Hq,d] bf16, lse [B,Hq] fp32."""
+    torch = _torch()
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k_pages, "k_pages", torch.bfloat16, dev)
+    _need(v_pages, "v_pages", torch.bfloat16, dev)
+    _need(page_table, "page_table", torch.int32, dev)
+    _need(seqlens, "seqlens", torch.int32, dev)
+    B, Hq, d = q.shape
+    P, page, Hkv, dk = k_pages.shape
+    if dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages/v_pages shapes disagree with q")
+    if page_table.dim() != 2 or page_table.shape[0] != B or seqlens.numel() != B:
+        raise ValueError("page_table must be [B, max_pages] and seqlens [B]")
+    if o is None:
+        o = torch.empty_like(q)
+    _need(o, "o", torch.bfloat16, dev)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    need = attn_decode_workspace_size(B, Hq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib.attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                               _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, Hkv, d, page,
+                               page_table.shape[1], P, int(num_splits), scale, _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_decode_paged")
+    return o, lse
+
+
+def attn_device_status(stream=None) -> int:
+    """Synchronises the stream; returns and clears the device status word."""
+    return int(lib.attn_device_status(_stream(stream)))
+
+
+def attn_check_wait_timeout(limit_us: int, stream=None) -> None:
+    _check(lib.attn_check_wait_timeout(int(limit_us), _stream(stream)), "attn_check_wait_timeout")

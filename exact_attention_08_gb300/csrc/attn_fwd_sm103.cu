@@ -1,0 +1,631 @@
+// Exact attention forward for sm_103a: tcgen05 MMAs with accumulators in
+// tensor memory, TMA-fed K/V ring, online softmax fused between the two
+// matrix products.
+//
+// One CTA owns 256 consecutive query rows of one (batch or sequence, query
+// head): two 128-row Q tiles, resident in shared memory for the whole key
+// loop (the FA-2 order: query tiles in the grid, key/value tiles in the inner
+// loop; "TileLang in practice: FlashAttention forward kernel", sections 3.1
+// and 5; "TileLang tutorial, ch.15 Operators: Attention", section 2.5).
+// Keys and values stream through a ring of 128-key tiles.
+//
+// Warp roles (12 warps, three warpgroups):
+//   warps 0-3   softmax for Q tile 0 (thread r owns query row r: TMEM lane r)
+//   warps 4-7   softmax for Q tile 1
+//   warp  8     TMA producer (Q once, then the K/V ring); allocates TMEM
+//   warp  9     MMA issuer (one thread)
+//   warps 10-11 idle
+// Tensor memory (512 columns): S_i = Q_i K^T at columns [128 i, 128 i + 128)
+// (fp32), O_i at [256 + D i, 256 + D i + D) (fp32).  The softmax writes the
+// probabilities P_i back over the first 64 columns of S_i as packed bf16
+// pairs, and the second product O_i += P_i V reads P_i straight from tensor
+// memory, so neither S nor P ever leaves the SM.
+//
+// MMA issue order per key tile j:  O_0 += P_0(j-1) V(j-1), S_0 = Q_0 K(j)^T,
+// O_1 += P_1(j-1) V(j-1), S_1 = Q_1 K(j)^T.  While warpgroup 0 turns S_0(j)
+// into P_0(j), the tensor core runs O_1(j-1) and S_1(j), and vice versa, so
+// the exponentials of one tile overlap the matrix products of the other.
+//
+// Online softmax per row (ch.15 section 2.3): raw row maximum m (the scale is
+// applied inside the exponent, ch.15 section 3.2: max(s x) = s max(x)),
+// exponent base 2 with log2(e) folded into the scale, running sum l, final
+// O / l, LSE = m * scale + ln(l).  The rescale of O and l by
+// exp2((m_old - m_new) * scale * log2 e) is applied only when the maximum grows
+// by more than 8 in log2 units; otherwise the stale maximum is kept, which is
+// exact (any common shift cancels between O and l, ch.15 section 2.4) and
+// keeps every probability below 2^8.  A maximum of -inf (no visible key yet)
+// is replaced by 0 in the exponent (check_inf, ch.15 section 5.1(1)); a row
+// that never sees a key returns O = 0 and LSE = -inf (section 5.1(2)).
+//
+// Masks (ch.15 sections 3.4, 5.2): tiles that no row of a Q tile can see are
+// never loaded (causal upper bound, window lower bound, sink tiles kept);
+// tiles every row sees in full skip the mask; only boundary tiles compare
+// key indices, in registers after the tensor-memory load.
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <cuda_bf16.h>
+#include <climits>
+#include <mutex>
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;       // query rows per Q tile (= TMEM lanes)
+constexpr int kQT = 2;         // Q tiles per CTA
+constexpr int kBN = 128;       // keys per K/V tile
+constexpr int kThreads = 384;  // 12 warps
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct Cfg {
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kTileBytes = kBM * D * 2;  // 128 rows x D bf16 (Q, K and V tiles alike)
+  static constexpr int kAtoms = D / 64;           // 128-byte swizzle atoms per row
+  static constexpr int kAtomBytes = 128 * 128;    // one atom column of a tile: 128 rows x 128 B
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQT * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_ready[2], o_done[2], drain
+  static constexpr int kNumBars = 1 + 4 * kStages + 3 * kQT + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 2 * kBN;
+};
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  const int* cu_q;
+  const int* cu_k;
+  int B, Hq, Hkv, Sq, Skv, total_q;
+  int num_qpairs;
+  float scale, scale2;
+  int causal, window, n_sink;
+  uint64_t wait_limit_ns;
+  int* status;
+};
+
+// Rows [qa, qb) of one Q tile (sequence-relative) and the extreme visible-key
+// bounds over those rows: key k is visible to row q iff k <= hi(q) and, with a
+// window, (k > lo(q) or k < n_sink).
+struct TileMask {
+  int qa, qb;
+  int hi_min, hi_max;  // hi(qa), hi(qb - 1)
+  int lo_min, lo_max;  // lo(qa), lo(qb - 1)
+};
+
+__device__ __forceinline__ TileMask make_mask(int qa, int Lq, int Lk, int off, int causal,
+                                              int window) {
+  TileMask m;
+  m.qa = qa;
+  m.qb = min(qa + kBM, Lq);
+  const int last = max(m.qb - 1, qa);
+  m.hi_min = causal ? min(qa + off, Lk - 1) : Lk - 1;
+  m.hi_max = causal ? min(last + off, Lk - 1) : Lk - 1;
+  m.lo_min = (window > 0) ? qa + off - window : INT_MIN;
+  m.lo_max = (window > 0) ? last + off - window : INT_MIN;
+  return m;
+}
+
+// Does any row of the tile see any key of key tile j?
+__device__ __forceinline__ bool tile_active(const TileMask& m, int j, int Lk, int window,
+                                            int n_sink) {
+  if (m.qb <= m.qa) return false;
+  const int ka = j * kBN;
+  if (ka >= Lk || ka > m.hi_max) return false;
+  if (window > 0) {
+    const int kb1 = min(ka + kBN, Lk) - 1;
+    return kb1 > m.lo_min || ka < n_sink;
+  }
+  return true;
+}
+
+// Does every row of the tile see every key of key tile j (no mask needed)?
+__device__ __forceinline__ bool tile_interior(const TileMask& m, int j, int window, int n_sink) {
+  const int ka = j * kBN, kb1 = ka + kBN - 1;
+  if (kb1 > m.hi_min) return false;  // hi_min <= Lk - 1 also rules out the ragged tail
+  if (window > 0 && !(ka > m.lo_max || kb1 < n_sink)) return false;
+  return true;
+}
+
+__device__ __forceinline__ void reg_fence(uint32_t& r) { asm volatile("" : "+r"(r)); }
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void fail(int* status, volatile int* abort_flag) {
+  atomicOr(status, kStatusTimeout);
+  *abort_flag = 1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using C = Cfg<D>;
+  constexpr int ST = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + ST;
+  uint64_t* v_full = k_empty + ST;
+  uint64_t* v_empty = v_full + ST;
+  uint64_t* s_full = v_empty + ST;
+  uint64_t* p_ready = s_full + kQT;
+  uint64_t* o_done = p_ready + kQT;
+  uint64_t* drain = o_done + kQT;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  __shared__ int abort_flag_s;
+  volatile int* abort_flag = &abort_flag_s;
+
+  // ---------------------------------------------------------------- work item
+  int x = blockIdx.x;
+  const int h = x % p.Hq;
+  x /= p.Hq;
+  const int bseq = x % p.B;
+  int qp = x / p.B;
+  if (p.causal) qp = p.num_qpairs - 1 - qp;  // longest key ranges first
+
+  int Lq, Lk, q_base, k_base, b_coord;
+  if (p.cu_q != nullptr) {
+    const int a = p.cu_q[bseq], e = p.cu_q[bseq + 1];
+    const int ka = p.cu_k[bseq], ke = p.cu_k[bseq + 1];
+    if (a < 0 || e < a || e > p.total_q || ka < 0 || ke < ka || e - a > p.Sq) {
+      if (threadIdx.x == 0) atomicOr(p.status, kStatusBadInput);
+      return;
+    }
+    Lq = e - a;
+    Lk = ke - ka;
+    q_base = a;
+    k_base = ka;
+    b_coord = 0;
+  } else {
+    Lq = p.Sq;
+    Lk = p.Skv;
+    q_base = 0;
+    k_base = 0;
+    b_coord = bseq;
+  }
+  const int q0 = qp * (kQT * kBM);
+  if (q0 >= Lq) return;  // uniform over the CTA, before any barrier or TMEM use
+
+  const int off = Lk - Lq;
+  const int hk = h / (p.Hq / p.Hkv);
+  const int nT = (Lk + kBN - 1) / kBN;
+  TileMask mk[kQT];
+#pragma unroll
+  for (int i = 0; i < kQT; ++i) mk[i] = make_mask(q0 + i * kBM, Lq, Lk, off, p.causal, p.window);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  // ---------------------------------------------------------------- setup
+  if (threadIdx.x == 0) {
+    abort_flag_s = 0;
+    mbar_init(q_full, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int i = 0; i < kQT; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_ready[i], 128);
+      mbar_init(&o_done[i], 1);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kWarpLoad) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpLoad) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      bool any = false;
+      for (int j = 0; j < nT && !any; ++j)
+        any = tile_active(mk[0], j, Lk, p.window, p.n_sink) ||
+              tile_active(mk[1], j, Lk, p.window, p.n_sink);
+      if (any) {  // no copy is issued that nobody waits for
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        mbar_arrive_expect_tx(q_full, kQT * C::kTileBytes);
+#pragma unroll
+        for (int i = 0; i < kQT; ++i)
+#pragma unroll
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_4d(sQ + i * C::kTileBytes + a * C::kAtomBytes, &tmQ, q_full, a * 64, h,
+                        q_base + q0 + i * kBM, b_coord);
+      }
+      int u = 0;
+      bool ring_ok = true;
+      for (int j = 0; j < nT; ++j) {
+        if (!tile_active(mk[0], j, Lk, p.window, p.n_sink) &&
+            !tile_active(mk[1], j, Lk, p.window, p.n_sink))
+          continue;
+        const int s = u % ST;
+        const uint32_t ph = (u / ST) & 1;
+        if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag, p.wait_limit_ns)) {
+          fail(p.status, abort_flag);
+          ring_ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_4d(sK + s * C::kTileBytes + a * C::kAtomBytes, &tmK, &k_full[s], a * 64, hk,
+                      k_base + j * kBN, b_coord);
+        if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag, p.wait_limit_ns)) {
+          fail(p.status, abort_flag);
+          ring_ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_4d(sV + s * C::kTileBytes + a * C::kAtomBytes, &tmV, &v_full[s], a * 64, hk,
+                      k_base + j * kBN, b_coord);
+        ++u;
+      }
+      // Tail: wait for the last release of every ring slot, so that no
+      // tensor-core commit still has to arrive on this CTA's barriers when
+      // it exits.  Slot s was used n_s times.
+      for (int s = 0; ring_ok && s < ST; ++s) {
+        const int n_s = (u > s) ? (u - s + ST - 1) / ST : 0;
+        if (n_s == 0) continue;
+        const uint32_t par = (n_s - 1) & 1;
+        if (!mbar_wait(&k_empty[s], par, abort_flag, p.wait_limit_ns) ||
+            !mbar_wait(&v_empty[s], par, abort_flag, p.wait_limit_ns)) {
+          fail(p.status, abort_flag);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+      int tot[kQT], pv_cnt[kQT], pend[kQT];
+#pragma unroll
+      for (int i = 0; i < kQT; ++i) {
+        tot[i] = 0;
+        pv_cnt[i] = 0;
+        pend[i] = -1;
+        for (int j = 0; j < nT; ++j) tot[i] += tile_active(mk[i], j, Lk, p.window, p.n_sink);
+      }
+      bool ok = (tot[0] + tot[1] == 0) || mbar_wait(q_full, 0, abort_flag, p.wait_limit_ns);
+      if (!ok) fail(p.status, abort_flag);
+      int u = 0, j = 0;
+      while (ok) {
+        while (j < nT && !tile_active(mk[0], j, Lk, p.window, p.n_sink) &&
+               !tile_active(mk[1], j, Lk, p.window, p.n_sink))
+          ++j;
+        const bool have = j < nT;
+        const int s = u % ST;
+        if (have) {
+          if (!mbar_wait(&k_full[s], (u / ST) & 1, abort_flag, p.wait_limit_ns)) {
+            fail(p.status, abort_flag);
+            break;
+          }
+          tc_fence_after_sync();
+        }
+#pragma unroll
+        for (int i = 0; i < kQT; ++i) {
+          if (pend[i] >= 0) {
+            // O_i += P_i V for the previous key tile of this Q tile
+            const int sv = pend[i] % ST;
+            if (!mbar_wait(&v_full[sv], (pend[i] / ST) & 1, abort_flag, p.wait_limit_ns) ||
+                !mbar_wait(&p_ready[i], pv_cnt[i] & 1, abort_flag, p.wait_limit_ns)) {
+              fail(p.status, abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t vbase = smem_addr(sV + sv * C::kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk) {
+              const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, C::kAtomBytes, 1024);
+              mma_bf16_ts(tmem + C::kColO + i * D, tmem + i * kBN + kk * 8, bdesc, idesc_o,
+                          (pv_cnt[i] > 0 || kk > 0) ? 1u : 0u);
+            }
+            ++pv_cnt[i];
+            if (pv_cnt[i] == tot[i]) mma_commit(&o_done[i]);
+            pend[i] = -1;
+          }
+          if (have && tile_active(mk[i], j, Lk, p.window, p.n_sink)) {
+            // S_i = Q_i K^T for key tile j
+            const uint32_t qbase = smem_addr(sQ + i * C::kTileBytes);
+            const uint32_t kbase = smem_addr(sK + s * C::kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk / 4) * C::kAtomBytes + (kk % 4) * 32;
+              mma_bf16_ss(tmem + i * kBN, sdesc_sw128(qbase + koff, 16, 1024),
+                          sdesc_sw128(kbase + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&s_full[i]);
+            pend[i] = u;
+          }
+        }
+        if (!ok) break;
+        if (have) mma_commit(&k_empty[s]);
+        if (u >= 1) mma_commit(&v_empty[(u - 1) % ST]);
+        if (!have) break;
+        ++u;
+        ++j;
+      }
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ============================================================ softmax warpgroups
+    const int i = warp / 4;
+    const int wq = warp % 4;
+    const int r = wq * 32 + lane;
+    const int row = q0 + i * kBM + r;  // sequence-relative query index
+    const bool valid = row < Lq;
+    const int hi_row = p.causal ? min(row + off, Lk - 1) : Lk - 1;
+    const int lo_row = (p.window > 0) ? row + off - p.window : INT_MIN;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t colS = i * kBN;
+    const uint32_t colO = C::kColO + i * D;
+    const float scale2 = p.scale2;
+    const TileMask m = mk[i];
+
+    float m_used = -INFINITY;  // raw (unscaled) running maximum in use
+    float l = 0.f;             // running sum of the fp32 probabilities (for LSE)
+    float lr = 0.f;            // running sum of the bf16-rounded probabilities (for O)
+    int t = 0;
+    bool ok = true;
+    for (int j = 0; j < nT; ++j) {
+      if (!tile_active(m, j, Lk, p.window, p.n_sink)) continue;
+      bool w_ok = mbar_wait(&s_full[i], t & 1, abort_flag, p.wait_limit_ns);
+      w_ok = __all_sync(0xffffffffu, w_ok);
+      if (!w_ok) {
+        if (lane == 0) fail(p.status, abort_flag);
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t s[kBN];
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) tmem_ld_x32(taddr + colS + c * 32, &s[c * 32]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) reg_fence(s[c]);
+
+      if (!tile_interior(m, j, p.window, p.n_sink)) {
+        const int kb = j * kBN;
+        const int lim_hi = hi_row - kb;
+        const int lim_lo = (p.window > 0) ? ((lo_row == INT_MIN) ? INT_MIN : lo_row - kb) : INT_MIN;
+        const int lim_sink = p.n_sink - kb;
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          const bool vis = (c <= lim_hi) && (c > lim_lo || c < lim_sink);
+          if (!vis) s[c] = __float_as_uint(-INFINITY);
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+
+      bool do_rescale = false;
+      float alpha = 1.f;
+      if (mx > m_used) {
+        if (m_used == -INFINITY) {
+          m_used = mx;
+        } else if ((mx - m_used) * scale2 > kRescaleLog2) {
+          alpha = ex2_approx((m_used - mx) * scale2);
+          l *= alpha;
+          lr *= alpha;
+          m_used = mx;
+          do_rescale = true;
+        }
+      }
+      const float ms = (m_used == -INFINITY) ? 0.f : m_used * scale2;
+      // O is normalised by the sum of the probabilities exactly as the second
+      // product sees them (rounded to bf16), so the rounding of a dominant
+      // probability cancels between numerator and denominator; the LSE keeps
+      // the unrounded fp32 sum.
+      float l0 = 0.f, l1 = 0.f, r0 = 0.f, r1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c * 32 + 2 * e]), scale2, -ms));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c * 32 + 2 * e + 1]), scale2, -ms));
+          l0 += p0;
+          l1 += p1;
+          pk[e] = pack_bf16x2(p0, p1);
+          r0 += __uint_as_float(pk[e] << 16);
+          r1 += __uint_as_float(pk[e] & 0xffff0000u);
+        }
+        tmem_st_x16(taddr + colS + c * 16, pk);
+      }
+      l += l0 + l1;
+      lr += r0 + r1;
+      if (__any_sync(0xffffffffu, do_rescale)) {
+        // O of this row was last written by the product issued before S(j),
+        // which has completed (the commit behind s_full covers it); the next
+        // product into O waits for this warpgroup's p_ready arrival below.
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_x32(taddr + colO + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            reg_fence(o[e]);
+            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          }
+          tmem_st_x32(taddr + colO + c * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&p_ready[i]);
+      ++t;
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    bool have_o = ok && t > 0;
+    if (have_o) {
+      bool w_ok = mbar_wait(&o_done[i], 0, abort_flag, p.wait_limit_ns);
+      w_ok = __all_sync(0xffffffffu, w_ok);
+      if (!w_ok) {
+        if (lane == 0) fail(p.status, abort_flag);
+        have_o = false;
+      }
+    }
+    const size_t orow = p.cu_q ? (static_cast<size_t>(q_base + row) * p.Hq + h) * D
+                               : ((static_cast<size_t>(bseq) * p.Sq + row) * p.Hq + h) * D;
+    uint4* dst = reinterpret_cast<uint4*>(p.o + orow);
+    const bool seen = have_o && l > 0.f;
+    if (have_o) {
+      tc_fence_after_sync();
+      const float inv = seen ? 1.f / lr : 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld_x32(taddr + colO + c * 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) reg_fence(o[e]);
+        if (valid) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int idx = v4 * 8 + 2 * e;
+              w[e] = seen ? pack_bf16x2(__uint_as_float(o[idx]) * inv,
+                                        __uint_as_float(o[idx + 1]) * inv)
+                          : 0u;
+            }
+            dst[c * 4 + v4] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    } else if (valid && ok) {
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (valid && p.lse != nullptr && (ok || !have_o)) {
+      const size_t li = p.cu_q ? static_cast<size_t>(h) * p.total_q + q_base + row
+                               : (static_cast<size_t>(bseq) * p.Hq + h) * p.Sq + row;
+      p.lse[li] = seen ? fmaf(m_used, p.scale, logf(l)) : -INFINITY;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (*abort_flag) {
+    // Let every tensor-core operation and bulk copy already issued land
+    // before the tensor memory and shared memory are given back.
+    if (warp == kWarpMma && lane == 0) {
+      mma_commit(drain);
+      mbar_wait(drain, 0, nullptr, 100000000ull);
+    }
+    if (warp == kWarpLoad && lane == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 2000000ull) {
+      }
+    }
+    __syncthreads();
+  }
+  tc_fence_after_sync();
+  if (warp == kWarpLoad) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// O = 0 and LSE = -inf everywhere: every query sees no key (no keys at all).
+__global__ void attn_fill_empty_kernel(__nv_bfloat16* o, size_t o_elems, float* lse,
+                                       size_t lse_elems) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t e = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; e < o_elems;
+       e += stride)
+    o[e] = __float2bfloat16(0.f);
+  if (lse)
+    for (size_t e = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; e < lse_elems;
+         e += stride)
+      lse[e] = -INFINITY;
+}
+
+template <int D>
+cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
+  using C = Cfg<D>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  Params p;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.Sq = a.Sq;
+  p.Skv = a.Skv;
+  p.total_q = a.total_q;
+  p.num_qpairs = (a.Sq + kQT * kBM - 1) / (kQT * kBM);
+  p.scale = a.scale;
+  p.scale2 = a.scale * kLog2e;
+  p.causal = a.causal;
+  p.window = a.window;
+  p.n_sink = a.n_sink;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.status = a.status;
+  const long long ctas = static_cast<long long>(p.num_qpairs) * a.B * a.Hq;
+  if (ctas <= 0) return cudaSuccess;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  attn_fwd_kernel<D><<<static_cast<unsigned>(ctas), kThreads, C::kSmemBytes, stream>>>(
+      a.tmQ, a.tmK, a.tmV, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const FwdLaunch& a, cudaStream_t stream) {
+  if (a.d == 128) return launch_d<128>(a, stream);
+  if (a.d == 64) return launch_d<64>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_fill_empty(const FwdLaunch& a, cudaStream_t stream) {
+  const size_t rows = a.cu_q ? static_cast<size_t>(a.total_q) : static_cast<size_t>(a.B) * a.Sq;
+  const size_t o_elems = rows * a.Hq * a.d;
+  const size_t lse_elems = rows * a.Hq;
+  if (o_elems == 0) return cudaSuccess;
+  attn_fill_empty_kernel<<<1216, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(a.o), o_elems,
+                                                   a.lse, lse_elems);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

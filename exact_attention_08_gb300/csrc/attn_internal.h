@@ -1,0 +1,56 @@
+// Internal interface between the C-ABI host code and the kernel translation
+// units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+// device status bits (the status word is an int in device memory)
+enum : int {
+  kStatusTimeout = 1,   // a bounded wait ran out
+  kStatusBadInput = 2,  // out-of-range device data (page index, cu_seqlens)
+};
+
+// Default limit of every bounded wait in the production kernels.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
+
+struct FwdLaunch {
+  CUtensorMap tmQ, tmK, tmV;  // 4-D maps (d, H, S, B) with 64 x 1 x 128 x 1 boxes
+  void* o;                    // bf16 output
+  float* lse;                 // fp32 log-sum-exp, may be null
+  const int* cu_q;            // null: dense layout
+  const int* cu_k;
+  int B, Hq, Hkv;
+  int Sq, Skv;                // dense sizes, or the maxima for varlen
+  int total_q, total_k;       // varlen totals (dense: unused)
+  int d;
+  float scale;
+  int causal, window, n_sink;
+  int* status;
+};
+
+struct DecodeLaunch {
+  CUtensorMap tmK, tmV;  // 4-D maps over the page pools (d, Hkv, page, pages), 64 x 1 x 16 x 1 boxes
+  const void* q;
+  void* o;
+  float* lse;
+  const int* page_table;
+  const int* seqlens;
+  float* ws_o;    // [B, Hq, S, d] fp32 split outputs (normalised)
+  float* ws_lse;  // [B, Hq, S] fp32 split log-sum-exps (natural log)
+  int B, Hq, Hkv, d, page, max_pages, num_pages, num_splits;
+  float scale;
+  int* status;
+};
+
+// Kernel launchers (return cudaError_t of the launch).
+cudaError_t launch_attn_fwd(const FwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_attn_fill_empty(const FwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_attn_decode(const DecodeLaunch& a, cudaStream_t stream);
+cudaError_t launch_wait_timeout_check(int* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,168 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) exact-attention library
+ * (libattn_gb300.so).
+ *
+ * What it computes.  Exact scaled dot-product attention,
+ *     O = softmax(scale * Q K^T) V,   LSE_i = ln sum_j exp(scale * q_i . k_j),
+ * evaluated tile by tile with the online-softmax recurrence (running row max,
+ * rescale factor exp(m_old - m_new), running sum, unnormalised output, one
+ * final division), so the score and probability matrices never reach device
+ * memory.  Definitions: "TileLang tutorial, ch.15 Operators: Attention",
+ * sections 1.1 and 2.1-2.5; "llm-course, ch.19 Flash Attention", sections
+ * 19.1 and 19.5; "TileLang in practice: FlashAttention forward kernel",
+ * sections 2.3-2.4 and 4.  The result is exact up to rounding: the only
+ * precision drop is the bf16 rounding of the probabilities before the second
+ * matrix product (ch.15 section 3.2; TileLang in practice section 4.5).
+ *
+ * Masks (ch.15 sections 3.4, 5.2, 5.3).  With off = Skv - Sq (queries are
+ * aligned to the END of the keys, the KV-cache convention), key j is visible
+ * to query i iff
+ *     j < Skv
+ *     and, if causal:              j <= i + off
+ *     and, if window W > 0:        j > i + off - W   or   j < n_sink.
+ * A query that sees no key gets O = +0.0 and LSE = -inf (ch.15 section
+ * 5.1(2)).  The sliding window is only defined together with causal.
+ *
+ * Grouped-query attention (ch.15 section 4.8(1)): query head h reads
+ * key/value head h / (Hq / Hkv); Hq must be a multiple of Hkv.
+ *
+ * Common rules for every entry point.
+ *   - Pointers to tensors are DEVICE pointers owned by the caller, 16-byte
+ *     aligned, to contiguous row-major tensors in the layouts stated below.
+ *     The library never allocates, frees or keeps device memory.
+ *   - Element types: q, k, v, o are bf16 (uint16 storage); lse is fp32.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream: they return after
+ *     launching and never synchronise, except attn_device_status.
+ *   - Return value: an attn_status code.  On any error nothing is launched.
+ *     Errors found by a kernel (a bounded wait that ran out, an out-of-range
+ *     page index) cannot be returned by the launching call; the kernel
+ *     records them in a device-side status word read by attn_device_status.
+ *   - Head dimension d must be 64 or 128.  The device must be sm_103.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+typedef enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, Hq % Hkv != 0,
+                               window without causal, workspace too small, ... */
+  ATTN_ERR_UNSUPPORTED = 2, /* head dim not 64/128, page size not 16, device not sm_103 */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed */
+  ATTN_ERR_TIMEOUT = 4,     /* a kernel's bounded wait ran out (device status) */
+  ATTN_ERR_BAD_INPUT = 5    /* a kernel met out-of-range device data, e.g. a page
+                               index outside [0, num_pages_total) (device status) */
+} attn_status;
+
+/*
+ * Dense attention forward, BSHD layout.
+ *   q   [B, Sq,  Hq,  d]   bf16       k, v [B, Skv, Hkv, d]  bf16
+ *   o   [B, Sq,  Hq,  d]   bf16 (out) lse  [B, Hq,  Sq]      fp32 (out, may be NULL)
+ *   scale: multiplies Q K^T (1/sqrt(d) in the usual convention).
+ *   causal: 0/1.  window: <= 0 for none, else W keys including the diagonal
+ *   (requires causal).  No sink keys (see attn_fwd_ex).
+ * Sizes: B, Hq, Hkv >= 1; Sq, Skv >= 0 (Sq == 0 or B == 0 launches nothing;
+ * Skv == 0 writes O = 0, LSE = -inf).  q/k/v may be NULL only when their
+ * tensor is empty.
+ */
+ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                      float scale, int causal, int window, void* stream);
+
+/*
+ * Attention forward with sink keys and optional variable-length packing.
+ *   cu_seqlens_q, cu_seqlens_k: NULL for the dense layout of attn_fwd (then
+ *     B is the batch, max_Sq/max_Skv are Sq/Skv, total_q/total_k unused);
+ *     otherwise DEVICE int32 arrays [B + 1] of prefix sums over B packed
+ *     sequences (ch.15 section 5.3) and the layouts are
+ *       q, o [total_q, Hq, d]   k, v [total_k, Hkv, d]   lse [Hq, total_q]
+ *     with total_q = cu_seqlens_q[B], total_k = cu_seqlens_k[B] passed by
+ *     the caller; max_Sq bounds every query length (it sizes the grid).
+ *     Causal alignment is per sequence, to the end of its keys.
+ *   n_sink: with a window, keys 0..n_sink-1 of each sequence stay visible
+ *     to every query that may see them causally (n_sink > 0 needs window > 0).
+ * Device-side checks: cu_seqlens entries that decrease or exceed the totals
+ * are reported as ATTN_ERR_BAD_INPUT through attn_device_status and that
+ * sequence is skipped.
+ */
+ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                         const int* cu_seqlens_q, const int* cu_seqlens_k,
+                         int B, int Hq, int Hkv, int max_Sq, int max_Skv,
+                         int total_q, int total_k, int d,
+                         float scale, int causal, int window, int n_sink, void* stream);
+
+/*
+ * Bytes of device workspace attn_decode_paged needs for these sizes (split
+ * partial outputs and log-sum-exps, fp32).  0 on invalid sizes.
+ */
+ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits);
+
+/*
+ * One-token decode over a paged KV cache, split-KV with a log-sum-exp merge
+ * ("TileLang tutorial, ch.15", sections 4.6 and 4.8(2)-(3), 5.4;
+ * "learn-cuda-from-scratch, ch.12 FlashAttention", section 12.9.4).
+ *   q        [B, Hq, d] bf16              o   [B, Hq, d] bf16 (out)
+ *   lse      [B, Hq] fp32 (out, may be NULL)
+ *   k_pages, v_pages [num_pages_total, page_size, Hkv, d] bf16
+ *   page_table [B, max_pages_per_seq] int32: logical page p of request b is
+ *     physical page page_table[b*max_pages_per_seq + p]; entries at or past
+ *     ceil(seqlens[b] / page_size) are never read.
+ *   seqlens  [B] int32, 0 <= seqlens[b] <= max_pages_per_seq * page_size.
+ *   Request b's query sees its first seqlens[b] keys.  A request with no key
+ *   gets O = 0, LSE = -inf.
+ *   num_splits (1..64): the keys of each request are cut at page granularity,
+ *   pps = ceil(npages_b / num_splits) pages per split; the partial results
+ *   are merged in ascending split order, so repeated calls give identical
+ *   bits.
+ *   workspace: device buffer of at least attn_decode_workspace_size(...)
+ *   bytes, no initial contents required; it is overwritten by every call, so
+ *   calls sharing one workspace must not overlap in time.
+ * page_size must be 16.  Out-of-range page indices are not dereferenced:
+ * they read as zero keys and set ATTN_ERR_BAD_INPUT in the device status.
+ */
+ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                               const int* page_table, const int* seqlens, void* o, float* lse,
+                               int B, int Hq, int Hkv, int d, int page_size,
+                               int max_pages_per_seq, int num_pages_total, int num_splits,
+                               float scale, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device-side status word
+ * of the current device (ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_BAD_INPUT), or
+ * ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+ATTN_API int attn_device_status(void* stream);
+
+/*
+ * Launches a one-warp kernel whose bounded wait (the same helper every
+ * kernel of the library uses) waits on a barrier that nothing completes,
+ * with a limit of `limit_us` microseconds (1..1000000).  The kernel returns
+ * cleanly and the next attn_device_status reports ATTN_ERR_TIMEOUT.  Used to
+ * test failure reporting without faulting or hanging the GPU.
+ */
+ATTN_API int attn_check_wait_timeout(int limit_us, void* stream);
+
+/* Static English text for a status code. */
+ATTN_API const char* attn_status_string(int status);
+
+/* Text of the last ATTN_ERR_CUDA / argument error seen by this thread. */
+ATTN_API const char* attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */
