@@ -125,6 +125,18 @@ __global__ void wait_timeout_check_kernel(int* status, uint64_t limit_ns) {
   if (!ok && threadIdx.x == 0) atomicOr(status, kStatusTimeout);
 }
 
+// ---------------------------------------------------------------- fixed scratch
+// Scratch for attn_decode_paged_noalloc: the split partial outputs and
+// log-sum-exps live in this array instead of a caller-provided workspace.
+// Every device that loads the library holds these 16 MiB until the process
+// exits.  Host code must not use the symbol as a pointer: its device address
+// is looked up once per device (cudaGetSymbolAddress, with that device
+// current) and kept in g_noalloc_scratch_ptr.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+std::mutex g_noalloc_mutex;
+void* g_noalloc_scratch_ptr[kMaxDevices];
+
 }  // namespace
 
 cudaError_t launch_wait_timeout_check(int* status, uint64_t limit_ns, cudaStream_t stream) {
@@ -293,6 +305,38 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v
   a.status = ds->status;
   cudaError_t e = launch_attn_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_error(e, "attn_decode_paged launch");
+}
+
+ATTN_API int attn_decode_paged_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                       const int* page_table, const int* seqlens, void* o,
+                                       float* lse, int B, int Hq, int Hkv, int d, int page_size,
+                                       int max_pages_per_seq, int num_pages_total, int num_splits,
+                                       float scale, void* stream) {
+  t_last_error.clear();
+  const size_t need = attn_decode_workspace_size(B, Hq, d, num_splits);
+  if (need > kNoAllocScratchBytes)
+    return set_error(ATTN_ERR_INVALID_ARG,
+                     "needs %zu bytes of scratch but the built-in scratch holds %zu; lower B, Hq "
+                     "or num_splits, or use attn_decode_paged with a workspace",
+                     need, kNoAllocScratchBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return set_error(ATTN_ERR_UNSUPPORTED, "device %d", dev);
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_scratch_ptr[dev] == nullptr) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress(scratch)");
+      g_noalloc_scratch_ptr[dev] = ptr;
+    }
+    scratch = g_noalloc_scratch_ptr[dev];
+  }
+  return attn_decode_paged(q, k_pages, v_pages, page_table, seqlens, o, lse, B, Hq, Hkv, d,
+                           page_size, max_pages_per_seq, num_pages_total, num_splits, scale,
+                           scratch, kNoAllocScratchBytes, stream);
 }
 
 ATTN_API int attn_device_status(void* stream) {

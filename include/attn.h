@@ -29,7 +29,9 @@
  * Common rules for every entry point.
  *   - Pointers to tensors are DEVICE pointers owned by the caller, 16-byte
  *     aligned, to contiguous row-major tensors in the layouts stated below.
- *     The library never allocates, frees or keeps device memory.
+ *     The library never allocates or frees device memory; its only device
+ *     state is a status word and the fixed scratch array of
+ *     attn_decode_paged_noalloc.
  *   - Element types: q, k, v, o are bf16 (uint16 storage); lse is fp32.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are asynchronous on that stream: they return after
@@ -138,6 +140,33 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v
                                int max_pages_per_seq, int num_pages_total, int num_splits,
                                float scale, void* workspace, size_t workspace_bytes,
                                void* stream);
+
+/*
+ * attn_decode_paged without a workspace argument: the same decode, for
+ * callers that cannot allocate device memory themselves (a serving loop that
+ * must not allocate once it is running, a host program whose plugins may only
+ * use memory handed to them, code that cannot afford the device-wide
+ * synchronisation an allocation may cause).  There is no counterpart on the
+ * source pages: it is an addition of this library.
+ *   The split partials go to one scratch array built into the library
+ *   (16 MiB, held on every device that loads the library until the process
+ *   exits).  Calls needing more than that (attn_decode_workspace_size(...)
+ *   > 16 MiB) return ATTN_ERR_INVALID_ARG and launch nothing.  The library
+ *   allocates nothing on this path.
+ *   The first call on a device looks up the scratch array's device address
+ *   (with that device current) and keeps it; make that first call before
+ *   any stream capture.
+ *   Every call on a device shares the one scratch array and leaves its last
+ *   contents there (nothing in it needs to start at zero), so calls whose
+ *   executions overlap on the GPU race with each other: issue them on one
+ *   stream, or order them.
+ * Arguments, layouts and results are those of attn_decode_paged.
+ */
+ATTN_API int attn_decode_paged_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                       const int* page_table, const int* seqlens, void* o,
+                                       float* lse, int B, int Hq, int Hkv, int d, int page_size,
+                                       int max_pages_per_seq, int num_pages_total, int num_splits,
+                                       float scale, void* stream);
 
 /*
  * Synchronises `stream`, then returns and clears the device-side status word
