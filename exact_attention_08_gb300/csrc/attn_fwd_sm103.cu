@@ -17,7 +17,7 @@
 //   warps 10-11 idle
 // Tensor memory (512 columns): S_i = Q_i K^T at columns [128 i, 128 i + 128)
 // (fp32), O_i at [256 + D i, 256 + D i + D) (fp32).  The softmax writes the
-// probabilities P_i back over the first 64 columns of S_i as packed bf16
+// probabilities P_i back over the last 64 columns of S_i as packed bf16
 // pairs, and the second product O_i += P_i V reads P_i straight from tensor
 // memory, so neither S nor P ever leaves the SM.
 //
@@ -144,6 +144,81 @@ __device__ __forceinline__ void tmem_ld_wait() {
 __device__ __forceinline__ void fail(int* status, volatile int* abort_flag) {
   atomicOr(status, kStatusTimeout);
   *abort_flag = 1;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+
+// Packed pairs of fp32 (one 64-bit register, two lanes of arithmetic per
+// instruction).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Maximum of 32 scores (and a running value), as a shallow tree.
+__device__ __forceinline__ float max32(const uint32_t* v, float run) {
+  float a[11];
+#pragma unroll
+  for (int t = 0; t < 10; ++t)
+    a[t] = max3(__uint_as_float(v[3 * t]), __uint_as_float(v[3 * t + 1]),
+                __uint_as_float(v[3 * t + 2]));
+  a[10] = max3(__uint_as_float(v[30]), __uint_as_float(v[31]), run);
+  const float b0 = max3(a[0], a[1], a[2]), b1 = max3(a[3], a[4], a[5]);
+  const float b2 = max3(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
+  return max3(b0, b1, fmaxf(b2, b3));
+}
+
+// Sets scores of keys a row may not see to -inf: column c of the chunk is
+// key kc0 + c, visible iff c <= lim_hi and (c > lim_lo or c < lim_sink),
+// all limits relative to kc0.
+__device__ __forceinline__ void mask32(uint32_t* v, int lim_hi, int lim_lo, int lim_sink) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const bool vis = (c <= lim_hi) && (c > lim_lo || c < lim_sink);
+    if (!vis) v[c] = __float_as_uint(-INFINITY);
+  }
+}
+
+// Exponentials of 32 scores: p = 2^(s * scale2 - ms), accumulated into the
+// packed running sums and packed to bf16 pairs in pk[16].
+__device__ __forceinline__ void exp32(const uint32_t* v, uint64_t sc2, uint64_t nms,
+                                      uint64_t& sum_a, uint64_t& sum_b, uint32_t* pk) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const uint64_t x = f2_fma(f2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2,
+                              nms);
+    float x0, x1;
+    f2_split(x, x0, x1);
+    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    if (e & 1)
+      sum_b = f2_add(sum_b, f2(p0, p1));
+    else
+      sum_a = f2_add(sum_a, f2(p0, p1));
+    pk[e] = pack_bf16x2(p0, p1);
+  }
 }
 
 template <int D>
@@ -308,6 +383,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+      // Descriptors are built once; every operand of every MMA is a base
+      // descriptor plus a compile-time offset in its 16-byte address field
+      // (shared-memory offsets stay below 256 KB, so the field never carries).
+      const uint64_t dq0 = sdesc_sw128(smem_addr(sQ), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(smem_addr(sK), 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(smem_addr(sV), C::kAtomBytes, 1024);
+      constexpr uint64_t kTileDesc = C::kTileBytes >> 4;
       int tot[kQT], pv_cnt[kQT], pend[kQT];
 #pragma unroll
       for (int i = 0; i < kQT; ++i) {
@@ -332,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
         }
+        const uint64_t dk = dk0 + static_cast<uint64_t>(s) * kTileDesc;
 #pragma unroll
         for (int i = 0; i < kQT; ++i) {
           if (pend[i] >= 0) {
@@ -344,26 +427,26 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after_sync();
-            const uint32_t vbase = smem_addr(sV + sv * C::kTileBytes);
+            const uint64_t dv = dv0 + static_cast<uint64_t>(sv) * kTileDesc;
+            const uint32_t tO = tmem + C::kColO + i * D;
+            const uint32_t tP = tmem + i * kBN + 64;
+            mma_bf16_ts(tO, tP, dv, idesc_o, pv_cnt[i] > 0 ? 1u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-              const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, C::kAtomBytes, 1024);
-              mma_bf16_ts(tmem + C::kColO + i * D, tmem + i * kBN + kk * 8, bdesc, idesc_o,
-                          (pv_cnt[i] > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 1; kk < kBN / 16; ++kk)
+              mma_bf16_ts_c<1>(tO, tP + kk * 8, dv + kk * (2048 >> 4), idesc_o);
             ++pv_cnt[i];
             if (pv_cnt[i] == tot[i]) mma_commit(&o_done[i]);
             pend[i] = -1;
           }
           if (have && tile_active(mk[i], j, Lk, p.window, p.n_sink)) {
             // S_i = Q_i K^T for key tile j
-            const uint32_t qbase = smem_addr(sQ + i * C::kTileBytes);
-            const uint32_t kbase = smem_addr(sK + s * C::kTileBytes);
+            const uint64_t dq = dq0 + i * kTileDesc;
+            const uint32_t tS = tmem + i * kBN;
+            mma_bf16_ss_c<0>(tS, dq, dk, idesc_s);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t koff = (kk / 4) * C::kAtomBytes + (kk % 4) * 32;
-              mma_bf16_ss(tmem + i * kBN, sdesc_sw128(qbase + koff, 16, 1024),
-                          sdesc_sw128(kbase + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 1; kk < D / 16; ++kk) {
+              const uint64_t koff = ((kk / 4) * C::kAtomBytes + (kk % 4) * 32) >> 4;
+              mma_bf16_ss_c<1>(tS, dq + koff, dk + koff, idesc_s);
             }
             mma_commit(&s_full[i]);
             pend[i] = u;
@@ -394,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const TileMask m = mk[i];
 
     float m_used = -INFINITY;  // raw (unscaled) running maximum in use
-    float l = 0.f;             // running sum of the fp32 probabilities (for LSE)
-    float lr = 0.f;            // running sum of the bf16-rounded probabilities (for O)
+    float l = 0.f;             // running sum of the fp32 probabilities
+    float corr = 0.f;          // running sum of (p - bf16(p)) over each tile's largest p
     int t = 0;
     bool ok = true;
     for (int j = 0; j < nT; ++j) {
@@ -408,27 +491,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      uint32_t s[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) tmem_ld_x32(taddr + colS + c * 32, &s[c * 32]);
+      const bool edge = !tile_interior(m, j, p.window, p.n_sink);
+      const int kb = j * kBN;
+      const int lim_hi = hi_row - kb;
+      const int lim_lo = (p.window > 0) ? lo_row - kb : INT_MIN;
+      const int lim_sink = p.n_sink - kb;
+      const uint32_t sS = taddr + colS;
+
+      // pass 1: row maximum over the four 32-column chunks of S
+      uint32_t ra[32], rb[32], rc[32];
+      tmem_ld_x32(sS + 0, ra);
+      tmem_ld_x32(sS + 32, rb);
       tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) reg_fence(s[c]);
-
-      if (!tile_interior(m, j, p.window, p.n_sink)) {
-        const int kb = j * kBN;
-        const int lim_hi = hi_row - kb;
-        const int lim_lo = (p.window > 0) ? ((lo_row == INT_MIN) ? INT_MIN : lo_row - kb) : INT_MIN;
-        const int lim_sink = p.n_sink - kb;
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          const bool vis = (c <= lim_hi) && (c > lim_lo || c < lim_sink);
-          if (!vis) s[c] = __float_as_uint(-INFINITY);
-        }
+      for (int c = 0; c < 32; ++c) {
+        reg_fence(ra[c]);
+        reg_fence(rb[c]);
       }
-      float mx = -INFINITY;
+      if (edge) {
+        mask32(ra, lim_hi, lim_lo, lim_sink);
+        mask32(rb, lim_hi - 32, lim_lo - 32, lim_sink - 32);
+      }
+      float mx = max32(rb, max32(ra, -INFINITY));
+      tmem_ld_x32(sS + 64, ra);
+      tmem_ld_x32(sS + 96, rb);
+      tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+      for (int c = 0; c < 32; ++c) {
+        reg_fence(ra[c]);
+        reg_fence(rb[c]);
+      }
+      if (edge) {
+        mask32(ra, lim_hi - 64, lim_lo - 64, lim_sink - 64);
+        mask32(rb, lim_hi - 96, lim_lo - 96, lim_sink - 96);
+      }
+      mx = max32(rb, max32(ra, mx));
 
       bool do_rescale = false;
       float alpha = 1.f;
@@ -438,49 +535,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if ((mx - m_used) * scale2 > kRescaleLog2) {
           alpha = ex2_approx((m_used - mx) * scale2);
           l *= alpha;
-          lr *= alpha;
+          corr *= alpha;
           m_used = mx;
           do_rescale = true;
         }
       }
       const float ms = (m_used == -INFINITY) ? 0.f : m_used * scale2;
-      // O is normalised by the sum of the probabilities exactly as the second
-      // product sees them (rounded to bf16), so the rounding of a dominant
-      // probability cancels between numerator and denominator; the LSE keeps
-      // the unrounded fp32 sum.
-      float l0 = 0.f, l1 = 0.f, r0 = 0.f, r1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
+      const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
+      uint64_t sum_a = 0, sum_b = 0;  // bit pattern 0 is (+0.f, +0.f)
+
+      // pass 2: probabilities into the upper half of the S columns as bf16
+      // pairs (P column 64 + c/2 for score column c), each store landing on
+      // score columns that have already been read.
+      tmem_ld_x32(sS + 0, rc);  // reload chunk 0 while chunks 2 and 3 are exponentiated
+      {
         uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c * 32 + 2 * e]), scale2, -ms));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c * 32 + 2 * e + 1]), scale2, -ms));
-          l0 += p0;
-          l1 += p1;
-          pk[e] = pack_bf16x2(p0, p1);
-          r0 += __uint_as_float(pk[e] << 16);
-          r1 += __uint_as_float(pk[e] & 0xffff0000u);
-        }
-        tmem_st_x16(taddr + colS + c * 16, pk);
+        exp32(ra, sc2, nms, sum_a, sum_b, pk);
+        tmem_st_x16(sS + 96, pk);
+        exp32(rb, sc2, nms, sum_a, sum_b, pk);
+        tmem_st_x16(sS + 112, pk);
       }
-      l += l0 + l1;
-      lr += r0 + r1;
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 32; ++c) reg_fence(rc[c]);
+      tmem_ld_x32(sS + 32, ra);  // chunk 1
+      if (edge) mask32(rc, lim_hi, lim_lo, lim_sink);
+      {
+        uint32_t pk[16];
+        exp32(rc, sc2, nms, sum_a, sum_b, pk);
+        tmem_st_x16(sS + 64, pk);
+      }
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
+      if (edge) mask32(ra, lim_hi - 32, lim_lo - 32, lim_sink - 32);
+      {
+        uint32_t pk[16];
+        exp32(ra, sc2, nms, sum_a, sum_b, pk);
+        tmem_st_x16(sS + 80, pk);
+      }
+      float s0, s1, s2, s3;
+      f2_split(sum_a, s0, s1);
+      f2_split(sum_b, s2, s3);
+      l += (s0 + s1) + (s2 + s3);
+      // The second product sees bf16-rounded probabilities.  When one key
+      // dominates a row, its rounding error would not cancel between O and l;
+      // track it for the largest probability of every tile (recomputed with
+      // the arithmetic exp32 used for it, so the same value) and take it out
+      // of the normaliser of O.
+      {
+        const float ptop = ex2_approx(__fmaf_rn(mx, scale2, -ms));
+        const float ptop_r = __uint_as_float(pack_bf16x2(0.f, ptop) & 0xffff0000u);
+        corr += ptop - ptop_r;
+      }
       if (__any_sync(0xffffffffu, do_rescale)) {
         // O of this row was last written by the product issued before S(j),
         // which has completed (the commit behind s_full covers it); the next
         // product into O waits for this warpgroup's p_ready arrival below.
+        const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld_x32(taddr + colO + c * 32, o);
+          tmem_ld_x32(taddr + colO + c * 32, rb);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            reg_fence(o[e]);
-            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          for (int e = 0; e < 16; ++e) {
+            reg_fence(rb[2 * e]);
+            reg_fence(rb[2 * e + 1]);
+            float o0, o1;
+            f2_split(f2_mul(f2(__uint_as_float(rb[2 * e]), __uint_as_float(rb[2 * e + 1])), a2),
+                     o0, o1);
+            rb[2 * e] = __float_as_uint(o0);
+            rb[2 * e + 1] = __float_as_uint(o1);
           }
-          tmem_st_x32(taddr + colO + c * 32, o);
+          tmem_st_x32(taddr + colO + c * 32, rb);
         }
       }
       tmem_st_wait();
@@ -505,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool seen = have_o && l > 0.f;
     if (have_o) {
       tc_fence_after_sync();
-      const float inv = seen ? 1.f / lr : 0.f;
+      const float inv = seen ? 1.f / (l - corr) : 0.f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
