@@ -61,6 +61,9 @@ constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
+// Lower visibility bound when there is no window: far below every key index,
+// yet chunk offsets (at most a few hundred) can be subtracted without overflow.
+constexpr int kNoLowerBound = -(1 << 29);
 
 template <int D>
 struct Cfg {
@@ -109,8 +112,8 @@ __device__ __forceinline__ TileMask make_mask(int qa, int Lq, int Lk, int off, i
   const int last = max(m.qb - 1, qa);
   m.hi_min = causal ? min(qa + off, Lk - 1) : Lk - 1;
   m.hi_max = causal ? min(last + off, Lk - 1) : Lk - 1;
-  m.lo_min = (window > 0) ? qa + off - window : INT_MIN;
-  m.lo_max = (window > 0) ? last + off - window : INT_MIN;
+  m.lo_min = (window > 0) ? qa + off - window : kNoLowerBound;
+  m.lo_max = (window > 0) ? last + off - window : kNoLowerBound;
   return m;
 }
 
@@ -248,12 +251,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &abort_flag_s;
 
   // ---------------------------------------------------------------- work item
-  int x = blockIdx.x;
-  const int h = x % p.Hq;
-  x /= p.Hq;
-  const int bseq = x % p.B;
-  int qp = x / p.B;
-  if (p.causal) qp = p.num_qpairs - 1 - qp;  // longest key ranges first
+  // Without causal masking every CTA does the same work: all query pairs of
+  // one (batch, head) are consecutive, so the CTAs streaming the same keys
+  // and values run together and share them through L2.  With causal masking
+  // the work of a pair grows with its index: the longest pairs of every head
+  // go first, so the last wave holds the shortest ones.  Heads of one KV
+  // group are adjacent either way.
+  int x = blockIdx.x, h, bseq, qp;
+  if (p.causal) {
+    h = x % p.Hq;
+    x /= p.Hq;
+    bseq = x % p.B;
+    qp = p.num_qpairs - 1 - x / p.B;
+  } else {
+    qp = x % p.num_qpairs;
+    x /= p.num_qpairs;
+    h = x % p.Hq;
+    bseq = x / p.Hq;
+  }
 
   int Lq, Lk, q_base, k_base, b_coord;
   if (p.cu_q != nullptr) {
@@ -390,16 +405,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dk0 = sdesc_sw128(smem_addr(sK), 16, 1024);
       const uint64_t dv0 = sdesc_sw128(smem_addr(sV), C::kAtomBytes, 1024);
       constexpr uint64_t kTileDesc = C::kTileBytes >> 4;
-      int tot[kQT], pv_cnt[kQT], pend[kQT];
-#pragma unroll
-      for (int i = 0; i < kQT; ++i) {
-        tot[i] = 0;
-        pv_cnt[i] = 0;
-        pend[i] = -1;
-        for (int j = 0; j < nT; ++j) tot[i] += tile_active(mk[i], j, Lk, p.window, p.n_sink);
+      // Per Q tile: active key tiles, products P V issued, union index of the
+      // S whose P V is still to be issued (-1: none).  Scalars, not arrays:
+      // this loop must stay in registers.
+      int tot0 = 0, tot1 = 0;
+      for (int jj = 0; jj < nT; ++jj) {
+        tot0 += tile_active(mk[0], jj, Lk, p.window, p.n_sink);
+        tot1 += tile_active(mk[1], jj, Lk, p.window, p.n_sink);
       }
-      bool ok = (tot[0] + tot[1] == 0) || mbar_wait(q_full, 0, abort_flag, p.wait_limit_ns);
+      int pv0 = 0, pv1 = 0, pend0 = -1, pend1 = -1;
+      bool ok = (tot0 + tot1 == 0) || mbar_wait(q_full, 0, abort_flag, p.wait_limit_ns);
       if (!ok) fail(p.status, abort_flag);
+      // O_i += P_i V for the key tile with union index pend of Q tile i.
+      auto issue_pv = [&](int i, int pend, int& pv, int tot) -> bool {
+        const int sv = pend % ST;
+        if (!mbar_wait(&v_full[sv], (pend / ST) & 1, abort_flag, p.wait_limit_ns) ||
+            !mbar_wait(&p_ready[i], pv & 1, abort_flag, p.wait_limit_ns))
+          return false;
+        tc_fence_after_sync();
+        const uint64_t dv = dv0 + static_cast<uint64_t>(sv) * kTileDesc;
+        const uint32_t tO = tmem + C::kColO + i * D;
+        const uint32_t tP = tmem + i * kBN + 64;
+        mma_bf16_ts(tO, tP, dv, idesc_o, pv > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 1; kk < kBN / 16; ++kk)
+          mma_bf16_ts_c<1>(tO, tP + kk * 8, dv + kk * (2048 >> 4), idesc_o);
+        ++pv;
+        if (pv == tot) mma_commit(&o_done[i]);
+        return true;
+      };
+      // S_i = Q_i K^T for the key tile in ring slot s.
+      auto issue_s = [&](int i, uint64_t dk) {
+        const uint64_t dq = dq0 + i * kTileDesc;
+        const uint32_t tS = tmem + i * kBN;
+        mma_bf16_ss_c<0>(tS, dq, dk, idesc_s);
+#pragma unroll
+        for (int kk = 1; kk < D / 16; ++kk) {
+          const uint64_t koff = ((kk / 4) * C::kAtomBytes + (kk % 4) * 32) >> 4;
+          mma_bf16_ss_c<1>(tS, dq + koff, dk + koff, idesc_s);
+        }
+        mma_commit(&s_full[i]);
+      };
       int u = 0, j = 0;
       while (ok) {
         while (j < nT && !tile_active(mk[0], j, Lk, p.window, p.n_sink) &&
@@ -415,44 +461,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after_sync();
         }
         const uint64_t dk = dk0 + static_cast<uint64_t>(s) * kTileDesc;
-#pragma unroll
-        for (int i = 0; i < kQT; ++i) {
-          if (pend[i] >= 0) {
-            // O_i += P_i V for the previous key tile of this Q tile
-            const int sv = pend[i] % ST;
-            if (!mbar_wait(&v_full[sv], (pend[i] / ST) & 1, abort_flag, p.wait_limit_ns) ||
-                !mbar_wait(&p_ready[i], pv_cnt[i] & 1, abort_flag, p.wait_limit_ns)) {
-              fail(p.status, abort_flag);
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-            const uint64_t dv = dv0 + static_cast<uint64_t>(sv) * kTileDesc;
-            const uint32_t tO = tmem + C::kColO + i * D;
-            const uint32_t tP = tmem + i * kBN + 64;
-            mma_bf16_ts(tO, tP, dv, idesc_o, pv_cnt[i] > 0 ? 1u : 0u);
-#pragma unroll
-            for (int kk = 1; kk < kBN / 16; ++kk)
-              mma_bf16_ts_c<1>(tO, tP + kk * 8, dv + kk * (2048 >> 4), idesc_o);
-            ++pv_cnt[i];
-            if (pv_cnt[i] == tot[i]) mma_commit(&o_done[i]);
-            pend[i] = -1;
+        // order: O_0 += P_0 V(u-1), S_0(u), O_1 += P_1 V(u-1), S_1(u)
+        if (pend0 >= 0) {
+          if (!issue_pv(0, pend0, pv0, tot0)) {
+            fail(p.status, abort_flag);
+            break;
           }
-          if (have && tile_active(mk[i], j, Lk, p.window, p.n_sink)) {
-            // S_i = Q_i K^T for key tile j
-            const uint64_t dq = dq0 + i * kTileDesc;
-            const uint32_t tS = tmem + i * kBN;
-            mma_bf16_ss_c<0>(tS, dq, dk, idesc_s);
-#pragma unroll
-            for (int kk = 1; kk < D / 16; ++kk) {
-              const uint64_t koff = ((kk / 4) * C::kAtomBytes + (kk % 4) * 32) >> 4;
-              mma_bf16_ss_c<1>(tS, dq + koff, dk + koff, idesc_s);
-            }
-            mma_commit(&s_full[i]);
-            pend[i] = u;
-          }
+          pend0 = -1;
         }
-        if (!ok) break;
+        if (have && tile_active(mk[0], j, Lk, p.window, p.n_sink)) {
+          issue_s(0, dk);
+          pend0 = u;
+        }
+        if (pend1 >= 0) {
+          if (!issue_pv(1, pend1, pv1, tot1)) {
+            fail(p.status, abort_flag);
+            break;
+          }
+          pend1 = -1;
+        }
+        if (have && tile_active(mk[1], j, Lk, p.window, p.n_sink)) {
+          issue_s(1, dk);
+          pend1 = u;
+        }
         if (have) mma_commit(&k_empty[s]);
         if (u >= 1) mma_commit(&v_empty[(u - 1) % ST]);
         if (!have) break;
@@ -469,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q0 + i * kBM + r;  // sequence-relative query index
     const bool valid = row < Lq;
     const int hi_row = p.causal ? min(row + off, Lk - 1) : Lk - 1;
-    const int lo_row = (p.window > 0) ? row + off - p.window : INT_MIN;
+    const int lo_row = (p.window > 0) ? row + off - p.window : kNoLowerBound;
     const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t colS = i * kBN;
     const uint32_t colO = C::kColO + i * D;
@@ -492,87 +523,112 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after_sync();
       const bool edge = !tile_interior(m, j, p.window, p.n_sink);
-      const int kb = j * kBN;
-      const int lim_hi = hi_row - kb;
-      const int lim_lo = (p.window > 0) ? lo_row - kb : INT_MIN;
-      const int lim_sink = p.n_sink - kb;
       const uint32_t sS = taddr + colS;
-
-      // pass 1: row maximum over the four 32-column chunks of S
-      uint32_t ra[32], rb[32], rc[32];
-      tmem_ld_x32(sS + 0, ra);
-      tmem_ld_x32(sS + 32, rb);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        reg_fence(ra[c]);
-        reg_fence(rb[c]);
-      }
-      if (edge) {
-        mask32(ra, lim_hi, lim_lo, lim_sink);
-        mask32(rb, lim_hi - 32, lim_lo - 32, lim_sink - 32);
-      }
-      float mx = max32(rb, max32(ra, -INFINITY));
-      tmem_ld_x32(sS + 64, ra);
-      tmem_ld_x32(sS + 96, rb);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        reg_fence(ra[c]);
-        reg_fence(rb[c]);
-      }
-      if (edge) {
-        mask32(ra, lim_hi - 64, lim_lo - 64, lim_sink - 64);
-        mask32(rb, lim_hi - 96, lim_lo - 96, lim_sink - 96);
-      }
-      mx = max32(rb, max32(ra, mx));
-
+      uint64_t sum_a = 0, sum_b = 0;  // bit pattern 0 is (+0.f, +0.f)
+      float mx = -INFINITY;
       bool do_rescale = false;
       float alpha = 1.f;
-      if (mx > m_used) {
-        if (m_used == -INFINITY) {
-          m_used = mx;
-        } else if ((mx - m_used) * scale2 > kRescaleLog2) {
-          alpha = ex2_approx((m_used - mx) * scale2);
-          l *= alpha;
-          corr *= alpha;
-          m_used = mx;
-          do_rescale = true;
+      float ms = 0.f;
+      // Online-softmax state update from this tile's raw row maximum mx.
+      auto update_max = [&]() {
+        if (mx > m_used) {
+          if (m_used == -INFINITY) {
+            m_used = mx;
+          } else if ((mx - m_used) * scale2 > kRescaleLog2) {
+            alpha = ex2_approx((m_used - mx) * scale2);
+            l *= alpha;
+            corr *= alpha;
+            m_used = mx;
+            do_rescale = true;
+          }
         }
-      }
-      const float ms = (m_used == -INFINITY) ? 0.f : m_used * scale2;
-      const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
-      uint64_t sum_a = 0, sum_b = 0;  // bit pattern 0 is (+0.f, +0.f)
-
-      // pass 2: probabilities into the upper half of the S columns as bf16
-      // pairs (P column 64 + c/2 for score column c), each store landing on
-      // score columns that have already been read.
-      tmem_ld_x32(sS + 0, rc);  // reload chunk 0 while chunks 2 and 3 are exponentiated
-      {
-        uint32_t pk[16];
-        exp32(ra, sc2, nms, sum_a, sum_b, pk);
-        tmem_st_x16(sS + 96, pk);
-        exp32(rb, sc2, nms, sum_a, sum_b, pk);
-        tmem_st_x16(sS + 112, pk);
-      }
-      tmem_ld_wait();
+        ms = (m_used == -INFINITY) ? 0.f : m_used * scale2;
+      };
+      // P goes to the upper half of the S columns as bf16 pairs: P column
+      // 64 + c/2 for score column c.  Every store must land on scores that
+      // have already been read.
+      if (!edge) {
+        // Interior tile, no mask.  pass 1: row maximum over the four 32-column
+        // chunks; pass 2: chunks 2 and 3 are still in registers, chunks 0
+        // and 1 are read again, each reload overlapped with arithmetic.
+        uint32_t ra[32], rb[32], rc[32];
+        tmem_ld_x32(sS + 0, ra);
+        tmem_ld_x32(sS + 32, rb);
+        tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 32; ++c) reg_fence(rc[c]);
-      tmem_ld_x32(sS + 32, ra);  // chunk 1
-      if (edge) mask32(rc, lim_hi, lim_lo, lim_sink);
-      {
-        uint32_t pk[16];
-        exp32(rc, sc2, nms, sum_a, sum_b, pk);
-        tmem_st_x16(sS + 64, pk);
-      }
-      tmem_ld_wait();
+        for (int c = 0; c < 32; ++c) {
+          reg_fence(ra[c]);
+          reg_fence(rb[c]);
+        }
+        mx = max32(rb, max32(ra, -INFINITY));
+        tmem_ld_x32(sS + 64, ra);
+        tmem_ld_x32(sS + 96, rb);
+        tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
-      if (edge) mask32(ra, lim_hi - 32, lim_lo - 32, lim_sink - 32);
-      {
-        uint32_t pk[16];
-        exp32(ra, sc2, nms, sum_a, sum_b, pk);
-        tmem_st_x16(sS + 80, pk);
+        for (int c = 0; c < 32; ++c) {
+          reg_fence(ra[c]);
+          reg_fence(rb[c]);
+        }
+        mx = max32(rb, max32(ra, mx));
+        update_max();
+        const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
+        tmem_ld_x32(sS + 0, rc);
+        {
+          uint32_t pk[16];
+          exp32(ra, sc2, nms, sum_a, sum_b, pk);
+          tmem_st_x16(sS + 96, pk);
+          exp32(rb, sc2, nms, sum_a, sum_b, pk);
+          tmem_st_x16(sS + 112, pk);
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) reg_fence(rc[c]);
+        tmem_ld_x32(sS + 32, ra);
+        {
+          uint32_t pk[16];
+          exp32(rc, sc2, nms, sum_a, sum_b, pk);
+          tmem_st_x16(sS + 64, pk);
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
+        {
+          uint32_t pk[16];
+          exp32(ra, sc2, nms, sum_a, sum_b, pk);
+          tmem_st_x16(sS + 80, pk);
+        }
+      } else {
+        // Boundary tile (causal diagonal, window edge, sink, ragged tail):
+        // the same arithmetic through compact chunk loops, with the mask.
+        const int kb = j * kBN;
+        const int lim_hi = hi_row - kb;
+        const int lim_lo = (p.window > 0) ? lo_row - kb : kNoLowerBound;
+        const int lim_sink = p.n_sink - kb;
+        uint32_t ra[32];
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld_x32(sS + 32 * c, ra);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) reg_fence(ra[e]);
+          mask32(ra, lim_hi - 32 * c, lim_lo - 32 * c, lim_sink - 32 * c);
+          mx = max32(ra, mx);
+        }
+        update_max();
+        const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
+        // chunks 3, 2, 1, 0: the P of chunk c lands on columns 64 + 16c..,
+        // inside chunks already processed
+#pragma unroll 1
+        for (int c = 3; c >= 0; --c) {
+          tmem_ld_x32(sS + 32 * c, ra);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) reg_fence(ra[e]);
+          mask32(ra, lim_hi - 32 * c, lim_lo - 32 * c, lim_sink - 32 * c);
+          uint32_t pk[16];
+          exp32(ra, sc2, nms, sum_a, sum_b, pk);
+          tmem_st_x16(sS + 64 + 16 * c, pk);
+        }
       }
       float s0, s1, s2, s3;
       f2_split(sum_a, s0, s1);
@@ -593,21 +649,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // which has completed (the commit behind s_full covers it); the next
         // product into O waits for this warpgroup's p_ready arrival below.
         const uint64_t a2 = f2(alpha, alpha);
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
-          tmem_ld_x32(taddr + colO + c * 32, rb);
+          uint32_t ro[32];
+          tmem_ld_x32(taddr + colO + c * 32, ro);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            reg_fence(rb[2 * e]);
-            reg_fence(rb[2 * e + 1]);
+            reg_fence(ro[2 * e]);
+            reg_fence(ro[2 * e + 1]);
             float o0, o1;
-            f2_split(f2_mul(f2(__uint_as_float(rb[2 * e]), __uint_as_float(rb[2 * e + 1])), a2),
+            f2_split(f2_mul(f2(__uint_as_float(ro[2 * e]), __uint_as_float(ro[2 * e + 1])), a2),
                      o0, o1);
-            rb[2 * e] = __float_as_uint(o0);
-            rb[2 * e + 1] = __float_as_uint(o1);
+            ro[2 * e] = __float_as_uint(o0);
+            ro[2 * e + 1] = __float_as_uint(o1);
           }
-          tmem_st_x32(taddr + colO + c * 32, rb);
+          tmem_st_x32(taddr + colO + c * 32, ro);
         }
       }
       tmem_st_wait();
