@@ -139,6 +139,20 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of a list of floats over all ranks (identity on one
+    process).  This is the only cross-rank step of the bench: every rank runs
+    its own copy of the workload (weak scaling) and the slowest rank sets the
+    time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def run_reference(args):
     """The oracle (fp64, CPU) as the reference arm: bounded sample per step."""
     world, rank, _ = dist_env()
@@ -175,22 +189,22 @@ def run_reference(args):
 
 
 def cpu_baseline():
-    """The oracle as it stands on this host: a bounded sample (~10 s) of the
-    prefill workload, reported in the same unit."""
+    """The oracle as it stands on this host, on the bench's own prefill
+    workload (both calls of one step, all batch elements and heads), reported
+    in the same unit.  Takes a few seconds of all host cores."""
     import oracle
     import workloads
-    x = workloads.prefill_mha(False)
-    heads, rows = 16, 2048
-    q = x.q[:1, :rows].double().numpy()
-    k = x.k[:1].double().numpy()
-    v = x.v[:1].double().numpy()
-    t0 = time.perf_counter()
-    oracle.attn_fwd(q, k, v, x.scale)
-    sec = time.perf_counter() - t0
-    flops = prefill_flops(1, heads, rows, 2048, 128, False)
+    flops, sec = 0.0, 0.0
+    for causal in (False, True):
+        x = workloads.prefill_mha(causal)
+        q, k, v = x.q.double().numpy(), x.k.double().numpy(), x.v.double().numpy()
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v, x.scale, causal)
+        sec += time.perf_counter() - t0
+        flops += prefill_flops(4, 16, 2048, 2048, 128, causal)
     return {"value": flops / sec / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle", "seconds": sec,
-            "sample": "prefill non-causal, batch element 0 of 4 (16 heads x 2048 rows)"}
+            "sample": "the full prefill part of one step: B=4 H=16 S=2048 d=128, non-causal + causal"}
 
 
 def main():
@@ -286,12 +300,7 @@ def main():
     t_dec = [e[2].elapsed_time(e[3]) for e in evs]
     tot_pre = sum(t_nc) + sum(t_c)
     tot_step = sum(t_nc) + sum(t_c) + sum(t_dec)
-    if world > 1:
-        tt = torch.tensor([tot_pre, tot_step, sum(t_dec)], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        tot_pre, tot_step, tot_dec = tt.tolist()
-    else:
-        tot_dec = sum(t_dec)
+    tot_pre, tot_step, tot_dec = max_over_ranks([tot_pre, tot_step, sum(t_dec)], dev)
     K = args.steps
     value = world * K * (f_nc + f_c) / (tot_pre / 1e3) / 1e12
     dec_gbs = world * K * kv_bytes / (tot_dec / 1e3) / 1e9
@@ -332,11 +341,7 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = tt.item()
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1)], dev)[0]
     e2e_val = world * e2e_steps * (f_nc + f_c) / (e2e_ms / 1e3) / 1e12
 
     if rank == 0:
