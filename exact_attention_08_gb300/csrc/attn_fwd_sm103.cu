@@ -57,6 +57,12 @@ constexpr int kBM = 128;       // query rows per Q tile (= TMEM lanes)
 constexpr int kQT = 2;         // Q tiles per CTA
 constexpr int kBN = 128;       // keys per K/V tile
 constexpr int kThreads = 384;  // 12 warps
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsOther = 88;
+// Registers the three warpgroups hold after setmaxnreg; must not exceed what
+// the block is launched with (checked on the host before every launch).
+constexpr int kRegsSplit = 2 * 128 * kRegsSoftmax + 128 * kRegsOther;
+static_assert(kRegsSplit <= kThreads * 168, "register split");
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -329,6 +335,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // Register budget: the block is launched with 168 registers a thread (three
+  // warps share SMSP 0).  Each warpgroup changes its budget at the head of
+  // the branch holding all of its code: the producer / MMA warpgroup drops to
+  // kRegsOther, the softmax warpgroups rise to kRegsSoftmax
+  // (2*128*kRegsSoftmax + 128*kRegsOther <= 384*168).
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther) : "memory");
   if (warp == kWarpLoad) {
     // ============================================================ TMA producer
     if (lane == 0) {
@@ -492,7 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 8) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax) : "memory");
     // ============================================================ softmax warpgroups
     const int i = warp / 4;
     const int wq = warp % 4;
@@ -548,55 +563,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 64 + c/2 for score column c.  Every store must land on scores that
       // have already been read.
       if (!edge) {
-        // Interior tile, no mask.  pass 1: row maximum over the four 32-column
-        // chunks; pass 2: chunks 2 and 3 are still in registers, chunks 0
-        // and 1 are read again, each reload overlapped with arithmetic.
-        uint32_t ra[32], rb[32], rc[32];
-        tmem_ld_x32(sS + 0, ra);
-        tmem_ld_x32(sS + 32, rb);
+        // Interior tile, no mask: S is read from tensor memory once (one wait
+        // for all four 32-column chunks), then exponentiated from registers.
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld_x32(sS + 0, r0);
+        tmem_ld_x32(sS + 32, r1);
+        tmem_ld_x32(sS + 64, r2);
+        tmem_ld_x32(sS + 96, r3);
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          reg_fence(ra[c]);
-          reg_fence(rb[c]);
+          reg_fence(r0[c]);
+          reg_fence(r1[c]);
+          reg_fence(r2[c]);
+          reg_fence(r3[c]);
         }
-        mx = max32(rb, max32(ra, -INFINITY));
-        tmem_ld_x32(sS + 64, ra);
-        tmem_ld_x32(sS + 96, rb);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          reg_fence(ra[c]);
-          reg_fence(rb[c]);
-        }
-        mx = max32(rb, max32(ra, mx));
+        mx = max32(r3, max32(r2, max32(r1, max32(r0, -INFINITY))));
         update_max();
         const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
-        tmem_ld_x32(sS + 0, rc);
-        {
-          uint32_t pk[16];
-          exp32(ra, sc2, nms, sum_a, sum_b, pk);
-          tmem_st_x16(sS + 96, pk);
-          exp32(rb, sc2, nms, sum_a, sum_b, pk);
-          tmem_st_x16(sS + 112, pk);
-        }
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) reg_fence(rc[c]);
-        tmem_ld_x32(sS + 32, ra);
-        {
-          uint32_t pk[16];
-          exp32(rc, sc2, nms, sum_a, sum_b, pk);
-          tmem_st_x16(sS + 64, pk);
-        }
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
-        {
-          uint32_t pk[16];
-          exp32(ra, sc2, nms, sum_a, sum_b, pk);
-          tmem_st_x16(sS + 80, pk);
-        }
+        // Separate registers for each chunk's packed P: a tcgen05.st reads its
+        // source registers asynchronously, so reusing them would make every
+        // chunk wait for the previous store.
+        uint32_t pk0[16], pk1[16], pk2[16], pk3[16];
+        exp32(r0, sc2, nms, sum_a, sum_b, pk0);
+        tmem_st_x16(sS + 64, pk0);
+        exp32(r1, sc2, nms, sum_a, sum_b, pk1);
+        tmem_st_x16(sS + 80, pk1);
+        exp32(r2, sc2, nms, sum_a, sum_b, pk2);
+        tmem_st_x16(sS + 96, pk2);
+        exp32(r3, sc2, nms, sum_a, sum_b, pk3);
+        tmem_st_x16(sS + 112, pk3);
       } else {
         // Boundary tile (causal diagonal, window edge, sink, ragged tail):
         // the same arithmetic through compact chunk loops, with the mask.
@@ -765,6 +761,13 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(attn_fwd_kernel<D>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (attr_err != cudaSuccess) return;
+    // setmaxnreg.inc waits for registers the block was launched with: never
+    // launch a build whose register count cannot cover the split.
+    cudaFuncAttributes fa;
+    attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D>);
+    if (attr_err == cudaSuccess && fa.numRegs * kThreads < kRegsSplit)
+      attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return attr_err;
   Params p;
