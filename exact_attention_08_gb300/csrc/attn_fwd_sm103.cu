@@ -13,7 +13,7 @@
 //   warps 0-3   softmax for Q tile 0 (thread r owns query row r: TMEM lane r)
 //   warps 4-7   softmax for Q tile 1
 //   warp  8     TMA producer (Q once, then the K/V ring); allocates TMEM
-//   warp  9     MMA issuer (one thread)
+//   warp  9     MMA issuer (whole warp, one elected lane issues)
 //   warps 10-11 idle
 // Tensor memory (512 columns): S_i = Q_i K^T at columns [128 i, 128 i + 128)
 // (fp32), O_i at [256 + D i, 256 + D i + D) (fp32).  The softmax writes the
@@ -81,8 +81,8 @@ struct Cfg {
   static constexpr int kOffK = kOffQ + kQT * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_ready[2], o_done[2], drain
-  static constexpr int kNumBars = 1 + 4 * kStages + 3 * kQT + 1;
+  // q_full, k_full[S], v_full[S], step[S], s_full[2], p_ready[2], o_done[2], drain
+  static constexpr int kNumBars = 1 + 3 * kStages + 3 * kQT + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 2 * kBN;
@@ -123,17 +123,35 @@ __device__ __forceinline__ TileMask make_mask(int qa, int Lq, int Lk, int off, i
   return m;
 }
 
-// Does any row of the tile see any key of key tile j?
-__device__ __forceinline__ bool tile_active(const TileMask& m, int j, int Lk, int window,
-                                            int n_sink) {
-  if (m.qb <= m.qa) return false;
-  const int ka = j * kBN;
-  if (ka >= Lk || ka > m.hi_max) return false;
-  if (window > 0) {
-    const int kb1 = min(ka + kBN, Lk) - 1;
-    return kb1 > m.lo_min || ka < n_sink;
+// The key tiles a Q tile touches, as two ranges: tile j is active iff
+// j <= hi and (j >= lo or j < sinkT), sinkT = ceil(n_sink / kBN) the tiles
+// holding sink keys.  The same set as "does any row of the tile see any key
+// of tile j": hi is the last tile holding a key at or below the largest
+// causal bound (and below Lk), lo the first tile holding a key above the
+// smallest window bound.
+struct TileRange {
+  int lo, hi;
+};
+
+__device__ __forceinline__ TileRange tile_range(const TileMask& m, int Lk, int window) {
+  TileRange r;
+  if (m.qb <= m.qa || m.hi_max < 0 || Lk <= 0) {
+    r.lo = 0;
+    r.hi = -1;
+    return r;
   }
-  return true;
+  r.hi = min((Lk - 1) / kBN, m.hi_max / kBN);
+  if (window <= 0)
+    r.lo = 0;
+  else if (m.lo_min >= Lk - 1)
+    r.lo = r.hi + 1;  // only sink keys are visible
+  else
+    r.lo = (m.lo_min < 0) ? 0 : (m.lo_min + 1) / kBN;
+  return r;
+}
+
+__device__ __forceinline__ bool in_range(const TileRange& r, int j, int sinkT) {
+  return j <= r.hi && (j >= r.lo || j < sinkT);
 }
 
 // Does every row of the tile see every key of key tile j (no mask needed)?
@@ -245,10 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = k_full + ST;
-  uint64_t* v_full = k_empty + ST;
-  uint64_t* v_empty = v_full + ST;
-  uint64_t* s_full = v_empty + ST;
+  uint64_t* v_full = k_full + ST;
+  uint64_t* step = v_full + ST;  // step[u % ST]: every product of key step u is done
+  uint64_t* s_full = step + ST;
   uint64_t* p_ready = s_full + kQT;
   uint64_t* o_done = p_ready + kQT;
   uint64_t* drain = o_done + kQT;
@@ -305,6 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   TileMask mk[kQT];
 #pragma unroll
   for (int i = 0; i < kQT; ++i) mk[i] = make_mask(q0 + i * kBM, Lq, Lk, off, p.causal, p.window);
+  const TileRange rg0 = tile_range(mk[0], Lk, p.window);
+  const TileRange rg1 = tile_range(mk[1], Lk, p.window);
+  const int sinkT = (p.window > 0 && p.n_sink > 0) ? (p.n_sink + kBN - 1) / kBN : 0;
+  const int lastT = max(rg0.hi, rg1.hi);  // last key tile any row touches (-1: none)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -314,9 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&step[s], 1);
     }
     for (int i = 0; i < kQT; ++i) {
       mbar_init(&s_full[i], 1);
@@ -344,165 +364,171 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther) : "memory");
   if (warp == kWarpLoad) {
     // ============================================================ TMA producer
-    if (lane == 0) {
-      bool any = false;
-      for (int j = 0; j < nT && !any; ++j)
-        any = tile_active(mk[0], j, Lk, p.window, p.n_sink) ||
-              tile_active(mk[1], j, Lk, p.window, p.n_sink);
-      if (any) {  // no copy is issued that nobody waits for
+    // The whole warp runs the loop (every branch below is warp-uniform); one
+    // elected lane issues each copy and byte-count arrival.  Key tile u of
+    // the union of active tiles goes to ring slot u % ST.  Its K slot last
+    // held K(u - ST), free once key step u - ST is done; its V slot last held
+    // V(u - ST), read by the products of key step u - ST + 1.
+    if (lastT >= 0) {  // no copy is issued that nobody waits for
+      if (lane == 0) {
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
-        mbar_arrive_expect_tx(q_full, kQT * C::kTileBytes);
+      }
+      __syncwarp();
+      mbar_arrive_expect_tx_w(q_full, kQT * C::kTileBytes);
 #pragma unroll
-        for (int i = 0; i < kQT; ++i)
+      for (int i = 0; i < kQT; ++i)
 #pragma unroll
-          for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_4d(sQ + i * C::kTileBytes + a * C::kAtomBytes, &tmQ, q_full, a * 64, h,
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_4d_w(sQ + i * C::kTileBytes + a * C::kAtomBytes, &tmQ, q_full, a * 64, h,
                         q_base + q0 + i * kBM, b_coord);
+    }
+    int u = 0;
+    bool ring_ok = true;
+    for (int j = 0; j <= lastT; ++j) {
+      if (!in_range(rg0, j, sinkT) && !in_range(rg1, j, sinkT)) continue;
+      const int s = u % ST;
+      if (u >= ST && !mbar_wait_warp(&step[s], ((u / ST) - 1) & 1, abort_flag, p.wait_limit_ns)) {
+        if (lane == 0) fail(p.status, abort_flag);
+        ring_ok = false;
+        break;
       }
-      int u = 0;
-      bool ring_ok = true;
-      for (int j = 0; j < nT; ++j) {
-        if (!tile_active(mk[0], j, Lk, p.window, p.n_sink) &&
-            !tile_active(mk[1], j, Lk, p.window, p.n_sink))
-          continue;
-        const int s = u % ST;
-        const uint32_t ph = (u / ST) & 1;
-        if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag, p.wait_limit_ns)) {
-          fail(p.status, abort_flag);
-          ring_ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
+      mbar_arrive_expect_tx_w(&k_full[s], C::kTileBytes);
 #pragma unroll
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_4d(sK + s * C::kTileBytes + a * C::kAtomBytes, &tmK, &k_full[s], a * 64, hk,
+      for (int a = 0; a < C::kAtoms; ++a)
+        tma_load_4d_w(sK + s * C::kTileBytes + a * C::kAtomBytes, &tmK, &k_full[s], a * 64, hk,
                       k_base + j * kBN, b_coord);
-        if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag, p.wait_limit_ns)) {
-          fail(p.status, abort_flag);
-          ring_ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
+      if (u >= ST && !mbar_wait_warp(&step[(u + 1) % ST], (((u + 1) / ST) - 1) & 1, abort_flag,
+                                     p.wait_limit_ns)) {
+        if (lane == 0) fail(p.status, abort_flag);
+        ring_ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx_w(&v_full[s], C::kTileBytes);
 #pragma unroll
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_4d(sV + s * C::kTileBytes + a * C::kAtomBytes, &tmV, &v_full[s], a * 64, hk,
+      for (int a = 0; a < C::kAtoms; ++a)
+        tma_load_4d_w(sV + s * C::kTileBytes + a * C::kAtomBytes, &tmV, &v_full[s], a * 64, hk,
                       k_base + j * kBN, b_coord);
-        ++u;
-      }
-      // Tail: wait for the last release of every ring slot, so that no
-      // tensor-core commit still has to arrive on this CTA's barriers when
-      // it exits.  Slot s was used n_s times.
-      for (int s = 0; ring_ok && s < ST; ++s) {
-        const int n_s = (u > s) ? (u - s + ST - 1) / ST : 0;
-        if (n_s == 0) continue;
-        const uint32_t par = (n_s - 1) & 1;
-        if (!mbar_wait(&k_empty[s], par, abort_flag, p.wait_limit_ns) ||
-            !mbar_wait(&v_empty[s], par, abort_flag, p.wait_limit_ns)) {
-          fail(p.status, abort_flag);
-          break;
-        }
-      }
+      ++u;
+    }
+    // Tail: the MMA issuer commits key steps 0..u (the last one holds only
+    // products P V); wait for step u, after which no tensor-core commit is
+    // left to arrive on this CTA's barriers when it exits.
+    if (ring_ok && u > 0 &&
+        !mbar_wait_warp(&step[u % ST], (u / ST) & 1, abort_flag, p.wait_limit_ns)) {
+      if (lane == 0) fail(p.status, abort_flag);
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ============================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
-      // Descriptors are built once; every operand of every MMA is a base
-      // descriptor plus a compile-time offset in its 16-byte address field
-      // (shared-memory offsets stay below 256 KB, so the field never carries).
-      const uint64_t dq0 = sdesc_sw128(smem_addr(sQ), 16, 1024);
-      const uint64_t dk0 = sdesc_sw128(smem_addr(sK), 16, 1024);
-      const uint64_t dv0 = sdesc_sw128(smem_addr(sV), C::kAtomBytes, 1024);
-      constexpr uint64_t kTileDesc = C::kTileBytes >> 4;
-      // Per Q tile: active key tiles, products P V issued, union index of the
-      // S whose P V is still to be issued (-1: none).  Scalars, not arrays:
-      // this loop must stay in registers.
-      int tot0 = 0, tot1 = 0;
-      for (int jj = 0; jj < nT; ++jj) {
-        tot0 += tile_active(mk[0], jj, Lk, p.window, p.n_sink);
-        tot1 += tile_active(mk[1], jj, Lk, p.window, p.n_sink);
+    // The whole warp runs the loop (warp-uniform control flow); one elected
+    // lane issues every MMA and commit.  The tensor pipe queues only a few
+    // MMAs, so the issuer's own latency between groups (barrier tests of the
+    // order of 100 cycles each, commits) can leave it idle: the barriers a
+    // group needs are tested together, and key step u ends with one commit
+    // that releases both K(u) and V(u - 1).
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+    // Descriptors are built once; every operand of every MMA is a base
+    // descriptor plus a compile-time offset in its 16-byte address field
+    // (shared-memory offsets stay below 256 KB, so the field never carries).
+    constexpr uint64_t kTileDesc = C::kTileBytes >> 4;
+    const uint64_t dq0 = sdesc_sw128(smem_addr(sQ), 16, 1024);
+    const uint64_t dk0 = sdesc_sw128(smem_addr(sK), 16, 1024);
+    const uint64_t dv0 = sdesc_sw128(smem_addr(sV), C::kAtomBytes, 1024);
+    // Per Q tile: active key tiles, products P V issued, union index of the
+    // S whose P V is still to be issued (-1: none).
+    int tot0 = 0, tot1 = 0;
+    for (int jj = 0; jj <= lastT; ++jj) {
+      tot0 += in_range(rg0, jj, sinkT);
+      tot1 += in_range(rg1, jj, sinkT);
+    }
+    int pv0 = 0, pv1 = 0, pend0 = -1, pend1 = -1;
+    // No active tile: nothing is loaded and nothing is issued or committed.
+    bool ok = lastT >= 0;
+    if (ok && !mbar_wait_warp(q_full, 0, abort_flag, p.wait_limit_ns)) {
+      ok = false;
+      if (lane == 0) fail(p.status, abort_flag);
+    }
+    // O_i += P_i V for the key tile with union index pend of Q tile i
+    // (its V and P already waited for).
+    auto issue_pv = [&](int i, int pend, int& pv, int tot) {
+      const uint64_t dv = dv0 + static_cast<uint64_t>(pend % ST) * kTileDesc;
+      const uint32_t tO = tmem + C::kColO + i * D;
+      const uint32_t tP = tmem + i * kBN + 64;
+      mma_bf16_ts_w(tO, tP, dv, idesc_o, pv > 0 ? 1u : 0u);
+#pragma unroll
+      for (int kk = 1; kk < kBN / 16; ++kk)
+        mma_bf16_ts_wc<1>(tO, tP + kk * 8, dv + kk * (2048 >> 4), idesc_o);
+      ++pv;
+      if (pv == tot) mma_commit_w(&o_done[i]);
+    };
+    // S_i = Q_i K^T for the key tile in ring slot s.
+    auto issue_s = [&](int i, uint64_t dk) {
+      const uint64_t dq = dq0 + i * kTileDesc;
+      const uint32_t tS = tmem + i * kBN;
+      mma_bf16_ss_wc<0>(tS, dq, dk, idesc_s);
+#pragma unroll
+      for (int kk = 1; kk < D / 16; ++kk) {
+        const uint64_t koff = ((kk / 4) * C::kAtomBytes + (kk % 4) * 32) >> 4;
+        mma_bf16_ss_wc<1>(tS, dq + koff, dk + koff, idesc_s);
       }
-      int pv0 = 0, pv1 = 0, pend0 = -1, pend1 = -1;
-      bool ok = (tot0 + tot1 == 0) || mbar_wait(q_full, 0, abort_flag, p.wait_limit_ns);
-      if (!ok) fail(p.status, abort_flag);
-      // O_i += P_i V for the key tile with union index pend of Q tile i.
-      auto issue_pv = [&](int i, int pend, int& pv, int tot) -> bool {
-        const int sv = pend % ST;
-        if (!mbar_wait(&v_full[sv], (pend / ST) & 1, abort_flag, p.wait_limit_ns) ||
-            !mbar_wait(&p_ready[i], pv & 1, abort_flag, p.wait_limit_ns))
-          return false;
+      mma_commit_w(&s_full[i]);
+    };
+    int u = 0, j = 0;
+    while (ok) {
+      while (j <= lastT && !in_range(rg0, j, sinkT) && !in_range(rg1, j, sinkT)) ++j;
+      const bool have = j <= lastT;
+      const bool a0 = have && in_range(rg0, j, sinkT);
+      const bool a1 = have && in_range(rg1, j, sinkT);
+      const int s = u % ST;
+      const int sv = (u + ST - 1) % ST;  // V(u - 1)
+      const uint32_t pk = (u / ST) & 1, pvv = ((u - 1) / ST) & 1;
+      // Needed now: K(u) for S_0(u) / S_1(u), V(u - 1) and P_0 for O_0 += P_0 V(u - 1).
+      // Test them together (one round trip when all are ready), then wait on
+      // each in turn only if one is not.  A barrier not needed is replaced by
+      // q_full, phase 0, complete by now.
+      const bool need_k = have, need_v = (pend0 >= 0 || pend1 >= 0), need_p0 = pend0 >= 0;
+      if (!__all_sync(0xffffffffu,
+                      mbar_test3(need_k ? &k_full[s] : q_full, need_k ? pk : 0u,
+                                 need_v ? &v_full[sv] : q_full, need_v ? pvv : 0u,
+                                 need_p0 ? &p_ready[0] : q_full, need_p0 ? (pv0 & 1) : 0u))) {
+        if ((need_k && !mbar_wait_warp(&k_full[s], pk, abort_flag, p.wait_limit_ns)) ||
+            (need_v && !mbar_wait_warp(&v_full[sv], pvv, abort_flag, p.wait_limit_ns)) ||
+            (need_p0 && !mbar_wait_warp(&p_ready[0], pv0 & 1, abort_flag, p.wait_limit_ns))) {
+          if (lane == 0) fail(p.status, abort_flag);
+          break;
+        }
+      }
+      tc_fence_after_sync();
+      const uint64_t dk = dk0 + static_cast<uint64_t>(s) * kTileDesc;
+      // order: O_0 += P_0 V(u-1), S_0(u), O_1 += P_1 V(u-1), S_1(u)
+      if (pend0 >= 0) {
+        issue_pv(0, pend0, pv0, tot0);
+        pend0 = -1;
+      }
+      if (a0) {
+        issue_s(0, dk);
+        pend0 = u;
+      }
+      if (pend1 >= 0) {
+        if (!mbar_wait_warp(&p_ready[1], pv1 & 1, abort_flag, p.wait_limit_ns)) {
+          if (lane == 0) fail(p.status, abort_flag);
+          break;
+        }
         tc_fence_after_sync();
-        const uint64_t dv = dv0 + static_cast<uint64_t>(sv) * kTileDesc;
-        const uint32_t tO = tmem + C::kColO + i * D;
-        const uint32_t tP = tmem + i * kBN + 64;
-        mma_bf16_ts(tO, tP, dv, idesc_o, pv > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 1; kk < kBN / 16; ++kk)
-          mma_bf16_ts_c<1>(tO, tP + kk * 8, dv + kk * (2048 >> 4), idesc_o);
-        ++pv;
-        if (pv == tot) mma_commit(&o_done[i]);
-        return true;
-      };
-      // S_i = Q_i K^T for the key tile in ring slot s.
-      auto issue_s = [&](int i, uint64_t dk) {
-        const uint64_t dq = dq0 + i * kTileDesc;
-        const uint32_t tS = tmem + i * kBN;
-        mma_bf16_ss_c<0>(tS, dq, dk, idesc_s);
-#pragma unroll
-        for (int kk = 1; kk < D / 16; ++kk) {
-          const uint64_t koff = ((kk / 4) * C::kAtomBytes + (kk % 4) * 32) >> 4;
-          mma_bf16_ss_c<1>(tS, dq + koff, dk + koff, idesc_s);
-        }
-        mma_commit(&s_full[i]);
-      };
-      int u = 0, j = 0;
-      while (ok) {
-        while (j < nT && !tile_active(mk[0], j, Lk, p.window, p.n_sink) &&
-               !tile_active(mk[1], j, Lk, p.window, p.n_sink))
-          ++j;
-        const bool have = j < nT;
-        const int s = u % ST;
-        if (have) {
-          if (!mbar_wait(&k_full[s], (u / ST) & 1, abort_flag, p.wait_limit_ns)) {
-            fail(p.status, abort_flag);
-            break;
-          }
-          tc_fence_after_sync();
-        }
-        const uint64_t dk = dk0 + static_cast<uint64_t>(s) * kTileDesc;
-        // order: O_0 += P_0 V(u-1), S_0(u), O_1 += P_1 V(u-1), S_1(u)
-        if (pend0 >= 0) {
-          if (!issue_pv(0, pend0, pv0, tot0)) {
-            fail(p.status, abort_flag);
-            break;
-          }
-          pend0 = -1;
-        }
-        if (have && tile_active(mk[0], j, Lk, p.window, p.n_sink)) {
-          issue_s(0, dk);
-          pend0 = u;
-        }
-        if (pend1 >= 0) {
-          if (!issue_pv(1, pend1, pv1, tot1)) {
-            fail(p.status, abort_flag);
-            break;
-          }
-          pend1 = -1;
-        }
-        if (have && tile_active(mk[1], j, Lk, p.window, p.n_sink)) {
-          issue_s(1, dk);
-          pend1 = u;
-        }
-        if (have) mma_commit(&k_empty[s]);
-        if (u >= 1) mma_commit(&v_empty[(u - 1) % ST]);
-        if (!have) break;
-        ++u;
-        ++j;
+        issue_pv(1, pend1, pv1, tot1);
+        pend1 = -1;
       }
+      if (a1) {
+        issue_s(1, dk);
+        pend1 = u;
+      }
+      mma_commit_w(&step[s]);  // key step u: K(u) and V(u - 1) free once done
+      if (!have) break;
+      ++u;
+      ++j;
     }
     __syncwarp();
   }
@@ -520,7 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t colS = i * kBN;
     const uint32_t colO = C::kColO + i * D;
     const float scale2 = p.scale2;
-    const TileMask m = mk[i];
+    const TileMask m = i ? mk[1] : mk[0];
+    const TileRange rg = i ? rg1 : rg0;
 
     float m_used = -INFINITY;  // raw (unscaled) running maximum in use
     float l = 0.f;             // running sum of the fp32 probabilities
@@ -528,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int t = 0;
     bool ok = true;
     for (int j = 0; j < nT; ++j) {
-      if (!tile_active(m, j, Lk, p.window, p.n_sink)) continue;
+      if (!in_range(rg, j, sinkT)) continue;
       bool w_ok = mbar_wait(&s_full[i], t & 1, abort_flag, p.wait_limit_ns);
       w_ok = __all_sync(0xffffffffu, w_ok);
       if (!w_ok) {
@@ -725,9 +752,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (*abort_flag) {
     // Let every tensor-core operation and bulk copy already issued land
     // before the tensor memory and shared memory are given back.
-    if (warp == kWarpMma && lane == 0) {
-      mma_commit(drain);
-      mbar_wait(drain, 0, nullptr, 100000000ull);
+    if (warp == kWarpMma) {
+      mma_commit_w(drain);
+      mbar_wait_warp(drain, 0, nullptr, 100000000ull);
     }
     if (warp == kWarpLoad && lane == 0) {
       const uint64_t t0 = globaltimer_ns();

@@ -63,6 +63,23 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* bar, uint32_t parity
   return ok;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps (the hardware wakes it when the phase completes, or after about
+// `hint_ns`) instead of spinning, so waiting warps leave the issue slots of
+// their SM sub-partition to the warps that share it.
+__device__ __forceinline__ uint32_t mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                        uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P1;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2, %3;\n\t"
+      "selp.b32 %0, 1, 0, P1;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok;
+}
+
 // Waits until the barrier's phase with the given parity has completed.
 // Returns false (without completing) when `abort_flag` becomes non-zero or
 // `limit_ns` of wall time pass; the caller then records the failure.
@@ -71,12 +88,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if ((it & 31u) == 0) {
       if (abort_flag && *abort_flag) return false;
       if (globaltimer_ns() - t0 > limit_ns) return false;
     }
   }
+}
+
+// Non-blocking test of three barrier phases at once (1 if all three have
+// completed): the three tests are in flight together, so a warp that finds
+// everything ready pays one round trip instead of three.
+__device__ __forceinline__ uint32_t mbar_test3(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
+                                               uint64_t* c, uint32_t pc) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred x, y, z;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 x, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 y, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 z, [%5], %6;\n\t"
+      "and.pred x, x, y;\n\tand.pred x, x, z;\n\t"
+      "selp.b32 %0, 1, 0, x;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(a)), "r"(pa), "r"(smem_addr(b)), "r"(pb), "r"(smem_addr(c)), "r"(pc)
+      : "memory");
+  return ok;
+}
+
+// Warp-collective form of mbar_wait: every lane of a converged warp calls it
+// and all get the same answer (false if any lane gave up).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               const volatile int* abort_flag, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, limit_ns));
 }
 
 // ---------------------------------------------------------------- TMA
@@ -115,6 +158,46 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- warp-collective issue
+// The single-thread asynchronous instructions below (TMA copies, barrier
+// arrivals with a byte count, tensor-core MMAs and commits) are called by
+// every lane of a converged warp; elect.sync picks one lane to issue them
+// inside the asm.  Issuing from a converged warp keeps the operands warp-
+// uniform; measured on sm_103a, a tcgen05.mma issued this way costs the warp
+// a few cycles, against about 60 from a lane-0-only branch, which is nearly
+// the MMA's own 64-cycle execution time at M=128, N=128, K=16.  The same
+// lane is elected every time the full warp is converged, so the MMAs and the
+// commits that track them come from one thread.
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_w(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_w(void* smem_dst, const CUtensorMap* map,
+                                              uint64_t* bar, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];\n\t}" ::"r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d_w(const CUtensorMap* map, int c0, int c1, int c2,
+                                                  int c3) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n\t}" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
 
@@ -191,6 +274,50 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Warp-collective MMA forms (see "warp-collective issue" above).  _w takes the
+// accumulate flag at run time, _wc as a compile-time constant.
+__device__ __forceinline__ void mma_bf16_ss_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+template <int kAcc>
+__device__ __forceinline__ void mma_bf16_ss_wc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, %4;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "n"(kAcc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+template <int kAcc>
+__device__ __forceinline__ void mma_bf16_ts_wc(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                               uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, %4;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "n"(kAcc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_addr(bar))
       : "memory");
 }
 
