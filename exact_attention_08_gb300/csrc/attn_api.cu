@@ -41,6 +41,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool checked = false;
   bool supported = false;
+  int num_sms = 0;
   int* status = nullptr;
 };
 std::mutex g_dev_mutex;
@@ -65,6 +66,8 @@ int device_state(DeviceState** out) {
       e = cudaGetSymbolAddress(&ptr, g_attn_status);
       if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress(status)");
       s.status = static_cast<int*>(ptr);
+      e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return cuda_error(e, "cudaDeviceGetAttribute(SM count)");
     }
     s.checked = true;
     if (!s.supported)
@@ -219,6 +222,7 @@ ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, f
   a.causal = causal;
   a.window = window;
   a.n_sink = n_sink;
+  a.num_sms = ds->num_sms;
   a.status = ds->status;
   if (rows_k == 0) {
     cudaError_t e = launch_attn_fill_empty(a, st);
@@ -230,6 +234,7 @@ ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, f
   if ((rc = make_map(&a.tmQ, q, d, Hq, sq, nb, 128, "q")) != ATTN_OK) return rc;
   if ((rc = make_map(&a.tmK, k, d, Hkv, sk, nb, 128, "k")) != ATTN_OK) return rc;
   if ((rc = make_map(&a.tmV, v, d, Hkv, sk, nb, 128, "v")) != ATTN_OK) return rc;
+  if ((rc = make_map(&a.tmO, o, d, Hq, sq, nb, 128, "o")) != ATTN_OK) return rc;
   cudaError_t e = launch_attn_fwd(a, st);
   return e == cudaSuccess ? ATTN_OK : cuda_error(e, "attn_fwd launch");
 }

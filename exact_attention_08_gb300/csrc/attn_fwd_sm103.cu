@@ -45,6 +45,7 @@
 #include "sm103_ptx.cuh"
 
 #include <cuda_bf16.h>
+#include <algorithm>
 #include <climits>
 #include <mutex>
 
@@ -74,16 +75,19 @@ constexpr int kNoLowerBound = -(1 << 29);
 template <int D>
 struct Cfg {
   static constexpr int kStages = (D == 128) ? 2 : 4;
-  static constexpr int kTileBytes = kBM * D * 2;  // 128 rows x D bf16 (Q, K and V tiles alike)
+  static constexpr int kTileBytes = kBM * D * 2;  // 128 rows x D bf16 (Q, K, V and O tiles alike)
   static constexpr int kAtoms = D / 64;           // 128-byte swizzle atoms per row
   static constexpr int kAtomBytes = 128 * 128;    // one atom column of a tile: 128 rows x 128 B
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQT * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  // q_full, k_full[S], v_full[S], step[S], s_full[2], p_ready[2], o_done[2], drain
-  static constexpr int kNumBars = 1 + 3 * kStages + 3 * kQT + 1;
+  static constexpr int kOffStage = kOffV + kStages * kTileBytes;  // O tile on its way out
+  static constexpr int kOffBar = kOffStage + kTileBytes;
+  // q_full, k_full[S], v_full[S], step[S], s_full[2], p_ready[2], o_done[2], stage_full[2],
+  // stage_free, drain
+  static constexpr int kNumBars = 1 + 3 * kStages + 4 * kQT + 2;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 2 * kBN;
 };
@@ -94,7 +98,7 @@ struct Params {
   const int* cu_q;
   const int* cu_k;
   int B, Hq, Hkv, Sq, Skv, total_q;
-  int num_qpairs;
+  int num_qpairs, num_items;
   float scale, scale2;
   int causal, window, n_sink;
   uint64_t wait_limit_ns;
@@ -248,10 +252,88 @@ __device__ __forceinline__ void exp32(const uint32_t* v, uint64_t sc2, uint64_t 
   }
 }
 
+// Work item k (a pair of Q tiles of one (batch or sequence, query head)):
+// its coordinates, lengths, masks and active key-tile ranges.
+struct Work {
+  int bseq, h, hk, q0, Lq, Lk, off, q_base, k_base, b_coord, lastT;
+  TileMask m0, m1;
+  TileRange r0, r1;
+};
+
+// Item order.  Without causal masking every item is the same work; the
+// query pairs of one (batch, head) are consecutive, so CTAs streaming the
+// same keys and values run together and share them through L2.  With
+// causal masking the work of a pair grows with its index: the longest pairs
+// of every head come first.  Heads of one KV group are adjacent either way.
+// Returns false when the item has no query rows or its sequence offsets are
+// invalid (reported once, by the caller that passes report).
+__device__ __forceinline__ bool decode_work(const Params& p, int k, int sinkT, Work& w,
+                                            bool report) {
+  int x = k, qp;
+  if (p.causal) {
+    w.h = x % p.Hq;
+    x /= p.Hq;
+    w.bseq = x % p.B;
+    qp = p.num_qpairs - 1 - x / p.B;
+  } else {
+    qp = x % p.num_qpairs;
+    x /= p.num_qpairs;
+    w.h = x % p.Hq;
+    w.bseq = x / p.Hq;
+  }
+  if (p.cu_q != nullptr) {
+    const int a = p.cu_q[w.bseq], e = p.cu_q[w.bseq + 1];
+    const int ka = p.cu_k[w.bseq], ke = p.cu_k[w.bseq + 1];
+    if (a < 0 || e < a || e > p.total_q || ka < 0 || ke < ka || e - a > p.Sq) {
+      if (report) atomicOr(p.status, kStatusBadInput);
+      return false;
+    }
+    w.Lq = e - a;
+    w.Lk = ke - ka;
+    w.q_base = a;
+    w.k_base = ka;
+    w.b_coord = 0;
+  } else {
+    w.Lq = p.Sq;
+    w.Lk = p.Skv;
+    w.q_base = 0;
+    w.k_base = 0;
+    w.b_coord = w.bseq;
+  }
+  w.q0 = qp * (kQT * kBM);
+  if (w.q0 >= w.Lq) return false;
+  w.off = w.Lk - w.Lq;
+  w.hk = w.h / (p.Hq / p.Hkv);
+  w.m0 = make_mask(w.q0, w.Lq, w.Lk, w.off, p.causal, p.window);
+  w.m1 = make_mask(w.q0 + kBM, w.Lq, w.Lk, w.off, p.causal, p.window);
+  w.r0 = tile_range(w.m0, w.Lk, p.window);
+  w.r1 = tile_range(w.m1, w.Lk, p.window);
+  w.lastT = max(w.r0.hi, w.r1.hi);  // last key tile any row touches (-1: none)
+  (void)sinkT;
+  return true;
+}
+
+// Number of active key tiles of a range.
+__device__ __forceinline__ int range_count(const TileRange& r, int sinkT) {
+  if (r.hi < 0) return 0;
+  return min(sinkT, r.hi + 1) + max(0, r.hi - max(r.lo, sinkT) + 1);
+}
+
+// The n-th item of this CTA: items are dealt out in bands of gridDim.x, every
+// other band in reverse CTA order, so that with the longest items first the
+// CTAs' totals even out.  -1 when the CTA has no n-th item.
+__device__ __forceinline__ int item_of(int n, int num_items) {
+  const int G = gridDim.x;
+  const int pos = (n & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const long long k = static_cast<long long>(n) * G + pos;
+  return k < num_items ? static_cast<int>(k) : -1;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const Params p) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const Params p) {
   using C = Cfg<D>;
   constexpr int ST = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -260,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
+  uint8_t* sO = smem + C::kOffStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
@@ -268,66 +351,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = step + ST;
   uint64_t* p_ready = s_full + kQT;
   uint64_t* o_done = p_ready + kQT;
-  uint64_t* drain = o_done + kQT;
+  uint64_t* stage_full = o_done + kQT;  // [2]: the four warps of warpgroup i wrote its O rows
+  uint64_t* stage_free = stage_full + kQT;
+  uint64_t* drain = stage_free + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   __shared__ int abort_flag_s;
   volatile int* abort_flag = &abort_flag_s;
 
-  // ---------------------------------------------------------------- work item
-  // Without causal masking every CTA does the same work: all query pairs of
-  // one (batch, head) are consecutive, so the CTAs streaming the same keys
-  // and values run together and share them through L2.  With causal masking
-  // the work of a pair grows with its index: the longest pairs of every head
-  // go first, so the last wave holds the shortest ones.  Heads of one KV
-  // group are adjacent either way.
-  int x = blockIdx.x, h, bseq, qp;
-  if (p.causal) {
-    h = x % p.Hq;
-    x /= p.Hq;
-    bseq = x % p.B;
-    qp = p.num_qpairs - 1 - x / p.B;
-  } else {
-    qp = x % p.num_qpairs;
-    x /= p.num_qpairs;
-    h = x % p.Hq;
-    bseq = x / p.Hq;
-  }
-
-  int Lq, Lk, q_base, k_base, b_coord;
-  if (p.cu_q != nullptr) {
-    const int a = p.cu_q[bseq], e = p.cu_q[bseq + 1];
-    const int ka = p.cu_k[bseq], ke = p.cu_k[bseq + 1];
-    if (a < 0 || e < a || e > p.total_q || ka < 0 || ke < ka || e - a > p.Sq) {
-      if (threadIdx.x == 0) atomicOr(p.status, kStatusBadInput);
-      return;
-    }
-    Lq = e - a;
-    Lk = ke - ka;
-    q_base = a;
-    k_base = ka;
-    b_coord = 0;
-  } else {
-    Lq = p.Sq;
-    Lk = p.Skv;
-    q_base = 0;
-    k_base = 0;
-    b_coord = bseq;
-  }
-  const int q0 = qp * (kQT * kBM);
-  if (q0 >= Lq) return;  // uniform over the CTA, before any barrier or TMEM use
-
-  const int off = Lk - Lq;
-  const int hk = h / (p.Hq / p.Hkv);
-  const int nT = (Lk + kBN - 1) / kBN;
-  TileMask mk[kQT];
-#pragma unroll
-  for (int i = 0; i < kQT; ++i) mk[i] = make_mask(q0 + i * kBM, Lq, Lk, off, p.causal, p.window);
-  const TileRange rg0 = tile_range(mk[0], Lk, p.window);
-  const TileRange rg1 = tile_range(mk[1], Lk, p.window);
-  const int sinkT = (p.window > 0 && p.n_sink > 0) ? (p.n_sink + kBN - 1) / kBN : 0;
-  const int lastT = max(rg0.hi, rg1.hi);  // last key tile any row touches (-1: none)
-
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int sinkT = (p.window > 0 && p.n_sink > 0) ? (p.n_sink + kBN - 1) / kBN : 0;
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
@@ -343,6 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&p_ready[i], 128);
       mbar_init(&o_done[i], 1);
     }
+    for (int i = 0; i < kQT; ++i) mbar_init(&stage_full[i], 4);
+    mbar_init(stage_free, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -355,6 +389,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // The CTA is persistent: every role walks the same item sequence
+  // (item_of), skipping the same items, and its ring, barrier-phase and
+  // step counters carry over from one item to the next.
+  //
+  // Key steps.  Ring tile u (the u-th active key tile loaded by this CTA,
+  // counted over all its items) is key step u of the MMA issuer: S_0(u),
+  // S_1(u) and the products P V of the tile before it, then one commit on
+  // step[u % ST].  So K(u) is free once step u is done and V(u) once step
+  // u + 1 is; the producer waits for those before it refills a slot.  At the
+  // first tile of an item, the products of the previous item's last tile are
+  // issued before the wait for the new Q (they do not need it); after the
+  // last item a final step holds only those products.
+  //
   // Register budget: the block is launched with 168 registers a thread (three
   // warps share SMSP 0).  Each warpgroup changes its budget at the head of
   // the branch holding all of its code: the producer / MMA warpgroup drops to
@@ -365,57 +412,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpLoad) {
     // ============================================================ TMA producer
     // The whole warp runs the loop (every branch below is warp-uniform); one
-    // elected lane issues each copy and byte-count arrival.  Key tile u of
-    // the union of active tiles goes to ring slot u % ST.  Its K slot last
-    // held K(u - ST), free once key step u - ST is done; its V slot last held
-    // V(u - ST), read by the products of key step u - ST + 1.
-    if (lastT >= 0) {  // no copy is issued that nobody waits for
-      if (lane == 0) {
-        prefetch_tmap(&tmQ);
-        prefetch_tmap(&tmK);
-        prefetch_tmap(&tmV);
+    // elected lane issues each copy and byte-count arrival.
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+    }
+    __syncwarp();
+    int u = 0;   // ring tiles loaded
+    int nq = 0;  // Q pairs loaded
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int k = item_of(n, p.num_items);
+      if (k < 0) break;
+      Work w;
+      if (!decode_work(p, k, sinkT, w, lane == 0) || w.lastT < 0) continue;
+      // The Q buffers are free once every S of the previous pair is done:
+      // its last key step, u - 1.
+      if (nq > 0 &&
+          !mbar_wait_warp(&step[(u - 1) % ST], ((u - 1) / ST) & 1, abort_flag, p.wait_limit_ns)) {
+        if (lane == 0) fail(p.status, abort_flag);
+        ok = false;
+        break;
       }
-      __syncwarp();
       mbar_arrive_expect_tx_w(q_full, kQT * C::kTileBytes);
 #pragma unroll
       for (int i = 0; i < kQT; ++i)
 #pragma unroll
         for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_4d_w(sQ + i * C::kTileBytes + a * C::kAtomBytes, &tmQ, q_full, a * 64, h,
-                        q_base + q0 + i * kBM, b_coord);
-    }
-    int u = 0;
-    bool ring_ok = true;
-    for (int j = 0; j <= lastT; ++j) {
-      if (!in_range(rg0, j, sinkT) && !in_range(rg1, j, sinkT)) continue;
-      const int s = u % ST;
-      if (u >= ST && !mbar_wait_warp(&step[s], ((u / ST) - 1) & 1, abort_flag, p.wait_limit_ns)) {
-        if (lane == 0) fail(p.status, abort_flag);
-        ring_ok = false;
-        break;
-      }
-      mbar_arrive_expect_tx_w(&k_full[s], C::kTileBytes);
+          tma_load_4d_w(sQ + i * C::kTileBytes + a * C::kAtomBytes, &tmQ, q_full, a * 64, w.h,
+                        w.q_base + w.q0 + i * kBM, w.b_coord);
+      ++nq;
+      for (int j = 0; j <= w.lastT; ++j) {
+        if (!in_range(w.r0, j, sinkT) && !in_range(w.r1, j, sinkT)) continue;
+        const int s = u % ST;
+        if (u >= ST &&
+            !mbar_wait_warp(&step[s], ((u / ST) - 1) & 1, abort_flag, p.wait_limit_ns)) {
+          if (lane == 0) fail(p.status, abort_flag);
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx_w(&k_full[s], C::kTileBytes);
 #pragma unroll
-      for (int a = 0; a < C::kAtoms; ++a)
-        tma_load_4d_w(sK + s * C::kTileBytes + a * C::kAtomBytes, &tmK, &k_full[s], a * 64, hk,
-                      k_base + j * kBN, b_coord);
-      if (u >= ST && !mbar_wait_warp(&step[(u + 1) % ST], (((u + 1) / ST) - 1) & 1, abort_flag,
-                                     p.wait_limit_ns)) {
-        if (lane == 0) fail(p.status, abort_flag);
-        ring_ok = false;
-        break;
-      }
-      mbar_arrive_expect_tx_w(&v_full[s], C::kTileBytes);
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_4d_w(sK + s * C::kTileBytes + a * C::kAtomBytes, &tmK, &k_full[s], a * 64,
+                        w.hk, w.k_base + j * kBN, w.b_coord);
+        if (u >= ST && !mbar_wait_warp(&step[(u + 1) % ST], (((u + 1) / ST) - 1) & 1, abort_flag,
+                                       p.wait_limit_ns)) {
+          if (lane == 0) fail(p.status, abort_flag);
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx_w(&v_full[s], C::kTileBytes);
 #pragma unroll
-      for (int a = 0; a < C::kAtoms; ++a)
-        tma_load_4d_w(sV + s * C::kTileBytes + a * C::kAtomBytes, &tmV, &v_full[s], a * 64, hk,
-                      k_base + j * kBN, b_coord);
-      ++u;
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_4d_w(sV + s * C::kTileBytes + a * C::kAtomBytes, &tmV, &v_full[s], a * 64,
+                        w.hk, w.k_base + j * kBN, w.b_coord);
+        ++u;
+      }
     }
-    // Tail: the MMA issuer commits key steps 0..u (the last one holds only
-    // products P V); wait for step u, after which no tensor-core commit is
-    // left to arrive on this CTA's barriers when it exits.
-    if (ring_ok && u > 0 &&
+    // Tail: the last commit of the MMA issuer is step u (the final products
+    // P V); once it is done no tensor-core commit is left to arrive on this
+    // CTA's barriers.
+    if (ok && u > 0 &&
         !mbar_wait_warp(&step[u % ST], (u / ST) & 1, abort_flag, p.wait_limit_ns)) {
       if (lane == 0) fail(p.status, abort_flag);
     }
@@ -437,32 +496,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dq0 = sdesc_sw128(smem_addr(sQ), 16, 1024);
     const uint64_t dk0 = sdesc_sw128(smem_addr(sK), 16, 1024);
     const uint64_t dv0 = sdesc_sw128(smem_addr(sV), C::kAtomBytes, 1024);
-    // Per Q tile: active key tiles, products P V issued, union index of the
-    // S whose P V is still to be issued (-1: none).
-    int tot0 = 0, tot1 = 0;
-    for (int jj = 0; jj <= lastT; ++jj) {
-      tot0 += in_range(rg0, jj, sinkT);
-      tot1 += in_range(rg1, jj, sinkT);
-    }
-    int pv0 = 0, pv1 = 0, pend0 = -1, pend1 = -1;
-    // No active tile: nothing is loaded and nothing is issued or committed.
-    bool ok = lastT >= 0;
-    if (ok && !mbar_wait_warp(q_full, 0, abort_flag, p.wait_limit_ns)) {
-      ok = false;
-      if (lane == 0) fail(p.status, abort_flag);
-    }
-    // O_i += P_i V for the key tile with union index pend of Q tile i
-    // (its V and P already waited for).
-    auto issue_pv = [&](int i, int pend, int& pv, int tot) {
+    int u = 0;                    // key steps (ring tiles) issued
+    int nq = 0;                   // Q pairs consumed
+    int pv0 = 0, pv1 = 0;         // products P V issued per Q tile (p_ready phases)
+    int left0 = 0, left1 = 0;     // products still due in the current item
+    int pend0 = -1, pend1 = -1;   // ring tile whose product P V is still to be issued
+    bool ok = true;
+    // O_i += P_i V for ring tile pend (its V and P already waited for).
+    // The first product of an item overwrites O (the previous item's O has
+    // been read out by then: it waits for the p_ready arrival the softmax
+    // warpgroup makes after its epilogue).
+    bool fresh0 = true, fresh1 = true;
+    auto issue_pv = [&](int i, int pend, int& pv, int& left, bool& fresh) {
       const uint64_t dv = dv0 + static_cast<uint64_t>(pend % ST) * kTileDesc;
       const uint32_t tO = tmem + C::kColO + i * D;
       const uint32_t tP = tmem + i * kBN + 64;
-      mma_bf16_ts_w(tO, tP, dv, idesc_o, pv > 0 ? 1u : 0u);
+      mma_bf16_ts_w(tO, tP, dv, idesc_o, fresh ? 0u : 1u);
+      fresh = false;
 #pragma unroll
       for (int kk = 1; kk < kBN / 16; ++kk)
         mma_bf16_ts_wc<1>(tO, tP + kk * 8, dv + kk * (2048 >> 4), idesc_o);
       ++pv;
-      if (pv == tot) mma_commit_w(&o_done[i]);
+      if (--left == 0) mma_commit_w(&o_done[i]);
     };
     // S_i = Q_i K^T for the key tile in ring slot s.
     auto issue_s = [&](int i, uint64_t dk) {
@@ -476,60 +531,104 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit_w(&s_full[i]);
     };
-    int u = 0, j = 0;
-    while (ok) {
-      while (j <= lastT && !in_range(rg0, j, sinkT) && !in_range(rg1, j, sinkT)) ++j;
-      const bool have = j <= lastT;
-      const bool a0 = have && in_range(rg0, j, sinkT);
-      const bool a1 = have && in_range(rg1, j, sinkT);
-      const int s = u % ST;
-      const int sv = (u + ST - 1) % ST;  // V(u - 1)
-      const uint32_t pk = (u / ST) & 1, pvv = ((u - 1) / ST) & 1;
-      // Needed now: K(u) for S_0(u) / S_1(u), V(u - 1) and P_0 for O_0 += P_0 V(u - 1).
-      // Test them together (one round trip when all are ready), then wait on
-      // each in turn only if one is not.  A barrier not needed is replaced by
-      // q_full, phase 0, complete by now.
-      const bool need_k = have, need_v = (pend0 >= 0 || pend1 >= 0), need_p0 = pend0 >= 0;
-      if (!__all_sync(0xffffffffu,
-                      mbar_test3(need_k ? &k_full[s] : q_full, need_k ? pk : 0u,
-                                 need_v ? &v_full[sv] : q_full, need_v ? pvv : 0u,
-                                 need_p0 ? &p_ready[0] : q_full, need_p0 ? (pv0 & 1) : 0u))) {
-        if ((need_k && !mbar_wait_warp(&k_full[s], pk, abort_flag, p.wait_limit_ns)) ||
-            (need_v && !mbar_wait_warp(&v_full[sv], pvv, abort_flag, p.wait_limit_ns)) ||
-            (need_p0 && !mbar_wait_warp(&p_ready[0], pv0 & 1, abort_flag, p.wait_limit_ns))) {
-          if (lane == 0) fail(p.status, abort_flag);
-          break;
-        }
-      }
-      tc_fence_after_sync();
-      const uint64_t dk = dk0 + static_cast<uint64_t>(s) * kTileDesc;
-      // order: O_0 += P_0 V(u-1), S_0(u), O_1 += P_1 V(u-1), S_1(u)
+    // The products P V still due for ring tile u - 1 (end of an item).
+    auto flush = [&]() -> bool {
+      if (pend0 < 0 && pend1 < 0) return true;
+      const int sv = (u + ST - 1) % ST;
+      const uint32_t pvv = ((u - 1) / ST) & 1;
+      if (!mbar_wait_warp(&v_full[sv], pvv, abort_flag, p.wait_limit_ns)) return false;
       if (pend0 >= 0) {
-        issue_pv(0, pend0, pv0, tot0);
+        if (!mbar_wait_warp(&p_ready[0], pv0 & 1, abort_flag, p.wait_limit_ns)) return false;
+        tc_fence_after_sync();
+        issue_pv(0, pend0, pv0, left0, fresh0);
         pend0 = -1;
       }
-      if (a0) {
-        issue_s(0, dk);
-        pend0 = u;
-      }
       if (pend1 >= 0) {
-        if (!mbar_wait_warp(&p_ready[1], pv1 & 1, abort_flag, p.wait_limit_ns)) {
-          if (lane == 0) fail(p.status, abort_flag);
-          break;
-        }
+        if (!mbar_wait_warp(&p_ready[1], pv1 & 1, abort_flag, p.wait_limit_ns)) return false;
         tc_fence_after_sync();
-        issue_pv(1, pend1, pv1, tot1);
+        issue_pv(1, pend1, pv1, left1, fresh1);
         pend1 = -1;
       }
-      if (a1) {
-        issue_s(1, dk);
-        pend1 = u;
+      return true;
+    };
+    for (int n = 0; ok; ++n) {
+      const int k = item_of(n, p.num_items);
+      if (k < 0) break;
+      Work w;
+      if (!decode_work(p, k, sinkT, w, false) || w.lastT < 0) continue;
+      if (!flush()) {
+        ok = false;
+        break;
       }
-      mma_commit_w(&step[s]);  // key step u: K(u) and V(u - 1) free once done
-      if (!have) break;
-      ++u;
-      ++j;
+      left0 = range_count(w.r0, sinkT);
+      left1 = range_count(w.r1, sinkT);
+      fresh0 = fresh1 = true;
+      if (!mbar_wait_warp(q_full, nq & 1, abort_flag, p.wait_limit_ns)) {
+        ok = false;
+        break;
+      }
+      ++nq;
+      bool first = true;
+      for (int j = 0; j <= w.lastT; ++j) {
+        const bool a0 = in_range(w.r0, j, sinkT), a1 = in_range(w.r1, j, sinkT);
+        if (!a0 && !a1) continue;
+        const int s = u % ST;
+        const int sv = (u + ST - 1) % ST;  // V(u - 1)
+        const uint32_t pk = (u / ST) & 1, pvv = ((u - 1) / ST) & 1;
+        // Needed now: K(u), and for O_0 += P_0 V(u - 1) also V(u - 1) and
+        // P_0.  Tested together (one round trip when all are ready), then
+        // waited on in turn only if one is not.  A barrier not needed is
+        // replaced by q_full in its current, completed phase.
+        const bool need_v = !first && (pend0 >= 0 || pend1 >= 0), need_p0 = !first && pend0 >= 0;
+        const uint32_t qpar = (nq - 1) & 1;
+        if (!__all_sync(0xffffffffu,
+                        mbar_test3(&k_full[s], pk, need_v ? &v_full[sv] : q_full,
+                                   need_v ? pvv : qpar, need_p0 ? &p_ready[0] : q_full,
+                                   need_p0 ? (pv0 & 1) : qpar))) {
+          if (!mbar_wait_warp(&k_full[s], pk, abort_flag, p.wait_limit_ns) ||
+              (need_v && !mbar_wait_warp(&v_full[sv], pvv, abort_flag, p.wait_limit_ns)) ||
+              (need_p0 && !mbar_wait_warp(&p_ready[0], pv0 & 1, abort_flag, p.wait_limit_ns))) {
+            ok = false;
+            break;
+          }
+        }
+        tc_fence_after_sync();
+        const uint64_t dk = dk0 + static_cast<uint64_t>(s) * kTileDesc;
+        // order: O_0 += P_0 V(u-1), S_0(u), O_1 += P_1 V(u-1), S_1(u)
+        if (pend0 >= 0) {
+          issue_pv(0, pend0, pv0, left0, fresh0);
+          pend0 = -1;
+        }
+        if (a0) {
+          issue_s(0, dk);
+          pend0 = u;
+        }
+        if (pend1 >= 0) {
+          if (!mbar_wait_warp(&p_ready[1], pv1 & 1, abort_flag, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_pv(1, pend1, pv1, left1, fresh1);
+          pend1 = -1;
+        }
+        if (a1) {
+          issue_s(1, dk);
+          pend1 = u;
+        }
+        mma_commit_w(&step[s]);  // key step u: K(u) and V(u - 1) free once done
+        ++u;
+        first = false;
+      }
     }
+    // Final key step: the products of the last tile.
+    if (ok && u > 0) {
+      if (flush())
+        mma_commit_w(&step[u % ST]);
+      else
+        ok = false;
+    }
+    if (!ok && lane == 0) fail(p.status, abort_flag);
     __syncwarp();
   }
   } else {
@@ -538,212 +637,347 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = warp / 4;
     const int wq = warp % 4;
     const int r = wq * 32 + lane;
-    const int row = q0 + i * kBM + r;  // sequence-relative query index
-    const bool valid = row < Lq;
-    const int hi_row = p.causal ? min(row + off, Lk - 1) : Lk - 1;
-    const int lo_row = (p.window > 0) ? row + off - p.window : kNoLowerBound;
     const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t colS = i * kBN;
     const uint32_t colO = C::kColO + i * D;
     const float scale2 = p.scale2;
-    const TileMask m = i ? mk[1] : mk[0];
-    const TileRange rg = i ? rg1 : rg0;
-
-    float m_used = -INFINITY;  // raw (unscaled) running maximum in use
-    float l = 0.f;             // running sum of the fp32 probabilities
-    float corr = 0.f;          // running sum of (p - bf16(p)) over each tile's largest p
-    int t = 0;
+    int t = 0;     // key tiles processed (s_full / p_ready phases)
+    int no = 0;    // o_done phases consumed
+    int use = 0;    // this CTA's uses of the staging buffer so far (two per item)
+    int nbulk = 0;  // bulk stores made by this warpgroup (stage_full phases)
     bool ok = true;
-    for (int j = 0; j < nT; ++j) {
-      if (!in_range(rg, j, sinkT)) continue;
-      bool w_ok = mbar_wait(&s_full[i], t & 1, abort_flag, p.wait_limit_ns);
-      w_ok = __all_sync(0xffffffffu, w_ok);
-      if (!w_ok) {
-        if (lane == 0) fail(p.status, abort_flag);
-        ok = false;
-        break;
+    for (int n = 0; ok; ++n) {
+      const int k = item_of(n, p.num_items);
+      if (k < 0) break;
+      // Only what the key loop needs stays live through it; the epilogue
+      // decodes the item again.
+      TileMask m;
+      TileRange rg;
+      int hi_row, lo_row;
+      {
+        Work w;
+        if (!decode_work(p, k, sinkT, w, false)) continue;
+        const int row = w.q0 + i * kBM + r;  // sequence-relative query index
+        hi_row = p.causal ? min(row + w.off, w.Lk - 1) : w.Lk - 1;
+        lo_row = (p.window > 0) ? row + w.off - p.window : kNoLowerBound;
+        m = i ? w.m1 : w.m0;
+        rg = i ? w.r1 : w.r0;
       }
-      tc_fence_after_sync();
-      const bool edge = !tile_interior(m, j, p.window, p.n_sink);
-      const uint32_t sS = taddr + colS;
-      uint64_t sum_a = 0, sum_b = 0;  // bit pattern 0 is (+0.f, +0.f)
-      float mx = -INFINITY;
-      bool do_rescale = false;
-      float alpha = 1.f;
-      float ms = 0.f;
-      // Online-softmax state update from this tile's raw row maximum mx.
-      auto update_max = [&]() {
-        if (mx > m_used) {
-          if (m_used == -INFINITY) {
-            m_used = mx;
-          } else if ((mx - m_used) * scale2 > kRescaleLog2) {
-            alpha = ex2_approx((m_used - mx) * scale2);
-            l *= alpha;
-            corr *= alpha;
-            m_used = mx;
-            do_rescale = true;
+
+      float m_used = -INFINITY;  // raw (unscaled) running maximum in use
+      float l = 0.f;             // running sum of the fp32 probabilities
+      float corr = 0.f;          // running sum of (p - bf16(p)) over each tile's largest p
+      int t_item = 0;
+      for (int j = 0; j <= rg.hi; ++j) {
+        if (!in_range(rg, j, sinkT)) continue;
+        bool w_ok = mbar_wait(&s_full[i], t & 1, abort_flag, p.wait_limit_ns);
+        w_ok = __all_sync(0xffffffffu, w_ok);
+        if (!w_ok) {
+          if (lane == 0) fail(p.status, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const bool edge = !tile_interior(m, j, p.window, p.n_sink);
+        const uint32_t sS = taddr + colS;
+        uint64_t sum_a = 0, sum_b = 0;  // bit pattern 0 is (+0.f, +0.f)
+        float mx = -INFINITY;
+        bool do_rescale = false;
+        float alpha = 1.f;
+        float ms = 0.f;
+        // Online-softmax state update from this tile's raw row maximum mx.
+        auto update_max = [&]() {
+          if (mx > m_used) {
+            if (m_used == -INFINITY) {
+              m_used = mx;
+            } else if ((mx - m_used) * scale2 > kRescaleLog2) {
+              alpha = ex2_approx((m_used - mx) * scale2);
+              l *= alpha;
+              corr *= alpha;
+              m_used = mx;
+              do_rescale = true;
+            }
+          }
+          ms = (m_used == -INFINITY) ? 0.f : m_used * scale2;
+        };
+        // P goes to the upper half of the S columns as bf16 pairs: P column
+        // 64 + c/2 for score column c.  Every store must land on scores that
+        // have already been read.
+        if (!edge) {
+          // Interior tile, no mask.  Pass 1 reads all of S (one wait) for the
+          // row maximum; pass 2 reads it again chunk by chunk (the next chunk
+          // in flight while one is exponentiated), so that at most two chunks
+          // are held in registers while the probabilities are formed.  Chunks
+          // go 3, 2, 1, 0: the P of chunk c lands on columns 64 + 16c..,
+          // inside chunks already read.
+          {
+            uint32_t r0[32], r1[32], r2[32], r3[32];
+            tmem_ld_x32(sS + 0, r0);
+            tmem_ld_x32(sS + 32, r1);
+            tmem_ld_x32(sS + 64, r2);
+            tmem_ld_x32(sS + 96, r3);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              reg_fence(r0[c]);
+              reg_fence(r1[c]);
+              reg_fence(r2[c]);
+              reg_fence(r3[c]);
+            }
+            mx = max32(r3, max32(r2, max32(r1, max32(r0, -INFINITY))));
+          }
+          update_max();
+          const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
+          uint32_t ra[32], rb[32], pk[16];
+          tmem_ld_x32(sS + 96, ra);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
+          tmem_ld_x32(sS + 64, rb);
+          exp32(ra, sc2, nms, sum_a, sum_b, pk);
+          tmem_st_x16(sS + 112, pk);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) reg_fence(rb[c]);
+          tmem_ld_x32(sS + 32, ra);
+          exp32(rb, sc2, nms, sum_a, sum_b, pk);
+          tmem_st_x16(sS + 96, pk);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
+          tmem_ld_x32(sS + 0, rb);
+          exp32(ra, sc2, nms, sum_a, sum_b, pk);
+          tmem_st_x16(sS + 80, pk);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) reg_fence(rb[c]);
+          exp32(rb, sc2, nms, sum_a, sum_b, pk);
+          tmem_st_x16(sS + 64, pk);
+        } else {
+          // Boundary tile (causal diagonal, window edge, sink, ragged tail):
+          // the same arithmetic through compact chunk loops, with the mask.
+          const int kb = j * kBN;
+          const int lim_hi = hi_row - kb;
+          const int lim_lo = (p.window > 0) ? lo_row - kb : kNoLowerBound;
+          const int lim_sink = p.n_sink - kb;
+          uint32_t ra[32];
+  #pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld_x32(sS + 32 * c, ra);
+            tmem_ld_wait();
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) reg_fence(ra[e]);
+            mask32(ra, lim_hi - 32 * c, lim_lo - 32 * c, lim_sink - 32 * c);
+            mx = max32(ra, mx);
+          }
+          update_max();
+          const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
+          // chunks 3, 2, 1, 0: the P of chunk c lands on columns 64 + 16c..,
+          // inside chunks already processed
+  #pragma unroll 1
+          for (int c = 3; c >= 0; --c) {
+            tmem_ld_x32(sS + 32 * c, ra);
+            tmem_ld_wait();
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) reg_fence(ra[e]);
+            mask32(ra, lim_hi - 32 * c, lim_lo - 32 * c, lim_sink - 32 * c);
+            uint32_t pk[16];
+            exp32(ra, sc2, nms, sum_a, sum_b, pk);
+            tmem_st_x16(sS + 64 + 16 * c, pk);
           }
         }
-        ms = (m_used == -INFINITY) ? 0.f : m_used * scale2;
-      };
-      // P goes to the upper half of the S columns as bf16 pairs: P column
-      // 64 + c/2 for score column c.  Every store must land on scores that
-      // have already been read.
-      if (!edge) {
-        // Interior tile, no mask: S is read from tensor memory once (one wait
-        // for all four 32-column chunks), then exponentiated from registers.
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld_x32(sS + 0, r0);
-        tmem_ld_x32(sS + 32, r1);
-        tmem_ld_x32(sS + 64, r2);
-        tmem_ld_x32(sS + 96, r3);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          reg_fence(r0[c]);
-          reg_fence(r1[c]);
-          reg_fence(r2[c]);
-          reg_fence(r3[c]);
+        float s0, s1, s2, s3;
+        f2_split(sum_a, s0, s1);
+        f2_split(sum_b, s2, s3);
+        l += (s0 + s1) + (s2 + s3);
+        // The second product sees bf16-rounded probabilities.  When one key
+        // dominates a row, its rounding error would not cancel between O and l;
+        // track it for the largest probability of every tile (recomputed with
+        // the arithmetic exp32 used for it, so the same value) and take it out
+        // of the normaliser of O.
+        {
+          const float ptop = ex2_approx(__fmaf_rn(mx, scale2, -ms));
+          const float ptop_r = __uint_as_float(pack_bf16x2(0.f, ptop) & 0xffff0000u);
+          corr += ptop - ptop_r;
         }
-        mx = max32(r3, max32(r2, max32(r1, max32(r0, -INFINITY))));
-        update_max();
-        const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
-        // Separate registers for each chunk's packed P: a tcgen05.st reads its
-        // source registers asynchronously, so reusing them would make every
-        // chunk wait for the previous store.
-        uint32_t pk0[16], pk1[16], pk2[16], pk3[16];
-        exp32(r0, sc2, nms, sum_a, sum_b, pk0);
-        tmem_st_x16(sS + 64, pk0);
-        exp32(r1, sc2, nms, sum_a, sum_b, pk1);
-        tmem_st_x16(sS + 80, pk1);
-        exp32(r2, sc2, nms, sum_a, sum_b, pk2);
-        tmem_st_x16(sS + 96, pk2);
-        exp32(r3, sc2, nms, sum_a, sum_b, pk3);
-        tmem_st_x16(sS + 112, pk3);
-      } else {
-        // Boundary tile (causal diagonal, window edge, sink, ragged tail):
-        // the same arithmetic through compact chunk loops, with the mask.
-        const int kb = j * kBN;
-        const int lim_hi = hi_row - kb;
-        const int lim_lo = (p.window > 0) ? lo_row - kb : kNoLowerBound;
-        const int lim_sink = p.n_sink - kb;
-        uint32_t ra[32];
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld_x32(sS + 32 * c, ra);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) reg_fence(ra[e]);
-          mask32(ra, lim_hi - 32 * c, lim_lo - 32 * c, lim_sink - 32 * c);
-          mx = max32(ra, mx);
+        if (__any_sync(0xffffffffu, do_rescale)) {
+          // O of this row was last written by the product issued before S(j),
+          // which has completed (the commit behind s_full covers it); the next
+          // product into O waits for this warpgroup's p_ready arrival below.
+          const uint64_t a2 = f2(alpha, alpha);
+  #pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ro[32];
+            tmem_ld_x32(taddr + colO + c * 32, ro);
+            tmem_ld_wait();
+  #pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              reg_fence(ro[2 * e]);
+              reg_fence(ro[2 * e + 1]);
+              float o0, o1;
+              f2_split(f2_mul(f2(__uint_as_float(ro[2 * e]), __uint_as_float(ro[2 * e + 1])), a2),
+                       o0, o1);
+              ro[2 * e] = __float_as_uint(o0);
+              ro[2 * e + 1] = __float_as_uint(o1);
+            }
+            tmem_st_x32(taddr + colO + c * 32, ro);
+          }
         }
-        update_max();
-        const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
-        // chunks 3, 2, 1, 0: the P of chunk c lands on columns 64 + 16c..,
-        // inside chunks already processed
-#pragma unroll 1
-        for (int c = 3; c >= 0; --c) {
-          tmem_ld_x32(sS + 32 * c, ra);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) reg_fence(ra[e]);
-          mask32(ra, lim_hi - 32 * c, lim_lo - 32 * c, lim_sink - 32 * c);
-          uint32_t pk[16];
-          exp32(ra, sc2, nms, sum_a, sum_b, pk);
-          tmem_st_x16(sS + 64 + 16 * c, pk);
-        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&p_ready[i]);
+        ++t;
+        ++t_item;
       }
-      float s0, s1, s2, s3;
-      f2_split(sum_a, s0, s1);
-      f2_split(sum_b, s2, s3);
-      l += (s0 + s1) + (s2 + s3);
-      // The second product sees bf16-rounded probabilities.  When one key
-      // dominates a row, its rounding error would not cancel between O and l;
-      // track it for the largest probability of every tile (recomputed with
-      // the arithmetic exp32 used for it, so the same value) and take it out
-      // of the normaliser of O.
-      {
-        const float ptop = ex2_approx(__fmaf_rn(mx, scale2, -ms));
-        const float ptop_r = __uint_as_float(pack_bf16x2(0.f, ptop) & 0xffff0000u);
-        corr += ptop - ptop_r;
+      if (!ok) break;
+
+      // ---------------------------------------------------------------- epilogue
+      Work w;
+      decode_work(p, k, sinkT, w, false);
+      const int row = w.q0 + i * kBM + r;
+      const bool valid = row < w.Lq;
+      bool have_o = t_item > 0;
+      if (have_o) {
+        bool w_ok = mbar_wait(&o_done[i], no & 1, abort_flag, p.wait_limit_ns);
+        w_ok = __all_sync(0xffffffffu, w_ok);
+        ++no;
+        if (!w_ok) {
+          if (lane == 0) fail(p.status, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
       }
-      if (__any_sync(0xffffffffu, do_rescale)) {
-        // O of this row was last written by the product issued before S(j),
-        // which has completed (the commit behind s_full covers it); the next
-        // product into O waits for this warpgroup's p_ready arrival below.
-        const uint64_t a2 = f2(alpha, alpha);
+      const bool seen = have_o && l > 0.f;
+      const float inv = seen ? 1.f / (l - corr) : 0.f;
+      // O goes out through the staging buffer and one bulk tensor store per
+      // swizzle atom, unless the tile is a varlen tail (rows past the
+      // sequence belong to the next one and must not be written); those rows
+      // are stored directly.  Every branch below is uniform over the
+      // warpgroup, and the tensor-memory loads (warp-collective) are made by
+      // every lane whatever its row.
+      const bool tile_rows = w.q0 + i * kBM < w.Lq;  // the Q tile has any row
+      const bool bulk = tile_rows && (p.cu_q == nullptr || w.q0 + (i + 1) * kBM <= w.Lq);
+      // The buffer is used by warpgroup 0 then 1 for every item: wait until
+      // the store of the previous use has read it.
+      const int my_use = use + i;
+      use += 2;
+      if (bulk) {
+        if (my_use > 0) {
+          const bool w_ok = __all_sync(
+              0xffffffffu, mbar_wait(stage_free, (my_use - 1) & 1, abort_flag, p.wait_limit_ns));
+          if (!w_ok) {
+            if (lane == 0) fail(p.status, abort_flag);
+            ok = false;
+            break;
+          }
+        }
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t ro[32];
-          tmem_ld_x32(taddr + colO + c * 32, ro);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            reg_fence(ro[2 * e]);
-            reg_fence(ro[2 * e + 1]);
-            float o0, o1;
-            f2_split(f2_mul(f2(__uint_as_float(ro[2 * e]), __uint_as_float(ro[2 * e + 1])), a2),
-                     o0, o1);
-            ro[2 * e] = __float_as_uint(o0);
-            ro[2 * e + 1] = __float_as_uint(o1);
+          uint32_t o[32];
+          if (have_o) {
+            tmem_ld_x32(taddr + colO + c * 32, o);
+            tmem_ld_wait();
           }
-          tmem_st_x32(taddr + colO + c * 32, ro);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&p_ready[i]);
-      ++t;
-    }
-
-    // ---------------------------------------------------------------- epilogue
-    bool have_o = ok && t > 0;
-    if (have_o) {
-      bool w_ok = mbar_wait(&o_done[i], 0, abort_flag, p.wait_limit_ns);
-      w_ok = __all_sync(0xffffffffu, w_ok);
-      if (!w_ok) {
-        if (lane == 0) fail(p.status, abort_flag);
-        have_o = false;
-      }
-    }
-    const size_t orow = p.cu_q ? (static_cast<size_t>(q_base + row) * p.Hq + h) * D
-                               : ((static_cast<size_t>(bseq) * p.Sq + row) * p.Hq + h) * D;
-    uint4* dst = reinterpret_cast<uint4*>(p.o + orow);
-    const bool seen = have_o && l > 0.f;
-    if (have_o) {
-      tc_fence_after_sync();
-      const float inv = seen ? 1.f / (l - corr) : 0.f;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld_x32(taddr + colO + c * 32, o);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) reg_fence(o[e]);
-        if (valid) {
+          for (int e = 0; e < 32; ++e) reg_fence(o[e]);
+          // 32 columns = 4 chunks of 16 bytes in swizzle atom c / 2; chunk k
+          // of row r sits at position k ^ (r % 8) (the 128-byte swizzle).
+          uint8_t* atom = sO + (c / 2) * C::kAtomBytes + r * 128;
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
-            uint32_t w[4];
+            uint32_t wv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int idx = v4 * 8 + 2 * e;
-              w[e] = seen ? pack_bf16x2(__uint_as_float(o[idx]) * inv,
-                                        __uint_as_float(o[idx + 1]) * inv)
-                          : 0u;
+              wv[e] = seen ? pack_bf16x2(__uint_as_float(o[idx]) * inv,
+                                         __uint_as_float(o[idx + 1]) * inv)
+                           : 0u;
             }
-            dst[c * 4 + v4] = make_uint4(w[0], w[1], w[2], w[3]);
+            const int chunk = (c % 2) * 4 + v4;
+            *reinterpret_cast<uint4*>(atom + ((chunk ^ (r & 7)) * 16)) =
+                make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         }
-      }
-    } else if (valid && ok) {
+        // Rows written: make them visible to the bulk copy, then let warp 0
+        // of the warpgroup issue it once all four warps are done.
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&stage_full[i]);
+        if (wq == 0) {
+          const bool f_ok = __all_sync(
+              0xffffffffu, mbar_wait(&stage_full[i], nbulk & 1, abort_flag, p.wait_limit_ns));
+          if (f_ok && lane == 0) {
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            for (int a = 0; a < C::kAtoms; ++a)
+              tma_store_4d(&tmO, sO + a * C::kAtomBytes, a * 64, w.h, w.q_base + w.q0 + i * kBM,
+                           w.b_coord);
+            bulk_commit_group();
+            bulk_wait_read_all();
+            mbar_arrive(stage_free);
+          }
+          __syncwarp();
+          if (!f_ok) {
+            if (lane == 0) fail(p.status, abort_flag);
+            ok = false;
+            break;
+          }
+        }
+        ++nbulk;
+      } else {
+        // Direct stores (varlen tail tile, or no row at all); the buffer's
+        // turn is passed on.
+        if (wq == 0 && my_use > 0) {
+          const bool w_ok = __all_sync(
+              0xffffffffu, mbar_wait(stage_free, (my_use - 1) & 1, abort_flag, p.wait_limit_ns));
+          if (!w_ok) {
+            if (lane == 0) fail(p.status, abort_flag);
+            ok = false;
+            break;
+          }
+        }
+        const size_t orow = p.cu_q ? (static_cast<size_t>(w.q_base + row) * p.Hq + w.h) * D
+                                   : ((static_cast<size_t>(w.bseq) * p.Sq + row) * p.Hq + w.h) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          if (have_o) {
+            tmem_ld_x32(taddr + colO + c * 32, o);
+            tmem_ld_wait();
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) reg_fence(o[e]);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(p.o + orow);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint32_t wv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int idx = v4 * 8 + 2 * e;
+                wv[e] = seen ? pack_bf16x2(__uint_as_float(o[idx]) * inv,
+                                           __uint_as_float(o[idx + 1]) * inv)
+                             : 0u;
+              }
+              dst[c * 4 + v4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
+          }
+        }
+        if (wq == 0 && lane == 0) mbar_arrive(stage_free);
+        __syncwarp();
+      }
+      if (valid && p.lse != nullptr) {
+        const size_t li = p.cu_q ? static_cast<size_t>(w.h) * p.total_q + w.q_base + row
+                                 : (static_cast<size_t>(w.bseq) * p.Hq + w.h) * p.Sq + row;
+        p.lse[li] = seen ? fmaf(m_used, p.scale, logf(l)) : -INFINITY;
+      }
+      // The next item's first product into O must wait until O has been read:
+      // it waits for this warpgroup's next p_ready arrival, made after this.
+      tc_fence_before_sync();
     }
-    if (valid && p.lse != nullptr && (ok || !have_o)) {
-      const size_t li = p.cu_q ? static_cast<size_t>(h) * p.total_q + q_base + row
-                               : (static_cast<size_t>(bseq) * p.Hq + h) * p.Sq + row;
-      p.lse[li] = seen ? fmaf(m_used, p.scale, logf(l)) : -INFINITY;
-    }
+    // Bulk stores of this CTA complete before it exits.
+    if (wq == 0 && lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   // ---------------------------------------------------------------- teardown
@@ -816,11 +1050,14 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   p.n_sink = a.n_sink;
   p.wait_limit_ns = kWaitLimitNs;
   p.status = a.status;
-  const long long ctas = static_cast<long long>(p.num_qpairs) * a.B * a.Hq;
-  if (ctas <= 0) return cudaSuccess;
-  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  attn_fwd_kernel<D><<<static_cast<unsigned>(ctas), kThreads, C::kSmemBytes, stream>>>(
-      a.tmQ, a.tmK, a.tmV, p);
+  const long long items = static_cast<long long>(p.num_qpairs) * a.B * a.Hq;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  p.num_items = static_cast<int>(items);
+  // Persistent: one CTA per SM (shared and tensor memory hold one), each
+  // walking its share of the items.
+  const int grid = static_cast<int>(std::min<long long>(items, std::max(a.num_sms, 1)));
+  attn_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK, a.tmV, a.tmO, p);
   return cudaGetLastError();
 }
 

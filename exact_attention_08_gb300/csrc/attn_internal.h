@@ -19,7 +19,7 @@ enum : int {
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 
 struct FwdLaunch {
-  CUtensorMap tmQ, tmK, tmV;  // 4-D maps (d, H, S, B) with 64 x 1 x 128 x 1 boxes
+  CUtensorMap tmQ, tmK, tmV, tmO;  // 4-D maps (d, H, S, B) with 64 x 1 x 128 x 1 boxes
   void* o;                    // bf16 output
   float* lse;                 // fp32 log-sum-exp, may be null
   const int* cu_q;            // null: dense layout
@@ -30,6 +30,7 @@ struct FwdLaunch {
   int d;
   float scale;
   int causal, window, n_sink;
+  int num_sms;  // SMs of the device (the persistent grid)
   int* status;
 };
 
