@@ -14,7 +14,8 @@
 //   warps 4-7   softmax for Q tile 1
 //   warp  8     TMA producer (Q once, then the K/V ring); allocates TMEM
 //   warp  9     MMA issuer (whole warp, one elected lane issues)
-//   warps 10-11 idle
+//   warp  10    O store warp (bulk tensor stores of the staging tile)
+//   warp  11    idle
 // Tensor memory (512 columns): S_i = Q_i K^T at columns [128 i, 128 i + 128)
 // (fp32), O_i at [256 + D i, 256 + D i + D) (fp32).  The softmax writes the
 // probabilities P_i back over the last 64 columns of S_i as packed bf16
@@ -66,6 +67,8 @@ constexpr int kRegsSplit = 2 * 128 * kRegsSoftmax + 128 * kRegsOther;
 static_assert(kRegsSplit <= kThreads * 168, "register split");
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpStore = 10;
+constexpr int kPrefetch = 2;  // key/value tiles warmed in L2 ahead of their load
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
 // Lower visibility bound when there is no window: far below every key index,
@@ -92,6 +95,31 @@ struct Cfg {
   static constexpr uint32_t kColO = 2 * kBN;
 };
 
+// Division of a non-negative 31-bit integer by a fixed divisor d >= 1 with a
+// multiplier computed once on the host (Granlund and Montgomery, "Division
+// by invariant integers using multiplication", 1994: l = ceil(log2 d),
+// m = floor(2^32 (2^l - d) / d) + 1, n / d = (mulhi(n, m) + n) >> l; the sum
+// cannot overflow for n < 2^31).  Item decoding divides by the head count,
+// the batch and the pair count on every item of every role, and a plain
+// integer division there costs tens of instructions.
+struct FastDiv {
+  uint32_t d, m, l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  f.l = 0;
+  while ((1ull << f.l) < d) ++f.l;
+  f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << f.l) - d)) / d + 1);
+  return f;
+}
+
+__device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
+  const uint32_t u = static_cast<uint32_t>(n);
+  return static_cast<int>((__umulhi(u, f.m) + u) >> f.l);
+}
+
 struct Params {
   __nv_bfloat16* o;
   float* lse;
@@ -99,6 +127,7 @@ struct Params {
   const int* cu_k;
   int B, Hq, Hkv, Sq, Skv, total_q;
   int num_qpairs, num_items;
+  FastDiv div_hq, div_b, div_qp, div_group;  // by Hq, B, num_qpairs, Hq / Hkv
   float scale, scale2;
   int causal, window, n_sink;
   uint64_t wait_limit_ns;
@@ -269,17 +298,17 @@ struct Work {
 // invalid (reported once, by the caller that passes report).
 __device__ __forceinline__ bool decode_work(const Params& p, int k, int sinkT, Work& w,
                                             bool report) {
-  int x = k, qp;
+  int qp;
   if (p.causal) {
-    w.h = x % p.Hq;
-    x /= p.Hq;
-    w.bseq = x % p.B;
-    qp = p.num_qpairs - 1 - x / p.B;
+    const int x = fdiv(k, p.div_hq), y = fdiv(x, p.div_b);
+    w.h = k - x * p.Hq;
+    w.bseq = x - y * p.B;
+    qp = p.num_qpairs - 1 - y;
   } else {
-    qp = x % p.num_qpairs;
-    x /= p.num_qpairs;
-    w.h = x % p.Hq;
-    w.bseq = x / p.Hq;
+    const int x = fdiv(k, p.div_qp), y = fdiv(x, p.div_hq);
+    qp = k - x * p.num_qpairs;
+    w.h = x - y * p.Hq;
+    w.bseq = y;
   }
   if (p.cu_q != nullptr) {
     const int a = p.cu_q[w.bseq], e = p.cu_q[w.bseq + 1];
@@ -303,7 +332,7 @@ __device__ __forceinline__ bool decode_work(const Params& p, int k, int sinkT, W
   w.q0 = qp * (kQT * kBM);
   if (w.q0 >= w.Lq) return false;
   w.off = w.Lk - w.Lq;
-  w.hk = w.h / (p.Hq / p.Hkv);
+  w.hk = fdiv(w.h, p.div_group);
   w.m0 = make_mask(w.q0, w.Lq, w.Lk, w.off, p.causal, p.window);
   w.m1 = make_mask(w.q0 + kBM, w.Lq, w.Lk, w.off, p.causal, p.window);
   w.r0 = tile_range(w.m0, w.Lk, p.window);
@@ -311,6 +340,16 @@ __device__ __forceinline__ bool decode_work(const Params& p, int k, int sinkT, W
   w.lastT = max(w.r0.hi, w.r1.hi);  // last key tile any row touches (-1: none)
   (void)sinkT;
   return true;
+}
+
+// Does Q tile i of the item leave through the staging tile and bulk tensor
+// stores?  Not when it has no row, nor when it is the tail of a varlen
+// sequence (rows past the sequence belong to the next one and must not be
+// written): those rows are stored directly.  Dense tails are clipped by the
+// tensor bounds.
+__device__ __forceinline__ bool epilogue_bulk(const Params& p, const Work& w, int i) {
+  const bool tile_rows = w.q0 + i * kBM < w.Lq;
+  return tile_rows && (p.cu_q == nullptr || w.q0 + (i + 1) * kBM <= w.Lq);
 }
 
 // Number of active key tiles of a range.
@@ -443,6 +482,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d_w(sQ + i * C::kTileBytes + a * C::kAtomBytes, &tmQ, q_full, a * 64, w.h,
                         w.q_base + w.q0 + i * kBM, w.b_coord);
       ++nq;
+      // Warm L2 with the next item's Q: its load waits until every S of
+      // this item is done and would otherwise start from HBM then.
+      {
+        const int k2 = item_of(n + 1, p.num_items);
+        Work w2;
+        if (k2 >= 0 && decode_work(p, k2, sinkT, w2, false) && w2.lastT >= 0) {
+#pragma unroll
+          for (int i = 0; i < kQT; ++i)
+#pragma unroll
+            for (int a = 0; a < C::kAtoms; ++a)
+              tma_prefetch_4d_w(&tmQ, a * 64, w2.h, w2.q_base + w2.q0 + i * kBM, w2.b_coord);
+        }
+      }
       for (int j = 0; j <= w.lastT; ++j) {
         if (!in_range(w.r0, j, sinkT) && !in_range(w.r1, j, sinkT)) continue;
         const int s = u % ST;
@@ -451,6 +503,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) fail(p.status, abort_flag);
           ok = false;
           break;
+        }
+        // Warm L2 with the key and value tiles kPrefetch active tiles ahead:
+        // a ring slot is refilled only about one key step before it is read,
+        // less than a load from HBM takes.
+        {
+          int jp = j, ahead = 0;
+          while (ahead < kPrefetch && jp < w.lastT) {
+            ++jp;
+            if (in_range(w.r0, jp, sinkT) || in_range(w.r1, jp, sinkT)) ++ahead;
+          }
+          if (ahead == kPrefetch) {
+#pragma unroll
+            for (int a = 0; a < C::kAtoms; ++a) {
+              tma_prefetch_4d_w(&tmK, a * 64, w.hk, w.k_base + jp * kBN, w.b_coord);
+              tma_prefetch_4d_w(&tmV, a * 64, w.hk, w.k_base + jp * kBN, w.b_coord);
+            }
+          }
         }
         mbar_arrive_expect_tx_w(&k_full[s], C::kTileBytes);
 #pragma unroll
@@ -584,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__all_sync(0xffffffffu,
                         mbar_test3(&k_full[s], pk, need_v ? &v_full[sv] : q_full,
                                    need_v ? pvv : qpar, need_p0 ? &p_ready[0] : q_full,
-                                   need_p0 ? (pv0 & 1) : qpar))) {
+                                   need_p0 ? (pv0 & 1) : qpar) == 7u)) {
           if (!mbar_wait_warp(&k_full[s], pk, abort_flag, p.wait_limit_ns) ||
               (need_v && !mbar_wait_warp(&v_full[sv], pvv, abort_flag, p.wait_limit_ns)) ||
               (need_p0 && !mbar_wait_warp(&p_ready[0], pv0 & 1, abort_flag, p.wait_limit_ns))) {
@@ -630,6 +699,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) fail(p.status, abort_flag);
     __syncwarp();
+  } else if (warp == kWarpStore) {
+    // ============================================================ O store warp
+    // Takes the bulk stores of O off the softmax warpgroups: once the four
+    // warps of warpgroup i have written their rows to the staging tile, this
+    // warp issues the tensor stores, waits until they have read the tile and
+    // hands the tile on (uses: warpgroup 0 then 1, item after item).
+    int nb0 = 0, nb1 = 0;  // bulk stores per warpgroup (stage_full phases)
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int k = item_of(n, p.num_items);
+      if (k < 0) break;
+      Work w;
+      if (!decode_work(p, k, sinkT, w, false)) continue;
+#pragma unroll 1
+      for (int i = 0; i < kQT; ++i) {
+        if (!epilogue_bulk(p, w, i)) continue;
+        int& nb = i ? nb1 : nb0;
+        if (!mbar_wait_warp(&stage_full[i], nb & 1, abort_flag, p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        ++nb;
+        if (lane == 0) {
+#pragma unroll
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_store_4d(&tmO, sO + a * C::kAtomBytes, a * 64, w.h, w.q_base + w.q0 + i * kBM,
+                         w.b_coord);
+          bulk_commit_group();
+          bulk_wait_read_all();
+          mbar_arrive(stage_free);
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0) fail(p.status, abort_flag);
+    // The bulk stores of this CTA complete before it exits.
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax) : "memory");
@@ -643,8 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale2 = p.scale2;
     int t = 0;     // key tiles processed (s_full / p_ready phases)
     int no = 0;    // o_done phases consumed
-    int use = 0;    // this CTA's uses of the staging buffer so far (two per item)
-    int nbulk = 0;  // bulk stores made by this warpgroup (stage_full phases)
+    int use = 0;  // this CTA's uses of the staging buffer so far (two per item)
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int k = item_of(n, p.num_items);
@@ -703,7 +809,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P goes to the upper half of the S columns as bf16 pairs: P column
         // 64 + c/2 for score column c.  Every store must land on scores that
         // have already been read.
-        if (!edge) {
+        // Interior tile after the first of the item: speculate that no row's
+        // maximum grows past the rescale threshold, so the maximum in use
+        // stays.  S is read chunk by chunk (the next chunk in flight) and
+        // exponentiated with that maximum while this tile's maximum is
+        // reduced alongside; P is held in registers.  If a row of the warp
+        // does exceed the threshold (rare after the first tile), nothing has
+        // been written yet: the warp starts again on the full path below,
+        // S being still intact in tensor memory.
+        bool spec_ok = false;
+        if (!edge && !__any_sync(0xffffffffu, m_used == -INFINITY)) {
+          ms = m_used * scale2;
+          const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
+          uint32_t ra[32], rb[32], pk0[16], pk1[16], pk2[16], pk3[16];
+          float mxa = -INFINITY;
+          tmem_ld_x32(sS + 0, ra);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
+          tmem_ld_x32(sS + 32, rb);
+          mxa = max32(ra, mxa);
+          exp32(ra, sc2, nms, sum_a, sum_b, pk0);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) reg_fence(rb[c]);
+          tmem_ld_x32(sS + 64, ra);
+          mxa = max32(rb, mxa);
+          exp32(rb, sc2, nms, sum_a, sum_b, pk1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
+          tmem_ld_x32(sS + 96, rb);
+          mxa = max32(ra, mxa);
+          exp32(ra, sc2, nms, sum_a, sum_b, pk2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) reg_fence(rb[c]);
+          mxa = max32(rb, mxa);
+          exp32(rb, sc2, nms, sum_a, sum_b, pk3);
+          mx = mxa;
+          if (!__any_sync(0xffffffffu, (mx - m_used) * scale2 > kRescaleLog2)) {
+            tmem_st_x16(sS + 64, pk0);
+            tmem_st_x16(sS + 80, pk1);
+            tmem_st_x16(sS + 96, pk2);
+            tmem_st_x16(sS + 112, pk3);
+            spec_ok = true;
+          } else {
+            sum_a = sum_b = 0;  // start again
+            mx = -INFINITY;
+          }
+        }
+        if (spec_ok) {
+        } else if (!edge) {
           // Interior tile, no mask.  Pass 1 reads all of S (one wait) for the
           // row maximum; pass 2 reads it again chunk by chunk (the next chunk
           // in flight while one is exponentiated), so that at most two chunks
@@ -850,14 +1007,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool seen = have_o && l > 0.f;
       const float inv = seen ? 1.f / (l - corr) : 0.f;
-      // O goes out through the staging buffer and one bulk tensor store per
-      // swizzle atom, unless the tile is a varlen tail (rows past the
-      // sequence belong to the next one and must not be written); those rows
-      // are stored directly.  Every branch below is uniform over the
-      // warpgroup, and the tensor-memory loads (warp-collective) are made by
-      // every lane whatever its row.
-      const bool tile_rows = w.q0 + i * kBM < w.Lq;  // the Q tile has any row
-      const bool bulk = tile_rows && (p.cu_q == nullptr || w.q0 + (i + 1) * kBM <= w.Lq);
+      // O goes out through the staging tile and bulk tensor stores (issued by
+      // the store warp), or by direct stores (epilogue_bulk).  Every branch
+      // below is uniform over the warpgroup, and the tensor-memory loads
+      // (warp-collective) are made by every lane whatever its row.
+      const bool bulk = epilogue_bulk(p, w, i);
       // The buffer is used by warpgroup 0 then 1 for every item: wait until
       // the store of the previous use has read it.
       const int my_use = use + i;
@@ -872,17 +1026,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
         }
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          if (have_o) {
-            tmem_ld_x32(taddr + colO + c * 32, o);
-            tmem_ld_wait();
-          }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) reg_fence(o[e]);
-          // 32 columns = 4 chunks of 16 bytes in swizzle atom c / 2; chunk k
-          // of row r sits at position k ^ (r % 8) (the 128-byte swizzle).
+        // 32 columns at a time (the next chunk's load in flight), scaled by
+        // 1 / l in pairs, packed to bf16 and written as four 16-byte pieces:
+        // chunk k of row r of swizzle atom a sits at position k ^ (r % 8)
+        // (the 128-byte swizzle the tensor store expects).
+        const uint64_t inv2 = f2(inv, inv);
+        auto stage32 = [&](const uint32_t* o, int c) {
           uint8_t* atom = sO + (c / 2) * C::kAtomBytes + r * 128;
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
@@ -890,40 +1039,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int idx = v4 * 8 + 2 * e;
-              wv[e] = seen ? pack_bf16x2(__uint_as_float(o[idx]) * inv,
-                                         __uint_as_float(o[idx + 1]) * inv)
-                           : 0u;
+              float a0, a1;
+              f2_split(f2_mul(f2(__uint_as_float(o[idx]), __uint_as_float(o[idx + 1])), inv2), a0,
+                       a1);
+              wv[e] = seen ? pack_bf16x2(a0, a1) : 0u;
             }
             const int chunk = (c % 2) * 4 + v4;
             *reinterpret_cast<uint4*>(atom + ((chunk ^ (r & 7)) * 16)) =
                 make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
+        };
+        uint32_t oa[32], ob[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) oa[e] = ob[e] = 0u;
+        if (have_o) {
+          tmem_ld_x32(taddr + colO, oa);
+          tmem_ld_wait();
         }
-        // Rows written: make them visible to the bulk copy, then let warp 0
-        // of the warpgroup issue it once all four warps are done.
+#pragma unroll
+        for (int c = 0; c < D / 32; c += 2) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) reg_fence(oa[e]);
+          if (have_o) tmem_ld_x32(taddr + colO + (c + 1) * 32, ob);
+          stage32(oa, c);
+          if (have_o) tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) reg_fence(ob[e]);
+          if (have_o && c + 2 < D / 32) tmem_ld_x32(taddr + colO + (c + 2) * 32, oa);
+          stage32(ob, c + 1);
+          if (have_o && c + 2 < D / 32) tmem_ld_wait();
+        }
+        // Rows written: make them visible to the bulk copy; the store warp
+        // issues it once all four warps have arrived.
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&stage_full[i]);
-        if (wq == 0) {
-          const bool f_ok = __all_sync(
-              0xffffffffu, mbar_wait(&stage_full[i], nbulk & 1, abort_flag, p.wait_limit_ns));
-          if (f_ok && lane == 0) {
-#pragma unroll
-            for (int a = 0; a < C::kAtoms; ++a)
-              tma_store_4d(&tmO, sO + a * C::kAtomBytes, a * 64, w.h, w.q_base + w.q0 + i * kBM,
-                           w.b_coord);
-            bulk_commit_group();
-            bulk_wait_read_all();
-            mbar_arrive(stage_free);
-          }
-          __syncwarp();
-          if (!f_ok) {
-            if (lane == 0) fail(p.status, abort_flag);
-            ok = false;
-            break;
-          }
-        }
-        ++nbulk;
       } else {
         // Direct stores (varlen tail tile, or no row at all); the buffer's
         // turn is passed on.
@@ -975,9 +1125,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // it waits for this warpgroup's next p_ready arrival, made after this.
       tc_fence_before_sync();
     }
-    // Bulk stores of this CTA complete before it exits.
-    if (wq == 0 && lane == 0) bulk_wait_all();
-    __syncwarp();
   }
 
   // ---------------------------------------------------------------- teardown
@@ -1043,6 +1190,10 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   p.Skv = a.Skv;
   p.total_q = a.total_q;
   p.num_qpairs = (a.Sq + kQT * kBM - 1) / (kQT * kBM);
+  p.div_hq = make_fastdiv(static_cast<uint32_t>(a.Hq));
+  p.div_b = make_fastdiv(static_cast<uint32_t>(std::max(a.B, 1)));
+  p.div_qp = make_fastdiv(static_cast<uint32_t>(std::max(p.num_qpairs, 1)));
+  p.div_group = make_fastdiv(static_cast<uint32_t>(a.Hq / a.Hkv));
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.causal = a.causal;

@@ -83,36 +83,43 @@ __device__ __forceinline__ uint32_t mbar_try_wait_sleep(uint64_t* bar, uint32_t 
 // Waits until the barrier's phase with the given parity has completed.
 // Returns false (without completing) when `abort_flag` becomes non-zero or
 // `limit_ns` of wall time pass; the caller then records the failure.
+// The wall clock is first read after 32 unsuccessful tests (each may sleep
+// up to the suspend hint), so a wait that completes soon pays no timer read;
+// the limit therefore counts from then, a few microseconds at most late.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort_flag, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if ((it & 31u) == 0) {
       if (abort_flag && *abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0)
+        t0 = now;
+      else if (now - t0 > limit_ns)
+        return false;
     }
   }
 }
 
-// Non-blocking test of three barrier phases at once (1 if all three have
-// completed): the three tests are in flight together, so a warp that finds
-// everything ready pays one round trip instead of three.
+// Non-blocking test of three barrier phases at once: bit 0, 1, 2 set when
+// the phase of a, b, c has completed.  The three tests are in flight
+// together, so a warp that finds everything ready pays one round trip
+// instead of three, and one that does not knows which to wait for.
 __device__ __forceinline__ uint32_t mbar_test3(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
                                                uint64_t* c, uint32_t pc) {
-  uint32_t ok;
+  uint32_t ra, rb, rc;
   asm volatile(
       "{\n\t.reg .pred x, y, z;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 x, [%1], %2;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 y, [%3], %4;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 z, [%5], %6;\n\t"
-      "and.pred x, x, y;\n\tand.pred x, x, z;\n\t"
-      "selp.b32 %0, 1, 0, x;\n\t}"
-      : "=r"(ok)
+      "mbarrier.test_wait.parity.shared::cta.b64 x, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 y, [%5], %6;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 z, [%7], %8;\n\t"
+      "selp.b32 %0, 1, 0, x;\n\tselp.b32 %1, 2, 0, y;\n\tselp.b32 %2, 4, 0, z;\n\t}"
+      : "=r"(ra), "=r"(rb), "=r"(rc)
       : "r"(smem_addr(a)), "r"(pa), "r"(smem_addr(b)), "r"(pb), "r"(smem_addr(c)), "r"(pc)
       : "memory");
-  return ok;
+  return ra | rb | rc;
 }
 
 // Warp-collective form of mbar_wait: every lane of a converged warp calls it
