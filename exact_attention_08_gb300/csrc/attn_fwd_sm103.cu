@@ -18,9 +18,12 @@
 //   warp  11    idle
 // Tensor memory (512 columns): S_i = Q_i K^T at columns [128 i, 128 i + 128)
 // (fp32), O_i at [256 + D i, 256 + D i + D) (fp32).  The softmax writes the
-// probabilities P_i back over the last 64 columns of S_i as packed bf16
-// pairs, and the second product O_i += P_i V reads P_i straight from tensor
-// memory, so neither S nor P ever leaves the SM.
+// probabilities P_i back over the first 64 columns of S_i as packed bf16
+// pairs (32 key columns at a time, over scores it has already read), and the
+// second product O_i += P_i V reads P_i straight from tensor memory, so
+// neither S nor P ever leaves the SM.  P_i is published in two halves: the
+// tensor core starts O_i += P_i V on keys 0..63 while the softmax still forms
+// keys 64..127.
 //
 // MMA issue order per key tile j:  O_0 += P_0(j-1) V(j-1), S_0 = Q_0 K(j)^T,
 // O_1 += P_1(j-1) V(j-1), S_1 = Q_1 K(j)^T.  While warpgroup 0 turns S_0(j)
@@ -86,9 +89,9 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffStage = kOffV + kStages * kTileBytes;  // O tile on its way out
   static constexpr int kOffBar = kOffStage + kTileBytes;
-  // q_full, k_full[S], v_full[S], step[S], s_full[2], p_ready[2], o_done[2], stage_full[2],
-  // stage_free, drain
-  static constexpr int kNumBars = 1 + 3 * kStages + 4 * kQT + 2;
+  // q_full, k_full[S], v_full[S], step[S], s_full[2], p_half[2], p_ready[2], o_done[2],
+  // stage_full[2], stage_free, drain
+  static constexpr int kNumBars = 1 + 3 * kStages + 5 * kQT + 2;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static constexpr uint32_t kTmemCols = 512;
@@ -388,7 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_full = k_full + ST;
   uint64_t* step = v_full + ST;  // step[u % ST]: every product of key step u is done
   uint64_t* s_full = step + ST;
-  uint64_t* p_ready = s_full + kQT;
+  uint64_t* p_half = s_full + kQT;   // [2]: P_i of keys 0..63 written
+  uint64_t* p_ready = p_half + kQT;  // [2]: all of P_i written
   uint64_t* o_done = p_ready + kQT;
   uint64_t* stage_full = o_done + kQT;  // [2]: the four warps of warpgroup i wrote its O rows
   uint64_t* stage_free = stage_full + kQT;
@@ -411,6 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kQT; ++i) {
       mbar_init(&s_full[i], 1);
+      mbar_init(&p_half[i], 128);
       mbar_init(&p_ready[i], 128);
       mbar_init(&o_done[i], 1);
     }
@@ -571,22 +576,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     int left0 = 0, left1 = 0;     // products still due in the current item
     int pend0 = -1, pend1 = -1;   // ring tile whose product P V is still to be issued
     bool ok = true;
-    // O_i += P_i V for ring tile pend (its V and P already waited for).
     // The first product of an item overwrites O (the previous item's O has
-    // been read out by then: it waits for the p_ready arrival the softmax
+    // been read out by then: it waits for the p_half arrival the softmax
     // warpgroup makes after its epilogue).
     bool fresh0 = true, fresh1 = true;
-    auto issue_pv = [&](int i, int pend, int& pv, int& left, bool& fresh) {
+    // O_i += P_i V for ring tile pend (its V already waited for): the first
+    // half of P (keys 0..63, its p_half arrival already waited for) right
+    // away, the second half once the softmax has published it (p_ready).
+    auto issue_pv = [&](int i, int pend, int& pv, int& left, bool& fresh) -> bool {
       const uint64_t dv = dv0 + static_cast<uint64_t>(pend % ST) * kTileDesc;
       const uint32_t tO = tmem + C::kColO + i * D;
-      const uint32_t tP = tmem + i * kBN + 64;
+      const uint32_t tP = tmem + i * kBN;
       mma_bf16_ts_w(tO, tP, dv, idesc_o, fresh ? 0u : 1u);
       fresh = false;
 #pragma unroll
-      for (int kk = 1; kk < kBN / 16; ++kk)
+      for (int kk = 1; kk < kBN / 32; ++kk)
+        mma_bf16_ts_wc<1>(tO, tP + kk * 8, dv + kk * (2048 >> 4), idesc_o);
+      if (!mbar_wait_warp(&p_ready[i], pv & 1, abort_flag, p.wait_limit_ns)) return false;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = kBN / 32; kk < kBN / 16; ++kk)
         mma_bf16_ts_wc<1>(tO, tP + kk * 8, dv + kk * (2048 >> 4), idesc_o);
       ++pv;
       if (--left == 0) mma_commit_w(&o_done[i]);
+      return true;
     };
     // S_i = Q_i K^T for the key tile in ring slot s.
     auto issue_s = [&](int i, uint64_t dk) {
@@ -607,15 +620,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t pvv = ((u - 1) / ST) & 1;
       if (!mbar_wait_warp(&v_full[sv], pvv, abort_flag, p.wait_limit_ns)) return false;
       if (pend0 >= 0) {
-        if (!mbar_wait_warp(&p_ready[0], pv0 & 1, abort_flag, p.wait_limit_ns)) return false;
+        if (!mbar_wait_warp(&p_half[0], pv0 & 1, abort_flag, p.wait_limit_ns)) return false;
         tc_fence_after_sync();
-        issue_pv(0, pend0, pv0, left0, fresh0);
+        if (!issue_pv(0, pend0, pv0, left0, fresh0)) return false;
         pend0 = -1;
       }
       if (pend1 >= 0) {
-        if (!mbar_wait_warp(&p_ready[1], pv1 & 1, abort_flag, p.wait_limit_ns)) return false;
+        if (!mbar_wait_warp(&p_half[1], pv1 & 1, abort_flag, p.wait_limit_ns)) return false;
         tc_fence_after_sync();
-        issue_pv(1, pend1, pv1, left1, fresh1);
+        if (!issue_pv(1, pend1, pv1, left1, fresh1)) return false;
         pend1 = -1;
       }
       return true;
@@ -652,11 +665,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qpar = (nq - 1) & 1;
         if (!__all_sync(0xffffffffu,
                         mbar_test3(&k_full[s], pk, need_v ? &v_full[sv] : q_full,
-                                   need_v ? pvv : qpar, need_p0 ? &p_ready[0] : q_full,
+                                   need_v ? pvv : qpar, need_p0 ? &p_half[0] : q_full,
                                    need_p0 ? (pv0 & 1) : qpar) == 7u)) {
           if (!mbar_wait_warp(&k_full[s], pk, abort_flag, p.wait_limit_ns) ||
               (need_v && !mbar_wait_warp(&v_full[sv], pvv, abort_flag, p.wait_limit_ns)) ||
-              (need_p0 && !mbar_wait_warp(&p_ready[0], pv0 & 1, abort_flag, p.wait_limit_ns))) {
+              (need_p0 && !mbar_wait_warp(&p_half[0], pv0 & 1, abort_flag, p.wait_limit_ns))) {
             ok = false;
             break;
           }
@@ -665,7 +678,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dk = dk0 + static_cast<uint64_t>(s) * kTileDesc;
         // order: O_0 += P_0 V(u-1), S_0(u), O_1 += P_1 V(u-1), S_1(u)
         if (pend0 >= 0) {
-          issue_pv(0, pend0, pv0, left0, fresh0);
+          if (!issue_pv(0, pend0, pv0, left0, fresh0)) {
+            ok = false;
+            break;
+          }
           pend0 = -1;
         }
         if (a0) {
@@ -673,12 +689,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           pend0 = u;
         }
         if (pend1 >= 0) {
-          if (!mbar_wait_warp(&p_ready[1], pv1 & 1, abort_flag, p.wait_limit_ns)) {
+          if (!mbar_wait_warp(&p_half[1], pv1 & 1, abort_flag, p.wait_limit_ns)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          issue_pv(1, pend1, pv1, left1, fresh1);
+          if (!issue_pv(1, pend1, pv1, left1, fresh1)) {
+            ok = false;
+            break;
+          }
           pend1 = -1;
         }
         if (a1) {
@@ -791,37 +810,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool do_rescale = false;
         float alpha = 1.f;
         float ms = 0.f;
-        // Online-softmax state update from this tile's raw row maximum mx.
-        auto update_max = [&]() {
-          if (mx > m_used) {
-            if (m_used == -INFINITY) {
-              m_used = mx;
-            } else if ((mx - m_used) * scale2 > kRescaleLog2) {
-              alpha = ex2_approx((m_used - mx) * scale2);
-              l *= alpha;
-              corr *= alpha;
-              m_used = mx;
-              do_rescale = true;
-            }
-          }
-          ms = (m_used == -INFINITY) ? 0.f : m_used * scale2;
-        };
-        // P goes to the upper half of the S columns as bf16 pairs: P column
-        // 64 + c/2 for score column c.  Every store must land on scores that
-        // have already been read.
+        // P goes over the first 64 columns of S as bf16 pairs: the P of score
+        // chunk c (32 columns) to columns 16c..16c+15, on scores already read.
+        // P of keys 0..63 is published (p_half) as soon as it is written, so
+        // the tensor core starts the second product on it while keys 64..127
+        // are still exponentiated; p_ready follows the rest.
+        //
         // Interior tile after the first of the item: speculate that no row's
         // maximum grows past the rescale threshold, so the maximum in use
-        // stays.  S is read chunk by chunk (the next chunk in flight) and
-        // exponentiated with that maximum while this tile's maximum is
-        // reduced alongside; P is held in registers.  If a row of the warp
-        // does exceed the threshold (rare after the first tile), nothing has
-        // been written yet: the warp starts again on the full path below,
-        // S being still intact in tensor memory.
+        // stays.  Chunks 0 and 1 are exponentiated with it as they arrive,
+        // chunks 2 and 3 are held; once the whole tile's maximum confirms the
+        // guess, the first half of P is written and published and the second
+        // half formed.  If a row of the warp does exceed the threshold (rare
+        // after the first tile), nothing has been written yet: the warp
+        // starts again on the full path below, S being intact.
         bool spec_ok = false;
         if (!edge && !__any_sync(0xffffffffu, m_used == -INFINITY)) {
           ms = m_used * scale2;
           const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
-          uint32_t ra[32], rb[32], pk0[16], pk1[16], pk2[16], pk3[16];
+          uint32_t ra[32], rb[32], pk0[16], pk1[16];
           float mxa = -INFINITY;
           tmem_ld_x32(sS + 0, ra);
           tmem_ld_wait();
@@ -836,37 +843,76 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_x32(sS + 64, ra);
           mxa = max32(rb, mxa);
           exp32(rb, sc2, nms, sum_a, sum_b, pk1);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
           tmem_ld_x32(sS + 96, rb);
-          mxa = max32(ra, mxa);
-          exp32(ra, sc2, nms, sum_a, sum_b, pk2);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) reg_fence(rb[c]);
-          mxa = max32(rb, mxa);
-          exp32(rb, sc2, nms, sum_a, sum_b, pk3);
-          mx = mxa;
+          for (int c = 0; c < 32; ++c) {
+            reg_fence(ra[c]);
+            reg_fence(rb[c]);
+          }
+          mx = max32(rb, max32(ra, mxa));
           if (!__any_sync(0xffffffffu, (mx - m_used) * scale2 > kRescaleLog2)) {
-            tmem_st_x16(sS + 64, pk0);
-            tmem_st_x16(sS + 80, pk1);
-            tmem_st_x16(sS + 96, pk2);
-            tmem_st_x16(sS + 112, pk3);
+            tmem_st_x16(sS + 0, pk0);
+            tmem_st_x16(sS + 16, pk1);
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&p_half[i]);
+            exp32(ra, sc2, nms, sum_a, sum_b, pk0);
+            tmem_st_x16(sS + 32, pk0);
+            exp32(rb, sc2, nms, sum_a, sum_b, pk1);
+            tmem_st_x16(sS + 48, pk1);
             spec_ok = true;
           } else {
             sum_a = sum_b = 0;  // start again
             mx = -INFINITY;
           }
         }
+        // Online-softmax state update from this tile's raw row maximum, and
+        // the rescale of O it may need.  O of this row was last written by the
+        // product issued before S(j), which has completed (the commit behind
+        // s_full covers it); the next product into O waits for the p_half
+        // arrival that follows, so the rescale comes before any P is
+        // published.
+        auto update_rescale = [&]() {
+          if (mx > m_used) {
+            if (m_used == -INFINITY) {
+              m_used = mx;
+            } else if ((mx - m_used) * scale2 > kRescaleLog2) {
+              alpha = ex2_approx((m_used - mx) * scale2);
+              l *= alpha;
+              corr *= alpha;
+              m_used = mx;
+              do_rescale = true;
+            }
+          }
+          ms = (m_used == -INFINITY) ? 0.f : m_used * scale2;
+          if (__any_sync(0xffffffffu, do_rescale)) {
+            const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ro[32];
+              tmem_ld_x32(taddr + colO + c * 32, ro);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                reg_fence(ro[2 * e]);
+                reg_fence(ro[2 * e + 1]);
+                float o0, o1;
+                f2_split(f2_mul(f2(__uint_as_float(ro[2 * e]), __uint_as_float(ro[2 * e + 1])), a2),
+                         o0, o1);
+                ro[2 * e] = __float_as_uint(o0);
+                ro[2 * e + 1] = __float_as_uint(o1);
+              }
+              tmem_st_x32(taddr + colO + c * 32, ro);
+            }
+          }
+        };
         if (spec_ok) {
         } else if (!edge) {
           // Interior tile, no mask.  Pass 1 reads all of S (one wait) for the
           // row maximum; pass 2 reads it again chunk by chunk (the next chunk
-          // in flight while one is exponentiated), so that at most two chunks
-          // are held in registers while the probabilities are formed.  Chunks
-          // go 3, 2, 1, 0: the P of chunk c lands on columns 64 + 16c..,
-          // inside chunks already read.
+          // in flight while one is exponentiated), publishing the first half
+          // of P once chunks 0 and 1 are written.
           {
             uint32_t r0[32], r1[32], r2[32], r3[32];
             tmem_ld_x32(sS + 0, r0);
@@ -881,108 +927,90 @@ __global__ void __launch_bounds__(kThreads, 1)
               reg_fence(r2[c]);
               reg_fence(r3[c]);
             }
-            mx = max32(r3, max32(r2, max32(r1, max32(r0, -INFINITY))));
+            mx = max32(r3, max32(r2, max32(r1, max32(r0, mx))));
           }
-          update_max();
+          update_rescale();
           const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
           uint32_t ra[32], rb[32], pk[16];
-          tmem_ld_x32(sS + 96, ra);
+          tmem_ld_x32(sS + 0, ra);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
-          tmem_ld_x32(sS + 64, rb);
+          tmem_ld_x32(sS + 32, rb);
           exp32(ra, sc2, nms, sum_a, sum_b, pk);
-          tmem_st_x16(sS + 112, pk);
+          tmem_st_x16(sS + 0, pk);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 32; ++c) reg_fence(rb[c]);
-          tmem_ld_x32(sS + 32, ra);
+          tmem_ld_x32(sS + 64, ra);
           exp32(rb, sc2, nms, sum_a, sum_b, pk);
-          tmem_st_x16(sS + 96, pk);
+          tmem_st_x16(sS + 16, pk);
+          tmem_st_wait();
+          tc_fence_before_sync();
+          mbar_arrive(&p_half[i]);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
-          tmem_ld_x32(sS + 0, rb);
+          tmem_ld_x32(sS + 96, rb);
           exp32(ra, sc2, nms, sum_a, sum_b, pk);
-          tmem_st_x16(sS + 80, pk);
+          tmem_st_x16(sS + 32, pk);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 32; ++c) reg_fence(rb[c]);
           exp32(rb, sc2, nms, sum_a, sum_b, pk);
-          tmem_st_x16(sS + 64, pk);
+          tmem_st_x16(sS + 48, pk);
         } else {
           // Boundary tile (causal diagonal, window edge, sink, ragged tail):
-          // the same arithmetic through compact chunk loops, with the mask.
+          // the same arithmetic through compact chunk loops, with the mask;
+          // both halves of P are published at the end.
           const int kb = j * kBN;
           const int lim_hi = hi_row - kb;
           const int lim_lo = (p.window > 0) ? lo_row - kb : kNoLowerBound;
           const int lim_sink = p.n_sink - kb;
           uint32_t ra[32];
-  #pragma unroll 1
+#pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             tmem_ld_x32(sS + 32 * c, ra);
             tmem_ld_wait();
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < 32; ++e) reg_fence(ra[e]);
             mask32(ra, lim_hi - 32 * c, lim_lo - 32 * c, lim_sink - 32 * c);
             mx = max32(ra, mx);
           }
-          update_max();
+          update_rescale();
           const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
-          // chunks 3, 2, 1, 0: the P of chunk c lands on columns 64 + 16c..,
-          // inside chunks already processed
-  #pragma unroll 1
-          for (int c = 3; c >= 0; --c) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
             tmem_ld_x32(sS + 32 * c, ra);
             tmem_ld_wait();
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < 32; ++e) reg_fence(ra[e]);
             mask32(ra, lim_hi - 32 * c, lim_lo - 32 * c, lim_sink - 32 * c);
             uint32_t pk[16];
             exp32(ra, sc2, nms, sum_a, sum_b, pk);
-            tmem_st_x16(sS + 64 + 16 * c, pk);
+            tmem_st_x16(sS + 16 * c, pk);
           }
+          tmem_st_wait();
+          tc_fence_before_sync();
+          mbar_arrive(&p_half[i]);
         }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&p_ready[i]);
         float s0, s1, s2, s3;
         f2_split(sum_a, s0, s1);
         f2_split(sum_b, s2, s3);
         l += (s0 + s1) + (s2 + s3);
         // The second product sees bf16-rounded probabilities.  When one key
-        // dominates a row, its rounding error would not cancel between O and l;
-        // track it for the largest probability of every tile (recomputed with
-        // the arithmetic exp32 used for it, so the same value) and take it out
-        // of the normaliser of O.
+        // dominates a row, its rounding error would not cancel between O and
+        // l; track it for the largest probability of every tile (recomputed
+        // with the arithmetic exp32 used for it, so the same value) and take
+        // it out of the normaliser of O.
         {
           const float ptop = ex2_approx(__fmaf_rn(mx, scale2, -ms));
           const float ptop_r = __uint_as_float(pack_bf16x2(0.f, ptop) & 0xffff0000u);
           corr += ptop - ptop_r;
         }
-        if (__any_sync(0xffffffffu, do_rescale)) {
-          // O of this row was last written by the product issued before S(j),
-          // which has completed (the commit behind s_full covers it); the next
-          // product into O waits for this warpgroup's p_ready arrival below.
-          const uint64_t a2 = f2(alpha, alpha);
-  #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ro[32];
-            tmem_ld_x32(taddr + colO + c * 32, ro);
-            tmem_ld_wait();
-  #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              reg_fence(ro[2 * e]);
-              reg_fence(ro[2 * e + 1]);
-              float o0, o1;
-              f2_split(f2_mul(f2(__uint_as_float(ro[2 * e]), __uint_as_float(ro[2 * e + 1])), a2),
-                       o0, o1);
-              ro[2 * e] = __float_as_uint(o0);
-              ro[2 * e + 1] = __float_as_uint(o1);
-            }
-            tmem_st_x32(taddr + colO + c * 32, ro);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before_sync();
-        mbar_arrive(&p_ready[i]);
         ++t;
         ++t_item;
       }
@@ -1122,7 +1150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.lse[li] = seen ? fmaf(m_used, p.scale, logf(l)) : -INFINITY;
       }
       // The next item's first product into O must wait until O has been read:
-      // it waits for this warpgroup's next p_ready arrival, made after this.
+      // it waits for this warpgroup's next p_half arrival, made after this.
       tc_fence_before_sync();
     }
   }
