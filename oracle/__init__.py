@@ -52,13 +52,15 @@ def _load():
         if _lib is None:
             lib = ctypes.CDLL(build())
             i, d = ctypes.c_int, ctypes.c_double
-            lib.oracle_attn_fwd.argtypes = [_D, _D, _D, _D, _D, i, i, i, i, i, i, d, i, i, i, _I, i]
-            lib.oracle_attn_fwd_varlen.argtypes = [_D, _D, _D, _D, _D, _I, _I, i, i, i, i, d, i, i, i]
-            lib.oracle_attn_decode.argtypes = [_D, _D, _D, _I, _D, _D, i, i, i, i, i, d]
+            lib.oracle_attn_fwd.argtypes = [_D, _D, _D, _D, _D, i, i, i, i, i, i, d, i, i, i, _I, i,
+                                            _D]
+            lib.oracle_attn_fwd_varlen.argtypes = [_D, _D, _D, _D, _D, _I, _I, i, i, i, i, d, i, i, i,
+                                                   _D]
+            lib.oracle_attn_decode.argtypes = [_D, _D, _D, _I, _D, _D, i, i, i, i, i, d, _D]
             lib.oracle_attn_fwd_blockwise.argtypes = [_D, _D, _D, _D, _D, i, i, i, i, i, i, d, i, i,
-                                                      i, i, _D]
+                                                      i, i, _D, _D]
             lib.oracle_decode_split.argtypes = [_D, _D, _D, _I, _D, _D, i, i, i, i, i, d, i, i]
-            lib.oracle_combine.argtypes = [_D, _D, _D, _D, ctypes.c_long, i, i]
+            lib.oracle_combine.argtypes = [_D, _D, _D, _D, ctypes.c_long, i, i, _D]
             lib.oracle_num_threads.argtypes = []
             for f in ("oracle_attn_fwd", "oracle_attn_fwd_varlen", "oracle_attn_decode",
                       "oracle_attn_fwd_blockwise", "oracle_decode_split", "oracle_combine",
@@ -84,6 +86,16 @@ def _pi(a: np.ndarray):
     return a.ctypes.data_as(_I)
 
 
+def _sink(sink, n: int, what: str):
+    """(array or None, pointer or None) for an optional logit-sink vector of n values."""
+    if sink is None:
+        return None, None
+    a = _f64(sink).reshape(-1)
+    if a.size != n:
+        raise ValueError(f"{what}: sink has {a.size} values, {n} expected")
+    return a, _pd(a)
+
+
 def _check(rc: int, what: str) -> None:
     if rc != 0:
         raise RuntimeError(f"oracle {what} failed with code {rc}")
@@ -94,8 +106,9 @@ def num_threads() -> int:
     return int(_load().oracle_num_threads())
 
 
-def attn_fwd(q, k, v, scale, causal=False, window=0, n_sink=0, rows=None):
-    """Dense forward; returns (o [B,R,Hq,d], lse [B,Hq,R]) with R = Sq or len(rows)."""
+def attn_fwd(q, k, v, scale, causal=False, window=0, n_sink=0, rows=None, sink=None):
+    """Dense forward; returns (o [B,R,Hq,d], lse [B,Hq,R]) with R = Sq or len(rows).
+    sink: optional logit sink per query head [Hq] (-inf: none)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Sq, Hq, d = q.shape
     _, Skv, Hkv, _ = k.shape
@@ -106,43 +119,49 @@ def attn_fwd(q, k, v, scale, causal=False, window=0, n_sink=0, rows=None):
         n_rows, prow = int(rows_arr.size), _pi(rows_arr)
     o = np.empty((B, n_rows, Hq, d), np.float64)
     lse = np.empty((B, Hq, n_rows), np.float64)
+    sk, psk = _sink(sink, Hq, "attn_fwd")
     rc = _load().oracle_attn_fwd(_pd(q), _pd(k), _pd(v), _pd(o), _pd(lse), B, Hq, Hkv, Sq, Skv, d,
                                  float(scale), int(bool(causal)), int(window), int(n_sink), prow,
-                                 n_rows)
+                                 n_rows, psk)
     _check(rc, "attn_fwd")
     return o, lse
 
 
-def attn_fwd_varlen(q, k, v, cu_q, cu_k, scale, causal=False, window=0, n_sink=0):
-    """Packed forward; returns (o [Tq,Hq,d], lse [Hq,Tq])."""
+def attn_fwd_varlen(q, k, v, cu_q, cu_k, scale, causal=False, window=0, n_sink=0, sink=None):
+    """Packed forward; returns (o [Tq,Hq,d], lse [Hq,Tq]).  sink: as in attn_fwd."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     cu_q, cu_k = _i32(cu_q), _i32(cu_k)
     Tq, Hq, d = q.shape
     Hkv = k.shape[1]
     o = np.empty((Tq, Hq, d), np.float64)
     lse = np.empty((Hq, Tq), np.float64)
+    sk, psk = _sink(sink, Hq, "attn_fwd_varlen")
     rc = _load().oracle_attn_fwd_varlen(_pd(q), _pd(k), _pd(v), _pd(o), _pd(lse), _pi(cu_q),
                                         _pi(cu_k), int(cu_q.size - 1), Hq, Hkv, d, float(scale),
-                                        int(bool(causal)), int(window), int(n_sink))
+                                        int(bool(causal)), int(window), int(n_sink), psk)
     _check(rc, "attn_fwd_varlen")
     return o, lse
 
 
-def attn_decode(q, k, v, seqlens, scale):
-    """Decode over contiguous caches k,v [B,Lmax,Hkv,d]; returns (o [B,Hq,d], lse [B,Hq])."""
+def attn_decode(q, k, v, seqlens, scale, sink=None):
+    """Decode over contiguous caches k,v [B,Lmax,Hkv,d]; returns (o [B,Hq,d], lse [B,Hq]).
+    sink: as in attn_fwd."""
     q, k, v, seqlens = _f64(q), _f64(k), _f64(v), _i32(seqlens)
     B, Hq, d = q.shape
     _, Lmax, Hkv, _ = k.shape
     o = np.empty((B, Hq, d), np.float64)
     lse = np.empty((B, Hq), np.float64)
+    sk, psk = _sink(sink, Hq, "attn_decode")
     rc = _load().oracle_attn_decode(_pd(q), _pd(k), _pd(v), _pi(seqlens), _pd(o), _pd(lse), B, Hq,
-                                    Hkv, d, Lmax, float(scale))
+                                    Hkv, d, Lmax, float(scale), psk)
     _check(rc, "attn_decode")
     return o, lse
 
 
-def attn_fwd_blockwise(q, k, v, scale, causal=False, window=0, n_sink=0, block=128, trace=False):
-    """Online-softmax forward in key blocks; returns (o, lse[, trace [nblk, 2+d]])."""
+def attn_fwd_blockwise(q, k, v, scale, causal=False, window=0, n_sink=0, block=128, trace=False,
+                       sink=None):
+    """Online-softmax forward in key blocks; returns (o, lse[, trace [nblk, 2+d]]).
+    sink: as in attn_fwd, applied after the last block."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Sq, Hq, d = q.shape
     _, Skv, Hkv, _ = k.shape
@@ -150,10 +169,11 @@ def attn_fwd_blockwise(q, k, v, scale, causal=False, window=0, n_sink=0, block=1
     lse = np.empty((B, Hq, Sq), np.float64)
     nblk = (Skv + block - 1) // block
     tr = np.full((max(nblk, 1), 2 + d), np.nan) if trace else None
+    sk, psk = _sink(sink, Hq, "attn_fwd_blockwise")
     rc = _load().oracle_attn_fwd_blockwise(_pd(q), _pd(k), _pd(v), _pd(o), _pd(lse), B, Hq, Hkv,
                                            Sq, Skv, d, float(scale), int(bool(causal)), int(window),
                                            int(n_sink), int(block),
-                                           _pd(tr) if trace else None)
+                                           _pd(tr) if trace else None, psk)
     _check(rc, "attn_fwd_blockwise")
     return (o, lse, tr[:nblk]) if trace else (o, lse)
 
@@ -172,13 +192,15 @@ def decode_split(q, k, v, seqlens, scale, num_splits, page=16):
     return o_part, lse_part
 
 
-def combine(o_part, lse_part):
-    """LSE merge over the split axis (second to last of o_part, last of lse_part)."""
+def combine(o_part, lse_part, sink=None):
+    """LSE merge over the split axis (second to last of o_part, last of lse_part).
+    sink: optional logit sink per merged row (shape of lse_part without its last axis)."""
     o_part, lse_part = _f64(o_part), _f64(lse_part)
     *lead, S, d = o_part.shape
     rows = int(np.prod(lead)) if lead else 1
     o = np.empty((rows, d), np.float64)
     lse = np.empty((rows,), np.float64)
-    rc = _load().oracle_combine(_pd(o_part), _pd(lse_part), _pd(o), _pd(lse), rows, S, d)
+    sk, psk = _sink(sink, rows, "combine")
+    rc = _load().oracle_combine(_pd(o_part), _pd(lse_part), _pd(o), _pd(lse), rows, S, d, psk)
     _check(rc, "combine")
     return o.reshape(*lead, d), lse.reshape(*lead)

@@ -27,6 +27,17 @@
  *       (j > i + off - W  or  j < n_sink).
  *   A row that sees no key returns O = 0 and LSE = -inf (ch.15 section 5.1(2)).
  *
+ * Logit sink (optional, one value per query head; ch.15 section 4.6, the
+ * "attention sink" row of the variant table: the sink only adds one term to
+ * the softmax denominator).  Read here as a logit sigma_h in the units of S
+ * (natural log, after the scale) that joins the row's softmax as one more
+ * column with no value row:
+ *       m   = max(sigma_h, max_j S_ij)
+ *       O_i = sum_j exp(S_ij - m) V_j / (exp(sigma_h - m) + sum_j exp(S_ij - m))
+ *       LSE = m + ln(exp(sigma_h - m) + sum_j exp(S_ij - m))
+ *   sigma_h = -inf is no sink.  A row that sees no key but has a finite sink
+ *   returns O = 0 and LSE = sigma_h.
+ *
  * Layouts (row-major, contiguous):
  *   dense : q,o [B,Sq,Hq,d]   k,v [B,Skv,Hkv,d]   lse [B,Hq,Sq]
  *   varlen: q,o [Tq,Hq,d]     k,v [Tk,Hkv,d]      lse [Hq,Tq]
@@ -52,12 +63,13 @@ static int visible(long i, long j, long Sq, long Skv, int causal, int window, in
 
 /* One query row against one key/value head, two-pass definition.
  * qrow: d values; k, v: rows of stride kv_stride (elements), Skv of them.
+ * sink: the row's sink logit, -INFINITY for none.
  * srow: scratch of Skv doubles (holds S, then P). */
 static void row_two_pass(const double *qrow, const double *k, const double *v, long kv_stride,
                          long i, long Sq, long Skv, int d, double scale, int causal, int window,
-                         int n_sink, double *srow, double *orow, double *lse_out)
+                         int n_sink, double sink, double *srow, double *orow, double *lse_out)
 {
-    double m = -INFINITY;
+    double m = sink; /* the sink's column takes part in the row maximum */
     for (long j = 0; j < Skv; ++j) {
         if (!visible(i, j, Sq, Skv, causal, window, n_sink)) {
             srow[j] = -INFINITY;
@@ -69,12 +81,12 @@ static void row_two_pass(const double *qrow, const double *k, const double *v, l
         srow[j] = scale * dot;
         if (srow[j] > m) m = srow[j];
     }
-    if (m == -INFINITY) { /* no visible key */
+    if (m == -INFINITY) { /* no visible key and no sink */
         for (int t = 0; t < d; ++t) orow[t] = 0.0;
         *lse_out = -INFINITY;
         return;
     }
-    double sum = 0.0;
+    double sum = (sink == -INFINITY) ? 0.0 : exp(sink - m);
     for (long j = 0; j < Skv; ++j) {
         double p = (srow[j] == -INFINITY) ? 0.0 : exp(srow[j] - m);
         srow[j] = p;
@@ -95,11 +107,12 @@ static void row_two_pass(const double *qrow, const double *k, const double *v, l
  * rows / n_rows: optional subset of query rows (same subset for every batch
  * and head); rows == NULL means every row 0..Sq-1 and n_rows must equal Sq.
  * Outputs are compact over the subset: o [B, n_rows, Hq, d], lse [B, Hq, n_rows].
+ * sink: NULL, or the logit sink of every query head [Hq].
  */
 ORACLE_API int oracle_attn_fwd(const double *q, const double *k, const double *v, double *o,
                                double *lse, int B, int Hq, int Hkv, int Sq, int Skv, int d,
                                double scale, int causal, int window, int n_sink,
-                               const int *rows, int n_rows)
+                               const int *rows, int n_rows, const double *sink)
 {
     if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return 1;
     if (!rows && n_rows != Sq) return 1;
@@ -126,7 +139,7 @@ ORACLE_API int oracle_attn_fwd(const double *q, const double *k, const double *v
                 double *orow = o + (((b * n_rows + r) * Hq) + h) * d;
                 double *lrow = lse + ((b * Hq + h) * (long)n_rows + r);
                 row_two_pass(qrow, kb, vb, (long)Hkv * d, i, Sq, Skv, d, scale, causal, window,
-                             n_sink, srow, orow, lrow);
+                             n_sink, sink ? sink[h] : -INFINITY, srow, orow, lrow);
             }
             free(srow);
         }
@@ -139,11 +152,12 @@ ORACLE_API int oracle_attn_fwd(const double *q, const double *k, const double *v
  * cu_q / cu_k: [nseq + 1] prefix sums of the query / key lengths
  * (ch.15 section 5.3).  Causal alignment per sequence is bottom-right
  * (off = Lk - Lq).  o [Tq,Hq,d], lse [Hq,Tq], Tq = cu_q[nseq].
+ * sink: NULL, or the logit sink of every query head [Hq].
  */
 ORACLE_API int oracle_attn_fwd_varlen(const double *q, const double *k, const double *v,
                                       double *o, double *lse, const int *cu_q, const int *cu_k,
                                       int nseq, int Hq, int Hkv, int d, double scale, int causal,
-                                      int window, int n_sink)
+                                      int window, int n_sink, const double *sink)
 {
     if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return 1;
     const int groups = Hq / Hkv;
@@ -171,7 +185,8 @@ ORACLE_API int oracle_attn_fwd_varlen(const double *q, const double *k, const do
                 const double *kb = k + ((long)cu_k[s] * Hkv + hk) * d;
                 const double *vb = v + ((long)cu_k[s] * Hkv + hk) * d;
                 row_two_pass(qrow, kb, vb, (long)Hkv * d, i, Lq, Lk, d, scale, causal, window,
-                             n_sink, srow, o + (t * Hq + h) * d, lse + h * Tq + t);
+                             n_sink, sink ? sink[h] : -INFINITY, srow, o + (t * Hq + h) * d,
+                             lse + h * Tq + t);
             }
             free(srow);
         }
@@ -183,10 +198,11 @@ ORACLE_API int oracle_attn_fwd_varlen(const double *q, const double *k, const do
  * Single-token decode against contiguous per-request caches: query b sees
  * the first seqlens[b] keys of k[b] (the causal diagonal of a one-row query
  * aligned bottom-right, ch.15 sections 5.2-5.3).  k, v [B, Lmax, Hkv, d].
+ * sink: NULL, or the logit sink of every query head [Hq].
  */
 ORACLE_API int oracle_attn_decode(const double *q, const double *k, const double *v,
                                   const int *seqlens, double *o, double *lse, int B, int Hq,
-                                  int Hkv, int d, int Lmax, double scale)
+                                  int Hkv, int d, int Lmax, double scale, const double *sink)
 {
     if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return 1;
     const int groups = Hq / Hkv;
@@ -204,8 +220,8 @@ ORACLE_API int oracle_attn_decode(const double *q, const double *k, const double
                 long L = seqlens[b];
                 const double *kb = k + ((b * (long)Lmax) * Hkv + hk) * d;
                 const double *vb = v + ((b * (long)Lmax) * Hkv + hk) * d;
-                row_two_pass(q + w * d, kb, vb, (long)Hkv * d, 0, 1, L, d, scale, 0, 0, 0, srow,
-                             o + w * d, lse + w);
+                row_two_pass(q + w * d, kb, vb, (long)Hkv * d, 0, 1, L, d, scale, 0, 0, 0,
+                             sink ? sink[h] : -INFINITY, srow, o + w * d, lse + w);
             }
             free(srow);
         }
@@ -225,11 +241,17 @@ ORACLE_API int oracle_attn_decode(const double *q, const double *k, const double
  * and O / l is returned at the end (O = 0, LSE = -inf when l == 0).
  * trace (nullable): after each block, the (m, l, O[0..d)) state of query row 0
  * of batch 0, head 0 is appended: (2 + d) doubles per block.
+ * sink (nullable, [Hq]): the logit sink enters only after the last block, as
+ * one more term of the denominator taken against m* = max(sigma, m) (the
+ * epilogue form of ch.15 section 4.6; m* rather than m keeps exp(sigma - m*)
+ * finite when the sink exceeds every score):
+ *     l* = l exp(m - m*) + exp(sigma - m*),   O = acc exp(m - m*) / l*,
+ *     LSE = m* + ln(l*).
  */
 ORACLE_API int oracle_attn_fwd_blockwise(const double *q, const double *k, const double *v,
                                          double *o, double *lse, int B, int Hq, int Hkv, int Sq,
                                          int Skv, int d, double scale, int causal, int window,
-                                         int n_sink, int block, double *trace)
+                                         int n_sink, int block, double *trace, const double *sink)
 {
     if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || block <= 0) return 1;
     const int groups = Hq / Hkv;
@@ -287,7 +309,14 @@ ORACLE_API int oracle_attn_fwd_blockwise(const double *q, const double *k, const
                     }
                 }
                 double *orow = o + (((b * Sq + i) * Hq) + h) * d;
-                if (l == 0.0) {
+                const double sg = sink ? sink[h] : -INFINITY;
+                if (sg != -INFINITY) {
+                    double ms = (m > sg) ? m : sg;
+                    double e1 = (l == 0.0) ? 0.0 : exp(m - ms);
+                    double ls = l * e1 + exp(sg - ms);
+                    for (int t = 0; t < d; ++t) orow[t] = acc[t] * e1 / ls;
+                    lse[(b * Hq + h) * (long)Sq + i] = ms + log(ls);
+                } else if (l == 0.0) {
                     for (int t = 0; t < d; ++t) orow[t] = 0.0;
                     lse[(b * Hq + h) * (long)Sq + i] = -INFINITY;
                 } else {
@@ -338,7 +367,7 @@ ORACLE_API int oracle_decode_split(const double *q, const double *k, const doubl
                 const double *vb = v + ((b * (long)Lmax + t0) * Hkv + hk) * d;
                 /* the split's keys form their own row: no mask inside it */
                 row_two_pass(q + (b * Hq + h) * d, kb, vb, (long)Hkv * d, 0, 1, t1 - t0, d,
-                             scale, 0, 0, 0, srow, o_part + w * d, lse_part + w);
+                             scale, 0, 0, 0, -INFINITY, srow, o_part + w * d, lse_part + w);
             }
             free(srow);
         }
@@ -351,16 +380,21 @@ ORACLE_API int oracle_decode_split(const double *q, const double *k, const doubl
  * M = max_s lse_s and w_s = exp(lse_s - M),
  *     O   = sum_s w_s O_s / sum_s w_s,     LSE = M + ln(sum_s w_s),
  * summed in ascending split order.  All splits empty: O = 0, LSE = -inf.
+ * sink (nullable, one logit per row): the sink joins the merge as one more
+ * term of the denominator with no output, M = max(sigma, max_s lse_s),
+ *     O = sum_s w_s O_s / (exp(sigma - M) + sum_s w_s),
+ *     LSE = M + ln(exp(sigma - M) + sum_s w_s).
  */
 ORACLE_API int oracle_combine(const double *o_part, const double *lse_part, double *o,
-                              double *lse, long rows, int num_splits, int d)
+                              double *lse, long rows, int num_splits, int d, const double *sink)
 {
     if (num_splits <= 0 || d <= 0) return 1;
 #pragma omp parallel for schedule(static)
     for (long r = 0; r < rows; ++r) {
         const double *ls = lse_part + r * num_splits;
         const double *os = o_part + r * num_splits * (long)d;
-        double M = -INFINITY;
+        const double sg = sink ? sink[r] : -INFINITY;
+        double M = sg;
         for (int s = 0; s < num_splits; ++s)
             if (ls[s] > M) M = ls[s];
         double *orow = o + r * d;
@@ -369,7 +403,7 @@ ORACLE_API int oracle_combine(const double *o_part, const double *lse_part, doub
             lse[r] = -INFINITY;
             continue;
         }
-        double wsum = 0.0;
+        double wsum = (sg == -INFINITY) ? 0.0 : exp(sg - M);
         for (int s = 0; s < num_splits; ++s) {
             double wt = exp(ls[s] - M);
             wsum += wt;

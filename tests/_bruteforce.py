@@ -15,8 +15,10 @@ def allowed_keys(i, Sq, Skv, causal, window, n_sink):
     return sorted(keys)
 
 
-def attention(q, k, v, scale, causal=False, window=0, n_sink=0):
-    """q [B][Sq][Hq][d], k/v [B][Skv][Hkv][d] nested lists -> (o, lse) lists."""
+def attention(q, k, v, scale, causal=False, window=0, n_sink=0, sink=None):
+    """q [B][Sq][Hq][d], k/v [B][Skv][Hkv][d] nested lists -> (o, lse) lists.
+    sink: optional list of Hq logits, each a softmax column of its own whose
+    value row is zero (None or -inf: no such column)."""
     B, Sq, Hq, d = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
     Skv, Hkv = len(k[0]), len(k[0][0])
     G = Hq // Hkv
@@ -27,14 +29,15 @@ def attention(q, k, v, scale, causal=False, window=0, n_sink=0):
             kh = h // G
             for i in range(Sq):
                 keys = allowed_keys(i, Sq, Skv, causal, window, n_sink)
-                if not keys:
+                extra = [] if sink is None or sink[h] == -math.inf else [sink[h]]
+                if not keys and not extra:
                     lse[b][h][i] = -math.inf
                     continue
                 logit = {j: scale * math.fsum(q[b][i][h][t] * k[b][j][kh][t] for t in range(d))
                          for j in keys}
-                top = max(logit.values())
+                top = max(list(logit.values()) + extra)
                 w = {j: math.exp(logit[j] - top) for j in keys}
-                z = math.fsum(w.values())
+                z = math.fsum(list(w.values()) + [math.exp(x - top) for x in extra])
                 for t in range(d):
                     o[b][i][h][t] = math.fsum(w[j] * v[b][j][kh][t] for j in keys) / z
                 lse[b][h][i] = top + math.log(z)
