@@ -10,6 +10,8 @@ call fails if the library reports an error.
     o, lse = attn_fwd(q, k, v, causal=True)          # q [B,Sq,Hq,d], k/v [B,Skv,Hkv,d]
     o, lse = attn_fwd_ex(q, k, v, cu_q, cu_k, max_seqlen_q=..., causal=True)
     o, lse = attn_decode_paged(q, k_pages, v_pages, page_table, seqlens, num_splits=8)
+    o, lse = attn_fwd_ex_sink(q, k, v, sink_logit, causal=True)   # sink_logit [Hq] fp32
+    o, lse = attn_decode_paged_sink(q, k_pages, v_pages, page_table, seqlens, sink_logit)
 """
 from __future__ import annotations
 
@@ -21,8 +23,8 @@ from . import _build
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT",
-    "ATTN_ERR_BAD_INPUT", "AttnError", "attn_fwd", "attn_fwd_ex", "attn_decode_workspace_size",
-    "attn_decode_paged", "attn_device_status", "attn_check_wait_timeout", "attn_status_string",
+    "ATTN_ERR_BAD_INPUT", "AttnError", "attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink",
+    "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout", "attn_status_string",
     "attn_last_error", "library_path", "lib",
 ]
 
@@ -47,18 +49,22 @@ def _load() -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
     L.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, i, i, vp]
+    L.attn_fwd_ex_sink.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, i, i,
+                                   vp, vp]
     L.attn_decode_workspace_size.argtypes = [i, i, i, i]
     L.attn_decode_workspace_size.restype = sz
     L.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, sz,
                                     vp]
+    L.attn_decode_paged_sink.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp,
+                                         vp, sz, vp]
     L.attn_device_status.argtypes = [vp]
     L.attn_check_wait_timeout.argtypes = [i, vp]
     L.attn_status_string.argtypes = [i]
     L.attn_status_string.restype = ctypes.c_char_p
     L.attn_last_error.argtypes = []
     L.attn_last_error.restype = ctypes.c_char_p
-    for fn in ("attn_fwd", "attn_fwd_ex", "attn_decode_paged", "attn_device_status",
-               "attn_check_wait_timeout"):
+    for fn in ("attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink", "attn_decode_paged",
+               "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout"):
         getattr(L, fn).restype = ctypes.c_int
     return L
 
@@ -148,6 +154,21 @@ def attn_fwd_ex(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, *, max_seqlen_q=N
     """Forward with sink keys and optional packing.  With cu_seqlens (int32 CUDA
     tensors [nseq+1]): q [Tq,Hq,d], k/v [Tk,Hkv,d], o [Tq,Hq,d], lse [Hq,Tq].
     Without: the dense layout of attn_fwd."""
+    return _fwd_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, None, max_seqlen_q, max_seqlen_k, o, lse,
+                   causal, window, n_sink, scale, stream, want_lse)
+
+
+def attn_fwd_ex_sink(q, k, v, sink_logit, cu_seqlens_q=None, cu_seqlens_k=None, *,
+                     max_seqlen_q=None, max_seqlen_k=None, o=None, lse=None, causal=False,
+                     window=0, n_sink=0, scale=None, stream=None, want_lse=True):
+    """attn_fwd_ex with a logit sink per query head: sink_logit fp32 CUDA tensor [Hq]
+    (-inf entries: no sink for that head)."""
+    return _fwd_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, sink_logit, max_seqlen_q, max_seqlen_k,
+                   o, lse, causal, window, n_sink, scale, stream, want_lse)
+
+
+def _fwd_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, sink_logit, max_seqlen_q, max_seqlen_k, o, lse,
+            causal, window, n_sink, scale, stream, want_lse):
     torch = _torch()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, q.device)
@@ -175,10 +196,20 @@ def attn_fwd_ex(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, *, max_seqlen_q=N
     if lse is not None:
         _need(lse, "lse", torch.float32, q.device)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    rc = lib.attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
-                         _ptr(cu_seqlens_k), B, Hq, Hkv, sq, sk, Tq, Tk, d, scale,
-                         int(bool(causal)), int(window), int(n_sink), _stream(stream))
-    _check(rc, "attn_fwd_ex")
+    if sink_logit is None:
+        rc = lib.attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
+                             _ptr(cu_seqlens_k), B, Hq, Hkv, sq, sk, Tq, Tk, d, scale,
+                             int(bool(causal)), int(window), int(n_sink), _stream(stream))
+        _check(rc, "attn_fwd_ex")
+    else:
+        _need(sink_logit, "sink_logit", torch.float32, q.device)
+        if sink_logit.numel() != Hq:
+            raise ValueError(f"sink_logit must hold Hq={Hq} values")
+        rc = lib.attn_fwd_ex_sink(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                  _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, Hq, Hkv, sq, sk, Tq,
+                                  Tk, d, scale, int(bool(causal)), int(window), int(n_sink),
+                                  _ptr(sink_logit), _stream(stream))
+        _check(rc, "attn_fwd_ex_sink")
     return o, lse
 
 
@@ -190,6 +221,20 @@ def attn_decode_paged(q, k_pages, v_pages, page_table, seqlens, o=None, lse=None
                       num_splits=8, scale=None, workspace=None, stream=None, want_lse=True):
     """One-token decode.  q [B,Hq,d] bf16, k/v_pages [P,16,Hkv,d] bf16, page_table
     [B,maxP] int32, seqlens [B] int32 -> o [B,Hq,d] bf16, lse [B,Hq] fp32."""
+    return _decode(q, k_pages, v_pages, page_table, seqlens, None, o, lse, num_splits, scale,
+                   workspace, stream, want_lse)
+
+
+def attn_decode_paged_sink(q, k_pages, v_pages, page_table, seqlens, sink_logit, o=None,
+                           lse=None, *, num_splits=8, scale=None, workspace=None, stream=None,
+                           want_lse=True):
+    """attn_decode_paged with a logit sink per query head: sink_logit fp32 CUDA tensor [Hq]."""
+    return _decode(q, k_pages, v_pages, page_table, seqlens, sink_logit, o, lse, num_splits,
+                   scale, workspace, stream, want_lse)
+
+
+def _decode(q, k_pages, v_pages, page_table, seqlens, sink_logit, o, lse, num_splits, scale,
+            workspace, stream, want_lse):
     torch = _torch()
     dev = q.device
     _need(q, "q", torch.bfloat16, dev)
@@ -214,11 +259,22 @@ def attn_decode_paged(q, k_pages, v_pages, page_table, seqlens, o=None, lse=None
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    rc = lib.attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
-                               _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, Hkv, d, page,
-                               page_table.shape[1], P, int(num_splits), scale, _ptr(workspace),
-                               workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(rc, "attn_decode_paged")
+    wbytes = workspace.numel() * workspace.element_size()
+    if sink_logit is None:
+        rc = lib.attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                   _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, Hkv, d, page,
+                                   page_table.shape[1], P, int(num_splits), scale, _ptr(workspace),
+                                   wbytes, _stream(stream))
+        _check(rc, "attn_decode_paged")
+    else:
+        _need(sink_logit, "sink_logit", torch.float32, dev)
+        if sink_logit.numel() != Hq:
+            raise ValueError(f"sink_logit must hold Hq={Hq} values")
+        rc = lib.attn_decode_paged_sink(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                        _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, Hkv, d, page,
+                                        page_table.shape[1], P, int(num_splits), scale,
+                                        _ptr(sink_logit), _ptr(workspace), wbytes, _stream(stream))
+        _check(rc, "attn_decode_paged_sink")
     return o, lse
 
 

@@ -167,10 +167,16 @@ ATTN_API const char* attn_status_string(int status) {
 
 ATTN_API const char* attn_last_error(void) { return t_last_error.c_str(); }
 
-ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
-                         const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq, int Hkv,
-                         int max_Sq, int max_Skv, int total_q, int total_k, int d, float scale,
-                         int causal, int window, int n_sink, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Every forward entry point: checks, tensor maps, launch.  sink: per-head
+// logit sink [Hq] (device, fp32) or null.
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+             const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq, int Hkv, int max_Sq,
+             int max_Skv, int total_q, int total_k, int d, float scale, int causal, int window,
+             int n_sink, const float* sink, void* stream) {
   t_last_error.clear();
   const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
   if (varlen && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr))
@@ -195,8 +201,9 @@ ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, f
   if (rows_k > 0 && (k == nullptr || v == nullptr))
     return set_error(ATTN_ERR_INVALID_ARG, "k and v must be set");
   if (!aligned16(q) || !aligned16(o) || !aligned16(k) || !aligned16(v) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return set_error(ATTN_ERR_INVALID_ARG, "tensors must be 16-byte aligned (lse 4-byte)");
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(sink) & 3u))
+    return set_error(ATTN_ERR_INVALID_ARG,
+                     "tensors must be 16-byte aligned (lse and sink 4-byte)");
   if (varlen && max_Sq == 0) return set_error(ATTN_ERR_INVALID_ARG, "max_Sq must bound the lengths");
 
   DeviceState* ds = nullptr;
@@ -208,6 +215,7 @@ ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, f
   std::memset(&a, 0, sizeof(a));
   a.o = o;
   a.lse = lse;
+  a.sink = sink;
   a.cu_q = cu_seqlens_q;
   a.cu_k = cu_seqlens_k;
   a.B = B;
@@ -239,6 +247,27 @@ ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, f
   return e == cudaSuccess ? ATTN_OK : cuda_error(e, "attn_fwd launch");
 }
 
+}  // namespace
+
+extern "C" {
+
+ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                         const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq, int Hkv,
+                         int max_Sq, int max_Skv, int total_q, int total_k, int d, float scale,
+                         int causal, int window, int n_sink, void* stream) {
+  return fwd_impl(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, max_Sq, max_Skv,
+                  total_q, total_k, d, scale, causal, window, n_sink, nullptr, stream);
+}
+
+ATTN_API int attn_fwd_ex_sink(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                              int Hkv, int max_Sq, int max_Skv, int total_q, int total_k, int d,
+                              float scale, int causal, int window, int n_sink,
+                              const float* sink_logit, void* stream) {
+  return fwd_impl(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, max_Sq, max_Skv,
+                  total_q, total_k, d, scale, causal, window, n_sink, sink_logit, stream);
+}
+
 ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                       int Hq, int Hkv, int Sq, int Skv, int d, float scale, int causal, int window,
                       void* stream) {
@@ -252,12 +281,16 @@ ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits)
   return rows * d * sizeof(float) + rows * sizeof(float);
 }
 
-ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
-                               const int* page_table, const int* seqlens, void* o, float* lse,
-                               int B, int Hq, int Hkv, int d, int page_size,
-                               int max_pages_per_seq, int num_pages_total, int num_splits,
-                               float scale, void* workspace, size_t workspace_bytes,
-                               void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Every paged-decode entry point.  sink: per-head logit sink [Hq] or null.
+int decode_impl(const void* q, const void* k_pages, const void* v_pages, const int* page_table,
+                const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv, int d,
+                int page_size, int max_pages_per_seq, int num_pages_total, int num_splits,
+                float scale, const float* sink, void* workspace, size_t workspace_bytes,
+                void* stream) {
   t_last_error.clear();
   if (B < 0 || Hq <= 0 || Hkv <= 0 || max_pages_per_seq <= 0 || num_pages_total <= 0)
     return set_error(ATTN_ERR_INVALID_ARG, "bad sizes");
@@ -274,7 +307,8 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v
     return set_error(ATTN_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
       !aligned16(workspace) || (reinterpret_cast<uintptr_t>(page_table) & 3u) ||
-      (reinterpret_cast<uintptr_t>(seqlens) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+      (reinterpret_cast<uintptr_t>(seqlens) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(sink) & 3u))
     return set_error(ATTN_ERR_INVALID_ARG, "misaligned pointer");
   const size_t need = attn_decode_workspace_size(B, Hq, d, num_splits);
   if (workspace_bytes < need)
@@ -294,6 +328,7 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v
   a.q = q;
   a.o = o;
   a.lse = lse;
+  a.sink = sink;
   a.page_table = page_table;
   a.seqlens = seqlens;
   a.ws_o = static_cast<float*>(workspace);
@@ -310,6 +345,32 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v
   a.status = ds->status;
   cudaError_t e = launch_attn_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_error(e, "attn_decode_paged launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                               const int* page_table, const int* seqlens, void* o, float* lse,
+                               int B, int Hq, int Hkv, int d, int page_size,
+                               int max_pages_per_seq, int num_pages_total, int num_splits,
+                               float scale, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  return decode_impl(q, k_pages, v_pages, page_table, seqlens, o, lse, B, Hq, Hkv, d, page_size,
+                     max_pages_per_seq, num_pages_total, num_splits, scale, nullptr, workspace,
+                     workspace_bytes, stream);
+}
+
+ATTN_API int attn_decode_paged_sink(const void* q, const void* k_pages, const void* v_pages,
+                                    const int* page_table, const int* seqlens, void* o,
+                                    float* lse, int B, int Hq, int Hkv, int d, int page_size,
+                                    int max_pages_per_seq, int num_pages_total, int num_splits,
+                                    float scale, const float* sink_logit, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  return decode_impl(q, k_pages, v_pages, page_table, seqlens, o, lse, B, Hq, Hkv, d, page_size,
+                     max_pages_per_seq, num_pages_total, num_splits, scale, sink_logit, workspace,
+                     workspace_bytes, stream);
 }
 
 ATTN_API int attn_decode_paged_noalloc(const void* q, const void* k_pages, const void* v_pages,

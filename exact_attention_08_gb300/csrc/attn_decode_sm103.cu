@@ -351,10 +351,13 @@ template <int D>
 __global__ void __launch_bounds__(D)
     attn_decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
                                __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-                               int num_splits) {
+                               int num_splits, const float* __restrict__ sink, int Hq) {
   const size_t row = blockIdx.x;  // b * Hq + h
   const float* ls = ws_lse + row * num_splits;
-  float M = -INFINITY;
+  // A logit sink joins the merge as one more denominator term with no output
+  // ("TileLang tutorial, ch.15", section 4.6), against M = max(sink, lse_s).
+  const float sg = sink ? sink[row % static_cast<size_t>(Hq)] : -INFINITY;
+  float M = sg;
   for (int s = 0; s < num_splits; ++s) M = fmaxf(M, ls[s]);
   const int t = threadIdx.x;
   if (M == -INFINITY) {
@@ -362,7 +365,7 @@ __global__ void __launch_bounds__(D)
     if (lse && t == 0) lse[row] = -INFINITY;
     return;
   }
-  float wsum = 0.f, acc = 0.f;
+  float wsum = (sg == -INFINITY) ? 0.f : expf(sg - M), acc = 0.f;
   for (int s = 0; s < num_splits; ++s) {
     const float w = expf(ls[s] - M);
     wsum += w;
@@ -405,7 +408,7 @@ cudaError_t launch_dec(const DecodeLaunch& a, cudaStream_t stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_decode_combine_kernel<D><<<a.B * a.Hq, D, 0, stream>>>(
-      a.ws_o, a.ws_lse, static_cast<__nv_bfloat16*>(a.o), a.lse, a.num_splits);
+      a.ws_o, a.ws_lse, static_cast<__nv_bfloat16*>(a.o), a.lse, a.num_splits, a.sink, a.Hq);
   return cudaGetLastError();
 }
 

@@ -90,8 +90,8 @@ struct Cfg {
   static constexpr int kOffStage = kOffV + kStages * kTileBytes;  // O tile on its way out
   static constexpr int kOffBar = kOffStage + kTileBytes;
   // q_full, k_full[S], v_full[S], step[S], s_full[2], p_half[2], p_ready[2], o_done[2],
-  // stage_full[2], stage_free, drain
-  static constexpr int kNumBars = 1 + 3 * kStages + 5 * kQT + 2;
+  // stage_full[2], turn[2], drain
+  static constexpr int kNumBars = 1 + 3 * kStages + 6 * kQT + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static constexpr uint32_t kTmemCols = 512;
@@ -126,6 +126,7 @@ __device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
 struct Params {
   __nv_bfloat16* o;
   float* lse;
+  const float* sink;  // logit sink per query head [Hq], or null
   const int* cu_q;
   const int* cu_k;
   int B, Hq, Hkv, Sq, Skv, total_q;
@@ -395,8 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_ready = p_half + kQT;  // [2]: all of P_i written
   uint64_t* o_done = p_ready + kQT;
   uint64_t* stage_full = o_done + kQT;  // [2]: the four warps of warpgroup i wrote its O rows
-  uint64_t* stage_free = stage_full + kQT;
-  uint64_t* drain = stage_free + 1;
+  // turn[i]: the staging tile is free for warpgroup i's next epilogue (its
+  // previous user, the other warpgroup, is done with it).  One barrier per
+  // warpgroup, so that every phase a warp waits for is at most one ahead of
+  // the phases it has already seen: with a single shared barrier a warp
+  // could come back two phases early and read the parity of an older one.
+  uint64_t* turn = stage_full + kQT;
+  uint64_t* drain = turn + kQT;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   __shared__ int abort_flag_s;
   volatile int* abort_flag = &abort_flag_s;
@@ -420,7 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_done[i], 1);
     }
     for (int i = 0; i < kQT; ++i) mbar_init(&stage_full[i], 4);
-    mbar_init(stage_free, 1);
+    mbar_init(&turn[0], 1);
+    mbar_init(&turn[1], 1);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -721,10 +728,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpStore) {
     // ============================================================ O store warp
     // Takes the bulk stores of O off the softmax warpgroups: once the four
-    // warps of warpgroup i have written their rows to the staging tile, this
-    // warp issues the tensor stores, waits until they have read the tile and
-    // hands the tile on (uses: warpgroup 0 then 1, item after item).
-    int nb0 = 0, nb1 = 0;  // bulk stores per warpgroup (stage_full phases)
+    // warps of warpgroup i have taken their turn (and, for a bulk store,
+    // written their rows to the staging tile), this warp issues the tensor
+    // stores, waits until they have read the tile and hands the turn on
+    // (warpgroup 0 then 1, item after item).
+    int nb0 = 0, nb1 = 0;  // epilogues per warpgroup (stage_full phases)
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int k = item_of(n, p.num_items);
@@ -733,7 +741,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!decode_work(p, k, sinkT, w, false)) continue;
 #pragma unroll 1
       for (int i = 0; i < kQT; ++i) {
-        if (!epilogue_bulk(p, w, i)) continue;
         int& nb = i ? nb1 : nb0;
         if (!mbar_wait_warp(&stage_full[i], nb & 1, abort_flag, p.wait_limit_ns)) {
           ok = false;
@@ -741,13 +748,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++nb;
         if (lane == 0) {
+          if (epilogue_bulk(p, w, i)) {
 #pragma unroll
-          for (int a = 0; a < C::kAtoms; ++a)
-            tma_store_4d(&tmO, sO + a * C::kAtomBytes, a * 64, w.h, w.q_base + w.q0 + i * kBM,
-                         w.b_coord);
-          bulk_commit_group();
-          bulk_wait_read_all();
-          mbar_arrive(stage_free);
+            for (int a = 0; a < C::kAtoms; ++a)
+              tma_store_4d(&tmO, sO + a * C::kAtomBytes, a * 64, w.h, w.q_base + w.q0 + i * kBM,
+                           w.b_coord);
+            bulk_commit_group();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(&turn[1 - i]);
         }
         __syncwarp();
       }
@@ -769,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale2 = p.scale2;
     int t = 0;     // key tiles processed (s_full / p_ready phases)
     int no = 0;    // o_done phases consumed
-    int use = 0;  // this CTA's uses of the staging buffer so far (two per item)
+    int ne = 0;   // epilogues done (one per item; turn[] phases)
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int k = item_of(n, p.num_items);
@@ -1034,26 +1043,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
       }
       const bool seen = have_o && l > 0.f;
-      const float inv = seen ? 1.f / (l - corr) : 0.f;
+      // Logit sink sigma of this head ("TileLang tutorial, ch.15", section
+      // 4.6): one more term of the denominator, taken against
+      // m* = max(sigma, m * scale) so that it cannot overflow; with no sink
+      // (-inf) the plain normalisation.
+      const float sg = p.sink ? p.sink[w.h] : -INFINITY;
+      float inv, lse_row;
+      if (sg == -INFINITY) {
+        inv = seen ? 1.f / (l - corr) : 0.f;
+        lse_row = seen ? fmaf(m_used, p.scale, logf(l)) : -INFINITY;
+      } else {
+        const float a = seen ? m_used * p.scale : -INFINITY;
+        const float mst = fmaxf(a, sg);
+        const float e1 = seen ? expf(a - mst) : 0.f;
+        const float e2 = expf(sg - mst);
+        inv = e1 / fmaf(l - corr, e1, e2);
+        lse_row = mst + logf(fmaf(l, e1, e2));
+      }
       // O goes out through the staging tile and bulk tensor stores (issued by
       // the store warp), or by direct stores (epilogue_bulk).  Every branch
       // below is uniform over the warpgroup, and the tensor-memory loads
       // (warp-collective) are made by every lane whatever its row.
       const bool bulk = epilogue_bulk(p, w, i);
-      // The buffer is used by warpgroup 0 then 1 for every item: wait until
-      // the store of the previous use has read it.
-      const int my_use = use + i;
-      use += 2;
-      if (bulk) {
-        if (my_use > 0) {
-          const bool w_ok = __all_sync(
-              0xffffffffu, mbar_wait(stage_free, (my_use - 1) & 1, abort_flag, p.wait_limit_ns));
-          if (!w_ok) {
-            if (lane == 0) fail(p.status, abort_flag);
-            ok = false;
-            break;
-          }
+      // The staging tile goes to warpgroup 0 then 1 for every item, whether
+      // or not a warpgroup uses it.  Every warp waits for its turn:
+      // warpgroup 0 of item e for warpgroup 1 of item e - 1 to be done with
+      // the tile, warpgroup 1 for warpgroup 0 of item e.  The four warps then
+      // arrive on stage_full[i] (after writing their rows, for a bulk
+      // store), and the store warp hands the turn on once its copy has read
+      // the tile; so a turn is passed only after all four warps have seen
+      // the previous one.
+      const int e_turn = i ? ne : ne - 1;  // phase of turn[i] to wait for
+      ++ne;
+      if (e_turn >= 0) {
+        const bool w_ok =
+            __all_sync(0xffffffffu, mbar_wait(&turn[i], e_turn & 1, abort_flag, p.wait_limit_ns));
+        if (!w_ok) {
+          if (lane == 0) fail(p.status, abort_flag);
+          ok = false;
+          break;
         }
+      }
+      if (bulk) {
         // 32 columns at a time (the next chunk's load in flight), scaled by
         // 1 / l in pairs, packed to bf16 and written as four 16-byte pieces:
         // chunk k of row r of swizzle atom a sits at position k ^ (r % 8)
@@ -1103,17 +1134,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&stage_full[i]);
       } else {
-        // Direct stores (varlen tail tile, or no row at all); the buffer's
-        // turn is passed on.
-        if (wq == 0 && my_use > 0) {
-          const bool w_ok = __all_sync(
-              0xffffffffu, mbar_wait(stage_free, (my_use - 1) & 1, abort_flag, p.wait_limit_ns));
-          if (!w_ok) {
-            if (lane == 0) fail(p.status, abort_flag);
-            ok = false;
-            break;
-          }
-        }
+        // Direct stores (varlen tail tile, or no row at all): the tile is not
+        // used; the store warp passes the turn on once all four warps have
+        // taken theirs.
+        if (lane == 0) mbar_arrive(&stage_full[i]);
         const size_t orow = p.cu_q ? (static_cast<size_t>(w.q_base + row) * p.Hq + w.h) * D
                                    : ((static_cast<size_t>(w.bseq) * p.Sq + row) * p.Hq + w.h) * D;
 #pragma unroll 1
@@ -1141,13 +1165,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (wq == 0 && lane == 0) mbar_arrive(stage_free);
         __syncwarp();
       }
       if (valid && p.lse != nullptr) {
         const size_t li = p.cu_q ? static_cast<size_t>(w.h) * p.total_q + w.q_base + row
                                  : (static_cast<size_t>(w.bseq) * p.Hq + w.h) * p.Sq + row;
-        p.lse[li] = seen ? fmaf(m_used, p.scale, logf(l)) : -INFINITY;
+        p.lse[li] = lse_row;
       }
       // The next item's first product into O must wait until O has been read:
       // it waits for this warpgroup's next p_half arrival, made after this.
@@ -1176,9 +1199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpLoad) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-// O = 0 and LSE = -inf everywhere: every query sees no key (no keys at all).
+// O = 0 and LSE = -inf (or the head's logit sink) everywhere: every query
+// sees no key (no keys at all).  LSE element e belongs to head
+// (e / lse_inner) % Hq.
 __global__ void attn_fill_empty_kernel(__nv_bfloat16* o, size_t o_elems, float* lse,
-                                       size_t lse_elems) {
+                                       size_t lse_elems, const float* sink, size_t lse_inner,
+                                       int Hq) {
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t e = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; e < o_elems;
        e += stride)
@@ -1186,7 +1212,7 @@ __global__ void attn_fill_empty_kernel(__nv_bfloat16* o, size_t o_elems, float* 
   if (lse)
     for (size_t e = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; e < lse_elems;
          e += stride)
-      lse[e] = -INFINITY;
+      lse[e] = sink ? sink[(e / lse_inner) % static_cast<size_t>(Hq)] : -INFINITY;
 }
 
 template <int D>
@@ -1209,6 +1235,7 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   Params p;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
+  p.sink = a.sink;
   p.cu_q = a.cu_q;
   p.cu_k = a.cu_k;
   p.B = a.B;
@@ -1253,8 +1280,9 @@ cudaError_t launch_attn_fill_empty(const FwdLaunch& a, cudaStream_t stream) {
   const size_t o_elems = rows * a.Hq * a.d;
   const size_t lse_elems = rows * a.Hq;
   if (o_elems == 0) return cudaSuccess;
+  const size_t lse_inner = a.cu_q ? static_cast<size_t>(a.total_q) : static_cast<size_t>(a.Sq);
   attn_fill_empty_kernel<<<1216, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(a.o), o_elems,
-                                                   a.lse, lse_elems);
+                                                   a.lse, lse_elems, a.sink, lse_inner, a.Hq);
   return cudaGetLastError();
 }
 

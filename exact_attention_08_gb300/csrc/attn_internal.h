@@ -22,6 +22,7 @@ struct FwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmO;  // 4-D maps (d, H, S, B) with 64 x 1 x 128 x 1 boxes
   void* o;                    // bf16 output
   float* lse;                 // fp32 log-sum-exp, may be null
+  const float* sink;          // fp32 logit sink per query head [Hq], may be null
   const int* cu_q;            // null: dense layout
   const int* cu_k;
   int B, Hq, Hkv;
@@ -39,6 +40,7 @@ struct DecodeLaunch {
   const void* q;
   void* o;
   float* lse;
+  const float* sink;  // fp32 logit sink per query head [Hq], may be null
   const int* page_table;
   const int* seqlens;
   float* ws_o;    // [B, Hq, S, d] fp32 split outputs (normalised)

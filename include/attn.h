@@ -106,6 +106,31 @@ ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, f
                          float scale, int causal, int window, int n_sink, void* stream);
 
 /*
+ * attn_fwd_ex with a logit sink per query head ("TileLang tutorial, ch.15
+ * Operators: Attention", section 4.6, the attention-sink variant: the sink
+ * adds one term to the softmax denominator).
+ *   sink_logit: DEVICE fp32 array [Hq] (4-byte aligned), or NULL for none
+ *     (then identical to attn_fwd_ex).  sink_logit[h] is a logit sigma_h in
+ *     the units of scale * q.k (natural log) that joins every row of head h
+ *     as one more softmax column with no value row:
+ *       O_i   = sum_j e^(S_ij) V_j / (e^sigma_h + sum_j e^(S_ij))
+ *       LSE_i = ln(e^sigma_h + sum_j e^(S_ij))       (j over visible keys)
+ *     computed against max(sigma_h, max_j S_ij), so a large sigma does not
+ *     overflow.  sigma_h = -inf means no sink for that head; +inf or NaN
+ *     give undefined results.  A row that sees no key gets O = 0 and
+ *     LSE = sigma_h.  The sink does not change which keys are visible; it
+ *     combines freely with causal, window, n_sink (sink keys), GQA and
+ *     varlen.
+ * Other arguments, layouts and results are those of attn_fwd_ex.
+ */
+ATTN_API int attn_fwd_ex_sink(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k,
+                              int B, int Hq, int Hkv, int max_Sq, int max_Skv,
+                              int total_q, int total_k, int d,
+                              float scale, int causal, int window, int n_sink,
+                              const float* sink_logit, void* stream);
+
+/*
  * Bytes of device workspace attn_decode_paged needs for these sizes (split
  * partial outputs and log-sum-exps, fp32).  0 on invalid sizes.
  */
@@ -140,6 +165,24 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v
                                int max_pages_per_seq, int num_pages_total, int num_splits,
                                float scale, void* workspace, size_t workspace_bytes,
                                void* stream);
+
+/*
+ * attn_decode_paged with a logit sink per query head (section 4.6 as for
+ * attn_fwd_ex_sink): sink_logit is a DEVICE fp32 array [Hq] or NULL.  The
+ * sink joins the merge of the split partials as one more denominator term
+ * with no output, M = max(sigma_h, lse_s):
+ *   O = sum_s e^(lse_s - M) O_s / (e^(sigma_h - M) + sum_s e^(lse_s - M)),
+ *   LSE = M + ln(e^(sigma_h - M) + sum_s e^(lse_s - M)),
+ * summed in ascending split order after the sink term.  A request with no
+ * key gets O = 0 and LSE = sigma_h.  Other arguments are those of
+ * attn_decode_paged.
+ */
+ATTN_API int attn_decode_paged_sink(const void* q, const void* k_pages, const void* v_pages,
+                                    const int* page_table, const int* seqlens, void* o,
+                                    float* lse, int B, int Hq, int Hkv, int d, int page_size,
+                                    int max_pages_per_seq, int num_pages_total, int num_splits,
+                                    float scale, const float* sink_logit, void* workspace,
+                                    size_t workspace_bytes, void* stream);
 
 /*
  * attn_decode_paged without a workspace argument: the same decode, for

@@ -209,6 +209,22 @@ def paged_decode_inputs(seed: int, B: int, Hq: int, Hkv: int, d: int, lo: int, h
                              num_splits, 1.0 / math.sqrt(d), seed)
 
 
+def logit_sinks(seed: int, Hq: int, lo: float = 4.0, hi: float = 12.0,
+                extremes: bool = False) -> torch.Tensor:
+    """Per-head logit sinks [Hq] fp32 (CPU), uniform in [lo, hi]: around the
+    log-sum-exp of a row of a few thousand N(0,1)-scaled scores, so the sink
+    takes anything from a few percent to nearly all of each row's weight.
+    extremes: head 0 gets -inf (no sink), head 1 (if any) +100 (e^100
+    overflows fp32: the sink dominates), head 2 (if any) -30 (negligible)."""
+    g = _gen(seed)
+    s = lo + (hi - lo) * torch.rand(Hq, generator=g, dtype=torch.float32)
+    if extremes:
+        for h, val in enumerate((-math.inf, 100.0, -30.0)):
+            if h < Hq:
+                s[h] = val
+    return s
+
+
 # --------------------------------------------------------------------------
 # The measured workloads, by name.  Each entry builds its inputs from a seed.
 # --------------------------------------------------------------------------
