@@ -165,3 +165,18 @@ def test_gqa_varlen_full_size(ea):
         idx = torch.as_tensor(rows.astype(np.int64) + a, device=o.device)
         compare(o.index_select(0, idx)[None], lse.index_select(1, idx)[None], ro, rl,
                 f"varlen seq {s}")
+
+
+def test_varlen_repeated_calls_report_ok(ea):
+    """Packed GQA prefill mixes bulk and direct O stores within one CTA; a
+    hand-off race between them once ended about one call in four in a bounded
+    wait.  Thirty calls in a row must all report ATTN_OK."""
+    x = workloads.gqa_varlen()
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    cu_q, cu_k = x.cu_q.cuda(), x.cu_k.cuda()
+    o, lse = ea.attn_fwd_ex(q, k, v, cu_q, cu_k, max_seqlen_q=x.max_q, max_seqlen_k=x.max_k,
+                            causal=True, scale=x.scale)
+    for rep in range(30):
+        ea.attn_fwd_ex(q, k, v, cu_q, cu_k, max_seqlen_q=x.max_q, max_seqlen_k=x.max_k, o=o,
+                       lse=lse, causal=True, scale=x.scale)
+        assert ea.attn_device_status() == ea.ATTN_OK, f"call {rep}"
