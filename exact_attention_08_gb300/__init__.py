@@ -24,7 +24,7 @@ from . import _build
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT",
     "ATTN_ERR_BAD_INPUT", "AttnError", "attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink",
-    "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout", "attn_status_string",
+    "attn_fwd_paged", "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout", "attn_status_string",
     "attn_last_error", "library_path", "lib",
 ]
 
@@ -51,6 +51,8 @@ def _load() -> ctypes.CDLL:
     L.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, i, i, vp]
     L.attn_fwd_ex_sink.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, i, i,
                                    vp, vp]
+    L.attn_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i,
+                                 i, i, vp, vp]
     L.attn_decode_workspace_size.argtypes = [i, i, i, i]
     L.attn_decode_workspace_size.restype = sz
     L.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, sz,
@@ -63,7 +65,7 @@ def _load() -> ctypes.CDLL:
     L.attn_status_string.restype = ctypes.c_char_p
     L.attn_last_error.argtypes = []
     L.attn_last_error.restype = ctypes.c_char_p
-    for fn in ("attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink", "attn_decode_paged",
+    for fn in ("attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink", "attn_fwd_paged", "attn_decode_paged",
                "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout"):
         getattr(L, fn).restype = ctypes.c_int
     return L
@@ -210,6 +212,51 @@ def _fwd_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, sink_logit, max_seqlen_q, max_s
                                   Tk, d, scale, int(bool(causal)), int(window), int(n_sink),
                                   _ptr(sink_logit), _stream(stream))
         _check(rc, "attn_fwd_ex_sink")
+    return o, lse
+
+
+def attn_fwd_paged(q, k_pages, v_pages, page_table, cu_seqlens_q, seqlens_k, o=None, lse=None, *,
+                   max_seqlen_q=None, causal=True, window=0, n_sink=0, sink_logit=None,
+                   scale=None, stream=None, want_lse=True):
+    """Packed queries q [Tq,Hq,d] bf16 against a paged cache k/v_pages [P,16,Hkv,d];
+    page_table [B,maxP] int32, cu_seqlens_q [B+1] int32, seqlens_k [B] int32 ->
+    o [Tq,Hq,d] bf16, lse [Hq,Tq] fp32.  Causal alignment is to the end of each
+    sequence's keys."""
+    torch = _torch()
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k_pages, "k_pages", torch.bfloat16, dev)
+    _need(v_pages, "v_pages", torch.bfloat16, dev)
+    _need(page_table, "page_table", torch.int32, dev)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, dev)
+    _need(seqlens_k, "seqlens_k", torch.int32, dev)
+    Tq, Hq, d = q.shape
+    P, page, Hkv, dk = k_pages.shape
+    if dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages/v_pages shapes disagree with q")
+    B = seqlens_k.numel()
+    if page_table.dim() != 2 or page_table.shape[0] != B or cu_seqlens_q.numel() != B + 1:
+        raise ValueError("page_table must be [B, max_pages], cu_seqlens_q [B+1], seqlens_k [B]")
+    if max_seqlen_q is None:
+        raise ValueError("max_seqlen_q is required")
+    if o is None:
+        o = torch.empty_like(q)
+    _need(o, "o", torch.bfloat16, dev)
+    if lse is None and want_lse:
+        lse = torch.empty(Hq, Tq, dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    if sink_logit is not None:
+        _need(sink_logit, "sink_logit", torch.float32, dev)
+        if sink_logit.numel() != Hq:
+            raise ValueError(f"sink_logit must hold Hq={Hq} values")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib.attn_fwd_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                            _ptr(cu_seqlens_q), _ptr(seqlens_k), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                            int(max_seqlen_q), Tq, d, page, page_table.shape[1], P, scale,
+                            int(bool(causal)), int(window), int(n_sink), _ptr(sink_logit),
+                            _stream(stream))
+    _check(rc, "attn_fwd_paged")
     return o, lse
 
 

@@ -275,6 +275,80 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
                      causal, window, 0, stream);
 }
 
+ATTN_API int attn_fwd_paged(const void* q, const void* k_pages, const void* v_pages,
+                            const int* page_table, const int* cu_seqlens_q, const int* seqlens_k,
+                            void* o, float* lse, int B, int Hq, int Hkv, int max_Sq, int total_q,
+                            int d, int page_size, int max_pages_per_seq, int num_pages_total,
+                            float scale, int causal, int window, int n_sink,
+                            const float* sink_logit, void* stream) {
+  t_last_error.clear();
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || max_Sq < 0 || total_q < 0 || max_pages_per_seq <= 0 ||
+      num_pages_total <= 0)
+    return set_error(ATTN_ERR_INVALID_ARG, "bad sizes (B=%d Hq=%d Hkv=%d)", B, Hq, Hkv);
+  if (Hq % Hkv != 0)
+    return set_error(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  if (d != 64 && d != 128) return set_error(ATTN_ERR_UNSUPPORTED, "head dim %d (64 or 128)", d);
+  if (page_size != 16) return set_error(ATTN_ERR_UNSUPPORTED, "page size %d (16)", page_size);
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return set_error(ATTN_ERR_INVALID_ARG, "scale must be finite and positive");
+  if (causal != 0 && causal != 1) return set_error(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (window < 0) window = 0;
+  if (window > 0 && !causal)
+    return set_error(ATTN_ERR_INVALID_ARG, "a sliding window requires causal");
+  if (n_sink < 0 || (n_sink > 0 && window == 0))
+    return set_error(ATTN_ERR_INVALID_ARG, "n_sink > 0 requires a window");
+  if (static_cast<long long>(max_pages_per_seq) * page_size > (1 << 30))
+    return set_error(ATTN_ERR_INVALID_ARG, "max_pages_per_seq too large");
+  if (B == 0 || total_q == 0) return ATTN_OK;
+  if (max_Sq == 0) return set_error(ATTN_ERR_INVALID_ARG, "max_Sq must bound the query lengths");
+  if (!q || !o || !k_pages || !v_pages || !page_table || !cu_seqlens_q || !seqlens_k)
+    return set_error(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(o) || !aligned16(k_pages) || !aligned16(v_pages) ||
+      (reinterpret_cast<uintptr_t>(page_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seqlens_k) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(sink_logit) & 3u))
+    return set_error(ATTN_ERR_INVALID_ARG, "misaligned pointer");
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != ATTN_OK) return rc;
+  FwdLaunch a;
+  std::memset(&a, 0, sizeof(a));
+  a.o = o;
+  a.lse = lse;
+  a.sink = sink_logit;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = nullptr;
+  a.page_table = page_table;
+  a.seqlens_k = seqlens_k;
+  a.max_pages = max_pages_per_seq;
+  a.num_pages = num_pages_total;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Sq = max_Sq;
+  a.Skv = max_pages_per_seq * page_size;
+  a.total_q = total_q;
+  a.total_k = 0;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal;
+  a.window = window;
+  a.n_sink = n_sink;
+  a.num_sms = ds->num_sms;
+  a.status = ds->status;
+  if ((rc = make_map(&a.tmQ, q, d, Hq, total_q, 1, 128, "q")) != ATTN_OK) return rc;
+  if ((rc = make_map(&a.tmO, o, d, Hq, total_q, 1, 128, "o")) != ATTN_OK) return rc;
+  if ((rc = make_map(&a.tmK, k_pages, d, Hkv, page_size, num_pages_total, 16, "k_pages")) !=
+      ATTN_OK)
+    return rc;
+  if ((rc = make_map(&a.tmV, v_pages, d, Hkv, page_size, num_pages_total, 16, "v_pages")) !=
+      ATTN_OK)
+    return rc;
+  cudaError_t e = launch_attn_fwd(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_error(e, "attn_fwd_paged launch");
+}
+
 ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
   if (B < 0 || Hq <= 0 || d <= 0 || num_splits <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * num_splits;

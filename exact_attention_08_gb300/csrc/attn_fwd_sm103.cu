@@ -61,6 +61,8 @@ using namespace ptx;
 constexpr int kBM = 128;       // query rows per Q tile (= TMEM lanes)
 constexpr int kQT = 2;         // Q tiles per CTA
 constexpr int kBN = 128;       // keys per K/V tile
+constexpr int kPage = 16;      // keys per page of a paged cache
+constexpr int kPagesPerTile = kBN / kPage;
 constexpr int kThreads = 384;  // 12 warps
 constexpr int kRegsSoftmax = 208;
 constexpr int kRegsOther = 88;
@@ -129,6 +131,9 @@ struct Params {
   const float* sink;  // logit sink per query head [Hq], or null
   const int* cu_q;
   const int* cu_k;
+  const int* page_table;  // paged K/V: [B, max_pages] physical pages, or null
+  const int* seqlens_k;   // paged K/V: key count of every sequence [B]
+  int max_pages, num_pages;
   int B, Hq, Hkv, Sq, Skv, total_q;
   int num_qpairs, num_items;
   FastDiv div_hq, div_b, div_qp, div_group;  // by Hq, B, num_qpairs, Hq / Hkv
@@ -314,7 +319,21 @@ __device__ __forceinline__ bool decode_work(const Params& p, int k, int sinkT, W
     w.h = x - y * p.Hq;
     w.bseq = y;
   }
-  if (p.cu_q != nullptr) {
+  if (p.page_table != nullptr) {
+    // Packed queries against a paged cache: the sequence's keys are its
+    // first seqlens_k[b] cache slots, reached through its page-table row.
+    const int a = p.cu_q[w.bseq], e = p.cu_q[w.bseq + 1];
+    const int lk = p.seqlens_k[w.bseq];
+    if (a < 0 || e < a || e > p.total_q || e - a > p.Sq || lk < 0 || lk > p.max_pages * kPage) {
+      if (report) atomicOr(p.status, kStatusBadInput);
+      return false;
+    }
+    w.Lq = e - a;
+    w.Lk = lk;
+    w.q_base = a;
+    w.k_base = 0;
+    w.b_coord = 0;
+  } else if (p.cu_q != nullptr) {
     const int a = p.cu_q[w.bseq], e = p.cu_q[w.bseq + 1];
     const int ka = p.cu_k[w.bseq], ke = p.cu_k[w.bseq + 1];
     if (a < 0 || e < a || e > p.total_q || ka < 0 || ke < ka || e - a > p.Sq) {
@@ -473,6 +492,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     int u = 0;   // ring tiles loaded
     int nq = 0;  // Q pairs loaded
     bool ok = true;
+    // Key or value tile j of the item into one ring slot (its barrier's
+    // byte count is one whole tile).  Dense and packed layouts: one box of
+    // 128 rows per swizzle atom.  Paged cache: one 16-row box per page; lane
+    // pp looks up the page of rows 16pp.., and pages past the sequence's
+    // last are replaced by that last page (their rows are masked).  A page
+    // index outside the pool is reported and page 0 read instead.
+    auto load_kv = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, const Work& w, int j) {
+      if (p.page_table == nullptr) {
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_4d_w(dst + a * C::kAtomBytes, map, bar, a * 64, w.hk, w.k_base + j * kBN,
+                        w.b_coord);
+        return;
+      }
+      int phys = 0;
+      if (lane < kPagesPerTile) {
+        const int np = (w.Lk + kPage - 1) / kPage;
+        const int lp = min(j * kPagesPerTile + lane, np - 1);
+        phys = p.page_table[static_cast<size_t>(w.bseq) * p.max_pages + lp];
+        if (phys < 0 || phys >= p.num_pages) {
+          atomicOr(p.status, kStatusBadInput);
+          phys = 0;
+        }
+      }
+#pragma unroll
+      for (int pp = 0; pp < kPagesPerTile; ++pp) {
+        const int pg = __shfl_sync(0xffffffffu, phys, pp);
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_4d_w(dst + a * C::kAtomBytes + pp * kPage * 128, map, bar, a * 64, w.hk, 0, pg);
+      }
+    };
     for (int n = 0; ok; ++n) {
       const int k = item_of(n, p.num_items);
       if (k < 0) break;
@@ -525,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++jp;
             if (in_range(w.r0, jp, sinkT) || in_range(w.r1, jp, sinkT)) ++ahead;
           }
-          if (ahead == kPrefetch) {
+          if (ahead == kPrefetch && p.page_table == nullptr) {
 #pragma unroll
             for (int a = 0; a < C::kAtoms; ++a) {
               tma_prefetch_4d_w(&tmK, a * 64, w.hk, w.k_base + jp * kBN, w.b_coord);
@@ -534,10 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mbar_arrive_expect_tx_w(&k_full[s], C::kTileBytes);
-#pragma unroll
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_4d_w(sK + s * C::kTileBytes + a * C::kAtomBytes, &tmK, &k_full[s], a * 64,
-                        w.hk, w.k_base + j * kBN, w.b_coord);
+        load_kv(&tmK, sK + s * C::kTileBytes, &k_full[s], w, j);
         if (u >= ST && !mbar_wait_warp(&step[(u + 1) % ST], (((u + 1) / ST) - 1) & 1, abort_flag,
                                        p.wait_limit_ns)) {
           if (lane == 0) fail(p.status, abort_flag);
@@ -545,10 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx_w(&v_full[s], C::kTileBytes);
-#pragma unroll
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_4d_w(sV + s * C::kTileBytes + a * C::kAtomBytes, &tmV, &v_full[s], a * 64,
-                        w.hk, w.k_base + j * kBN, w.b_coord);
+        load_kv(&tmV, sV + s * C::kTileBytes, &v_full[s], w, j);
         ++u;
       }
     }
@@ -1238,6 +1283,10 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   p.sink = a.sink;
   p.cu_q = a.cu_q;
   p.cu_k = a.cu_k;
+  p.page_table = a.page_table;
+  p.seqlens_k = a.seqlens_k;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
   p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;

@@ -25,6 +25,9 @@ struct FwdLaunch {
   const float* sink;          // fp32 logit sink per query head [Hq], may be null
   const int* cu_q;            // null: dense layout
   const int* cu_k;
+  const int* page_table;      // paged K/V [B, max_pages], or null
+  const int* seqlens_k;       // paged K/V key counts [B]
+  int max_pages, num_pages;
   int B, Hq, Hkv;
   int Sq, Skv;                // dense sizes, or the maxima for varlen
   int total_q, total_k;       // varlen totals (dense: unused)

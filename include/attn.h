@@ -131,6 +131,39 @@ ATTN_API int attn_fwd_ex_sink(const void* q, const void* k, const void* v, void*
                               const float* sink_logit, void* stream);
 
 /*
+ * Packed queries against a paged KV cache: chunked prefill, or several new
+ * tokens per request (speculative decoding) ("TileLang tutorial, ch.15",
+ * sections 3.4(2) and 5.3: the causal diagonal of a query block that ends at
+ * the cache's end, past_len = keys - queries; section 4.6 for the paged
+ * addressing of the decode variant, here with query blocks).
+ *   q, o       [total_q, Hq, d] bf16, sequence b's queries at rows
+ *              cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 (DEVICE int32 [B+1])
+ *   lse        [Hq, total_q] fp32 (out, may be NULL)
+ *   k_pages, v_pages [num_pages_total, page_size, Hkv, d] bf16 (page_size 16)
+ *   page_table [B, max_pages_per_seq] int32, seqlens_k [B] int32 (DEVICE):
+ *              sequence b's keys are its first seqlens_k[b] cache slots, slot
+ *              t in physical page page_table[b][t / 16], row t % 16.
+ *   causal: query i of sequence b (0-based in its block of Lq_b rows) sees
+ *     keys j <= i + (seqlens_k[b] - Lq_b); rows with no key (Lq_b >
+ *     seqlens_k[b]) get O = 0, LSE = -inf (or the sink).  window, n_sink and
+ *     sink_logit (may be NULL) as in attn_fwd_ex / attn_fwd_ex_sink.
+ *   Slots of a sequence's last page past seqlens_k[b] are read and given
+ *   weight zero, so they must hold finite values.  Page-table entries past
+ *   ceil(seqlens_k[b] / 16) are never read; an entry outside
+ *   [0, num_pages_total) is not dereferenced: page 0 is read instead and
+ *   ATTN_ERR_BAD_INPUT is set in the device status.  Sequence offsets that
+ *   decrease, exceed total_q or max_Sq, or key counts above
+ *   max_pages_per_seq * 16, likewise set ATTN_ERR_BAD_INPUT and that
+ *   sequence is skipped.
+ */
+ATTN_API int attn_fwd_paged(const void* q, const void* k_pages, const void* v_pages,
+                            const int* page_table, const int* cu_seqlens_q, const int* seqlens_k,
+                            void* o, float* lse, int B, int Hq, int Hkv, int max_Sq, int total_q,
+                            int d, int page_size, int max_pages_per_seq, int num_pages_total,
+                            float scale, int causal, int window, int n_sink,
+                            const float* sink_logit, void* stream);
+
+/*
  * Bytes of device workspace attn_decode_paged needs for these sizes (split
  * partial outputs and log-sum-exps, fp32).  0 on invalid sizes.
  */

@@ -209,6 +209,42 @@ def paged_decode_inputs(seed: int, B: int, Hq: int, Hkv: int, d: int, lo: int, h
                              num_splits, 1.0 / math.sqrt(d), seed)
 
 
+@dataclass
+class PagedPrefillInputs:
+    """Packed queries q [Tq,Hq,d] with cu_q [B+1] against the paged cache of
+    ``cache`` (its k_flat/v_flat [Tk,Hkv,d] with cu_kv [B+1] are the same keys
+    contiguously, for the oracle)."""
+    q: torch.Tensor
+    cu_q: torch.Tensor
+    max_q: int
+    cache: "PagedDecodeInputs"
+    scale: float
+    seed: int
+
+
+def paged_prefill_inputs(seed: int, B: int, Hq: int, Hkv: int, d: int, lk_lo: int, lk_hi: int,
+                         lq_lo: int, lq_hi: int, lengths_k: list[int] | None = None,
+                         lengths_q: list[int] | None = None) -> PagedPrefillInputs:
+    """A paged cache as for decode (key counts uniform in [lk_lo, lk_hi] unless
+    given, pages in a seeded random permutation, junk in unused slots), then
+    per sequence a block of query rows, lengths uniform in [lq_lo, lq_hi]
+    unless given, drawn from a second generator seeded seed + 500."""
+    cache = paged_decode_inputs(seed, B, Hq, Hkv, d, lk_lo, lk_hi, lengths=lengths_k)
+    g = _gen(seed + 500)
+    if lengths_q is None:
+        lengths_q = torch.randint(lq_lo, lq_hi + 1, (B,), generator=g).tolist()
+    cu_q = torch.tensor([0] + list(_cumsum(lengths_q)), dtype=torch.int32)
+    q = _randn_bf16(g, (int(cu_q[-1]), Hq, d))
+    return PagedPrefillInputs(q, cu_q, max(lengths_q) if lengths_q else 0, cache,
+                              1.0 / math.sqrt(d), seed)
+
+
+def chunked_prefill():
+    """Chunked prefill on a paged cache: B=8, Hq=32, Hkv=8, d=128, cache lengths
+    uniform in [2048, 8192], the last 512 tokens of each as the query block."""
+    return paged_prefill_inputs(6001, 8, 32, 8, 128, 2048, 8192, 512, 512)
+
+
 def logit_sinks(seed: int, Hq: int, lo: float = 4.0, hi: float = 12.0,
                 extremes: bool = False) -> torch.Tensor:
     """Per-head logit sinks [Hq] fp32 (CPU), uniform in [lo, hi]: around the
