@@ -394,6 +394,33 @@ def main():
     torch.cuda.synchronize(dev)
     if ea.attn_device_status(stream) != ea.ATTN_OK:
         raise RuntimeError("device status reported an error in the logit-sink calls")
+    # chunked prefill on a paged cache (512-row query blocks at the end of
+    # 2048-8192-key caches), same protocol
+    cx = workloads.chunked_prefill()
+    cc = cx.cache
+    cq, ckp, cvp = cx.q.to(dev), cc.k_pages.to(dev), cc.v_pages.to(dev)
+    cpt, ccu, csl = cc.page_table.to(dev), cx.cu_q.to(dev), cc.seqlens.to(dev)
+    co = torch.empty_like(cq)
+    clse = torch.empty(cq.shape[1], cq.shape[0], dtype=torch.float32, device=dev)
+    lqs = (cx.cu_q[1:] - cx.cu_q[:-1]).tolist()
+    lks = cc.seqlens.tolist()
+    c_pairs = sum(lq * (lk - lq) + lq * (lq + 1) // 2 for lq, lk in zip(lqs, lks))
+    c_flops = 4.0 * cq.shape[2] * cq.shape[1] * c_pairs
+    t_cp = []
+    for it in range(23):
+        with torch.cuda.stream(stream):
+            flush.fill_(3)
+            a, b = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+            a.record(stream)
+            ea.attn_fwd_paged(cq, ckp, cvp, cpt, ccu, csl, co, clse, max_seqlen_q=cx.max_q,
+                              causal=True, scale=cx.scale, stream=stream)
+            b.record(stream)
+        if it >= 3:
+            t_cp.append((a, b))
+    torch.cuda.synchronize(dev)
+    if ea.attn_device_status(stream) != ea.ATTN_OK:
+        raise RuntimeError("device status reported an error in the paged-prefill calls")
+    cp_ms = statistics.median(a.elapsed_time(b) for a, b in t_cp)
     sp_ms = statistics.median(a.elapsed_time(b) for a, b in t_sp)
     sd_ms = statistics.median(a.elapsed_time(b) for a, b in t_sd)
     variants = {"logit_sink": {
@@ -401,7 +428,13 @@ def main():
         "decode_ms": sd_ms, "decode_kv_gbs": kv_bytes / (sd_ms / 1e3) / 1e9,
         "same_calls_without_sink_ms": {"prefill_noncausal": statistics.median(t_nc),
                                        "decode": statistics.median(t_dec)},
-        "note": "20 calls each after 3 warm-up calls, L2 flushed before each; not in value"}}
+        "note": "20 calls each after 3 warm-up calls, L2 flushed before each; not in value"},
+        "chunked_prefill_paged": {
+            "workload": "B=8 Hq=32 Hkv=8 d=128 bf16, cache 2048-8192 keys in 16-key pages, "
+                        "last 512 tokens as the causal query block",
+            "ms": cp_ms, "flops": c_flops, "tflops": c_flops / (cp_ms / 1e3) / 1e12,
+            "note": "visible (query, key) pairs x 4d; 20 calls after 3 warm-up calls, "
+                    "L2 flushed before each; not in value"}}
 
     if rank == 0:
         achieved = (f_nc + f_c) * K / (tot_pre / 1e3) / 1e12

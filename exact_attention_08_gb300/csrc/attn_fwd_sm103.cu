@@ -305,6 +305,7 @@ struct Work {
 // of every head come first.  Heads of one KV group are adjacent either way.
 // Returns false when the item has no query rows or its sequence offsets are
 // invalid (reported once, by the caller that passes report).
+template <bool kPagedKV>
 __device__ __forceinline__ bool decode_work(const Params& p, int k, int sinkT, Work& w,
                                             bool report) {
   int qp;
@@ -319,7 +320,7 @@ __device__ __forceinline__ bool decode_work(const Params& p, int k, int sinkT, W
     w.h = x - y * p.Hq;
     w.bseq = y;
   }
-  if (p.page_table != nullptr) {
+  if (kPagedKV) {
     // Packed queries against a paged cache: the sequence's keys are its
     // first seqlens_k[b] cache slots, reached through its page-table row.
     const int a = p.cu_q[w.bseq], e = p.cu_q[w.bseq + 1];
@@ -391,7 +392,7 @@ __device__ __forceinline__ int item_of(int n, int num_items) {
   return k < num_items ? static_cast<int>(k) : -1;
 }
 
-template <int D>
+template <int D, bool kPagedKV>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -499,13 +500,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // last are replaced by that last page (their rows are masked).  A page
     // index outside the pool is reported and page 0 read instead.
     auto load_kv = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, const Work& w, int j) {
-      if (p.page_table == nullptr) {
+      if constexpr (!kPagedKV) {
 #pragma unroll
         for (int a = 0; a < C::kAtoms; ++a)
           tma_load_4d_w(dst + a * C::kAtomBytes, map, bar, a * 64, w.hk, w.k_base + j * kBN,
                         w.b_coord);
         return;
-      }
+      } else {
       int phys = 0;
       if (lane < kPagesPerTile) {
         const int np = (w.Lk + kPage - 1) / kPage;
@@ -523,12 +524,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < C::kAtoms; ++a)
           tma_load_4d_w(dst + a * C::kAtomBytes + pp * kPage * 128, map, bar, a * 64, w.hk, 0, pg);
       }
+      }
     };
     for (int n = 0; ok; ++n) {
       const int k = item_of(n, p.num_items);
       if (k < 0) break;
       Work w;
-      if (!decode_work(p, k, sinkT, w, lane == 0) || w.lastT < 0) continue;
+      if (!decode_work<kPagedKV>(p, k, sinkT, w, lane == 0) || w.lastT < 0) continue;
       // The Q buffers are free once every S of the previous pair is done:
       // its last key step, u - 1.
       if (nq > 0 &&
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int k2 = item_of(n + 1, p.num_items);
         Work w2;
-        if (k2 >= 0 && decode_work(p, k2, sinkT, w2, false) && w2.lastT >= 0) {
+        if (k2 >= 0 && decode_work<kPagedKV>(p, k2, sinkT, w2, false) && w2.lastT >= 0) {
 #pragma unroll
           for (int i = 0; i < kQT; ++i)
 #pragma unroll
@@ -576,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++jp;
             if (in_range(w.r0, jp, sinkT) || in_range(w.r1, jp, sinkT)) ++ahead;
           }
-          if (ahead == kPrefetch && p.page_table == nullptr) {
+          if (ahead == kPrefetch && !kPagedKV) {
 #pragma unroll
             for (int a = 0; a < C::kAtoms; ++a) {
               tma_prefetch_4d_w(&tmK, a * 64, w.hk, w.k_base + jp * kBN, w.b_coord);
@@ -689,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k = item_of(n, p.num_items);
       if (k < 0) break;
       Work w;
-      if (!decode_work(p, k, sinkT, w, false) || w.lastT < 0) continue;
+      if (!decode_work<kPagedKV>(p, k, sinkT, w, false) || w.lastT < 0) continue;
       if (!flush()) {
         ok = false;
         break;
@@ -783,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k = item_of(n, p.num_items);
       if (k < 0) break;
       Work w;
-      if (!decode_work(p, k, sinkT, w, false)) continue;
+      if (!decode_work<kPagedKV>(p, k, sinkT, w, false)) continue;
 #pragma unroll 1
       for (int i = 0; i < kQT; ++i) {
         int& nb = i ? nb1 : nb0;
@@ -835,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int hi_row, lo_row;
       {
         Work w;
-        if (!decode_work(p, k, sinkT, w, false)) continue;
+        if (!decode_work<kPagedKV>(p, k, sinkT, w, false)) continue;
         const int row = w.q0 + i * kBM + r;  // sequence-relative query index
         hi_row = p.causal ? min(row + w.off, w.Lk - 1) : w.Lk - 1;
         lo_row = (p.window > 0) ? row + w.off - p.window : kNoLowerBound;
@@ -1072,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---------------------------------------------------------------- epilogue
       Work w;
-      decode_work(p, k, sinkT, w, false);
+      decode_work<kPagedKV>(p, k, sinkT, w, false);
       const int row = w.q0 + i * kBM + r;
       const bool valid = row < w.Lq;
       bool have_o = t_item > 0;
@@ -1266,15 +1268,18 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_fwd_kernel<D>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (attr_err != cudaSuccess) return;
-    // setmaxnreg.inc waits for registers the block was launched with: never
-    // launch a build whose register count cannot cover the split.
-    cudaFuncAttributes fa;
-    attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D>);
-    if (attr_err == cudaSuccess && fa.numRegs * kThreads < kRegsSplit)
-      attr_err = cudaErrorInvalidConfiguration;
+    for (auto fn : {attn_fwd_kernel<D, false>, attn_fwd_kernel<D, true>}) {
+      attr_err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      C::kSmemBytes);
+      if (attr_err != cudaSuccess) return;
+      // setmaxnreg.inc waits for registers the block was launched with:
+      // never launch a build whose register count cannot cover the split.
+      cudaFuncAttributes fa;
+      attr_err = cudaFuncGetAttributes(&fa, fn);
+      if (attr_err == cudaSuccess && fa.numRegs * kThreads < kRegsSplit)
+        attr_err = cudaErrorInvalidConfiguration;
+      if (attr_err != cudaSuccess) return;
+    }
   });
   if (attr_err != cudaSuccess) return attr_err;
   Params p;
@@ -1312,7 +1317,14 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   // Persistent: one CTA per SM (shared and tensor memory hold one), each
   // walking its share of the items.
   const int grid = static_cast<int>(std::min<long long>(items, std::max(a.num_sms, 1)));
-  attn_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK, a.tmV, a.tmO, p);
+  // The paged cache has an instantiation of its own, so that the dense and
+  // packed kernels' code is not touched by its page lookups.
+  if (a.page_table != nullptr)
+    attn_fwd_kernel<D, true><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK, a.tmV,
+                                                                       a.tmO, p);
+  else
+    attn_fwd_kernel<D, false><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK, a.tmV,
+                                                                        a.tmO, p);
   return cudaGetLastError();
 }
 
