@@ -24,7 +24,7 @@ from . import _build
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT",
     "ATTN_ERR_BAD_INPUT", "AttnError", "attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink",
-    "attn_fwd_paged", "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout", "attn_status_string",
+    "attn_fwd_paged", "attn_fwd_strided", "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout", "attn_status_string",
     "attn_last_error", "library_path", "lib",
 ]
 
@@ -53,6 +53,9 @@ def _load() -> ctypes.CDLL:
                                    vp, vp]
     L.attn_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i,
                                  i, i, vp, vp]
+    i64p = ctypes.POINTER(ctypes.c_longlong)
+    L.attn_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i64p, i64p, i64p, i64p, f,
+                                   i, i, i, vp, vp]
     L.attn_decode_workspace_size.argtypes = [i, i, i, i]
     L.attn_decode_workspace_size.restype = sz
     L.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, sz,
@@ -65,7 +68,8 @@ def _load() -> ctypes.CDLL:
     L.attn_status_string.restype = ctypes.c_char_p
     L.attn_last_error.argtypes = []
     L.attn_last_error.restype = ctypes.c_char_p
-    for fn in ("attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink", "attn_fwd_paged", "attn_decode_paged",
+    for fn in ("attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink", "attn_fwd_paged", "attn_fwd_strided",
+               "attn_decode_paged",
                "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout"):
         getattr(L, fn).restype = ctypes.c_int
     return L
@@ -257,6 +261,47 @@ def attn_fwd_paged(q, k_pages, v_pages, page_table, cu_seqlens_q, seqlens_k, o=N
                             int(bool(causal)), int(window), int(n_sink), _ptr(sink_logit),
                             _stream(stream))
     _check(rc, "attn_fwd_paged")
+    return o, lse
+
+
+def attn_fwd_strided(q, k, v, o=None, lse=None, *, causal=False, window=0, n_sink=0,
+                     sink_logit=None, scale=None, stream=None, want_lse=True):
+    """Dense forward on q [B,Sq,Hq,d], k/v [B,Skv,Hkv,d] of any strides with d
+    contiguous (a BHSD tensor passed as ``t.transpose(1, 2)``, for instance).
+    o defaults to ``empty_like(q)`` (same layout); lse is [B,Hq,Sq] contiguous."""
+    torch = _torch()
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise ValueError(f"{n} must be a bf16 CUDA tensor")
+        if t.dim() != 4 or t.stride(3) != 1:
+            raise ValueError(f"{n} must be 4-D with a contiguous last dimension")
+    B, Sq, Hq, d = q.shape
+    Bk, Skv, Hkv, dk = k.shape
+    if Bk != B or dk != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q/k/v shapes disagree")
+    if o is None:
+        o = torch.empty_like(q)
+    if o.dtype != torch.bfloat16 or tuple(o.shape) != tuple(q.shape) or o.stride(3) != 1:
+        raise ValueError("o must be bf16, shaped like q, with a contiguous last dimension")
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    if sink_logit is not None:
+        _need(sink_logit, "sink_logit", torch.float32, dev)
+        if sink_logit.numel() != Hq:
+            raise ValueError(f"sink_logit must hold Hq={Hq} values")
+
+    def strides(t):
+        return (ctypes.c_longlong * 3)(t.stride(0), t.stride(1), t.stride(2))
+
+    sq, sk, sv, so = strides(q), strides(k), strides(v), strides(o)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib.attn_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv,
+                              d, sq, sk, sv, so, scale, int(bool(causal)), int(window),
+                              int(n_sink), _ptr(sink_logit), _stream(stream))
+    _check(rc, "attn_fwd_strided")
     return o, lse
 
 

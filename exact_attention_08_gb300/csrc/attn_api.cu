@@ -96,12 +96,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 4-D bf16 tensor (d, n1, n2, n3), innermost first, contiguous; box
 // 64 x 1 x box2 x 1 with the 128-byte swizzle.
+// s1, s2, s3: strides of dimensions 1..3 in elements (0: contiguous).
 int make_map(CUtensorMap* m, const void* ptr, uint64_t d, uint64_t n1, uint64_t n2, uint64_t n3,
-             uint32_t box2, const char* what) {
+             uint32_t box2, const char* what, uint64_t s1 = 0, uint64_t s2 = 0, uint64_t s3 = 0) {
   auto fn = encode_fn();
   if (!fn) return set_error(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   cuuint64_t dims[4] = {d, n1, n2, n3};
-  cuuint64_t strides[3] = {d * 2, n1 * d * 2, n2 * n1 * d * 2};
+  if (s1 == 0) s1 = d;
+  if (s2 == 0) s2 = n1 * d;
+  if (s3 == 0) s3 = n2 * n1 * d;
+  cuuint64_t strides[3] = {s1 * 2, s2 * 2, s3 * 2};
   cuuint32_t box[4] = {64, 1, box2, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides,
@@ -173,10 +177,19 @@ namespace {
 
 // Every forward entry point: checks, tensor maps, launch.  sink: per-head
 // logit sink [Hq] (device, fp32) or null.
+// Strides (host arrays of batch, row and head strides in elements, d
+// contiguous), null for the contiguous layout; dense calls only.
+struct Strides {
+  const long long* q = nullptr;
+  const long long* k = nullptr;
+  const long long* v = nullptr;
+  const long long* o = nullptr;
+};
+
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
              const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq, int Hkv, int max_Sq,
              int max_Skv, int total_q, int total_k, int d, float scale, int causal, int window,
-             int n_sink, const float* sink, void* stream) {
+             int n_sink, const float* sink, void* stream, const Strides& st_in = Strides()) {
   t_last_error.clear();
   const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
   if (varlen && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr))
@@ -205,6 +218,28 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
     return set_error(ATTN_ERR_INVALID_ARG,
                      "tensors must be 16-byte aligned (lse and sink 4-byte)");
   if (varlen && max_Sq == 0) return set_error(ATTN_ERR_INVALID_ARG, "max_Sq must bound the lengths");
+  // batch, row, head strides of every tensor (elements)
+  long long str[4][3];
+  {
+    const long long* given[4] = {st_in.q, st_in.k, st_in.v, st_in.o};
+    const long long H[4] = {Hq, Hkv, Hkv, Hq};
+    const long long S[4] = {max_Sq, max_Skv, max_Skv, max_Sq};
+    for (int t = 0; t < 4; ++t) {
+      if (given[t] == nullptr) {
+        str[t][2] = d;
+        str[t][1] = H[t] * d;
+        str[t][0] = S[t] * H[t] * d;
+        continue;
+      }
+      if (varlen) return set_error(ATTN_ERR_INVALID_ARG, "strides apply to the dense layout only");
+      for (int x = 0; x < 3; ++x) {
+        str[t][x] = given[t][x];
+        if (str[t][x] <= 0 || (str[t][x] % 8) != 0)
+          return set_error(ATTN_ERR_INVALID_ARG,
+                           "strides must be positive multiples of 8 elements (16 bytes)");
+      }
+    }
+  }
 
   DeviceState* ds = nullptr;
   int rc = device_state(&ds);
@@ -232,6 +267,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
   a.n_sink = n_sink;
   a.num_sms = ds->num_sms;
   a.status = ds->status;
+  a.o_sb = varlen ? 0 : str[3][0];
+  a.o_ss = varlen ? static_cast<long long>(Hq) * d : str[3][1];
+  a.o_sh = varlen ? d : str[3][2];
   if (rows_k == 0) {
     cudaError_t e = launch_attn_fill_empty(a, st);
     return e == cudaSuccess ? ATTN_OK : cuda_error(e, "fill launch");
@@ -239,10 +277,23 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
   const uint64_t sq = varlen ? static_cast<uint64_t>(total_q) : static_cast<uint64_t>(max_Sq);
   const uint64_t sk = varlen ? static_cast<uint64_t>(total_k) : static_cast<uint64_t>(max_Skv);
   const uint64_t nb = varlen ? 1u : static_cast<uint64_t>(B);
-  if ((rc = make_map(&a.tmQ, q, d, Hq, sq, nb, 128, "q")) != ATTN_OK) return rc;
-  if ((rc = make_map(&a.tmK, k, d, Hkv, sk, nb, 128, "k")) != ATTN_OK) return rc;
-  if ((rc = make_map(&a.tmV, v, d, Hkv, sk, nb, 128, "v")) != ATTN_OK) return rc;
-  if ((rc = make_map(&a.tmO, o, d, Hq, sq, nb, 128, "o")) != ATTN_OK) return rc;
+  if (varlen) {
+    if ((rc = make_map(&a.tmQ, q, d, Hq, sq, nb, 128, "q")) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.tmK, k, d, Hkv, sk, nb, 128, "k")) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.tmV, v, d, Hkv, sk, nb, 128, "v")) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.tmO, o, d, Hq, sq, nb, 128, "o")) != ATTN_OK) return rc;
+  } else {
+    const void* ptr[4] = {q, k, v, o};
+    CUtensorMap* map[4] = {&a.tmQ, &a.tmK, &a.tmV, &a.tmO};
+    const uint64_t H[4] = {static_cast<uint64_t>(Hq), static_cast<uint64_t>(Hkv),
+                           static_cast<uint64_t>(Hkv), static_cast<uint64_t>(Hq)};
+    const uint64_t S[4] = {sq, sk, sk, sq};
+    const char* nm[4] = {"q", "k", "v", "o"};
+    for (int t = 0; t < 4; ++t)
+      if ((rc = make_map(map[t], ptr[t], d, H[t], S[t], nb, 128, nm[t], str[t][2], str[t][1],
+                         str[t][0])) != ATTN_OK)
+        return rc;
+  }
   cudaError_t e = launch_attn_fwd(a, st);
   return e == cudaSuccess ? ATTN_OK : cuda_error(e, "attn_fwd launch");
 }
@@ -273,6 +324,21 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
                       void* stream) {
   return attn_fwd_ex(q, k, v, o, lse, nullptr, nullptr, B, Hq, Hkv, Sq, Skv, 0, 0, d, scale,
                      causal, window, 0, stream);
+}
+
+ATTN_API int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                              const long long* q_strides, const long long* k_strides,
+                              const long long* v_strides, const long long* o_strides, float scale,
+                              int causal, int window, int n_sink, const float* sink_logit,
+                              void* stream) {
+  Strides st;
+  st.q = q_strides;
+  st.k = k_strides;
+  st.v = v_strides;
+  st.o = o_strides;
+  return fwd_impl(q, k, v, o, lse, nullptr, nullptr, B, Hq, Hkv, Sq, Skv, 0, 0, d, scale, causal,
+                  window, n_sink, sink_logit, stream, st);
 }
 
 ATTN_API int attn_fwd_paged(const void* q, const void* k_pages, const void* v_pages,

@@ -1249,13 +1249,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 // O = 0 and LSE = -inf (or the head's logit sink) everywhere: every query
 // sees no key (no keys at all).  LSE element e belongs to head
 // (e / lse_inner) % Hq.
+// O element e of row r = b * lse_inner + s, head h, column t lives at
+// b * sb + s * ss + h * sh + t (the caller's strides, in elements).
 __global__ void attn_fill_empty_kernel(__nv_bfloat16* o, size_t o_elems, float* lse,
                                        size_t lse_elems, const float* sink, size_t lse_inner,
-                                       int Hq) {
+                                       int Hq, int d, long long sb, long long ss, long long sh) {
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t e = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; e < o_elems;
-       e += stride)
-    o[e] = __float2bfloat16(0.f);
+       e += stride) {
+    const size_t t = e % static_cast<size_t>(d), hr = e / static_cast<size_t>(d);
+    const size_t h = hr % static_cast<size_t>(Hq), r = hr / static_cast<size_t>(Hq);
+    const size_t b = r / lse_inner, sq = r % lse_inner;
+    o[b * sb + sq * ss + h * sh + t] = __float2bfloat16(0.f);
+  }
   if (lse)
     for (size_t e = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; e < lse_elems;
          e += stride)
@@ -1343,7 +1349,8 @@ cudaError_t launch_attn_fill_empty(const FwdLaunch& a, cudaStream_t stream) {
   if (o_elems == 0) return cudaSuccess;
   const size_t lse_inner = a.cu_q ? static_cast<size_t>(a.total_q) : static_cast<size_t>(a.Sq);
   attn_fill_empty_kernel<<<1216, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(a.o), o_elems,
-                                                   a.lse, lse_elems, a.sink, lse_inner, a.Hq);
+                                                   a.lse, lse_elems, a.sink, lse_inner, a.Hq, a.d,
+                                                   a.o_sb, a.o_ss, a.o_sh);
   return cudaGetLastError();
 }
 

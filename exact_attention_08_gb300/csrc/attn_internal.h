@@ -28,6 +28,7 @@ struct FwdLaunch {
   const int* page_table;      // paged K/V [B, max_pages], or null
   const int* seqlens_k;       // paged K/V key counts [B]
   int max_pages, num_pages;
+  long long o_sb, o_ss, o_sh;  // O strides (elements) of batch, row and head; d contiguous
   int B, Hq, Hkv;
   int Sq, Skv;                // dense sizes, or the maxima for varlen
   int total_q, total_k;       // varlen totals (dense: unused)

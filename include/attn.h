@@ -131,6 +131,28 @@ ATTN_API int attn_fwd_ex_sink(const void* q, const void* k, const void* v, void*
                               const float* sink_logit, void* stream);
 
 /*
+ * Dense forward on tensors of any layout whose head dimension is contiguous,
+ * e.g. BHSD ([B, H, S, d]) as well as BSHD ("TileLang tutorial, ch.15",
+ * section 4.6: the two layouts differ only in index order; what matters is
+ * that the copied dimension is contiguous).
+ *   q_strides, k_strides, v_strides, o_strides: HOST arrays of three int64
+ *     strides in elements, {batch, sequence row, head}, of q [B, Sq, Hq, d],
+ *     k/v [B, Skv, Hkv, d] and o [B, Sq, Hq, d] indexed in that order; the d
+ *     elements of a row are contiguous.  NULL means the contiguous BSHD
+ *     strides of attn_fwd.  Every stride must be a positive multiple of 8
+ *     elements (16 bytes); the tensor-map encoder may reject others
+ *     (ATTN_ERR_INVALID_ARG).  o must not overlap itself or the inputs.
+ *   lse stays [B, Hq, Sq] contiguous (may be NULL); sink_logit as in
+ *   attn_fwd_ex_sink (may be NULL).  Other arguments as in attn_fwd_ex.
+ */
+ATTN_API int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                              const long long* q_strides, const long long* k_strides,
+                              const long long* v_strides, const long long* o_strides,
+                              float scale, int causal, int window, int n_sink,
+                              const float* sink_logit, void* stream);
+
+/*
  * Packed queries against a paged KV cache: chunked prefill, or several new
  * tokens per request (speculative decoding) ("TileLang tutorial, ch.15",
  * sections 3.4(2) and 5.3: the causal diagonal of a query block that ends at
