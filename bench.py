@@ -421,6 +421,23 @@ def main():
     if ea.attn_device_status(stream) != ea.ATTN_OK:
         raise RuntimeError("device status reported an error in the paged-prefill calls")
     cp_ms = statistics.median(a.elapsed_time(b) for a, b in t_cp)
+    # the non-causal prefill of the step with BHSD-stored q, k, v and o
+    qb, kb, vb = (t.transpose(1, 2).contiguous().transpose(1, 2) for t in (q, k, v))
+    ob = torch.empty_like(qb)
+    t_bh = []
+    for it in range(23):
+        with torch.cuda.stream(stream):
+            flush.fill_(4)
+            a, b = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+            a.record(stream)
+            ea.attn_fwd_strided(qb, kb, vb, ob, lse, causal=False, scale=x.scale, stream=stream)
+            b.record(stream)
+        if it >= 3:
+            t_bh.append((a, b))
+    torch.cuda.synchronize(dev)
+    if ea.attn_device_status(stream) != ea.ATTN_OK:
+        raise RuntimeError("device status reported an error in the strided calls")
+    bh_ms = statistics.median(a.elapsed_time(b) for a, b in t_bh)
     sp_ms = statistics.median(a.elapsed_time(b) for a, b in t_sp)
     sd_ms = statistics.median(a.elapsed_time(b) for a, b in t_sd)
     variants = {"logit_sink": {
@@ -429,6 +446,10 @@ def main():
         "same_calls_without_sink_ms": {"prefill_noncausal": statistics.median(t_nc),
                                        "decode": statistics.median(t_dec)},
         "note": "20 calls each after 3 warm-up calls, L2 flushed before each; not in value"},
+        "prefill_noncausal_bhsd": {
+            "ms": bh_ms, "tflops": f_nc / (bh_ms / 1e3) / 1e12,
+            "note": "the step's non-causal prefill with q, k, v, o stored BHSD "
+                    "(attn_fwd_strided); 20 calls after 3 warm-up calls, L2 flushed before each"},
         "chunked_prefill_paged": {
             "workload": "B=8 Hq=32 Hkv=8 d=128 bf16, cache 2048-8192 keys in 16-key pages, "
                         "last 512 tokens as the causal query block",
