@@ -61,10 +61,11 @@ def _load():
                                                       i, i, _D, _D]
             lib.oracle_decode_split.argtypes = [_D, _D, _D, _I, _D, _D, i, i, i, i, i, d, i, i]
             lib.oracle_combine.argtypes = [_D, _D, _D, _D, ctypes.c_long, i, i, _D]
+            lib.oracle_attn_bwd.argtypes = [_D, _D, _D, _D, _D, _D, _D, i, i, i, i, i, i, d, i, i, i]
             lib.oracle_num_threads.argtypes = []
             for f in ("oracle_attn_fwd", "oracle_attn_fwd_varlen", "oracle_attn_decode",
                       "oracle_attn_fwd_blockwise", "oracle_decode_split", "oracle_combine",
-                      "oracle_num_threads"):
+                      "oracle_attn_bwd", "oracle_num_threads"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -204,3 +205,19 @@ def combine(o_part, lse_part, sink=None):
     rc = _load().oracle_combine(_pd(o_part), _pd(lse_part), _pd(o), _pd(lse), rows, S, d, psk)
     _check(rc, "combine")
     return o.reshape(*lead, d), lse.reshape(*lead)
+
+
+def attn_bwd(q, k, v, dout, scale, causal=False, window=0, n_sink=0):
+    """Gradients of the dense forward for output gradient dout [B,Sq,Hq,d];
+    returns (dq [B,Sq,Hq,d], dk [B,Skv,Hkv,d], dv [B,Skv,Hkv,d])."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, Sq, Hq, d = q.shape
+    _, Skv, Hkv, _ = k.shape
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    rc = _load().oracle_attn_bwd(_pd(q), _pd(k), _pd(v), _pd(dout), _pd(dq), _pd(dk), _pd(dv), B,
+                                 Hq, Hkv, Sq, Skv, d, float(scale), int(bool(causal)), int(window),
+                                 int(n_sink))
+    _check(rc, "attn_bwd")
+    return dq, dk, dv

@@ -416,6 +416,95 @@ ORACLE_API int oracle_combine(const double *o_part, const double *lse_part, doub
     return 0;
 }
 
+/*
+ * Backward pass of the dense forward (two-pass definition, per query row).
+ * The pages state no formulas for it ("TileLang tutorial, ch.15", section
+ * 5.4 only reports how much a low-precision, atomically accumulated dQ
+ * loses); these are the chain rule through O = P V and the row softmax.
+ * With P_i the row's probabilities and dO the gradient of O,
+ *     dV_j += P_ij dO_i,          dP_ij = dO_i . V_j,
+ *     D_i   = sum_j P_ij dP_ij,   dS_ij = P_ij (dP_ij - D_i),
+ *     dQ_i  = scale sum_j dS_ij K_j,   dK_j += scale dS_ij Q_i.
+ * Rows that see no key contribute nothing (their dQ is 0).  dK and dV of a
+ * key/value head sum over the Hq/Hkv query heads that read it, in ascending
+ * head, then row order.  dq [B,Sq,Hq,d], dk/dv [B,Skv,Hkv,d].
+ */
+ORACLE_API int oracle_attn_bwd(const double *q, const double *k, const double *v,
+                               const double *dout, double *dq, double *dk, double *dv, int B,
+                               int Hq, int Hkv, int Sq, int Skv, int d, double scale, int causal,
+                               int window, int n_sink)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return 1;
+    const int groups = Hq / Hkv;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (Skv > 0 ? Skv : 1));
+        double *dp = (double *)malloc(sizeof(double) * (Skv > 0 ? Skv : 1));
+        if (!p || !dp) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (long w = 0; w < (long)B * Hkv; ++w) {
+                long b = w / Hkv, hk = w % Hkv;
+                const long kvs = (long)Hkv * d;
+                const double *kb = k + ((b * (long)Skv) * Hkv + hk) * d;
+                const double *vb = v + ((b * (long)Skv) * Hkv + hk) * d;
+                double *dkb = dk + ((b * (long)Skv) * Hkv + hk) * d;
+                double *dvb = dv + ((b * (long)Skv) * Hkv + hk) * d;
+                for (long j = 0; j < Skv; ++j)
+                    for (int t = 0; t < d; ++t) dkb[j * kvs + t] = dvb[j * kvs + t] = 0.0;
+                for (long h = hk * groups; h < (hk + 1) * groups; ++h) {
+                    for (long i = 0; i < Sq; ++i) {
+                        const double *qi = q + (((b * Sq + i) * Hq) + h) * d;
+                        const double *gi = dout + (((b * Sq + i) * Hq) + h) * d;
+                        double *dqi = dq + (((b * Sq + i) * Hq) + h) * d;
+                        for (int t = 0; t < d; ++t) dqi[t] = 0.0;
+                        double m = -INFINITY;
+                        for (long j = 0; j < Skv; ++j) {
+                            if (!visible(i, j, Sq, Skv, causal, window, n_sink)) {
+                                p[j] = -INFINITY;
+                                continue;
+                            }
+                            double dot = 0.0;
+                            for (int t = 0; t < d; ++t) dot += qi[t] * kb[j * kvs + t];
+                            p[j] = scale * dot;
+                            if (p[j] > m) m = p[j];
+                        }
+                        if (m == -INFINITY) continue; /* no visible key */
+                        double sum = 0.0;
+                        for (long j = 0; j < Skv; ++j) {
+                            p[j] = (p[j] == -INFINITY) ? 0.0 : exp(p[j] - m);
+                            sum += p[j];
+                        }
+                        double D = 0.0;
+                        for (long j = 0; j < Skv; ++j) {
+                            p[j] /= sum;
+                            double g = 0.0;
+                            for (int t = 0; t < d; ++t) g += gi[t] * vb[j * kvs + t];
+                            dp[j] = g;
+                            D += p[j] * g;
+                        }
+                        for (long j = 0; j < Skv; ++j) {
+                            if (p[j] == 0.0) continue;
+                            const double ds = p[j] * (dp[j] - D);
+                            for (int t = 0; t < d; ++t) {
+                                dvb[j * kvs + t] += p[j] * gi[t];
+                                dqi[t] += scale * ds * kb[j * kvs + t];
+                                dkb[j * kvs + t] += scale * ds * qi[t];
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    return bad ? 2 : 0;
+}
+
 ORACLE_API int oracle_num_threads(void)
 {
     int n = 1;
