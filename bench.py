@@ -438,6 +438,31 @@ def main():
     if ea.attn_device_status(stream) != ea.ATTN_OK:
         raise RuntimeError("device status reported an error in the strided calls")
     bh_ms = statistics.median(a.elapsed_time(b) for a, b in t_bh)
+    # backward of the step's two prefill calls (same inputs, dO ~ N(0,1))
+    gout = workloads.grad_output(7001, q.shape).to(dev)
+    bws = torch.empty(ea.attn_bwd_workspace_size(*q.shape[:1], q.shape[2], q.shape[1]),
+                      dtype=torch.uint8, device=dev)
+    bw = {}
+    for (xb, qb_, kb_, vb_, ob_, lb_) in pre:
+        ea.attn_fwd(qb_, kb_, vb_, ob_, lb_, causal=xb.causal, scale=xb.scale, stream=stream)
+        gq, gk, gv = torch.empty_like(qb_), torch.empty_like(kb_), torch.empty_like(vb_)
+        tt = []
+        for it in range(13):
+            with torch.cuda.stream(stream):
+                flush.fill_(5)
+                a, b = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+                a.record(stream)
+                ea.attn_bwd(qb_, kb_, vb_, ob_, lb_, gout, gq, gk, gv, causal=xb.causal,
+                            scale=xb.scale, workspace=bws, stream=stream)
+                b.record(stream)
+            if it >= 3:
+                tt.append((a, b))
+        torch.cuda.synchronize(dev)
+        if ea.attn_device_status(stream) != ea.ATTN_OK:
+            raise RuntimeError("device status reported an error in the backward calls")
+        ms_ = statistics.median(a.elapsed_time(b) for a, b in tt)
+        fl = 2.5 * prefill_flops(B, H, S, S, d, xb.causal)
+        bw["causal" if xb.causal else "noncausal"] = {"ms": ms_, "tflops": fl / (ms_ / 1e3) / 1e12}
     sp_ms = statistics.median(a.elapsed_time(b) for a, b in t_sp)
     sd_ms = statistics.median(a.elapsed_time(b) for a, b in t_sd)
     variants = {"logit_sink": {
@@ -450,6 +475,9 @@ def main():
             "ms": bh_ms, "tflops": f_nc / (bh_ms / 1e3) / 1e12,
             "note": "the step's non-causal prefill with q, k, v, o stored BHSD "
                     "(attn_fwd_strided); 20 calls after 3 warm-up calls, L2 flushed before each"},
+        "backward": dict(bw, note="attn_bwd on the step's prefill inputs (B=4 H=16 S=2048 "
+                                  "d=128); FLOPs 2.5x the forward's (five products); "
+                                  "10 calls after 3 warm-up calls, L2 flushed before each"),
         "chunked_prefill_paged": {
             "workload": "B=8 Hq=32 Hkv=8 d=128 bf16, cache 2048-8192 keys in 16-key pages, "
                         "last 512 tokens as the causal query block",

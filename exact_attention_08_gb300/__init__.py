@@ -24,7 +24,8 @@ from . import _build
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT",
     "ATTN_ERR_BAD_INPUT", "AttnError", "attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink",
-    "attn_fwd_paged", "attn_fwd_strided", "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout", "attn_status_string",
+    "attn_fwd_paged", "attn_fwd_strided", "attn_bwd", "attn_bwd_workspace_size",
+    "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout", "attn_status_string",
     "attn_last_error", "library_path", "lib",
 ]
 
@@ -56,6 +57,9 @@ def _load() -> ctypes.CDLL:
     i64p = ctypes.POINTER(ctypes.c_longlong)
     L.attn_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i64p, i64p, i64p, i64p, f,
                                    i, i, i, vp, vp]
+    L.attn_bwd_workspace_size.argtypes = [i, i, i]
+    L.attn_bwd_workspace_size.restype = sz
+    L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
     L.attn_decode_workspace_size.argtypes = [i, i, i, i]
     L.attn_decode_workspace_size.restype = sz
     L.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, sz,
@@ -69,6 +73,7 @@ def _load() -> ctypes.CDLL:
     L.attn_last_error.argtypes = []
     L.attn_last_error.restype = ctypes.c_char_p
     for fn in ("attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink", "attn_fwd_paged", "attn_fwd_strided",
+               "attn_bwd",
                "attn_decode_paged",
                "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout"):
         getattr(L, fn).restype = ctypes.c_int
@@ -303,6 +308,46 @@ def attn_fwd_strided(q, k, v, o=None, lse=None, *, causal=False, window=0, n_sin
                               int(n_sink), _ptr(sink_logit), _stream(stream))
     _check(rc, "attn_fwd_strided")
     return o, lse
+
+
+def attn_bwd_workspace_size(B: int, Hq: int, Sq: int) -> int:
+    return int(lib.attn_bwd_workspace_size(int(B), int(Hq), int(Sq)))
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, *, causal=False, scale=None,
+             workspace=None, stream=None):
+    """Gradients of attn_fwd: q [B,Sq,Hq,d], k/v [B,Skv,Hkv,d], the forward's o and
+    lse [B,Hq,Sq], dout like o (all contiguous, bf16 except lse) -> (dq, dk, dv) bf16."""
+    torch = _torch()
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _need(t, n, torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    B, Sq, Hq, d = q.shape
+    Bk, Skv, Hkv, dk_ = k.shape
+    if Bk != B or dk_ != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q/k/v shapes disagree")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("o and dout must be shaped like q")
+    if tuple(lse.shape) != (B, Hq, Sq):
+        raise ValueError("lse must be [B, Hq, Sq]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n, ref in ((dq, "dq", q), (dk, "dk", k), (dv, "dv", v)):
+        _need(t, n, torch.bfloat16, dev)
+        if tuple(t.shape) != tuple(ref.shape):
+            raise ValueError(f"{n} has the wrong shape")
+    need = attn_bwd_workspace_size(B, Hq, Sq)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                      _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Skv, d, scale, int(bool(causal)),
+                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                      _stream(stream))
+    _check(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_decode_workspace_size(B: int, Hq: int, d: int, num_splits: int) -> int:

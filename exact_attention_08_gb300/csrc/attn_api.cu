@@ -415,6 +415,79 @@ ATTN_API int attn_fwd_paged(const void* q, const void* k_pages, const void* v_pa
   return e == cudaSuccess ? ATTN_OK : cuda_error(e, "attn_fwd_paged launch");
 }
 
+ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Sq) {
+  if (B < 0 || Hq <= 0 || Sq < 0) return 0;
+  return bwd_workspace_bytes(B, Hq, Sq);
+}
+
+ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                      int Sq, int Skv, int d, float scale, int causal, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  t_last_error.clear();
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv < 0)
+    return set_error(ATTN_ERR_INVALID_ARG, "negative or zero size (B=%d Hq=%d Hkv=%d)", B, Hq, Hkv);
+  if (Hq % Hkv != 0)
+    return set_error(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  if (d != 64 && d != 128) return set_error(ATTN_ERR_UNSUPPORTED, "head dim %d (64 or 128)", d);
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return set_error(ATTN_ERR_INVALID_ARG, "scale must be finite and positive");
+  if (causal != 0 && causal != 1) return set_error(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (B == 0) return ATTN_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t kv_bytes = static_cast<size_t>(B) * Skv * Hkv * d * 2;
+  if (Sq == 0) {  // no query: dK = dV = 0
+    if (kv_bytes == 0) return ATTN_OK;
+    if (!dk || !dv) return set_error(ATTN_ERR_INVALID_ARG, "dk and dv must be set");
+    cudaError_t e = cudaMemsetAsync(dk, 0, kv_bytes, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kv_bytes, st);
+    return e == cudaSuccess ? ATTN_OK : cuda_error(e, "zeroing dk/dv");
+  }
+  if (!q || !o || !lse || !dout || !dq || !workspace)
+    return set_error(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (Skv > 0 && (!k || !v || !dk || !dv))
+    return set_error(ATTN_ERR_INVALID_ARG, "k, v, dk and dv must be set");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return set_error(ATTN_ERR_INVALID_ARG, "tensors must be 16-byte aligned (lse 4-byte)");
+  const size_t need = bwd_workspace_bytes(B, Hq, Sq);
+  if (workspace_bytes < need)
+    return set_error(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                     need);
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != ATTN_OK) return rc;
+  BwdLaunch a;
+  std::memset(&a, 0, sizeof(a));
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  const size_t rows = need / (2 * sizeof(float));
+  a.ws_lse2 = static_cast<float*>(workspace);
+  a.ws_d = static_cast<float*>(workspace) + rows;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Skv = Skv;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal;
+  a.status = ds->status;
+  if ((rc = make_map(&a.tmQ, q, d, Hq, Sq, B, 128, "q")) != ATTN_OK) return rc;
+  if ((rc = make_map(&a.tmDO, dout, d, Hq, Sq, B, 128, "dout")) != ATTN_OK) return rc;
+  if (Skv > 0) {
+    if ((rc = make_map(&a.tmK, k, d, Hkv, Skv, B, 128, "k")) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.tmV, v, d, Hkv, Skv, B, 128, "v")) != ATTN_OK) return rc;
+  }
+  cudaError_t e = launch_attn_bwd(a, st);
+  return e == cudaSuccess ? ATTN_OK : cuda_error(e, "attn_bwd launch");
+}
+
 ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
   if (B < 0 || Hq <= 0 || d <= 0 || num_splits <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * num_splits;

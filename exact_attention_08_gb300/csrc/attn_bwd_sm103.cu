@@ -1,0 +1,673 @@
+// Backward pass of the dense exact-attention forward on sm_103a: dQ, dK, dV
+// for an output gradient dO, from Q, K, V, O and the forward's row LSE.
+//
+// The pages give no backward formulas ("TileLang tutorial, ch.15
+// Operators: Attention", section 5.4 only measures what a bf16, atomically
+// accumulated dQ loses); the kernels follow the chain rule through O = P V
+// and the row softmax, recomputing P from the saved LSE instead of storing
+// it:
+//   P  = exp(scale Q K^T - LSE),      dV = P^T dO,
+//   dP = dO V^T,   D = rowsum(dO * O) (= rowsum(P * dP)),
+//   dS = P * (dP - D),   dQ = scale dS K,   dK = scale dS^T Q.
+// Every gradient is accumulated in fp32 in tensor memory over its whole
+// reduction and written once, so the results do not depend on scheduling
+// (no atomics): dK and dV by one CTA per key tile, looping over every query
+// tile of every query head that reads the key head; dQ by one CTA per query
+// tile, looping over the key tiles.
+//
+// Kernels:
+//   attn_bwd_rowstat_kernel  D and LSE in base 2 per query row, padded to
+//                            whole 128-row tiles (+inf LSE on pad rows and
+//                            on rows that saw no key, so their P is 0);
+//   attn_bwd_dkdv_kernel<D>  warps 0-3: S^T -> P^T, dP^T -> dS^T (thread r
+//                            owns key row r of the tile); warp 4: TMA
+//                            producer (K, V once; Q, dO and the two row
+//                            vectors per query tile, two stages); warp 5:
+//                            MMA issuer.  Tensor memory: S^T [0,128),
+//                            dP^T [128,256), dV [256,256+D), dK [256+D,..).
+//   attn_bwd_dq_kernel<D>    the same roles over key tiles for one query
+//                            tile: S [0,128), dP [128,256), dQ [256,256+D).
+// Products (tcgen05, kind::f16, M=128, fp32 in tensor memory):
+//   S^T = K Q^T, dP^T = V dO^T   (both operands K-major in shared memory)
+//   dV += P^T dO, dK += dS^T Q   (A from tensor memory, B MN-major)
+//   S = Q K^T, dP = dO V^T, dQ += dS K.
+// P and dS enter the second products as bf16, like P in the forward.
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int kB = 128;          // rows of every tile (keys or queries)
+constexpr int kBwdThreads = 192;  // warps 0-3 compute, 4 producer, 5 MMA
+constexpr int kWarpProd = 4;
+constexpr int kWarpIssue = 5;
+constexpr float kLog2eB = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTile = kB * D * 2;       // one 128 x D bf16 tile
+  static constexpr int kAtoms = D / 64;          // 128-byte swizzle atoms per row
+  static constexpr int kAtomBytes = kB * 128;    // one atom column of a tile
+  static constexpr int kVec = kB * 4;            // one fp32 row vector of a tile
+  // dK/dV kernel: K, V resident; two stages of (Q, dO, LSE2, D)
+  static constexpr int kStageBytes = 2 * kTile + 2 * kVec;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTile;
+  static constexpr int kOffStage = 2 * kTile;
+  static constexpr int kOffBarKV = kOffStage + 2 * kStageBytes;
+  static constexpr int kSmemKV = kOffBarKV + 16 * 8 + 1024;
+  // dQ kernel: Q, dO resident; two stages of (K, V)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kTile;
+  static constexpr int kOffKV = 2 * kTile;
+  static constexpr int kOffBarQ = kOffKV + 2 * 2 * kTile;
+  static constexpr int kSmemQ = kOffBarQ + 16 * 8 + 1024;
+  static_assert(kSmemKV <= 227 * 1024 && kSmemQ <= 227 * 1024, "shared memory");
+  // Each CTA allocates all 512 tensor-memory columns: ask for enough shared
+  // memory that a second CTA never shares the SM (its allocation would wait).
+  static constexpr int kOneCta = 116 * 1024;
+  static constexpr int kLaunchKV = kSmemKV > kOneCta ? kSmemKV : kOneCta;
+  static constexpr int kLaunchQ = kSmemQ > kOneCta ? kSmemQ : kOneCta;
+};
+
+struct BwdParams {
+  const __nv_bfloat16* dout;  // [B, Sq, Hq, d] (row statistics only)
+  const __nv_bfloat16* o;
+  const float* lse;          // [B, Hq, Sq], natural log
+  float* lse2;               // [B, Hq, Sqp] workspace: LSE * log2(e), +inf on pad rows
+  float* dvec;               // [B, Hq, Sqp] workspace: rowsum(dO * O)
+  __nv_bfloat16* dq;         // [B, Sq, Hq, d]
+  __nv_bfloat16* dk;         // [B, Skv, Hkv, d]
+  __nv_bfloat16* dv;
+  int B, Hq, Hkv, Sq, Skv, Sqp, d;
+  float scale, scale2;
+  int causal;
+  uint64_t wait_limit_ns;
+  int* status;
+};
+
+__device__ __forceinline__ void reg_fence_b(uint32_t& r) { asm volatile("" : "+r"(r)); }
+
+__device__ __forceinline__ void tmem_ld_wait_b() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void bwd_fail(int* status, volatile int* abort_flag) {
+  atomicOr(status, kStatusTimeout);
+  if (abort_flag) *abort_flag = 1;
+}
+
+// One warp per query row: D = sum_t dO_t O_t (fp32) and LSE2 = LSE log2(e);
+// rows past Sq (to the tile boundary) and rows whose LSE is -inf (no key)
+// get LSE2 = +inf and D = 0, so every P built from them is 0.
+__global__ void attn_bwd_rowstat_kernel(BwdParams p) {
+  const int lane = threadIdx.x % 32;
+  const long long nrow = static_cast<long long>(p.B) * p.Hq * p.Sqp;
+  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  for (long long rw = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+       rw < nrow; rw += wstride) {
+    const int i = static_cast<int>(rw % p.Sqp);
+    const long long bh = rw / p.Sqp;
+    const int h = static_cast<int>(bh % p.Hq), b = static_cast<int>(bh / p.Hq);
+    float acc = 0.f, l2 = INFINITY;
+    if (i < p.Sq) {
+      const size_t base = ((static_cast<size_t>(b) * p.Sq + i) * p.Hq + h) * p.d;
+      for (int t = lane; t < p.d; t += 32)
+        acc += __bfloat162float(p.dout[base + t]) * __bfloat162float(p.o[base + t]);
+      const float l = p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Sq + i];
+      l2 = (l == -INFINITY) ? INFINITY : l * kLog2eB;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+      p.dvec[rw] = (i < p.Sq) ? acc : 0.f;
+      p.lse2[rw] = l2;
+    }
+  }
+}
+
+// Packs 32 fp32 values into 16 bf16 pairs (element 2e in the low half).
+__device__ __forceinline__ void pack32(const float* f, uint32_t* pk) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+}
+
+// K-step kk of a K-major SW128 operand: 32 bytes along a row inside a
+// 128-byte atom, then the next atom column.
+template <int kAtomBytes>
+__device__ __forceinline__ uint64_t kmajor_step(int kk) {
+  return static_cast<uint64_t>(((kk / 4) * kAtomBytes + (kk % 4) * 32) >> 4);
+}
+
+// Bounded wait by every lane of the warp; on failure the status is set once.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          const BwdParams& p) {
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.wait_limit_ns));
+  if (!ok && (threadIdx.x % 32) == 0) bwd_fail(p.status, abort_flag);
+  return ok;
+}
+
+// dK and dV of one key tile (128 keys) of key head hk: one CTA per
+// (key tile, key head, batch).
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmDO, BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBarKV);
+  uint64_t* kv_full = bars;       // K and V tiles landed
+  uint64_t* q_full = bars + 1;    // [2] Q, dO, LSE2, D of a query tile landed
+  uint64_t* q_free = bars + 3;    // [2] the products reading that stage are done
+  uint64_t* s_full = bars + 5;    // S^T and dP^T are in tensor memory
+  uint64_t* p_ready = bars + 7;   // P^T and dS^T written (128 arrivals)
+  uint64_t* done = bars + 8;      // every product of the CTA is done
+  uint64_t* drain = bars + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  __shared__ int abort_s;
+  volatile int* abort_flag = &abort_s;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int G = p.Hq / p.Hkv;
+  const int nqt = p.Sqp / kB;
+  const int off = p.Skv - p.Sq;
+  const int k0 = kt * kB;
+  int qt_lo = 0;
+  if (p.causal) {
+    const int qmin = k0 - off;  // first query that sees key k0
+    qt_lo = qmin <= 0 ? 0 : qmin / kB;
+  }
+  const int nq = nqt > qt_lo ? nqt - qt_lo : 0;
+  const int ntiles = G * nq;  // (query head, query tile) pairs, head-major
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_free[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(done, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    abort_s = 0;
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  auto stage = [&](int s) { return smem + C::kOffStage + s * C::kStageBytes; };
+
+  if (warp == kWarpProd) {
+    // ================================================================ producer
+    mbar_arrive_expect_tx_w(kv_full, 2 * C::kTile);
+#pragma unroll
+    for (int a = 0; a < C::kAtoms; ++a) {
+      tma_load_4d_w(sK + a * C::kAtomBytes, &tmK, kv_full, a * 64, hk, k0, b);
+      tma_load_4d_w(sV + a * C::kAtomBytes, &tmV, kv_full, a * 64, hk, k0, b);
+    }
+    int issued = 0;
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = t & 1;
+      if (t >= 2 && !warp_wait(&q_free[s], ((t >> 1) - 1) & 1, abort_flag, p)) break;
+      const int h = hk * G + t / nq, qt = qt_lo + t % nq;
+      uint8_t* st = stage(s);
+      mbar_arrive_expect_tx_w(&q_full[s], 2 * C::kTile + 2 * C::kVec);
+#pragma unroll
+      for (int a = 0; a < C::kAtoms; ++a) {
+        tma_load_4d_w(st + a * C::kAtomBytes, &tmQ, &q_full[s], a * 64, h, qt * kB, b);
+        tma_load_4d_w(st + C::kTile + a * C::kAtomBytes, &tmDO, &q_full[s], a * 64, h, qt * kB,
+                      b);
+      }
+      const size_t vrow = (static_cast<size_t>(b) * p.Hq + h) * p.Sqp + static_cast<size_t>(qt) * kB;
+      bulk_load_1d_w(st + 2 * C::kTile, p.lse2 + vrow, C::kVec, &q_full[s]);
+      bulk_load_1d_w(st + 2 * C::kTile + C::kVec, p.dvec + vrow, C::kVec, &q_full[s]);
+      issued = t + 1;
+    }
+    // Let every copy issued land before the CTA can leave.
+    warp_wait(kv_full, 0, nullptr, p);
+    for (int s = 0; s < 2; ++s) {
+      const int n_s = (issued - s + 1) / 2;  // loads issued into stage s
+      if (n_s > 0) warp_wait(&q_full[s], (n_s - 1) & 1, nullptr, p);
+    }
+  } else if (warp == kWarpIssue) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, kB, false);
+    constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, true);
+    const uint64_t dk = sdesc_sw128(smem_addr(sK), 16, 1024);
+    const uint64_t dvk = sdesc_sw128(smem_addr(sV), 16, 1024);
+    const uint32_t tS = tmem, tP = tmem + kB, tDV = tmem + 2 * kB, tDK = tmem + 2 * kB + D;
+    bool ok = warp_wait(kv_full, 0, abort_flag, p);
+    if (ok) tc_fence_after_sync();
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const int s = t & 1;
+      if (!warp_wait(&q_full[s], (t >> 1) & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t st = smem_addr(stage(s));
+      const uint64_t dqk = sdesc_sw128(st, 16, 1024);
+      const uint64_t ddok = sdesc_sw128(st + C::kTile, 16, 1024);
+      // S^T = K Q^T and dP^T = V dO^T (M = keys, N = queries, K = d)
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
+        mma_bf16_ss_w(tS, dk + ko, dqk + ko, idesc_s, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
+        mma_bf16_ss_w(tP, dvk + ko, ddok + ko, idesc_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(s_full);
+      if (!warp_wait(p_ready, t & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      // dV += P^T dO and dK += dS^T Q (A from tensor memory, K = queries;
+      // B MN-major: the stage's dO and Q tiles read along d)
+      const uint64_t dqm = sdesc_sw128(st, C::kAtomBytes, 1024);
+      const uint64_t ddom = sdesc_sw128(st + C::kTile, C::kAtomBytes, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kB / 16; ++kk)
+        mma_bf16_ts_w(tDV, tS + kk * 8, ddom + kk * (2048 >> 4), idesc_g,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < kB / 16; ++kk)
+        mma_bf16_ts_w(tDK, tP + kk * 8, dqm + kk * (2048 >> 4), idesc_g,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_w(&q_free[s]);
+    }
+    mma_commit_w(done);
+    // Every product issued has finished before tensor memory is released.
+    mma_commit_w(drain);
+    warp_wait(drain, 0, nullptr, p);
+  } else if (warp < 4) {
+    // ================================================================ compute warps
+    const int r = warp * 32 + lane;
+    const int k_idx = k0 + r;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = t & 1;
+      if (!warp_wait(s_full, t & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      // the stage's row vectors came by bulk copy: observe their barrier too
+      if (!warp_wait(&q_full[s], (t >> 1) & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const int qt = qt_lo + t % nq;
+      const float* lse2v = reinterpret_cast<const float*>(stage(s) + 2 * C::kTile);
+      const float* dvv = lse2v + kB;
+      // column c (query qt*128 + c) is visible to this key row iff c >= cmin
+      const int cmin = p.causal ? k_idx - off - qt * kB : -(1 << 30);
+#pragma unroll 1
+      for (int c4 = 0; c4 < kB / 32; ++c4) {
+        uint32_t ra[32];
+        float pf[32];
+        uint32_t pk[16];
+        tmem_ld_x32(taddr + 32 * c4, ra);
+        tmem_ld_wait_b();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          reg_fence_b(ra[e]);
+          const int col = 32 * c4 + e;
+          const float x = fmaf(__uint_as_float(ra[e]), p.scale2, -lse2v[col]);
+          pf[e] = (col >= cmin) ? ex2_approx(x) : 0.f;
+        }
+        pack32(pf, pk);
+        tmem_st_x16(taddr + 16 * c4, pk);
+        tmem_ld_x32(taddr + kB + 32 * c4, ra);
+        tmem_ld_wait_b();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          reg_fence_b(ra[e]);
+          pf[e] = pf[e] * (__uint_as_float(ra[e]) - dvv[32 * c4 + e]);
+        }
+        pack32(pf, pk);
+        tmem_st_x16(taddr + kB + 16 * c4, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(p_ready);
+    }
+    if (ok && warp_wait(done, 0, abort_flag, p)) {
+      tc_fence_after_sync();
+      const bool valid = k_idx < p.Skv;
+      const size_t orow = ((static_cast<size_t>(b) * p.Skv + k_idx) * p.Hkv + hk) * D;
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {  // 0: dV, 1: dK (times scale)
+        __nv_bfloat16* dst = (g == 0 ? p.dv : p.dk) + orow;
+        const float mul = g == 0 ? 1.f : p.scale;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ra[32];
+          if (ntiles > 0) {
+            tmem_ld_x32(taddr + 2 * kB + g * D + 32 * c, ra);
+            tmem_ld_wait_b();
+          }
+          float f[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            reg_fence_b(ra[e]);
+            f[e] = ntiles > 0 ? __uint_as_float(ra[e]) * mul : 0.f;
+          }
+          uint32_t pk[16];
+          pack32(f, pk);
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// dQ of one query tile (128 rows) of query head h: one CTA per
+// (query tile, query head, batch), looping over the visible key tiles.
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmDO, BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sDO = smem + C::kOffDO;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBarQ);
+  uint64_t* qd_full = bars;      // Q and dO landed
+  uint64_t* kv_full = bars + 1;  // [2] K and V of a key tile landed
+  uint64_t* kv_free = bars + 3;  // [2] the products reading that stage are done
+  uint64_t* s_full = bars + 5;   // S and dP are in tensor memory
+  uint64_t* p_ready = bars + 6;  // dS written (128 arrivals)
+  uint64_t* done = bars + 7;
+  uint64_t* drain = bars + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  __shared__ int abort_s;
+  volatile int* abort_flag = &abort_s;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / (p.Hq / p.Hkv);
+  const int q0 = qt * kB;
+  const int off = p.Skv - p.Sq;
+  int nkt = (p.Skv + kB - 1) / kB;
+  if (p.causal) {
+    const int qlast = min(q0 + kB - 1, p.Sq - 1);
+    const int kmax = min(p.Skv - 1, qlast + off);  // last key any row of the tile sees
+    nkt = kmax >= 0 ? kmax / kB + 1 : 0;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(qd_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_free[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(done, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    abort_s = 0;
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  auto stage = [&](int s) { return smem + C::kOffKV + s * 2 * C::kTile; };
+
+  if (warp == kWarpProd) {
+    // ================================================================ producer
+    mbar_arrive_expect_tx_w(qd_full, 2 * C::kTile);
+#pragma unroll
+    for (int a = 0; a < C::kAtoms; ++a) {
+      tma_load_4d_w(sQ + a * C::kAtomBytes, &tmQ, qd_full, a * 64, h, q0, b);
+      tma_load_4d_w(sDO + a * C::kAtomBytes, &tmDO, qd_full, a * 64, h, q0, b);
+    }
+    int issued = 0;
+    for (int t = 0; t < nkt; ++t) {
+      const int s = t & 1;
+      if (t >= 2 && !warp_wait(&kv_free[s], ((t >> 1) - 1) & 1, abort_flag, p)) break;
+      uint8_t* st = stage(s);
+      mbar_arrive_expect_tx_w(&kv_full[s], 2 * C::kTile);
+#pragma unroll
+      for (int a = 0; a < C::kAtoms; ++a) {
+        tma_load_4d_w(st + a * C::kAtomBytes, &tmK, &kv_full[s], a * 64, hk, t * kB, b);
+        tma_load_4d_w(st + C::kTile + a * C::kAtomBytes, &tmV, &kv_full[s], a * 64, hk, t * kB,
+                      b);
+      }
+      issued = t + 1;
+    }
+    warp_wait(qd_full, 0, nullptr, p);
+    for (int s = 0; s < 2; ++s) {
+      const int n_s = (issued - s + 1) / 2;
+      if (n_s > 0) warp_wait(&kv_full[s], (n_s - 1) & 1, nullptr, p);
+    }
+  } else if (warp == kWarpIssue) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, kB, false);
+    constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, true);
+    const uint64_t dq = sdesc_sw128(smem_addr(sQ), 16, 1024);
+    const uint64_t ddo = sdesc_sw128(smem_addr(sDO), 16, 1024);
+    const uint32_t tS = tmem, tP = tmem + kB, tDQ = tmem + 2 * kB;
+    bool ok = warp_wait(qd_full, 0, abort_flag, p);
+    if (ok) tc_fence_after_sync();
+    for (int t = 0; ok && t < nkt; ++t) {
+      const int s = t & 1;
+      if (!warp_wait(&kv_full[s], (t >> 1) & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t st = smem_addr(stage(s));
+      const uint64_t dkk = sdesc_sw128(st, 16, 1024);
+      const uint64_t dvk = sdesc_sw128(st + C::kTile, 16, 1024);
+      // S = Q K^T and dP = dO V^T (M = queries, N = keys, K = d)
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
+        mma_bf16_ss_w(tS, dq + ko, dkk + ko, idesc_s, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
+        mma_bf16_ss_w(tP, ddo + ko, dvk + ko, idesc_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(s_full);
+      if (!warp_wait(p_ready, t & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      // dQ += dS K (A = dS from tensor memory, K = keys; B = the K tile read along d)
+      const uint64_t dkm = sdesc_sw128(st, C::kAtomBytes, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kB / 16; ++kk)
+        mma_bf16_ts_w(tDQ, tP + kk * 8, dkm + kk * (2048 >> 4), idesc_g,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_w(&kv_free[s]);
+    }
+    mma_commit_w(done);
+    mma_commit_w(drain);
+    warp_wait(drain, 0, nullptr, p);
+  } else if (warp < 4) {
+    // ================================================================ compute warps
+    const int r = warp * 32 + lane;
+    const int q_idx = q0 + r;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const size_t vrow = (static_cast<size_t>(b) * p.Hq + h) * p.Sqp + q_idx;
+    const float lse2 = p.lse2[vrow];  // +inf past Sq: every P of the row is 0
+    const float dval = p.dvec[vrow];
+    bool ok = true;
+    for (int t = 0; t < nkt; ++t) {
+      if (!warp_wait(s_full, t & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      // column c (key t*128 + c) is visible to this row iff c <= cmax
+      int cmax = p.Skv - 1 - t * kB;
+      if (p.causal) cmax = min(cmax, q_idx + off - t * kB);
+#pragma unroll 1
+      for (int c4 = 0; c4 < kB / 32; ++c4) {
+        uint32_t ra[32], rb[32];
+        float pf[32];
+        uint32_t pk[16];
+        tmem_ld_x32(taddr + 32 * c4, ra);
+        tmem_ld_x32(taddr + kB + 32 * c4, rb);
+        tmem_ld_wait_b();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          reg_fence_b(ra[e]);
+          reg_fence_b(rb[e]);
+          const int col = 32 * c4 + e;
+          const float pv =
+              (col <= cmax) ? ex2_approx(fmaf(__uint_as_float(ra[e]), p.scale2, -lse2)) : 0.f;
+          pf[e] = pv * (__uint_as_float(rb[e]) - dval);
+        }
+        pack32(pf, pk);
+        tmem_st_x16(taddr + kB + 16 * c4, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(p_ready);
+    }
+    if (ok && warp_wait(done, 0, abort_flag, p)) {
+      tc_fence_after_sync();
+      const bool valid = q_idx < p.Sq;
+      __nv_bfloat16* dst = p.dq + ((static_cast<size_t>(b) * p.Sq + q_idx) * p.Hq + h) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ra[32];
+        if (nkt > 0) {
+          tmem_ld_x32(taddr + 2 * kB + 32 * c, ra);
+          tmem_ld_wait_b();
+        }
+        float f[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          reg_fence_b(ra[e]);
+          f[e] = nkt > 0 ? __uint_as_float(ra[e]) * p.scale : 0.f;
+        }
+        uint32_t pk[16];
+        pack32(f, pk);
+        if (valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchKV);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchQ);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  BwdParams p;
+  p.dout = static_cast<const __nv_bfloat16*>(a.dout);
+  p.o = static_cast<const __nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.lse2 = a.ws_lse2;
+  p.dvec = a.ws_d;
+  p.dq = static_cast<__nv_bfloat16*>(a.dq);
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.Sq = a.Sq;
+  p.Skv = a.Skv;
+  p.Sqp = (a.Sq + kB - 1) / kB * kB;
+  p.d = D;
+  p.scale = a.scale;
+  p.scale2 = a.scale * kLog2eB;
+  p.causal = a.causal;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.status = a.status;
+  attn_bwd_rowstat_kernel<<<1216, 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (a.Skv > 0) {
+    dim3 g1((a.Skv + kB - 1) / kB, a.Hkv, a.B);
+    attn_bwd_dkdv_kernel<D><<<g1, kBwdThreads, C::kLaunchKV, stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO,
+                                                                     p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  dim3 g2(p.Sqp / kB, a.Hq, a.B);
+  attn_bwd_dq_kernel<D><<<g2, kBwdThreads, C::kLaunchQ, stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int B, int Hq, int Sq) {
+  const size_t sqp = (static_cast<size_t>(Sq) + kB - 1) / kB * kB;
+  return 2 * static_cast<size_t>(B) * Hq * sqp * sizeof(float);
+}
+
+cudaError_t launch_attn_bwd(const BwdLaunch& a, cudaStream_t stream) {
+  if (a.d == 128) return launch_bwd_d<128>(a, stream);
+  if (a.d == 64) return launch_bwd_d<64>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

@@ -54,7 +54,28 @@ struct DecodeLaunch {
   int* status;
 };
 
+struct BwdLaunch {
+  CUtensorMap tmQ, tmK, tmV, tmDO;  // 4-D maps (d, H, S, B), 64 x 1 x 128 x 1 boxes
+  const void* o;                    // bf16 forward output [B, Sq, Hq, d]
+  const void* dout;                 // bf16 gradient of O, same layout
+  const float* lse;                 // forward LSE [B, Hq, Sq] (natural log)
+  void* dq;                         // bf16 [B, Sq, Hq, d]
+  void* dk;                         // bf16 [B, Skv, Hkv, d]
+  void* dv;
+  float* ws_lse2;                   // [B, Hq, Sqp] fp32 workspace
+  float* ws_d;                      // [B, Hq, Sqp] fp32 workspace
+  int B, Hq, Hkv, Sq, Skv, d;
+  float scale;
+  int causal;
+  int* status;
+};
+
+// Bytes of workspace the backward needs (two fp32 row vectors per query row,
+// padded to whole 128-row tiles).
+size_t bwd_workspace_bytes(int B, int Hq, int Sq);
+
 // Kernel launchers (return cudaError_t of the launch).
+cudaError_t launch_attn_bwd(const BwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_attn_fwd(const FwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_attn_fill_empty(const FwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_attn_decode(const DecodeLaunch& a, cudaStream_t stream);

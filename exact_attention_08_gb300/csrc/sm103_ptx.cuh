@@ -198,6 +198,18 @@ __device__ __forceinline__ void tma_load_4d_w(void* smem_dst, const CUtensorMap*
       : "memory");
 }
 
+// Bulk copy of `bytes` contiguous bytes from global to shared memory,
+// completing on `bar` (both addresses and the size multiples of 16 bytes).
+__device__ __forceinline__ void bulk_load_1d_w(void* smem_dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      "\n\t}" ::"r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_4d_w(const CUtensorMap* map, int c0, int c1, int c2,
                                                   int c3) {
   asm volatile(

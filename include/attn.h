@@ -186,6 +186,34 @@ ATTN_API int attn_fwd_paged(const void* q, const void* k_pages, const void* v_pa
                             const float* sink_logit, void* stream);
 
 /*
+ * Bytes of device workspace attn_bwd needs (two fp32 values per query row,
+ * rows padded to multiples of 128).  0 on invalid sizes.
+ */
+ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Sq);
+
+/*
+ * Backward pass of attn_fwd (dense BSHD, causal or not, GQA; no window,
+ * sink keys or logit sink): from q, k, v, the forward's o and lse and the
+ * gradient dout of o, writes
+ *   dq [B, Sq, Hq, d], dk, dv [B, Skv, Hkv, d]   (bf16, device, caller-owned)
+ * with dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO, P = exp(scale Q K^T -
+ * LSE) rebuilt from lse, dS = P (dO V^T - rowsum(dO * O)).  The pages give no
+ * backward formulas; "TileLang tutorial, ch.15", section 5.4 reports the
+ * error of a dQ accumulated atomically in bf16, which is why every gradient
+ * here is accumulated in fp32 over its whole reduction by one CTA and
+ * written once: results are bitwise repeatable.  dK and dV of a key head sum
+ * over the Hq/Hkv query heads that read it.
+ *   lse: the forward's [B, Hq, Sq] output (rows with -inf, which saw no key,
+ *   get dq = 0 and contribute nothing).  workspace: device buffer of at least
+ *   attn_bwd_workspace_size(B, Hq, Sq) bytes, overwritten.  Sq == 0 zeroes
+ *   dk and dv; Skv == 0 zeroes dq.  d must be 64 or 128.
+ */
+ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                      int B, int Hq, int Hkv, int Sq, int Skv, int d, float scale, int causal,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace attn_decode_paged needs for these sizes (split
  * partial outputs and log-sum-exps, fp32).  0 on invalid sizes.
  */

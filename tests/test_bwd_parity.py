@@ -1,0 +1,126 @@
+"""GPU parity of attn_bwd (through the C ABI) against the fp64 backward
+oracle on the same seeded inputs.
+
+Tolerance, from the arithmetic: P and dS enter the second products as bf16
+(relative rounding 2^-9 each) and the gradients are returned in bf16 (2^-9);
+accumulation is fp32.  Errors of that size average out over the 128+ terms
+of each sum, so per tensor the relative L2 error must stay below 1e-2 (the
+pages' own figure for a bf16, atomically accumulated dQ is 1.024 %, "TileLang
+tutorial, ch.15", section 5.4) and the largest error below 3e-2 of the
+tensor's largest magnitude."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._parity import np64
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-2
+REL_MAX = 3e-2
+
+
+@pytest.fixture(scope="module")
+def ea():
+    import exact_attention_08_gb300 as m
+    assert torch.cuda.is_available()
+    return m
+
+
+def _run(ea, x, g):
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    o, lse = ea.attn_fwd_ex(q, k, v, causal=x.causal, scale=x.scale)
+    dq, dk, dv = ea.attn_bwd(q, k, v, o, lse, g.cuda(), causal=x.causal, scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    return dq, dk, dv
+
+
+def _check(got, ref, what):
+    g = got.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite"
+    scale = np.abs(ref).max()
+    if scale == 0.0:
+        # e.g. a single visible key: dS = P (dP - D) vanishes exactly, and the
+        # kernel's D (from the bf16 O) and dP differ only by rounding
+        assert np.abs(g).max() <= 1e-4, f"{what}: expected ~0, got {np.abs(g).max():.3e}"
+        return 0.0, 0.0
+    l2 = np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-300)
+    mx = np.abs(g - ref).max() / scale
+    assert l2 <= REL_L2, f"{what}: relative L2 error {l2:.3e}"
+    assert mx <= REL_MAX, f"{what}: max error {mx:.3e} of the largest magnitude"
+    return l2, mx
+
+
+def _compare(ea, x, seed, what):
+    g = workloads.grad_output(seed, x.q.shape)
+    dq, dk, dv = _run(ea, x, g)
+    rq, rk, rv = oracle.attn_bwd(np64(x.q), np64(x.k), np64(x.v), np64(g), x.scale, x.causal)
+    return [_check(a, b, f"{what} {n}") for a, b, n in ((dq, rq, "dq"), (dk, rk, "dk"),
+                                                          (dv, rv, "dv"))]
+
+
+CASES = [
+    # (seed, B, Hq, Hkv, Sq, Skv, d, causal)
+    (101, 1, 1, 1, 128, 128, 64, False),
+    (102, 2, 3, 3, 300, 389, 128, False),     # ragged, several tiles
+    (103, 1, 2, 2, 333, 333, 128, True),      # ragged causal
+    (104, 1, 2, 2, 200, 700, 128, True),      # Sq < Skv: shifted diagonal
+    (105, 1, 2, 2, 500, 300, 128, True),      # Sq > Skv: rows with no key
+    (106, 2, 8, 2, 400, 400, 128, True),      # GQA 4:1
+    (107, 1, 4, 1, 300, 300, 64, True),       # d=64, MQA
+    (108, 1, 2, 2, 1, 1, 128, True),          # one query, one key
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"seed{c[0]}" for c in CASES])
+def test_small(ea, case):
+    seed, B, Hq, Hkv, Sq, Skv, d, causal = case
+    x = workloads.dense_inputs(seed, B, Hq, Hkv, Sq, Skv, d, causal)
+    _compare(ea, x, seed + 50, f"seed {seed}")
+
+
+def test_rows_without_keys_get_zero_dq(ea):
+    x = workloads.dense_inputs(109, 1, 2, 2, 300, 100, 128, True)
+    g = workloads.grad_output(159, x.q.shape)
+    dq, _, _ = _run(ea, x, g)
+    assert torch.all(dq[:, :200].view(torch.int16) == 0)
+
+
+def test_deterministic(ea):
+    x = workloads.dense_inputs(110, 1, 4, 2, 700, 700, 128, True)
+    g = workloads.grad_output(160, x.q.shape)
+    a = _run(ea, x, g)
+    b = _run(ea, x, g)
+    for t1, t2 in zip(a, b):
+        assert torch.equal(t1.view(torch.int16), t2.view(torch.int16))
+
+
+def test_empty_sizes(ea):
+    x = workloads.dense_inputs(111, 1, 2, 2, 0, 64, 128)  # no query: dk = dv = 0
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 2, 0, device="cuda")
+    dk = torch.full_like(k, 3.0)
+    dv = torch.full_like(v, 3.0)
+    ea.attn_bwd(q, k, v, o, lse, torch.empty_like(q), dk=dk, dv=dv, scale=x.scale)
+    torch.cuda.synchronize()
+    assert torch.all(dk == 0) and torch.all(dv == 0)
+    x = workloads.dense_inputs(112, 1, 2, 2, 70, 0, 128)  # no key: dq = 0
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    o, lse = ea.attn_fwd_ex(q, k, v, scale=x.scale)
+    dq, _, _ = ea.attn_bwd(q, k, v, o, lse, workloads.grad_output(162, q.shape).cuda(),
+                           scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    assert torch.all(dq.view(torch.int16) == 0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_full_length(ea, causal):
+    """S = 2048, d = 128 (the prefill workload's sequence length) on 4 heads."""
+    x = workloads.dense_inputs(113 + int(causal), 1, 4, 4, 2048, 2048, 128, causal)
+    errs = _compare(ea, x, 163 + int(causal), f"S=2048 causal={causal}")
+    print("bwd rel L2 / max:", errs)

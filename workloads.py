@@ -245,6 +245,11 @@ def chunked_prefill():
     return paged_prefill_inputs(6001, 8, 32, 8, 128, 2048, 8192, 512, 512)
 
 
+def grad_output(seed: int, shape) -> torch.Tensor:
+    """A seeded output gradient dO for the backward pass: iid N(0,1) cast to bf16."""
+    return _randn_bf16(_gen(seed), tuple(shape))
+
+
 def logit_sinks(seed: int, Hq: int, lo: float = 4.0, hi: float = 12.0,
                 extremes: bool = False) -> torch.Tensor:
     """Per-head logit sinks [Hq] fp32 (CPU), uniform in [lo, hi]: around the
