@@ -122,8 +122,17 @@ __global__ void attn_bwd_rowstat_kernel(BwdParams p) {
     float acc = 0.f, l2 = INFINITY;
     if (i < p.Sq) {
       const size_t base = ((static_cast<size_t>(b) * p.Sq + i) * p.Hq + h) * p.d;
-      for (int t = lane; t < p.d; t += 32)
-        acc += __bfloat162float(p.dout[base + t]) * __bfloat162float(p.o[base + t]);
+      for (int t = lane * 4; t < p.d; t += 128) {  // four bf16 (8 bytes) per lane
+        const uint2 g = *reinterpret_cast<const uint2*>(p.dout + base + t);
+        const uint2 o = *reinterpret_cast<const uint2*>(p.o + base + t);
+        const uint32_t gw[2] = {g.x, g.y}, ow[2] = {o.x, o.y};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          acc = fmaf(__uint_as_float(gw[e] << 16), __uint_as_float(ow[e] << 16), acc);
+          acc = fmaf(__uint_as_float(gw[e] & 0xffff0000u), __uint_as_float(ow[e] & 0xffff0000u),
+                     acc);
+        }
+      }
       const float l = p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Sq + i];
       l2 = (l == -INFINITY) ? INFINITY : l * kLog2eB;
     }
@@ -175,11 +184,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* kv_full = bars;       // K and V tiles landed
   uint64_t* q_full = bars + 1;    // [2] Q, dO, LSE2, D of a query tile landed
   uint64_t* q_free = bars + 3;    // [2] the products reading that stage are done
-  uint64_t* s_full = bars + 5;    // S^T and dP^T are in tensor memory
-  uint64_t* p_ready = bars + 7;   // P^T and dS^T written (128 arrivals)
+  uint64_t* sa_full = bars + 5;   // S^T is in tensor memory
+  uint64_t* sb_full = bars + 6;   // dP^T is in tensor memory
+  uint64_t* pa_ready = bars + 7;  // P^T written (128 arrivals)
+  uint64_t* pb_ready = bars + 11; // dS^T written (128 arrivals)
   uint64_t* done = bars + 8;      // every product of the CTA is done
   uint64_t* drain = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
   __shared__ int abort_s;
   volatile int* abort_flag = &abort_s;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -203,8 +214,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&q_full[s], 1);
       mbar_init(&q_free[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_ready, 128);
+    mbar_init(sa_full, 1);
+    mbar_init(sb_full, 1);
+    mbar_init(pa_ready, 128);
+    mbar_init(pb_ready, 128);
     mbar_init(done, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -254,48 +267,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpIssue) {
     // ================================================================ MMA issuer
+    // Per query tile t the pipe runs dP^T(t), dV(t), S^T(t+1), dK(t): S^T of
+    // the next tile overwrites P^T(t) once dV(t) has read it, while the
+    // compute warps form dS^T(t) from P^T kept in their registers; dP^T(t+1)
+    // overwrites dS^T(t) once dK(t) has read it.
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, kB, false);
     constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, true);
     const uint64_t dk = sdesc_sw128(smem_addr(sK), 16, 1024);
     const uint64_t dvk = sdesc_sw128(smem_addr(sV), 16, 1024);
     const uint32_t tS = tmem, tP = tmem + kB, tDV = tmem + 2 * kB, tDK = tmem + 2 * kB + D;
-    bool ok = warp_wait(kv_full, 0, abort_flag, p);
-    if (ok) tc_fence_after_sync();
-    for (int t = 0; ok && t < ntiles; ++t) {
+    auto issue_st = [&](int t) -> bool {  // S^T(t) = K Q(t)^T
       const int s = t & 1;
-      if (!warp_wait(&q_full[s], (t >> 1) & 1, abort_flag, p)) {
-        ok = false;
-        break;
-      }
+      if (!warp_wait(&q_full[s], (t >> 1) & 1, abort_flag, p)) return false;
       tc_fence_after_sync();
-      const uint32_t st = smem_addr(stage(s));
-      const uint64_t dqk = sdesc_sw128(st, 16, 1024);
-      const uint64_t ddok = sdesc_sw128(st + C::kTile, 16, 1024);
-      // S^T = K Q^T and dP^T = V dO^T (M = keys, N = queries, K = d)
+      const uint64_t dqk = sdesc_sw128(smem_addr(stage(s)), 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
         mma_bf16_ss_w(tS, dk + ko, dqk + ko, idesc_s, kk > 0 ? 1u : 0u);
       }
+      mma_commit_w(sa_full);
+      return true;
+    };
+    bool ok = warp_wait(kv_full, 0, abort_flag, p);
+    if (ok) tc_fence_after_sync();
+    if (ok && ntiles > 0) ok = issue_st(0);
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const int s = t & 1;
+      const uint32_t st = smem_addr(stage(s));
+      const uint64_t ddok = sdesc_sw128(st + C::kTile, 16, 1024);
+      // dP^T(t) = V dO(t)^T
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
         mma_bf16_ss_w(tP, dvk + ko, ddok + ko, idesc_s, kk > 0 ? 1u : 0u);
       }
-      mma_commit_w(s_full);
-      if (!warp_wait(p_ready, t & 1, abort_flag, p)) {
+      mma_commit_w(sb_full);
+      // dV += P^T dO(t) (A from tensor memory, K = queries; B read along d)
+      if (!warp_wait(pa_ready, t & 1, abort_flag, p)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      // dV += P^T dO and dK += dS^T Q (A from tensor memory, K = queries;
-      // B MN-major: the stage's dO and Q tiles read along d)
       const uint64_t dqm = sdesc_sw128(st, C::kAtomBytes, 1024);
       const uint64_t ddom = sdesc_sw128(st + C::kTile, C::kAtomBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < kB / 16; ++kk)
         mma_bf16_ts_w(tDV, tS + kk * 8, ddom + kk * (2048 >> 4), idesc_g,
                       (t > 0 || kk > 0) ? 1u : 0u);
+      if (t + 1 < ntiles && !issue_st(t + 1)) {
+        ok = false;
+        break;
+      }
+      // dK += dS^T Q(t)
+      if (!warp_wait(pb_ready, t & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < kB / 16; ++kk)
         mma_bf16_ts_w(tDK, tP + kk * 8, dqm + kk * (2048 >> 4), idesc_g,
@@ -314,12 +343,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t & 1;
-      if (!warp_wait(s_full, t & 1, abort_flag, p)) {
-        ok = false;
-        break;
-      }
       // the stage's row vectors came by bulk copy: observe their barrier too
-      if (!warp_wait(&q_full[s], (t >> 1) & 1, abort_flag, p)) {
+      if (!warp_wait(sa_full, t & 1, abort_flag, p) ||
+          !warp_wait(&q_full[s], (t >> 1) & 1, abort_flag, p)) {
         ok = false;
         break;
       }
@@ -329,11 +355,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* dvv = lse2v + kB;
       // column c (query qt*128 + c) is visible to this key row iff c >= cmin
       const int cmin = p.causal ? k_idx - off - qt * kB : -(1 << 30);
-#pragma unroll 1
+      // P^T: written to tensor memory for dV and kept in registers (bf16
+      // pairs) for dS^T, because S^T of the next tile replaces it.
+      uint32_t pkeep[kB / 2];
+#pragma unroll
       for (int c4 = 0; c4 < kB / 32; ++c4) {
         uint32_t ra[32];
         float pf[32];
-        uint32_t pk[16];
         tmem_ld_x32(taddr + 32 * c4, ra);
         tmem_ld_wait_b();
 #pragma unroll
@@ -343,21 +371,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const float x = fmaf(__uint_as_float(ra[e]), p.scale2, -lse2v[col]);
           pf[e] = (col >= cmin) ? ex2_approx(x) : 0.f;
         }
-        pack32(pf, pk);
-        tmem_st_x16(taddr + 16 * c4, pk);
+        pack32(pf, pkeep + 16 * c4);
+        tmem_st_x16(taddr + 16 * c4, pkeep + 16 * c4);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(pa_ready);
+      // dS^T = P^T (dP^T - D), from the bf16 P^T
+      if (!warp_wait(sb_full, t & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+#pragma unroll
+      for (int c4 = 0; c4 < kB / 32; ++c4) {
+        uint32_t ra[32];
+        float pf[32];
+        uint32_t pk[16];
         tmem_ld_x32(taddr + kB + 32 * c4, ra);
         tmem_ld_wait_b();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          reg_fence_b(ra[e]);
-          pf[e] = pf[e] * (__uint_as_float(ra[e]) - dvv[32 * c4 + e]);
+        for (int e = 0; e < 16; ++e) {
+          reg_fence_b(ra[2 * e]);
+          reg_fence_b(ra[2 * e + 1]);
+          const uint32_t w = pkeep[16 * c4 + e];
+          const float p0 = __uint_as_float(w << 16), p1 = __uint_as_float(w & 0xffff0000u);
+          pf[2 * e] = p0 * (__uint_as_float(ra[2 * e]) - dvv[32 * c4 + 2 * e]);
+          pf[2 * e + 1] = p1 * (__uint_as_float(ra[2 * e + 1]) - dvv[32 * c4 + 2 * e + 1]);
         }
         pack32(pf, pk);
         tmem_st_x16(taddr + kB + 16 * c4, pk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(p_ready);
+      mbar_arrive(pb_ready);
     }
     if (ok && warp_wait(done, 0, abort_flag, p)) {
       tc_fence_after_sync();
@@ -416,11 +463,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* qd_full = bars;      // Q and dO landed
   uint64_t* kv_full = bars + 1;  // [2] K and V of a key tile landed
   uint64_t* kv_free = bars + 3;  // [2] the products reading that stage are done
-  uint64_t* s_full = bars + 5;   // S and dP are in tensor memory
+  uint64_t* sa_full = bars + 5;  // S of a key tile is in tensor memory
   uint64_t* p_ready = bars + 6;  // dS written (128 arrivals)
+  uint64_t* sb_full = bars + 9;  // dP is in tensor memory
   uint64_t* done = bars + 7;
   uint64_t* drain = bars + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  static_assert(2 * kB + D + kB <= 512, "two S buffers, dP and dQ in tensor memory");
   __shared__ int abort_s;
   volatile int* abort_flag = &abort_s;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -442,7 +491,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_free[s], 1);
     }
-    mbar_init(s_full, 1);
+    mbar_init(sa_full, 1);
+    mbar_init(sb_full, 1);
     mbar_init(p_ready, 128);
     mbar_init(done, 1);
     mbar_init(drain, 1);
@@ -458,6 +508,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   auto stage = [&](int s) { return smem + C::kOffKV + s * 2 * C::kTile; };
+  // S of key tile t in one of two buffers: columns [0,128) or [384,512)
+  auto s_col = [&](int t) { return (t & 1) ? 3u * kB : 0u; };
 
   if (warp == kWarpProd) {
     // ================================================================ producer
@@ -488,41 +540,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpIssue) {
     // ================================================================ MMA issuer
+    // Per key tile t the pipe runs dP(t), S(t+1), dQ(t): S of the next tile
+    // goes to the other S buffer while the compute warps form dS(t).
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, kB, false);
     constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, true);
     const uint64_t dq = sdesc_sw128(smem_addr(sQ), 16, 1024);
     const uint64_t ddo = sdesc_sw128(smem_addr(sDO), 16, 1024);
-    const uint32_t tS = tmem, tP = tmem + kB, tDQ = tmem + 2 * kB;
-    bool ok = warp_wait(qd_full, 0, abort_flag, p);
-    if (ok) tc_fence_after_sync();
-    for (int t = 0; ok && t < nkt; ++t) {
+    const uint32_t tP = tmem + kB, tDQ = tmem + 2 * kB;
+    auto issue_s = [&](int t) -> bool {  // S(t) = Q K(t)^T
       const int s = t & 1;
-      if (!warp_wait(&kv_full[s], (t >> 1) & 1, abort_flag, p)) {
-        ok = false;
-        break;
-      }
+      if (!warp_wait(&kv_full[s], (t >> 1) & 1, abort_flag, p)) return false;
       tc_fence_after_sync();
-      const uint32_t st = smem_addr(stage(s));
-      const uint64_t dkk = sdesc_sw128(st, 16, 1024);
-      const uint64_t dvk = sdesc_sw128(st + C::kTile, 16, 1024);
-      // S = Q K^T and dP = dO V^T (M = queries, N = keys, K = d)
+      const uint64_t dkk = sdesc_sw128(smem_addr(stage(s)), 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
-        mma_bf16_ss_w(tS, dq + ko, dkk + ko, idesc_s, kk > 0 ? 1u : 0u);
+        mma_bf16_ss_w(tmem + s_col(t), dq + ko, dkk + ko, idesc_s, kk > 0 ? 1u : 0u);
       }
+      mma_commit_w(sa_full);
+      return true;
+    };
+    bool ok = warp_wait(qd_full, 0, abort_flag, p);
+    if (ok) tc_fence_after_sync();
+    if (ok && nkt > 0) ok = issue_s(0);
+    for (int t = 0; ok && t < nkt; ++t) {
+      const int s = t & 1;
+      const uint32_t st = smem_addr(stage(s));
+      const uint64_t dvk = sdesc_sw128(st + C::kTile, 16, 1024);
+      // dP(t) = dO V(t)^T (M = queries, N = keys, K = d)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
         mma_bf16_ss_w(tP, ddo + ko, dvk + ko, idesc_s, kk > 0 ? 1u : 0u);
       }
-      mma_commit_w(s_full);
+      mma_commit_w(sb_full);
+      if (t + 1 < nkt && !issue_s(t + 1)) {
+        ok = false;
+        break;
+      }
       if (!warp_wait(p_ready, t & 1, abort_flag, p)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      // dQ += dS K (A = dS from tensor memory, K = keys; B = the K tile read along d)
+      // dQ += dS K(t) (A = dS from tensor memory, K = keys; B = K(t) read along d)
       const uint64_t dkm = sdesc_sw128(st, C::kAtomBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < kB / 16; ++kk)
@@ -543,7 +604,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float dval = p.dvec[vrow];
     bool ok = true;
     for (int t = 0; t < nkt; ++t) {
-      if (!warp_wait(s_full, t & 1, abort_flag, p)) {
+      if (!warp_wait(sa_full, t & 1, abort_flag, p) || !warp_wait(sb_full, t & 1, abort_flag, p)) {
         ok = false;
         break;
       }
@@ -556,7 +617,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t ra[32], rb[32];
         float pf[32];
         uint32_t pk[16];
-        tmem_ld_x32(taddr + 32 * c4, ra);
+        tmem_ld_x32(taddr + s_col(t) + 32 * c4, ra);
         tmem_ld_x32(taddr + kB + 32 * c4, rb);
         tmem_ld_wait_b();
 #pragma unroll
