@@ -107,38 +107,43 @@ __device__ __forceinline__ void bwd_fail(int* status, volatile int* abort_flag) 
   if (abort_flag) *abort_flag = 1;
 }
 
-// One warp per query row: D = sum_t dO_t O_t (fp32) and LSE2 = LSE log2(e);
-// rows past Sq (to the tile boundary) and rows whose LSE is -inf (no key)
-// get LSE2 = +inf and D = 0, so every P built from them is 0.
+// Eight lanes per query row (four rows per warp at a time): D = sum_t dO_t
+// O_t (fp32) and LSE2 = LSE log2(e); rows past Sq (to the tile boundary) and
+// rows whose LSE is -inf (no key) get LSE2 = +inf and D = 0, so every P
+// built from them is 0.
 __global__ void attn_bwd_rowstat_kernel(BwdParams p) {
-  const int lane = threadIdx.x % 32;
+  const int lane = threadIdx.x % 32, sub = lane / 8, l8 = lane % 8;
   const long long nrow = static_cast<long long>(p.B) * p.Hq * p.Sqp;
-  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
-  for (long long rw = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
-       rw < nrow; rw += wstride) {
-    const int i = static_cast<int>(rw % p.Sqp);
-    const long long bh = rw / p.Sqp;
-    const int h = static_cast<int>(bh % p.Hq), b = static_cast<int>(bh / p.Hq);
+  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x / 32) * 4;
+  for (long long rw0 = (static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * 4;
+       rw0 < nrow; rw0 += wstride) {
+    const long long rw = rw0 + sub;
     float acc = 0.f, l2 = INFINITY;
-    if (i < p.Sq) {
-      const size_t base = ((static_cast<size_t>(b) * p.Sq + i) * p.Hq + h) * p.d;
-      for (int t = lane * 4; t < p.d; t += 128) {  // four bf16 (8 bytes) per lane
-        const uint2 g = *reinterpret_cast<const uint2*>(p.dout + base + t);
-        const uint2 o = *reinterpret_cast<const uint2*>(p.o + base + t);
-        const uint32_t gw[2] = {g.x, g.y}, ow[2] = {o.x, o.y};
+    int i = 0;
+    if (rw < nrow) {
+      i = static_cast<int>(rw % p.Sqp);
+      const long long bh = rw / p.Sqp;
+      const int h = static_cast<int>(bh % p.Hq), b = static_cast<int>(bh / p.Hq);
+      if (i < p.Sq) {
+        const size_t base = ((static_cast<size_t>(b) * p.Sq + i) * p.Hq + h) * p.d;
+        for (int t = l8 * 8; t < p.d; t += 64) {  // eight bf16 (16 bytes) per lane
+          const uint4 g = *reinterpret_cast<const uint4*>(p.dout + base + t);
+          const uint4 o = *reinterpret_cast<const uint4*>(p.o + base + t);
+          const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          acc = fmaf(__uint_as_float(gw[e] << 16), __uint_as_float(ow[e] << 16), acc);
-          acc = fmaf(__uint_as_float(gw[e] & 0xffff0000u), __uint_as_float(ow[e] & 0xffff0000u),
-                     acc);
+          for (int e = 0; e < 4; ++e) {
+            acc = fmaf(__uint_as_float(gw[e] << 16), __uint_as_float(ow[e] << 16), acc);
+            acc = fmaf(__uint_as_float(gw[e] & 0xffff0000u),
+                       __uint_as_float(ow[e] & 0xffff0000u), acc);
+          }
         }
+        const float l = p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Sq + i];
+        l2 = (l == -INFINITY) ? INFINITY : l * kLog2eB;
       }
-      const float l = p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Sq + i];
-      l2 = (l == -INFINITY) ? INFINITY : l * kLog2eB;
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
+    for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (l8 == 0 && rw < nrow) {
       p.dvec[rw] = (i < p.Sq) ? acc : 0.f;
       p.lse2[rw] = l2;
     }
