@@ -89,3 +89,34 @@ def test_decode_argument_errors_without_gpu():
     bad[8] = 3    # Hq % Hkv
     assert L.attn_decode_paged(*bad) == ea.ATTN_ERR_INVALID_ARG
     assert L.attn_check_wait_timeout(0, None) == ea.ATTN_ERR_INVALID_ARG
+
+
+def test_argument_errors_of_the_newer_entry_points_without_gpu():
+    """Checks that run before any CUDA call: the strided, paged, sink and
+    backward entry points reject bad arguments without a device."""
+    import exact_attention_08_gb300 as ea
+    L = ea.lib
+    buf = ctypes.create_string_buffer(256)
+    p = ctypes.cast(buf, ctypes.c_void_p).value
+    p16 = (p + 15) & ~15
+    S3 = ctypes.c_longlong * 3
+    # strided: a stride that is not a multiple of 16 bytes
+    bad = S3(128 * 2 * 64, 128 * 2 + 4, 128)
+    assert L.attn_fwd_strided(p16, p16, p16, p16, None, 1, 2, 2, 64, 64, 128, bad, None, None,
+                              None, 0.1, 0, 0, 0, None, None) == ea.ATTN_ERR_INVALID_ARG
+    # paged: page size other than 16, head dim 96, window without causal
+    assert L.attn_fwd_paged(p16, p16, p16, p16, p16, p16, p16, None, 1, 2, 2, 8, 8, 128, 32, 4,
+                            4, 0.1, 1, 0, 0, None, None) == ea.ATTN_ERR_UNSUPPORTED
+    assert L.attn_fwd_paged(p16, p16, p16, p16, p16, p16, p16, None, 1, 2, 2, 8, 8, 96, 16, 4,
+                            4, 0.1, 1, 0, 0, None, None) == ea.ATTN_ERR_UNSUPPORTED
+    assert L.attn_fwd_paged(p16, p16, p16, p16, p16, p16, p16, None, 1, 2, 2, 8, 8, 128, 16, 4,
+                            4, 0.1, 0, 8, 0, None, None) == ea.ATTN_ERR_INVALID_ARG
+    # sink: a misaligned sink pointer
+    assert L.attn_fwd_ex_sink(p16, p16, p16, p16, None, None, None, 1, 2, 2, 8, 8, 0, 0, 128, 0.1,
+                              0, 0, 0, p16 + 2, None) == ea.ATTN_ERR_INVALID_ARG
+    # backward: Hq not a multiple of Hkv, too small a workspace
+    assert L.attn_bwd(p16, p16, p16, p16, p16, p16, p16, p16, p16, 1, 3, 2, 8, 8, 128, 0.1, 0,
+                      p16, 1 << 20, None) == ea.ATTN_ERR_INVALID_ARG
+    assert L.attn_bwd(p16, p16, p16, p16, p16, p16, p16, p16, p16, 1, 2, 2, 300, 8, 128, 0.1, 0,
+                      p16, 16, None) == ea.ATTN_ERR_INVALID_ARG
+    assert ea.attn_bwd_workspace_size(1, 2, 300) == 2 * 2 * 384 * 4
