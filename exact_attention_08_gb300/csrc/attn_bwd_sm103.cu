@@ -84,8 +84,8 @@ struct BwdParams {
   const __nv_bfloat16* dout;  // [B, Sq, Hq, d] (row statistics only)
   const __nv_bfloat16* o;
   const float* lse;          // [B, Hq, Sq], natural log
-  float* lse2;               // [B, Hq, Sqp] workspace: LSE * log2(e), +inf on pad rows
-  float* dvec;               // [B, Hq, Sqp] workspace: rowsum(dO * O)
+  float* lse2;               // [B, Hq, Sqp] workspace: -LSE * log2(e), -inf on pad rows
+  float* dvec;               // [B, Hq, Sqp] workspace: -rowsum(dO * O)
   __nv_bfloat16* dq;         // [B, Sq, Hq, d]
   __nv_bfloat16* dk;         // [B, Skv, Hkv, d]
   __nv_bfloat16* dv;
@@ -98,6 +98,30 @@ struct BwdParams {
 
 __device__ __forceinline__ void reg_fence_b(uint32_t& r) { asm volatile("" : "+r"(r)); }
 
+__device__ __forceinline__ uint64_t pf2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void pf2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t pf2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t pf2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t pf2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 __device__ __forceinline__ void tmem_ld_wait_b() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -108,9 +132,9 @@ __device__ __forceinline__ void bwd_fail(int* status, volatile int* abort_flag) 
 }
 
 // Eight lanes per query row (four rows per warp at a time): D = sum_t dO_t
-// O_t (fp32) and LSE2 = LSE log2(e); rows past Sq (to the tile boundary) and
-// rows whose LSE is -inf (no key) get LSE2 = +inf and D = 0, so every P
-// built from them is 0.
+// O_t (fp32) and LSE2 = LSE log2(e), both stored negated (the kernels add
+// them); rows past Sq (to the tile boundary) and rows whose LSE is -inf (no
+// key) get -LSE2 = -inf and D = 0, so every P built from them is 0.
 __global__ void attn_bwd_rowstat_kernel(BwdParams p) {
   const int lane = threadIdx.x % 32, sub = lane / 8, l8 = lane % 8;
   const long long nrow = static_cast<long long>(p.B) * p.Hq * p.Sqp;
@@ -144,8 +168,8 @@ __global__ void attn_bwd_rowstat_kernel(BwdParams p) {
 #pragma unroll
     for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (l8 == 0 && rw < nrow) {
-      p.dvec[rw] = (i < p.Sq) ? acc : 0.f;
-      p.lse2[rw] = l2;
+      p.dvec[rw] = (i < p.Sq) ? -acc : 0.f;  // stored negated: added, not subtracted
+      p.lse2[rw] = -l2;
     }
   }
 }
@@ -360,6 +384,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* dvv = lse2v + kB;
       // column c (query qt*128 + c) is visible to this key row iff c >= cmin
       const int cmin = p.causal ? k_idx - off - qt * kB : -(1 << 30);
+      const uint64_t sc2 = pf2(p.scale2, p.scale2);
       // P^T: written to tensor memory for dV and kept in registers (bf16
       // pairs) for dS^T, because S^T of the next tile replaces it.
       uint32_t pkeep[kB / 2];
@@ -369,12 +394,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         float pf[32];
         tmem_ld_x32(taddr + 32 * c4, ra);
         tmem_ld_wait_b();
+        // x = S scale2 - LSE2 in pairs (the vector holds -LSE2); the mask is
+        // applied only to a chunk the diagonal crosses
+        const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(lse2v + 32 * c4);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          reg_fence_b(ra[e]);
-          const int col = 32 * c4 + e;
-          const float x = fmaf(__uint_as_float(ra[e]), p.scale2, -lse2v[col]);
-          pf[e] = (col >= cmin) ? ex2_approx(x) : 0.f;
+        for (int e = 0; e < 16; ++e) {
+          reg_fence_b(ra[2 * e]);
+          reg_fence_b(ra[2 * e + 1]);
+          const uint64_t x2 = pf2_fma(pf2(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])),
+                                      sc2, nl2[e]);
+          float x0, x1;
+          pf2_split(x2, x0, x1);
+          pf[2 * e] = ex2_approx(x0);
+          pf[2 * e + 1] = ex2_approx(x1);
+        }
+        if (cmin > 32 * c4) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * c4 + e < cmin) pf[e] = 0.f;
         }
         pack32(pf, pkeep + 16 * c4);
         tmem_st_x16(taddr + 16 * c4, pkeep + 16 * c4);
@@ -395,14 +432,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t pk[16];
         tmem_ld_x32(taddr + kB + 32 * c4, ra);
         tmem_ld_wait_b();
+        const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(dvv + 32 * c4);  // -D in pairs
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           reg_fence_b(ra[2 * e]);
           reg_fence_b(ra[2 * e + 1]);
           const uint32_t w = pkeep[16 * c4 + e];
-          const float p0 = __uint_as_float(w << 16), p1 = __uint_as_float(w & 0xffff0000u);
-          pf[2 * e] = p0 * (__uint_as_float(ra[2 * e]) - dvv[32 * c4 + 2 * e]);
-          pf[2 * e + 1] = p1 * (__uint_as_float(ra[2 * e + 1]) - dvv[32 * c4 + 2 * e + 1]);
+          const uint64_t p2 = pf2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+          const uint64_t g2 = pf2_add(pf2(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])),
+                                      nd2[e]);
+          pf2_split(pf2_mul(p2, g2), pf[2 * e], pf[2 * e + 1]);
         }
         pack32(pf, pk);
         tmem_st_x16(taddr + kB + 16 * c4, pk);
@@ -605,8 +644,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int q_idx = q0 + r;
     const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const size_t vrow = (static_cast<size_t>(b) * p.Hq + h) * p.Sqp + q_idx;
-    const float lse2 = p.lse2[vrow];  // +inf past Sq: every P of the row is 0
-    const float dval = p.dvec[vrow];
+    const float nlse2 = p.lse2[vrow];  // -LSE2; -inf past Sq: every P of the row is 0
+    const float ndval = p.dvec[vrow];  // -D
+    const uint64_t sc2 = pf2(p.scale2, p.scale2), nl2 = pf2(nlse2, nlse2), nd2 = pf2(ndval, ndval);
     bool ok = true;
     for (int t = 0; t < nkt; ++t) {
       if (!warp_wait(sa_full, t & 1, abort_flag, p) || !warp_wait(sb_full, t & 1, abort_flag, p)) {
@@ -626,13 +666,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld_x32(taddr + kB + 32 * c4, rb);
         tmem_ld_wait_b();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          reg_fence_b(ra[e]);
-          reg_fence_b(rb[e]);
-          const int col = 32 * c4 + e;
-          const float pv =
-              (col <= cmax) ? ex2_approx(fmaf(__uint_as_float(ra[e]), p.scale2, -lse2)) : 0.f;
-          pf[e] = pv * (__uint_as_float(rb[e]) - dval);
+        for (int e = 0; e < 16; ++e) {
+          reg_fence_b(ra[2 * e]);
+          reg_fence_b(ra[2 * e + 1]);
+          reg_fence_b(rb[2 * e]);
+          reg_fence_b(rb[2 * e + 1]);
+          float x0, x1;
+          pf2_split(pf2_fma(pf2(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])), sc2, nl2),
+                    x0, x1);
+          const uint64_t p2 = pf2(ex2_approx(x0), ex2_approx(x1));
+          const uint64_t g2 = pf2_add(pf2(__uint_as_float(rb[2 * e]), __uint_as_float(rb[2 * e + 1])),
+                                      nd2);
+          pf2_split(pf2_mul(p2, g2), pf[2 * e], pf[2 * e + 1]);
+        }
+        if (cmax < 32 * c4 + 31) {  // a chunk the diagonal or the key tail crosses
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * c4 + e > cmax) pf[e] = 0.f;
         }
         pack32(pf, pk);
         tmem_st_x16(taddr + kB + 16 * c4, pk);
