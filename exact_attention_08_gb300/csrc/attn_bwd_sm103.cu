@@ -224,7 +224,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = &abort_s;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  // Blocks go out in index order: key tile outermost, so that under a causal
+  // mask (where key tile 0 has the most query tiles) the longest come first.
+  const int kt = blockIdx.x / (p.B * p.Hkv), hk = (blockIdx.x / p.B) % p.Hkv, b = blockIdx.x % p.B;
   const int G = p.Hq / p.Hkv;
   const int nqt = p.Sqp / kB;
   const int off = p.Skv - p.Sq;
@@ -518,7 +520,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = &abort_s;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // Query tile outermost, the last (under a causal mask the longest) first.
+  const int nqt_all = p.Sqp / kB;
+  const int qt = nqt_all - 1 - static_cast<int>(blockIdx.x / (p.B * p.Hq));
+  const int h = (blockIdx.x / p.B) % p.Hq, b = blockIdx.x % p.B;
   const int hk = h / (p.Hq / p.Hkv);
   const int q0 = qt * kB;
   const int off = p.Skv - p.Sq;
@@ -763,12 +768,12 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.Skv > 0) {
-    dim3 g1((a.Skv + kB - 1) / kB, a.Hkv, a.B);
+    dim3 g1(((a.Skv + kB - 1) / kB) * a.Hkv * a.B);
     attn_bwd_dkdv_kernel<D><<<g1, kBwdThreads, C::kLaunchKV, stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO,
                                                                      p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  dim3 g2(p.Sqp / kB, a.Hq, a.B);
+  dim3 g2((p.Sqp / kB) * a.Hq * a.B);
   attn_bwd_dq_kernel<D><<<g2, kBwdThreads, C::kLaunchQ, stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO, p);
   return cudaGetLastError();
 }
