@@ -19,14 +19,17 @@
 //   attn_bwd_rowstat_kernel  D and LSE in base 2 per query row, padded to
 //                            whole 128-row tiles (+inf LSE on pad rows and
 //                            on rows that saw no key, so their P is 0);
-//   attn_bwd_dkdv_kernel<D>  warps 0-3: S^T -> P^T, dP^T -> dS^T (thread r
-//                            owns key row r of the tile); warp 4: TMA
-//                            producer (K, V once; Q, dO and the two row
-//                            vectors per query tile, two stages); warp 5:
+//   attn_bwd_dkdv_kernel<D>  warps 0-7: S^T -> P^T, dP^T -> dS^T (warps w
+//                            and w+4 share key row 32 (w % 4) + lane and
+//                            split the 128 query columns in halves); warp 8:
+//                            TMA producer (K, V once; Q, dO and the two row
+//                            vectors per query tile, two stages); warp 9:
 //                            MMA issuer.  Tensor memory: S^T [0,128),
 //                            dP^T [128,256), dV [256,256+D), dK [256+D,..).
 //   attn_bwd_dq_kernel<D>    the same roles over key tiles for one query
-//                            tile: S [0,128), dP [128,256), dQ [256,256+D).
+//                            tile: S [0,128) and [384,512) alternately,
+//                            dP [128,256), dQ [256,256+D); P is formed from
+//                            S(t) while dQ(t-1) and dP(t) run.
 // Products (tcgen05, kind::f16, M=128, fp32 in tensor memory):
 //   S^T = K Q^T, dP^T = V dO^T   (both operands K-major in shared memory)
 //   dV += P^T dO, dK += dS^T Q   (A from tensor memory, B MN-major)
@@ -48,9 +51,14 @@ namespace {
 using namespace ptx;
 
 constexpr int kB = 128;          // rows of every tile (keys or queries)
-constexpr int kBwdThreads = 192;  // warps 0-3 compute, 4 producer, 5 MMA
-constexpr int kWarpProd = 4;
-constexpr int kWarpIssue = 5;
+// Warps 0-7 compute, 8 producer, 9 MMA.  Compute warp w reads tensor-memory
+// lanes 32 (w % 4) .. +31 (its sub-partition's quarter) and the column half
+// w / 4 of every 128-column tile, so each sub-partition runs two of them.
+constexpr int kComputeWarps = 8;
+constexpr int kBwdThreads = 32 * (kComputeWarps + 2);
+constexpr int kWarpProd = kComputeWarps;
+constexpr int kWarpIssue = kComputeWarps + 1;
+constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr float kLog2eB = 1.4426950408889634f;
 
 template <int D>
@@ -122,8 +130,28 @@ __device__ __forceinline__ uint64_t pf2_mul(uint64_t a, uint64_t b) {
   return r;
 }
 
+// Four consecutive floats of shared memory as two pairs (one 16-byte load).
+// Volatile, so it stays after the barrier wait that makes the data valid.
+__device__ __forceinline__ void lds_pairs2(uint32_t addr, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
+}
+// One 32-column chunk of a row vector: 16 pairs.
+__device__ __forceinline__ void lds_chunk(uint32_t addr, uint64_t* v) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) lds_pairs2(addr + 16 * i, v[2 * i], v[2 * i + 1]);
+}
+
 __device__ __forceinline__ void tmem_ld_wait_b() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// A 128-column fp32 tile rewritten in place as bf16 pairs: the 32-column
+// chunk c goes to 16 columns at 64 (c / 2) + 16 (c % 2), inside the column
+// half that holds its source, so the warp that reads a half is the only one
+// that writes it.  K-step kk (16 columns of the tile) of an MMA that takes
+// the packed tile as its A operand starts at packed_col(kk).
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+  return static_cast<uint32_t>(64 * (kk / 4) + 8 * (kk % 4));
 }
 
 __device__ __forceinline__ void bwd_fail(int* status, volatile int* abort_flag) {
@@ -205,8 +233,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          const __grid_constant__ CUtensorMap tmDO, BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBarKV);
@@ -215,8 +242,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* q_free = bars + 3;    // [2] the products reading that stage are done
   uint64_t* sa_full = bars + 5;   // S^T is in tensor memory
   uint64_t* sb_full = bars + 6;   // dP^T is in tensor memory
-  uint64_t* pa_ready = bars + 7;  // P^T written (128 arrivals)
-  uint64_t* pb_ready = bars + 11; // dS^T written (128 arrivals)
+  uint64_t* pa_ready = bars + 7;  // P^T written (one arrival per compute thread)
+  uint64_t* pb_ready = bars + 11; // dS^T written (one arrival per compute thread)
   uint64_t* done = bars + 8;      // every product of the CTA is done
   uint64_t* drain = bars + 9;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
@@ -247,8 +274,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(sa_full, 1);
     mbar_init(sb_full, 1);
-    mbar_init(pa_ready, 128);
-    mbar_init(pb_ready, 128);
+    mbar_init(pa_ready, kComputeThreads);
+    mbar_init(pb_ready, kComputeThreads);
     mbar_init(done, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -344,7 +371,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t ddom = sdesc_sw128(st + C::kTile, C::kAtomBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < kB / 16; ++kk)
-        mma_bf16_ts_w(tDV, tS + kk * 8, ddom + kk * (2048 >> 4), idesc_g,
+        mma_bf16_ts_w(tDV, tS + packed_col(kk), ddom + kk * (2048 >> 4), idesc_g,
                       (t > 0 || kk > 0) ? 1u : 0u);
       if (t + 1 < ntiles && !issue_st(t + 1)) {
         ok = false;
@@ -358,7 +385,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < kB / 16; ++kk)
-        mma_bf16_ts_w(tDK, tP + kk * 8, dqm + kk * (2048 >> 4), idesc_g,
+        mma_bf16_ts_w(tDK, tP + packed_col(kk), dqm + kk * (2048 >> 4), idesc_g,
                       (t > 0 || kk > 0) ? 1u : 0u);
       mma_commit_w(&q_free[s]);
     }
@@ -366,11 +393,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // Every product issued has finished before tensor memory is released.
     mma_commit_w(drain);
     warp_wait(drain, 0, nullptr, p);
-  } else if (warp < 4) {
+  } else if (warp < kComputeWarps) {
     // ================================================================ compute warps
-    const int r = warp * 32 + lane;
+    const int wq = warp & 3, wh = warp >> 2;  // lane quarter, column half
+    const int r = wq * 32 + lane;
     const int k_idx = k0 + r;
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint64_t sc2 = pf2(p.scale2, p.scale2);
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t & 1;
@@ -382,41 +411,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tc_fence_after_sync();
       const int qt = qt_lo + t % nq;
-      const float* lse2v = reinterpret_cast<const float*>(stage(s) + 2 * C::kTile);
-      const float* dvv = lse2v + kB;
+      // this warp's 64 entries of the two row vectors (-LSE2, -D)
+      const uint32_t nl2_addr = smem_addr(stage(s) + 2 * C::kTile) + 4 * 64 * wh;
+      const uint32_t nd2_addr = nl2_addr + 4 * kB;
       // column c (query qt*128 + c) is visible to this key row iff c >= cmin
       const int cmin = p.causal ? k_idx - off - qt * kB : -(1 << 30);
-      const uint64_t sc2 = pf2(p.scale2, p.scale2);
-      // P^T: written to tensor memory for dV and kept in registers (bf16
-      // pairs) for dS^T, because S^T of the next tile replaces it.
-      uint32_t pkeep[kB / 2];
-#pragma unroll
-      for (int c4 = 0; c4 < kB / 32; ++c4) {
-        uint32_t ra[32];
-        float pf[32];
-        tmem_ld_x32(taddr + 32 * c4, ra);
+      // P^T of this warp's 64 columns: written to tensor memory for dV and
+      // kept in registers (bf16 pairs) for dS^T, because S^T of the next
+      // tile replaces it.
+      uint32_t pkeep[32];
+      {
+        uint32_t ra[64];
+        uint64_t nl2[16];
+        tmem_ld_x32(taddr + 64 * wh, ra);
+        tmem_ld_x32(taddr + 64 * wh + 32, ra + 32);
+        lds_chunk(nl2_addr, nl2);
         tmem_ld_wait_b();
-        // x = S scale2 - LSE2 in pairs (the vector holds -LSE2); the mask is
-        // applied only to a chunk the diagonal crosses
-        const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(lse2v + 32 * c4);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          reg_fence_b(ra[2 * e]);
-          reg_fence_b(ra[2 * e + 1]);
-          const uint64_t x2 = pf2_fma(pf2(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])),
-                                      sc2, nl2[e]);
-          float x0, x1;
-          pf2_split(x2, x0, x1);
-          pf[2 * e] = ex2_approx(x0);
-          pf[2 * e + 1] = ex2_approx(x1);
-        }
-        if (cmin > 32 * c4) {
+        for (int j = 0; j < 2; ++j) {
+          const int c4 = 2 * wh + j;
+          float pf[32];
+          // x = S scale2 - LSE2 in pairs (the vector holds -LSE2); the mask
+          // is applied only to a chunk the diagonal crosses
+          if (j == 1) lds_chunk(nl2_addr + 128, nl2);
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (32 * c4 + e < cmin) pf[e] = 0.f;
+          for (int e = 0; e < 16; ++e) {
+            reg_fence_b(ra[32 * j + 2 * e]);
+            reg_fence_b(ra[32 * j + 2 * e + 1]);
+            const uint64_t x2 = pf2_fma(
+                pf2(__uint_as_float(ra[32 * j + 2 * e]), __uint_as_float(ra[32 * j + 2 * e + 1])),
+                sc2, nl2[e]);
+            float x0, x1;
+            pf2_split(x2, x0, x1);
+            pf[2 * e] = ex2_approx(x0);
+            pf[2 * e + 1] = ex2_approx(x1);
+          }
+          if (cmin > 32 * c4) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (32 * c4 + e < cmin) pf[e] = 0.f;
+          }
+          pack32(pf, pkeep + 16 * j);
+          tmem_st_x16(taddr + 64 * wh + 16 * j, pkeep + 16 * j);
         }
-        pack32(pf, pkeep + 16 * c4);
-        tmem_st_x16(taddr + 16 * c4, pkeep + 16 * c4);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -427,26 +464,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after_sync();
-#pragma unroll
-      for (int c4 = 0; c4 < kB / 32; ++c4) {
-        uint32_t ra[32];
-        float pf[32];
-        uint32_t pk[16];
-        tmem_ld_x32(taddr + kB + 32 * c4, ra);
+      {
+        uint32_t ra[64];
+        uint64_t nd2[16];  // -D in pairs
+        tmem_ld_x32(taddr + kB + 64 * wh, ra);
+        tmem_ld_x32(taddr + kB + 64 * wh + 32, ra + 32);
+        lds_chunk(nd2_addr, nd2);
         tmem_ld_wait_b();
-        const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(dvv + 32 * c4);  // -D in pairs
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          reg_fence_b(ra[2 * e]);
-          reg_fence_b(ra[2 * e + 1]);
-          const uint32_t w = pkeep[16 * c4 + e];
-          const uint64_t p2 = pf2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-          const uint64_t g2 = pf2_add(pf2(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])),
-                                      nd2[e]);
-          pf2_split(pf2_mul(p2, g2), pf[2 * e], pf[2 * e + 1]);
+        for (int j = 0; j < 2; ++j) {
+          float pf[32];
+          uint32_t pk[16];
+          if (j == 1) lds_chunk(nd2_addr + 128, nd2);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            reg_fence_b(ra[32 * j + 2 * e]);
+            reg_fence_b(ra[32 * j + 2 * e + 1]);
+            const uint32_t w = pkeep[16 * j + e];
+            const uint64_t p2 = pf2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+            const uint64_t g2 = pf2_add(
+                pf2(__uint_as_float(ra[32 * j + 2 * e]), __uint_as_float(ra[32 * j + 2 * e + 1])),
+                nd2[e]);
+            pf2_split(pf2_mul(p2, g2), pf[2 * e], pf[2 * e + 1]);
+          }
+          pack32(pf, pk);
+          tmem_st_x16(taddr + kB + 64 * wh + 16 * j, pk);
         }
-        pack32(pf, pk);
-        tmem_st_x16(taddr + kB + 16 * c4, pk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -456,12 +499,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after_sync();
       const bool valid = k_idx < p.Skv;
       const size_t orow = ((static_cast<size_t>(b) * p.Skv + k_idx) * p.Hkv + hk) * D;
+      constexpr int kHalfChunks = D / 64;  // 32-column chunks in a column half
 #pragma unroll 1
       for (int g = 0; g < 2; ++g) {  // 0: dV, 1: dK (times scale)
         __nv_bfloat16* dst = (g == 0 ? p.dv : p.dk) + orow;
         const float mul = g == 0 ? 1.f : p.scale;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = wh * kHalfChunks; c < (wh + 1) * kHalfChunks; ++c) {
           uint32_t ra[32];
           if (ntiles > 0) {
             tmem_ld_x32(taddr + 2 * kB + g * D + 32 * c, ra);
@@ -501,8 +545,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tmDO, BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sDO = smem + C::kOffDO;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBarQ);
@@ -510,7 +553,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* kv_full = bars + 1;  // [2] K and V of a key tile landed
   uint64_t* kv_free = bars + 3;  // [2] the products reading that stage are done
   uint64_t* sa_full = bars + 5;  // S of a key tile is in tensor memory
-  uint64_t* p_ready = bars + 6;  // dS written (128 arrivals)
+  uint64_t* p_ready = bars + 6;  // dS written (one arrival per compute thread)
   uint64_t* sb_full = bars + 9;  // dP is in tensor memory
   uint64_t* done = bars + 7;
   uint64_t* drain = bars + 8;
@@ -542,7 +585,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(sa_full, 1);
     mbar_init(sb_full, 1);
-    mbar_init(p_ready, 128);
+    mbar_init(p_ready, kComputeThreads);
     mbar_init(done, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -636,25 +679,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t dkm = sdesc_sw128(st, C::kAtomBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < kB / 16; ++kk)
-        mma_bf16_ts_w(tDQ, tP + kk * 8, dkm + kk * (2048 >> 4), idesc_g,
+        mma_bf16_ts_w(tDQ, tP + packed_col(kk), dkm + kk * (2048 >> 4), idesc_g,
                       (t > 0 || kk > 0) ? 1u : 0u);
       mma_commit_w(&kv_free[s]);
     }
     mma_commit_w(done);
     mma_commit_w(drain);
     warp_wait(drain, 0, nullptr, p);
-  } else if (warp < 4) {
+  } else if (warp < kComputeWarps) {
     // ================================================================ compute warps
-    const int r = warp * 32 + lane;
+    const int wq = warp & 3, wh = warp >> 2;  // lane quarter, column half
+    const int r = wq * 32 + lane;
     const int q_idx = q0 + r;
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const size_t vrow = (static_cast<size_t>(b) * p.Hq + h) * p.Sqp + q_idx;
     const float nlse2 = p.lse2[vrow];  // -LSE2; -inf past Sq: every P of the row is 0
     const float ndval = p.dvec[vrow];  // -D
     const uint64_t sc2 = pf2(p.scale2, p.scale2), nl2 = pf2(nlse2, nlse2), nd2 = pf2(ndval, ndval);
     bool ok = true;
     for (int t = 0; t < nkt; ++t) {
-      if (!warp_wait(sa_full, t & 1, abort_flag, p) || !warp_wait(sb_full, t & 1, abort_flag, p)) {
+      // P of this warp's 64 columns from S(t), while dQ(t-1) and dP(t) run
+      if (!warp_wait(sa_full, t & 1, abort_flag, p)) {
         ok = false;
         break;
       }
@@ -662,35 +707,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // column c (key t*128 + c) is visible to this row iff c <= cmax
       int cmax = p.Skv - 1 - t * kB;
       if (p.causal) cmax = min(cmax, q_idx + off - t * kB);
-#pragma unroll 1
-      for (int c4 = 0; c4 < kB / 32; ++c4) {
-        uint32_t ra[32], rb[32];
-        float pf[32];
-        uint32_t pk[16];
-        tmem_ld_x32(taddr + s_col(t) + 32 * c4, ra);
-        tmem_ld_x32(taddr + kB + 32 * c4, rb);
+      uint64_t pp[32];  // P in fp32 pairs
+      {
+        uint32_t ra[64];
+        tmem_ld_x32(taddr + s_col(t) + 64 * wh, ra);
+        tmem_ld_x32(taddr + s_col(t) + 64 * wh + 32, ra + 32);
         tmem_ld_wait_b();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < 32; ++e) {
           reg_fence_b(ra[2 * e]);
           reg_fence_b(ra[2 * e + 1]);
-          reg_fence_b(rb[2 * e]);
-          reg_fence_b(rb[2 * e + 1]);
           float x0, x1;
           pf2_split(pf2_fma(pf2(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])), sc2, nl2),
                     x0, x1);
-          const uint64_t p2 = pf2(ex2_approx(x0), ex2_approx(x1));
-          const uint64_t g2 = pf2_add(pf2(__uint_as_float(rb[2 * e]), __uint_as_float(rb[2 * e + 1])),
-                                      nd2);
-          pf2_split(pf2_mul(p2, g2), pf[2 * e], pf[2 * e + 1]);
+          pp[e] = pf2(ex2_approx(x0), ex2_approx(x1));
         }
-        if (cmax < 32 * c4 + 31) {  // a chunk the diagonal or the key tail crosses
+      }
+      // dS = P (dP - D) once dP(t) is in tensor memory
+      if (!warp_wait(sb_full, t & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      {
+        uint32_t rb[64];
+        tmem_ld_x32(taddr + kB + 64 * wh, rb);
+        tmem_ld_x32(taddr + kB + 64 * wh + 32, rb + 32);
+        tmem_ld_wait_b();
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (32 * c4 + e > cmax) pf[e] = 0.f;
+        for (int j = 0; j < 2; ++j) {
+          const int c4 = 2 * wh + j;
+          float pf[32];
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            reg_fence_b(rb[32 * j + 2 * e]);
+            reg_fence_b(rb[32 * j + 2 * e + 1]);
+            const uint64_t g2 = pf2_add(
+                pf2(__uint_as_float(rb[32 * j + 2 * e]), __uint_as_float(rb[32 * j + 2 * e + 1])),
+                nd2);
+            pf2_split(pf2_mul(pp[16 * j + e], g2), pf[2 * e], pf[2 * e + 1]);
+          }
+          if (cmax < 32 * c4 + 31) {  // a chunk the diagonal or the key tail crosses
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (32 * c4 + e > cmax) pf[e] = 0.f;
+          }
+          pack32(pf, pk);
+          tmem_st_x16(taddr + kB + 64 * wh + 16 * j, pk);
         }
-        pack32(pf, pk);
-        tmem_st_x16(taddr + kB + 16 * c4, pk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -700,8 +765,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after_sync();
       const bool valid = q_idx < p.Sq;
       __nv_bfloat16* dst = p.dq + ((static_cast<size_t>(b) * p.Sq + q_idx) * p.Hq + h) * D;
+      constexpr int kHalfChunks = D / 64;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = wh * kHalfChunks; c < (wh + 1) * kHalfChunks; ++c) {
         uint32_t ra[32];
         if (nkt > 0) {
           tmem_ld_x32(taddr + 2 * kB + 32 * c, ra);

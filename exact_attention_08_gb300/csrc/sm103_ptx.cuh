@@ -16,6 +16,15 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory window rounded up to a 1024-byte boundary (the
+// 128-byte swizzle's atom).  Offsetting the array itself, rather than
+// rounding its address as an integer, keeps the shared address space visible
+// to the compiler, so accesses through the result are shared-memory loads and
+// stores rather than generic ones.
+__device__ __forceinline__ uint8_t* smem_align1024(uint8_t* raw) {
+  return raw + ((1024u - (smem_addr(raw) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
