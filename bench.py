@@ -463,6 +463,31 @@ def main():
         ms_ = statistics.median(a.elapsed_time(b) for a, b in tt)
         fl = 2.5 * prefill_flops(B, H, S, S, d, xb.causal)
         bw["causal" if xb.causal else "noncausal"] = {"ms": ms_, "tflops": fl / (ms_ / 1e3) / 1e12}
+    # head dimension 256 (one Q tile per CTA), B=4 H=16 S=2048
+    d256 = {}
+    for causal_ in (False, True):
+        xd = workloads.dense_inputs(7101 + int(causal_), B, H, H, S, S, 256, causal_)
+        qd, kd, vd = xd.q.to(dev), xd.k.to(dev), xd.v.to(dev)
+        od = torch.empty_like(qd)
+        ld = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+        tt = []
+        for it in range(23):
+            with torch.cuda.stream(stream):
+                flush.fill_(6)
+                a, b = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+                a.record(stream)
+                ea.attn_fwd(qd, kd, vd, od, ld, causal=causal_, scale=xd.scale, stream=stream)
+                b.record(stream)
+            if it >= 3:
+                tt.append((a, b))
+        torch.cuda.synchronize(dev)
+        if ea.attn_device_status(stream) != ea.ATTN_OK:
+            raise RuntimeError("device status reported an error in the d=256 calls")
+        ms_ = statistics.median(a.elapsed_time(b) for a, b in tt)
+        fl = prefill_flops(B, H, S, S, 256, causal_)
+        d256["causal" if causal_ else "noncausal"] = {"ms": ms_,
+                                                     "tflops": fl / (ms_ / 1e3) / 1e12}
+        del qd, kd, vd, od, ld
     sp_ms = statistics.median(a.elapsed_time(b) for a, b in t_sp)
     sd_ms = statistics.median(a.elapsed_time(b) for a, b in t_sd)
     variants = {"logit_sink": {
@@ -478,6 +503,9 @@ def main():
         "backward": dict(bw, note="attn_bwd on the step's prefill inputs (B=4 H=16 S=2048 "
                                   "d=128); FLOPs 2.5x the forward's (five products); "
                                   "10 calls after 3 warm-up calls, L2 flushed before each"),
+        "prefill_d256": dict(d256, workload="B=4 H=16 Sq=Skv=2048 d=256 bf16",
+                             note="attn_fwd, one 128-row Q tile per CTA; 20 calls after 3 "
+                                  "warm-up calls, L2 flushed before each; not in value"),
         "chunked_prefill_paged": {
             "workload": "B=8 Hq=32 Hkv=8 d=128 bf16, cache 2048-8192 keys in 16-key pages, "
                         "last 512 tokens as the causal query block",

@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libattn_gb300.so")
-SOURCES = ["attn_api.cu", "attn_fwd_sm103.cu", "attn_decode_sm103.cu", "attn_bwd_sm103.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd_sm103.cu", "attn_fwd256_sm103.cu", "attn_decode_sm103.cu",
+           "attn_bwd_sm103.cu"]
 HEADERS = ["sm103_ptx.cuh", "attn_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",

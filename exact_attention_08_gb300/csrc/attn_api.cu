@@ -198,7 +198,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
     return set_error(ATTN_ERR_INVALID_ARG, "negative or zero size (B=%d Hq=%d Hkv=%d)", B, Hq, Hkv);
   if (Hq % Hkv != 0)
     return set_error(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
-  if (d != 64 && d != 128) return set_error(ATTN_ERR_UNSUPPORTED, "head dim %d (64 or 128)", d);
+  if (d != 64 && d != 128 && d != 256)
+    return set_error(ATTN_ERR_UNSUPPORTED, "head dim %d (64, 128 or 256)", d);
   if (!(scale > 0.f) || !std::isfinite(scale))
     return set_error(ATTN_ERR_INVALID_ARG, "scale must be finite and positive");
   if (causal != 0 && causal != 1) return set_error(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");

@@ -1,0 +1,547 @@
+// Forward attention for head dimension 256 on sm_103a (tcgen05, TMA, TMEM).
+//
+// The method is the same as the d = 64 / 128 kernel (FlashAttention-2, Alg. 1:
+// S = Q K^T tile by tile, online softmax with a lazily rescaled O, P never
+// leaving the SM, O / l and the row log-sum-exp at the end), with the same
+// masks (causal aligned to the end of the keys, sliding window with sink keys,
+// varlen sequences, "TileLang tutorial, ch.15", sections 3.4 and 5.3) and the
+// same logit sink (section 4.6).  What changes is the budget: two 128-row Q
+// tiles would need 2 x (128 + 256) tensor-memory columns, more than 512, so a
+// CTA takes one Q tile and spends the columns on two S buffers and O:
+//
+//   tensor memory  S[0] [0,128)  S[1] [128,256)  O [256,512)
+//   shared memory  Q (4 atoms of 128 rows x 64 columns, 64 KB), K (4 atoms),
+//                  V (4 atoms), barriers: 192 KB + 1 KB
+//
+// Warps: 0-3 softmax (thread r owns query row q0 + r, lanes of its quarter of
+// tensor memory), 4 TMA producer, 5 MMA issuer.  Per key tile n the issuer
+// runs S(n+1) = Q K(n+1)^T into the other S buffer, then O += P(n) V(n) as soon
+// as the softmax has written P(n) (bf16 pairs over the first 64 columns of
+// S(n)'s buffer): the softmax of one tile overlaps the products of the next.
+// K is released atom by atom (each atom feeds four of the sixteen K-steps of
+// S), so K(n+1) streams in while S(n) is still running; V is released once
+// O += P V has read it.  O += P V is one N = 256 product per K-step.
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int kR = 128;                 // query rows per CTA, keys per key tile
+constexpr int kD = 256;                 // head dimension
+constexpr int kAtom = 128 * 128;        // one 128-row x 64-column bf16 atom (16 KB)
+constexpr int kNAtom = kD / 64;         // atoms per tile
+constexpr int kThr = 192;               // warps 0-3 softmax, 4 producer, 5 MMA issuer
+constexpr int kWarpProducer = 4;
+constexpr int kWarpIssuer = 5;
+constexpr int kOffQ = 0;
+constexpr int kOffK = kNAtom * kAtom;
+constexpr int kOffV = 2 * kNAtom * kAtom;
+constexpr int kOffBar = 3 * kNAtom * kAtom;
+// q_full, k_full[4], k_empty[4], v_full, v_empty, s_full[2], p_ready[2],
+// o_done[2], drain, and the tensor-memory address slot
+constexpr int kNumBars = 1 + kNAtom + kNAtom + 1 + 1 + 2 + 2 + 2 + 1;
+constexpr int kSmem = kOffBar + (kNumBars + 1) * 8 + 1024;
+static_assert(kSmem <= 227 * 1024, "shared memory");
+constexpr uint32_t kColO = 2 * kR;
+// O is rescaled only when the running maximum has grown by more than 2^8 in
+// the exponent since the value the exponentials are taken against (the
+// partial sums stay far from overflow, and the final O / l is unchanged).
+constexpr float kRescaleLog2 = 8.0f;
+constexpr int kNoLowerBound = -(1 << 29);
+
+struct P256 {
+  __nv_bfloat16* o;
+  float* lse;
+  const float* sink;  // logit sink per query head, or null
+  const int* cu_q;    // varlen sequence starts, or null (dense)
+  const int* cu_k;
+  long long o_sb, o_ss, o_sh;  // O strides (elements): batch, row, head
+  int B, Hq, Hkv, Sq, Skv, total_q, num_qt;
+  float scale, scale2;
+  int causal, window, n_sink;
+  uint64_t wait_limit_ns;
+  int* status;
+};
+
+// One CTA's Q tile: coordinates, lengths, and the visible-key bounds of its
+// first and last row (key k is visible to row q iff k <= hi(q) and, with a
+// window, k > lo(q) or k < n_sink).
+struct Tile {
+  int bseq, h, hk, q0, Lq, Lk, off, q_base, k_base, b_coord;
+  int hi_min, hi_max, lo_min, lo_max;
+  int jlo, jhi, sinkT, n_act;
+};
+
+// CTA order: without a causal mask the Q tiles of one (sequence, head) are
+// adjacent so that they read the same K and V through L2; with one, the
+// last (longest) Q tiles of every head come first.
+__device__ __forceinline__ bool decode_tile(const P256& p, Tile& w, bool report) {
+  const int per = p.Hq * p.B;
+  int x = static_cast<int>(blockIdx.x), qt;
+  if (p.causal) {
+    qt = p.num_qt - 1 - x / per;
+    x %= per;
+    w.h = x % p.Hq;
+    w.bseq = x / p.Hq;
+  } else {
+    qt = x % p.num_qt;
+    x /= p.num_qt;
+    w.h = x % p.Hq;
+    w.bseq = x / p.Hq;
+  }
+  if (p.cu_q != nullptr) {
+    const int a = p.cu_q[w.bseq], e = p.cu_q[w.bseq + 1];
+    const int ka = p.cu_k[w.bseq], ke = p.cu_k[w.bseq + 1];
+    if (a < 0 || e < a || e > p.total_q || ka < 0 || ke < ka || e - a > p.Sq) {
+      if (report) atomicOr(p.status, kStatusBadInput);
+      return false;
+    }
+    w.Lq = e - a;
+    w.Lk = ke - ka;
+    w.q_base = a;
+    w.k_base = ka;
+    w.b_coord = 0;
+  } else {
+    w.Lq = p.Sq;
+    w.Lk = p.Skv;
+    w.q_base = 0;
+    w.k_base = 0;
+    w.b_coord = w.bseq;
+  }
+  w.q0 = qt * kR;
+  if (w.q0 >= w.Lq) return false;
+  w.off = w.Lk - w.Lq;
+  w.hk = w.h / (p.Hq / p.Hkv);
+  const int last = min(w.q0 + kR, w.Lq) - 1;
+  w.hi_min = p.causal ? min(w.q0 + w.off, w.Lk - 1) : w.Lk - 1;
+  w.hi_max = p.causal ? min(last + w.off, w.Lk - 1) : w.Lk - 1;
+  w.lo_min = p.window > 0 ? w.q0 + w.off - p.window : kNoLowerBound;
+  w.lo_max = p.window > 0 ? last + w.off - p.window : kNoLowerBound;
+  // Active key tiles: j <= jhi and (j >= jlo or j < sinkT).
+  w.sinkT = p.window > 0 ? (p.n_sink + kR - 1) / kR : 0;
+  if (w.hi_max < 0 || w.Lk <= 0) {
+    w.jlo = 0;
+    w.jhi = -1;
+    w.n_act = 0;
+    return true;
+  }
+  w.jhi = w.hi_max / kR;
+  if (p.window <= 0)
+    w.jlo = 0;
+  else if (w.lo_min >= w.Lk - 1)
+    w.jlo = w.jhi + 1;  // only sink keys are visible
+  else
+    w.jlo = w.lo_min < 0 ? 0 : (w.lo_min + 1) / kR;
+  const int ns = min(w.sinkT, w.jhi + 1);
+  w.n_act = ns + max(0, w.jhi - max(w.jlo, w.sinkT) + 1);
+  return true;
+}
+
+// The n-th active key tile (sink tiles first, then the window's range).
+__device__ __forceinline__ int tile_at(const Tile& w, int n) {
+  const int ns = min(w.sinkT, w.jhi + 1);
+  return n < ns ? n : max(w.jlo, w.sinkT) + (n - ns);
+}
+
+// Does every row of the Q tile see every key of key tile j?
+__device__ __forceinline__ bool interior(const Tile& w, int j, int window, int n_sink) {
+  const int ka = j * kR, kb = ka + kR - 1;
+  if (kb > w.hi_min) return false;
+  if (window > 0 && !(ka > w.lo_max || kb < n_sink)) return false;
+  return true;
+}
+
+__device__ __forceinline__ void reg_fence256(uint32_t& r) { asm volatile("" : "+r"(r)); }
+
+__device__ __forceinline__ void tmem_wait_ld256() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void fail256(int* status, volatile int* abort_flag) {
+  atomicOr(status, kStatusTimeout);
+  *abort_flag = 1;
+}
+
+// Bounded wait by the whole warp (every lane tests; the result is uniform).
+__device__ __forceinline__ bool wwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                      const P256& p) {
+  const bool ok =
+      __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.wait_limit_ns));
+  if (!ok && (threadIdx.x & 31) == 0) fail256(p.status, abort_flag);
+  return ok;
+}
+
+__global__ void __launch_bounds__(kThr, 1)
+    attn_fwd256_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const P256 p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_align1024(smem_raw);
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sK = smem + kOffK;
+  uint8_t* sV = smem + kOffV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;               // [4] K atom a of the current key tile landed
+  uint64_t* k_empty = k_full + kNAtom;       // [4] S has read K atom a
+  uint64_t* v_full = k_empty + kNAtom;       // V tile landed
+  uint64_t* v_empty = v_full + 1;            // O += P V has read V
+  uint64_t* s_full = v_empty + 1;            // [2] S of a key tile is in tensor memory
+  uint64_t* p_ready = s_full + 2;            // [2] P written (128 arrivals)
+  uint64_t* o_done = p_ready + 2;            // [2] O += P V of an even / odd key tile done
+  uint64_t* drain = o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  __shared__ int abort_s;
+  volatile int* abort_flag = &abort_s;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  Tile w;
+  if (!decode_tile(p, w, threadIdx.x == 0)) return;  // uniform over the CTA
+  const int N = w.n_act;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int a = 0; a < kNAtom; ++a) {
+      mbar_init(&k_full[a], 1);
+      mbar_init(&k_empty[a], 1);
+    }
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_ready[b], kR);
+      mbar_init(&o_done[b], 1);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    abort_s = 0;
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpProducer) {
+    // ============================================================ TMA producer
+    int k_cnt[kNAtom] = {0, 0, 0, 0};  // loads issued into each K atom
+    int v_loads = 0;                   // V tiles whose loads were issued
+    if (N > 0) {
+      mbar_arrive_expect_tx_w(q_full, kNAtom * kAtom);
+#pragma unroll
+      for (int a = 0; a < kNAtom; ++a)
+        tma_load_4d_w(sQ + a * kAtom, &tmQ, q_full, a * 64, w.h, w.q_base + w.q0, w.b_coord);
+      auto load_k = [&](int n) {
+        const int k0 = w.k_base + tile_at(w, n) * kR;
+        for (int a = 0; a < kNAtom; ++a) {
+          // atom a is free once S(n - 1) has read it
+          if (n > 0 && !wwait(&k_empty[a], (n - 1) & 1, abort_flag, p)) return false;
+          mbar_arrive_expect_tx_w(&k_full[a], kAtom);
+          tma_load_4d_w(sK + a * kAtom, &tmK, &k_full[a], a * 64, w.hk, k0, w.b_coord);
+          ++k_cnt[a];
+        }
+        return true;
+      };
+      bool ok = load_k(0);
+      for (int n = 0; ok && n < N; ++n) {
+        // K runs one key tile ahead of V: K(n + 1) as S(n) releases its atoms,
+        // V(n) once O += P(n - 1) V(n - 1) has read V(n - 1).
+        if (n + 1 < N && !load_k(n + 1)) break;
+        if (n > 0 && !wwait(v_empty, (n - 1) & 1, abort_flag, p)) break;
+        const int k0 = w.k_base + tile_at(w, n) * kR;
+        mbar_arrive_expect_tx_w(v_full, kNAtom * kAtom);
+#pragma unroll
+        for (int a = 0; a < kNAtom; ++a)
+          tma_load_4d_w(sV + a * kAtom, &tmV, v_full, a * 64, w.hk, k0, w.b_coord);
+        ++v_loads;
+      }
+      // Every copy issued lands before the CTA can leave (a load is issued
+      // only after the previous one into the same buffer has been consumed,
+      // so waiting for the last phase of each barrier covers them all).
+      mbar_wait(q_full, 0, nullptr, p.wait_limit_ns);
+      for (int a = 0; a < kNAtom; ++a)
+        if (k_cnt[a] > 0) mbar_wait(&k_full[a], (k_cnt[a] - 1) & 1, nullptr, p.wait_limit_ns);
+      if (v_loads > 0) mbar_wait(v_full, (v_loads - 1) & 1, nullptr, p.wait_limit_ns);
+    }
+  } else if (warp == kWarpIssuer) {
+    // ============================================================ MMA issuer
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, kR, false);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(128, kD, true);
+    const uint64_t dq = sdesc_sw128(smem_addr(sQ), 16, 1024);
+    const uint64_t dk = sdesc_sw128(smem_addr(sK), 16, 1024);
+    const uint64_t dv = sdesc_sw128(smem_addr(sV), kAtom, 1024);
+    // S(n) = Q K(n)^T into buffer n % 2: K-steps 4a .. 4a+3 read atom a of Q
+    // and K; atom a of K is released as soon as its four steps are done.
+    auto issue_s = [&](int n) -> bool {
+      const uint32_t tS = tmem + (n & 1) * kR;
+#pragma unroll 1
+      for (int a = 0; a < kNAtom; ++a) {
+        if (!wwait(&k_full[a], n & 1, abort_flag, p)) return false;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const uint64_t ko = static_cast<uint64_t>((a * kAtom + s4 * 32) >> 4);
+          mma_bf16_ss_w(tS, dq + ko, dk + ko, idesc_s, (a > 0 || s4 > 0) ? 1u : 0u);
+        }
+        mma_commit_w(&k_empty[a]);
+      }
+      mma_commit_w(&s_full[n & 1]);
+      return true;
+    };
+    bool ok = N > 0 && wwait(q_full, 0, abort_flag, p);
+    if (ok) {
+      tc_fence_after_sync();
+      ok = issue_s(0);
+    }
+    for (int n = 0; ok && n < N; ++n) {
+      if (n + 1 < N && !issue_s(n + 1)) break;
+      // O += P(n) V(n): A = P(n) (bf16 pairs, key-step kk at column 8 kk of
+      // S(n)'s buffer), B = V read along d (N = 256, one product per step).
+      if (!wwait(&p_ready[n & 1], (n >> 1) & 1, abort_flag, p) ||
+          !wwait(v_full, n & 1, abort_flag, p))
+        break;
+      tc_fence_after_sync();
+      const uint32_t tP = tmem + (n & 1) * kR;
+#pragma unroll
+      for (int kk = 0; kk < kR / 16; ++kk)
+        mma_bf16_ts_w(tmem + kColO, tP + 8 * kk, dv + kk * (2048 >> 4), idesc_o,
+                      (n > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_w(v_empty);
+      mma_commit_w(&o_done[n & 1]);
+    }
+    // Every product issued has completed before tensor memory is released.
+    mma_commit_w(drain);
+    mbar_wait(drain, 0, nullptr, p.wait_limit_ns);
+  } else {
+    // ============================================================ softmax warps 0-3
+    const int r = warp * 32 + lane;
+    const int q = w.q0 + r;  // sequence-relative query row
+    const bool valid = q < w.Lq;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int hi = p.causal ? min(q + w.off, w.Lk - 1) : w.Lk - 1;
+    const int lo = p.window > 0 ? q + w.off - p.window : kNoLowerBound;
+    float m_run = -INFINITY;   // running maximum of the raw scores
+    float m_used = -INFINITY;  // maximum the exponentials are taken against
+    float l = 0.f;             // sum of the exponentials (against m_used)
+    // O is formed from bf16-rounded P while l sums the fp32 values; when one
+    // key dominates a row that rounding error does not cancel, so the
+    // difference p - bf16(p) of every tile's largest p is taken out of the
+    // normaliser of O (not of the log-sum-exp).
+    float corr = 0.f;
+    bool ok = true;
+    for (int n = 0; n < N; ++n) {
+      const int j = tile_at(w, n);
+      if (!wwait(&s_full[n & 1], (n >> 1) & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t tS = taddr + (n & 1) * kR;
+      uint32_t s[kR];
+#pragma unroll
+      for (int c = 0; c < kR / 32; ++c) tmem_ld_x32(tS + 32 * c, s + 32 * c);
+      tmem_wait_ld256();
+#pragma unroll
+      for (int e = 0; e < kR; ++e) reg_fence256(s[e]);
+      if (!interior(w, j, p.window, p.n_sink)) {
+        // key k = j*128 + c is visible iff k <= hi and (k > lo or k < n_sink)
+        const int ka = j * kR;
+#pragma unroll
+        for (int c = 0; c < kR; ++c) {
+          const int k = ka + c;
+          if (!(k <= hi && (k > lo || k < p.n_sink))) s[c] = __float_as_uint(-INFINITY);
+        }
+      }
+      float mx8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mx8[t] = __uint_as_float(s[t]);
+#pragma unroll
+      for (int c = 8; c < kR; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
+      const float tmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      m_run = fmaxf(m_run, tmax);
+      // Lazy rescale: move the reference maximum only when the scores have
+      // outgrown it by 2^8; O (already holding earlier tiles) is then scaled
+      // by 2^((m_used - m_run) scale2) once O += P V of the previous tile is
+      // done.  The tensor-memory accesses are warp-collective: a warp rescales
+      // if any of its rows must (the others multiply by 1).
+      const bool first = (m_used == -INFINITY);
+      const bool grow = first ? (m_run != -INFINITY) : ((m_run - m_used) * p.scale2 > kRescaleLog2);
+      const bool resc = grow && !first;
+      if (__any_sync(0xffffffffu, resc)) {
+        if (!wwait(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const float alpha = resc ? ex2_approx((m_used - m_run) * p.scale2) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_x32(taddr + kColO + 32 * c, o);
+          tmem_wait_ld256();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_x32(taddr + kColO + 32 * c, o);
+        }
+        tmem_st_wait();
+        l *= alpha;
+        corr *= alpha;
+      }
+      if (grow) m_used = m_run;
+      // P = 2^(S scale2 - m_used scale2) as bf16 pairs over the first 64
+      // columns of the buffer (key-step kk of O += P V at column 8 kk); a row
+      // that has seen no key yet has m_used = -inf and every P = 0.
+      const float nms = first && !grow ? 0.f : -m_used * p.scale2;
+      float sum0 = 0.f, sum1 = 0.f;
+      uint32_t pk[kR / 2];
+#pragma unroll
+      for (int e = 0; e < kR / 2; ++e) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * e]), p.scale2, nms));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * e + 1]), p.scale2, nms));
+        if (e & 1)
+          sum1 += p0 + p1;
+        else
+          sum0 += p0 + p1;
+        pk[e] = pack_bf16x2(p0, p1);
+      }
+      l += sum0 + sum1;
+      {  // the tile's largest p, with the arithmetic used for it above
+        const float ptop = ex2_approx(fmaf(tmax, p.scale2, nms));
+        corr += ptop - __uint_as_float(pack_bf16x2(0.f, ptop) & 0xffff0000u);
+      }
+      tmem_st_x32(tS, pk);
+      tmem_st_x32(tS + 32, pk + 32);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&p_ready[n & 1]);
+    }
+    // ---------------------------------------------------------------- epilogue
+    if (ok) {
+      const bool have_o = N > 0;
+      if (have_o) {
+        if (!wwait(&o_done[(N - 1) & 1], ((N - 1) >> 1) & 1, abort_flag, p))
+          ok = false;
+        else
+          tc_fence_after_sync();
+      }
+      if (ok) {
+        // O / l, or with a logit sink sigma of this head one more term of
+        // the denominator taken against m* = max(sigma, m scale) ("TileLang
+        // tutorial, ch.15", section 4.6); a row that saw no key gets O = 0.
+        const bool seen = have_o && l > 0.f;
+        const float sg = p.sink ? p.sink[w.h] : -INFINITY;
+        float inv, lse_row;
+        if (sg == -INFINITY) {
+          inv = seen ? 1.f / (l - corr) : 0.f;
+          lse_row = seen ? fmaf(m_used, p.scale, logf(l)) : -INFINITY;
+        } else {
+          const float am = seen ? m_used * p.scale : -INFINITY;
+          const float mst = fmaxf(am, sg);
+          const float e1 = seen ? expf(am - mst) : 0.f;
+          const float e2 = expf(sg - mst);
+          inv = e1 / fmaf(l - corr, e1, e2);
+          lse_row = mst + logf(fmaf(l, e1, e2));
+        }
+        const size_t orow =
+            (p.cu_q ? static_cast<size_t>(w.q_base + q) * p.o_ss
+                    : static_cast<size_t>(w.bseq) * p.o_sb + static_cast<size_t>(q) * p.o_ss) +
+            static_cast<size_t>(w.h) * p.o_sh;
+#pragma unroll 1
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t o[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+          if (have_o) {
+            tmem_ld_x32(taddr + kColO + 32 * c, o);
+            tmem_wait_ld256();
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) reg_fence256(o[e]);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(p.o + orow + 32 * c);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint32_t wv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int idx = v4 * 8 + 2 * e;
+                wv[e] = seen ? pack_bf16x2(__uint_as_float(o[idx]) * inv,
+                                           __uint_as_float(o[idx + 1]) * inv)
+                             : 0u;
+              }
+              dst[v4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
+          }
+        }
+        if (valid && p.lse != nullptr) {
+          const size_t li = p.cu_q ? static_cast<size_t>(w.h) * p.total_q + w.q_base + q
+                                   : (static_cast<size_t>(w.bseq) * p.Hq + w.h) * p.Sq + q;
+          p.lse[li] = lse_row;
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd256(const FwdLaunch& a, cudaStream_t stream) {
+  if (a.page_table != nullptr || a.d != kD) return cudaErrorInvalidValue;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attn_fwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  P256 p;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.sink = a.sink;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.o_sb = a.o_sb;
+  p.o_ss = a.o_ss;
+  p.o_sh = a.o_sh;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.Sq = a.Sq;
+  p.Skv = a.Skv;
+  p.total_q = a.total_q;
+  p.num_qt = (a.Sq + kR - 1) / kR;
+  p.scale = a.scale;
+  p.scale2 = a.scale * 1.4426950408889634f;
+  p.causal = a.causal;
+  p.window = a.window;
+  p.n_sink = a.n_sink;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.status = a.status;
+  const long long grid = static_cast<long long>(p.num_qt) * a.Hq * a.B;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  attn_fwd256_kernel<<<static_cast<unsigned>(grid), kThr, kSmem, stream>>>(a.tmQ, a.tmK, a.tmV, p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1339,6 +1339,7 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
 cudaError_t launch_attn_fwd(const FwdLaunch& a, cudaStream_t stream) {
   if (a.d == 128) return launch_d<128>(a, stream);
   if (a.d == 64) return launch_d<64>(a, stream);
+  if (a.d == 256) return launch_attn_fwd256(a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -77,6 +77,9 @@ size_t bwd_workspace_bytes(int B, int Hq, int Sq);
 // Kernel launchers (return cudaError_t of the launch).
 cudaError_t launch_attn_bwd(const BwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_attn_fwd(const FwdLaunch& a, cudaStream_t stream);
+// d = 256: one Q tile per CTA, two S buffers and O in tensor memory (dense,
+// varlen and strided inputs; not paged).
+cudaError_t launch_attn_fwd256(const FwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_attn_fill_empty(const FwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_attn_decode(const DecodeLaunch& a, cudaStream_t stream);
 cudaError_t launch_wait_timeout_check(int* status, uint64_t limit_ns, cudaStream_t stream);

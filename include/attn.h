@@ -40,7 +40,11 @@
  *     Errors found by a kernel (a bounded wait that ran out, an out-of-range
  *     page index) cannot be returned by the launching call; the kernel
  *     records them in a device-side status word read by attn_device_status.
- *   - Head dimension d must be 64 or 128.  The device must be sm_103.
+ *   - Head dimension d: 64, 128 or 256 for the dense, varlen and strided
+ *     forward (attn_fwd, attn_fwd_ex, attn_fwd_ex_sink, attn_fwd_strided; at
+ *     d = 256 a CTA takes one 128-row query tile, with two score buffers and
+ *     O in tensor memory); 64 or 128 for the paged forward, the decode and the
+ *     backward.  The device must be sm_103.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
@@ -61,7 +65,7 @@ typedef enum attn_status {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, Hq % Hkv != 0,
                                window without causal, workspace too small, ... */
-  ATTN_ERR_UNSUPPORTED = 2, /* head dim not 64/128, page size not 16, device not sm_103 */
+  ATTN_ERR_UNSUPPORTED = 2, /* head dim not supported by the call, page size not 16, device not sm_103 */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed */
   ATTN_ERR_TIMEOUT = 4,     /* a kernel's bounded wait ran out (device status) */
   ATTN_ERR_BAD_INPUT = 5    /* a kernel met out-of-range device data, e.g. a page
