@@ -63,9 +63,10 @@ def _load():
             lib.oracle_combine.argtypes = [_D, _D, _D, _D, ctypes.c_long, i, i, _D]
             lib.oracle_attn_bwd.argtypes = [_D, _D, _D, _D, _D, _D, _D, i, i, i, i, i, i, d, i, i, i]
             lib.oracle_num_threads.argtypes = []
+            lib.oracle_set_num_threads.argtypes = [i]
             for f in ("oracle_attn_fwd", "oracle_attn_fwd_varlen", "oracle_attn_decode",
                       "oracle_attn_fwd_blockwise", "oracle_decode_split", "oracle_combine",
-                      "oracle_attn_bwd", "oracle_num_threads"):
+                      "oracle_attn_bwd", "oracle_num_threads", "oracle_set_num_threads"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -105,6 +106,12 @@ def _check(rc: int, what: str) -> None:
 def num_threads() -> int:
     """Threads the oracle's OpenMP loops use."""
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> int:
+    """Threads later oracle calls use (timing only; results do not depend on
+    it).  Returns the previous count."""
+    return int(_load().oracle_set_num_threads(int(n)))
 
 
 def attn_fwd(q, k, v, scale, causal=False, window=0, n_sink=0, rows=None, sink=None):

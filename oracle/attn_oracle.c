@@ -520,3 +520,17 @@ ORACLE_API int oracle_num_threads(void)
     }
     return n;
 }
+
+/* Sets the number of OpenMP threads later calls use (n >= 1); returns the
+ * previous count.  Timing plumbing only: results do not depend on it. */
+ORACLE_API int oracle_set_num_threads(int n)
+{
+    int prev = oracle_num_threads();
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+    return prev;
+}

@@ -1,16 +1,35 @@
 """Comparison helpers for the GPU parity tests (CUDA path vs the fp64 oracle).
 
-Tolerances: O within 1e-2 absolute of the oracle's fp64 value, plus half a
-bf16 unit in the last place of that value (the output is bf16: above 4 the
-format itself cannot come within 1e-2, so the bound is read as applying to
-the value before its final rounding); LSE within 1e-3 absolute.  Rows that
-see no key must be exactly +0.0 in O and -inf in LSE.
+Tolerances: O within 1e-2 absolute of the oracle's fp64 value wherever
+|O_ref| < 4.  At |O_ref| >= 4 the bf16 output format itself is spaced 2^-5 =
+0.031 apart, so no bf16 value need lie within 1e-2 of the exact one: there
+the bound is 1e-2 plus half a bf16 unit in the last place of O_ref (the 1e-2
+read as applying to the value before its final rounding), and the number of
+elements that took this wider bound is returned.  LSE within 1e-3 absolute.
+Rows that see no key must be exactly +0.0 in O and -inf in LSE.
+
+Stress inputs (Q x 8): rows whose weight sits on two or three keys carry the
+rounding of those keys' probabilities to bf16 (the second product takes P in
+bf16; a relative error of up to 2^-8 on one key of weight w_B moves O by up
+to w_A w_B 2^-8 |v_A - v_B|, about 3e-3 for two keys of weight 1/2), and at
+|O| in [2, 4) the bf16 output step is 2^-6.  Together these can pass 1e-2 by
+a little, so for stress inputs the half-ulp allowance starts at |O_ref| >= 2
+(``stress=True``); every other input keeps the plain 1e-2 below 4.
+
+Full-size outputs are checked on sampled query rows (rows are independent of
+one another: each is its own softmax over the keys it sees); ``sample_rows``
+picks at least 512 rows per (batch, head), including the first and last row
+and one random row of every 128-row query tile.
 """
 import numpy as np
 import torch
 
 O_TOL = 1e-2
 LSE_TOL = 1e-3
+WIDE_AT = 4.0   # |O_ref| from which the bf16 spacing alone exceeds 2 * O_TOL
+WIDE_AT_STRESS = 2.0
+TILE = 128
+MIN_ROWS = 512
 
 
 def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
@@ -19,10 +38,34 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
     return 0.5 * np.exp2(e - 7)
 
 
+def o_bound(o_ref: np.ndarray, stress: bool = False) -> np.ndarray:
+    """Per-element O bound: 1e-2 where |O_ref| < 4 (2 for stress inputs), 1e-2
+    plus half a bf16 ulp of O_ref above."""
+    wide = WIDE_AT_STRESS if stress else WIDE_AT
+    return np.where(np.abs(o_ref) < wide, O_TOL, O_TOL + bf16_half_ulp(o_ref))
+
+
+def sample_rows(S: int, seed: int = 0, min_rows: int = MIN_ROWS) -> np.ndarray:
+    """Query rows to check at full size: every row when S <= min_rows, else the
+    first and last row of every 128-row tile, one random row inside every tile,
+    and random rows until at least min_rows are chosen (sorted, unique)."""
+    if S <= min_rows:
+        return np.arange(S, dtype=np.int32)
+    g = np.random.default_rng(seed)
+    rows = set()
+    for t0 in range(0, S, TILE):
+        t1 = min(S, t0 + TILE)
+        rows.update((t0, t1 - 1, int(g.integers(t0, t1))))
+    while len(rows) < min_rows:
+        rows.add(int(g.integers(0, S)))
+    return np.array(sorted(rows), dtype=np.int32)
+
+
 def compare(o_gpu: torch.Tensor, lse_gpu: torch.Tensor, o_ref: np.ndarray, lse_ref: np.ndarray,
-            what: str = ""):
+            what: str = "", stress: bool = False):
     """o_gpu/o_ref share a layout with the row axis aligned; lse likewise.
-    Returns (max_abs_err_o, max_abs_err_lse) over rows that see keys."""
+    Returns (max_abs_err_o, max_abs_err_lse, n_wide): the largest errors over
+    rows that see keys, and how many O elements took the wider bound."""
     og = o_gpu.float().cpu().numpy().astype(np.float64)
     lg = lse_gpu.float().cpu().numpy().astype(np.float64)
     assert og.shape == o_ref.shape, (og.shape, o_ref.shape)
@@ -34,11 +77,15 @@ def compare(o_gpu: torch.Tensor, lse_gpu: torch.Tensor, o_ref: np.ndarray, lse_r
     err_l = float(np.abs(lg[fin] - lse_ref[fin]).max()) if fin.any() else 0.0
     assert err_l <= LSE_TOL, f"{what}: LSE error {err_l:.3e}"
     diff = np.abs(og - o_ref)
-    bound = O_TOL + bf16_half_ulp(o_ref)
+    bound = o_bound(o_ref, stress)
     bad = diff > bound
-    assert not bad.any(), (f"{what}: O error {diff.max():.3e} at {np.unravel_index(diff.argmax(), diff.shape)}"
-                           f" ({int(bad.sum())} elements over bound)")
-    return float(diff.max()), err_l
+    if bad.any():
+        at = np.unravel_index(np.argmax(np.where(bad, diff - bound, -np.inf)), diff.shape)
+        raise AssertionError(f"{what}: O error {diff[at]:.3e} at {at} with |O_ref| "
+                             f"{abs(o_ref[at]):.3f} ({int(bad.sum())} elements over bound; "
+                             f"largest error {diff.max():.3e})")
+    n_wide = int((bound > O_TOL).sum())
+    return float(diff.max()), err_l, n_wide
 
 
 def assert_masked_rows_zero(o_gpu: torch.Tensor, row_mask_o: np.ndarray, what=""):

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import workloads
-from tests._parity import assert_masked_rows_zero, compare, np64
+from tests._parity import assert_masked_rows_zero, compare, np64, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -112,11 +112,9 @@ def test_chunked_prefill_full_size(ea):
     assert ea.attn_device_status() == ea.ATTN_OK
     c = x.cache
     cu_q, cu_k = x.cu_q.tolist(), c.cu_kv.tolist()
-    rng = np.random.default_rng(9)
     for b in range(len(cu_q) - 1):
         lq = cu_q[b + 1] - cu_q[b]
-        rows = np.unique(np.concatenate([[0, lq - 1], rng.choice(lq, 14, replace=False)]))
-        rows = rows.astype(np.int32)
+        rows = sample_rows(lq, seed=9 + b)
         qb = np64(x.q[cu_q[b]:cu_q[b + 1]])[None]
         kb = np64(c.k_flat[cu_k[b]:cu_k[b + 1]])[None]
         vb = np64(c.v_flat[cu_k[b]:cu_k[b + 1]])[None]

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import workloads
-from tests._parity import assert_masked_rows_zero, compare, np64
+from tests._parity import assert_masked_rows_zero, compare, np64, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -117,11 +117,7 @@ def test_prefill_full_size_with_sinks(ea, causal):
     """B=4, H=16, S=2048, d=128 with sinks in [4, 12]; sampled rows against the oracle."""
     x = workloads.prefill_mha(causal)
     sink = workloads.logit_sinks(2100 + int(causal), 16)
-    rng = np.random.default_rng(5)
-    rows = np.sort(np.concatenate([[0, 1, 127, 128, 2047],
-                                   rng.choice(2048, 91, replace=False)]))
-    rows = np.unique(rows).astype(np.int32)
-    _check(ea, x, sink, rows=rows, what=f"full size, causal={causal}")
+    _check(ea, x, sink, rows=sample_rows(2048, seed=5), what=f"full size, causal={causal}")
 
 
 @pytest.mark.parametrize("num_splits", [1, 8])
