@@ -404,6 +404,9 @@ ATTN_API int attn_fwd_paged(const void* q, const void* k_pages, const void* v_pa
   a.n_sink = n_sink;
   a.num_sms = ds->num_sms;
   a.status = ds->status;
+  a.o_sb = 0;
+  a.o_ss = static_cast<long long>(Hq) * d;
+  a.o_sh = d;
   if ((rc = make_map(&a.tmQ, q, d, Hq, total_q, 1, 128, "q")) != ATTN_OK) return rc;
   if ((rc = make_map(&a.tmO, o, d, Hq, total_q, 1, 128, "o")) != ATTN_OK) return rc;
   if ((rc = make_map(&a.tmK, k_pages, d, Hkv, page_size, num_pages_total, 16, "k_pages")) !=

@@ -10,12 +10,13 @@
 // Keys and values stream through a ring of 128-key tiles.
 //
 // Warp roles (12 warps, three warpgroups):
-//   warps 0-3   softmax for Q tile 0 (thread r owns query row r: TMEM lane r)
+//   warps 0-3   softmax for Q tile 0 (thread r owns query row r: TMEM lane r),
+//               and its O epilogue (direct stores of each thread's row)
 //   warps 4-7   softmax for Q tile 1
-//   warp  8     TMA producer (Q once, then the K/V ring); allocates TMEM
+//   warp  8     TMA producer (Q tiles through three slots, the K/V ring);
+//               allocates TMEM
 //   warp  9     MMA issuer (whole warp, one elected lane issues)
-//   warp  10    O store warp (bulk tensor stores of the staging tile)
-//   warp  11    idle
+//   warps 10-11 idle (the register split needs whole warpgroups)
 // Tensor memory (512 columns): S_i = Q_i K^T at columns [128 i, 128 i + 128)
 // (fp32), O_i at [256 + D i, 256 + D i + D) (fp32).  The softmax writes the
 // probabilities P_i back over the first 64 columns of S_i as packed bf16
@@ -59,20 +60,20 @@ namespace {
 using namespace ptx;
 
 constexpr int kBM = 128;       // query rows per Q tile (= TMEM lanes)
-constexpr int kQT = 2;         // Q tiles per CTA
+constexpr int kQT = 2;         // Q tiles per work item
+constexpr int kQSlots = 3;     // Q tile buffers in shared memory
 constexpr int kBN = 128;       // keys per K/V tile
 constexpr int kPage = 16;      // keys per page of a paged cache
 constexpr int kPagesPerTile = kBN / kPage;
 constexpr int kThreads = 384;  // 12 warps
-constexpr int kRegsSoftmax = 208;
-constexpr int kRegsOther = 88;
+constexpr int kRegsSoftmax = 192;
+constexpr int kRegsOther = 120;
 // Registers the three warpgroups hold after setmaxnreg; must not exceed what
 // the block is launched with (checked on the host before every launch).
 constexpr int kRegsSplit = 2 * 128 * kRegsSoftmax + 128 * kRegsOther;
 static_assert(kRegsSplit <= kThreads * 168, "register split");
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
-constexpr int kWarpStore = 10;
 constexpr int kPrefetch = 2;  // key/value tiles warmed in L2 ahead of their load
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -87,13 +88,12 @@ struct Cfg {
   static constexpr int kAtoms = D / 64;           // 128-byte swizzle atoms per row
   static constexpr int kAtomBytes = 128 * 128;    // one atom column of a tile: 128 rows x 128 B
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQT * kTileBytes;
+  static constexpr int kOffK = kOffQ + kQSlots * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffStage = kOffV + kStages * kTileBytes;  // O tile on its way out
-  static constexpr int kOffBar = kOffStage + kTileBytes;
-  // q_full, k_full[S], v_full[S], step[S], s_full[2], p_half[2], p_ready[2], o_done[2],
-  // stage_full[2], turn[2], drain
-  static constexpr int kNumBars = 1 + 3 * kStages + 6 * kQT + 1;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  // q_full[3], q_empty[3], k_full[S], v_full[S], step[S], s_full[2], p_half[2], p_ready[2],
+  // o_done[2], drain
+  static constexpr int kNumBars = 2 * kQSlots + 3 * kStages + 4 * kQT + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static constexpr uint32_t kTmemCols = 512;
@@ -127,6 +127,7 @@ __device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
 
 struct Params {
   __nv_bfloat16* o;
+  long long o_sb, o_ss, o_sh;  // O strides (elements): batch, row, head; d contiguous
   float* lse;
   const float* sink;  // logit sink per query head [Hq], or null
   const int* cu_q;
@@ -196,6 +197,21 @@ __device__ __forceinline__ bool in_range(const TileRange& r, int j, int sinkT) {
   return j <= r.hi && (j >= r.lo || j < sinkT);
 }
 
+// The first active tile of a range at or after c (INT_MAX: none): the sink
+// tiles, then the window's tiles from r.lo on.  Loops over a Q tile's keys
+// step from one active tile to the next, so a window far from the sink costs
+// no iterations over the tiles between.
+__device__ __forceinline__ int next_in_range(const TileRange& r, int c, int sinkT) {
+  const int n = (c < sinkT) ? c : max(c, r.lo);
+  return n <= r.hi ? n : INT_MAX;
+}
+
+// The first tile at or after c active for either Q tile of an item.
+__device__ __forceinline__ int next_in_pair(const TileRange& r0, const TileRange& r1, int c,
+                                            int sinkT) {
+  return min(next_in_range(r0, c, sinkT), next_in_range(r1, c, sinkT));
+}
+
 // Does every row of the tile see every key of key tile j (no mask needed)?
 __device__ __forceinline__ bool tile_interior(const TileMask& m, int j, int window, int n_sink) {
   const int ka = j * kBN, kb1 = ka + kBN - 1;
@@ -260,15 +276,27 @@ __device__ __forceinline__ float max32(const uint32_t* v, float run) {
   return max3(b0, b1, fmaxf(b2, b3));
 }
 
-// Sets scores of keys a row may not see to -inf: column c of the chunk is
-// key kc0 + c, visible iff c <= lim_hi and (c > lim_lo or c < lim_sink),
-// all limits relative to kc0.
+// Bits [0, n) of a 32-bit word, n clamped to [0, 32].
+__device__ __forceinline__ uint32_t low_bits(int n) {
+  return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);
+}
+
+// The keys of a 32-key chunk a row may see, as a bit mask: column c is key
+// kc0 + c, visible iff c <= lim_hi and (c > lim_lo or c < lim_sink), all
+// limits relative to kc0.
+__device__ __forceinline__ uint32_t visible32(int lim_hi, int lim_lo, int lim_sink) {
+  const int lo1 = max(lim_lo, -1) + 1;  // first column above the window's lower bound
+  return low_bits(lim_hi + 1) & (~low_bits(lo1) | low_bits(lim_sink));
+}
+
+// Sets the scores of the keys a row may not see to -inf (one bit test and
+// one select per score); nothing to do when the whole warp sees the chunk.
 __device__ __forceinline__ void mask32(uint32_t* v, int lim_hi, int lim_lo, int lim_sink) {
+  const uint32_t vis = visible32(lim_hi, lim_lo, lim_sink);
+  if (__all_sync(0xffffffffu, vis == 0xffffffffu)) return;
 #pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    const bool vis = (c <= lim_hi) && (c > lim_lo || c < lim_sink);
-    if (!vis) v[c] = __float_as_uint(-INFINITY);
-  }
+  for (int c = 0; c < 32; ++c)
+    if (!(vis & (1u << c))) v[c] = __float_as_uint(-INFINITY);
 }
 
 // Exponentials of 32 scores: p = 2^(s * scale2 - ms), accumulated into the
@@ -366,16 +394,6 @@ __device__ __forceinline__ bool decode_work(const Params& p, int k, int sinkT, W
   return true;
 }
 
-// Does Q tile i of the item leave through the staging tile and bulk tensor
-// stores?  Not when it has no row, nor when it is the tail of a varlen
-// sequence (rows past the sequence belong to the next one and must not be
-// written): those rows are stored directly.  Dense tails are clipped by the
-// tensor bounds.
-__device__ __forceinline__ bool epilogue_bulk(const Params& p, const Work& w, int i) {
-  const bool tile_rows = w.q0 + i * kBM < w.Lq;
-  return tile_rows && (p.cu_q == nullptr || w.q0 + (i + 1) * kBM <= w.Lq);
-}
-
 // Number of active key tiles of a range.
 __device__ __forceinline__ int range_count(const TileRange& r, int sinkT) {
   if (r.hi < 0) return 0;
@@ -395,8 +413,7 @@ __device__ __forceinline__ int item_of(int n, int num_items) {
 template <int D, bool kPagedKV>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                    const Params p) {
+                    const __grid_constant__ CUtensorMap tmV, const Params p) {
   using C = Cfg<D>;
   constexpr int ST = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -405,24 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
-  uint8_t* sO = smem + C::kOffStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
+  uint64_t* q_full = bars;                 // [kQSlots]: the Q tile in slot s has landed
+  uint64_t* q_empty = q_full + kQSlots;    // [kQSlots]: every S of the Q tile in slot s is done
+  uint64_t* k_full = q_empty + kQSlots;
   uint64_t* v_full = k_full + ST;
   uint64_t* step = v_full + ST;  // step[u % ST]: every product of key step u is done
   uint64_t* s_full = step + ST;
   uint64_t* p_half = s_full + kQT;   // [2]: P_i of keys 0..63 written
   uint64_t* p_ready = p_half + kQT;  // [2]: all of P_i written
   uint64_t* o_done = p_ready + kQT;
-  uint64_t* stage_full = o_done + kQT;  // [2]: the four warps of warpgroup i wrote its O rows
-  // turn[i]: the staging tile is free for warpgroup i's next epilogue (its
-  // previous user, the other warpgroup, is done with it).  One barrier per
-  // warpgroup, so that every phase a warp waits for is at most one ahead of
-  // the phases it has already seen: with a single shared barrier a warp
-  // could come back two phases early and read the parity of an older one.
-  uint64_t* turn = stage_full + kQT;
-  uint64_t* drain = turn + kQT;
+  uint64_t* drain = o_done + kQT;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   __shared__ int abort_flag_s;
   volatile int* abort_flag = &abort_flag_s;
@@ -433,7 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
     abort_flag_s = 0;
-    mbar_init(q_full, 1);
+    for (int s = 0; s < kQSlots; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
     for (int s = 0; s < ST; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
@@ -445,9 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&p_ready[i], 128);
       mbar_init(&o_done[i], 1);
     }
-    for (int i = 0; i < kQT; ++i) mbar_init(&stage_full[i], 4);
-    mbar_init(&turn[0], 1);
-    mbar_init(&turn[1], 1);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -464,14 +474,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (item_of), skipping the same items, and its ring, barrier-phase and
   // step counters carry over from one item to the next.
   //
+  // Q tiles.  The g-th Q tile this CTA loads (two per item with key tiles,
+  // tile 0 then tile 1) goes to slot g % 3; the slot is refilled once every
+  // S product of its previous tile, g - 3, is done (q_empty).  Tile 0 of an
+  // item therefore reuses the slot of the item two back and is loaded about
+  // one item ahead; tile 1 reuses the slot of tile 0 of the item before,
+  // free as soon as that item's last S_0 is done.
+  //
   // Key steps.  Ring tile u (the u-th active key tile loaded by this CTA,
-  // counted over all its items) is key step u of the MMA issuer: S_0(u),
-  // S_1(u) and the products P V of the tile before it, then one commit on
-  // step[u % ST].  So K(u) is free once step u is done and V(u) once step
-  // u + 1 is; the producer waits for those before it refills a slot.  At the
-  // first tile of an item, the products of the previous item's last tile are
-  // issued before the wait for the new Q (they do not need it); after the
-  // last item a final step holds only those products.
+  // counted over all its items) is key step u of the MMA issuer: the
+  // products P V of the tile before it (whichever item that tile belongs
+  // to), S_0(u) and S_1(u), then one commit on step[u % ST].  So K(u) is free
+  // once step u is done and V(u) once step u + 1 is.  An item change is an
+  // ordinary key step: the last P V of the old item and the first S of the
+  // new one share it, and the old item's O epilogue runs while the tensor
+  // core works on the new item's S.  After the last item a final step holds
+  // only the outstanding products P V.
   //
   // Register budget: the block is launched with 168 registers a thread (three
   // warps share SMSP 0).  Each warpgroup changes its budget at the head of
@@ -490,9 +508,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmV);
     }
     __syncwarp();
-    int u = 0;   // ring tiles loaded
-    int nq = 0;  // Q pairs loaded
+    int u = 0;  // ring tiles loaded
+    int g = 0;  // Q tiles loaded
     bool ok = true;
+    // Q tile i of the item into slot g % 3, once the slot's previous tile is
+    // done with.
+    auto load_q = [&](const Work& w, int i) -> bool {
+      const int slot = g % kQSlots, use = g / kQSlots;
+      if (use > 0 &&
+          !mbar_wait_warp(&q_empty[slot], (use - 1) & 1, abort_flag, p.wait_limit_ns))
+        return false;
+      mbar_arrive_expect_tx_w(&q_full[slot], C::kTileBytes);
+#pragma unroll
+      for (int a = 0; a < C::kAtoms; ++a)
+        tma_load_4d_w(sQ + slot * C::kTileBytes + a * C::kAtomBytes, &tmQ, &q_full[slot], a * 64,
+                      w.h, w.q_base + w.q0 + i * kBM, w.b_coord);
+      ++g;
+      return true;
+    };
     // Key or value tile j of the item into one ring slot (its barrier's
     // byte count is one whole tile).  Dense and packed layouts: one box of
     // 128 rows per swizzle atom.  Paged cache: one 16-row box per page; lane
@@ -531,24 +564,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (k < 0) break;
       Work w;
       if (!decode_work<kPagedKV>(p, k, sinkT, w, lane == 0) || w.lastT < 0) continue;
-      // The Q buffers are free once every S of the previous pair is done:
-      // its last key step, u - 1.
-      if (nq > 0 &&
-          !mbar_wait_warp(&step[(u - 1) % ST], ((u - 1) / ST) & 1, abort_flag, p.wait_limit_ns)) {
-        if (lane == 0) fail(p.status, abort_flag);
+      if (!load_q(w, 0)) {
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx_w(q_full, kQT * C::kTileBytes);
-#pragma unroll
-      for (int i = 0; i < kQT; ++i)
-#pragma unroll
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_4d_w(sQ + i * C::kTileBytes + a * C::kAtomBytes, &tmQ, q_full, a * 64, w.h,
-                        w.q_base + w.q0 + i * kBM, w.b_coord);
-      ++nq;
-      // Warm L2 with the next item's Q: its load waits until every S of
-      // this item is done and would otherwise start from HBM then.
+      // Warm L2 with the next item's Q tiles.
       {
         const int k2 = item_of(n + 1, p.num_items);
         Work w2;
@@ -560,12 +580,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_prefetch_4d_w(&tmQ, a * 64, w2.h, w2.q_base + w2.q0 + i * kBM, w2.b_coord);
         }
       }
-      for (int j = 0; j <= w.lastT; ++j) {
-        if (!in_range(w.r0, j, sinkT) && !in_range(w.r1, j, sinkT)) continue;
+      bool q1 = false;  // Q tile 1 loaded (after the item's first K tile)
+      for (int j = next_in_pair(w.r0, w.r1, 0, sinkT); j <= w.lastT;
+           j = next_in_pair(w.r0, w.r1, j + 1, sinkT)) {
         const int s = u % ST;
         if (u >= ST &&
             !mbar_wait_warp(&step[s], ((u / ST) - 1) & 1, abort_flag, p.wait_limit_ns)) {
-          if (lane == 0) fail(p.status, abort_flag);
           ok = false;
           break;
         }
@@ -574,9 +594,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // less than a load from HBM takes.
         {
           int jp = j, ahead = 0;
-          while (ahead < kPrefetch && jp < w.lastT) {
-            ++jp;
-            if (in_range(w.r0, jp, sinkT) || in_range(w.r1, jp, sinkT)) ++ahead;
+          while (ahead < kPrefetch) {
+            const int nx = next_in_pair(w.r0, w.r1, jp + 1, sinkT);
+            if (nx > w.lastT) break;
+            jp = nx;
+            ++ahead;
           }
           if (ahead == kPrefetch && !kPagedKV) {
 #pragma unroll
@@ -588,9 +610,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx_w(&k_full[s], C::kTileBytes);
         load_kv(&tmK, sK + s * C::kTileBytes, &k_full[s], w, j);
+        if (!q1) {
+          // Between the first K and V tiles: S_0 of the first key step needs
+          // K, S_1 needs this tile, and the first P V needs V last.
+          q1 = true;
+          if (!load_q(w, 1)) {
+            ok = false;
+            break;
+          }
+        }
         if (u >= ST && !mbar_wait_warp(&step[(u + 1) % ST], (((u + 1) / ST) - 1) & 1, abort_flag,
                                        p.wait_limit_ns)) {
-          if (lane == 0) fail(p.status, abort_flag);
           ok = false;
           break;
         }
@@ -598,14 +628,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_kv(&tmV, sV + s * C::kTileBytes, &v_full[s], w, j);
         ++u;
       }
+      if (ok && !q1 && !load_q(w, 1)) ok = false;
     }
     // Tail: the last commit of the MMA issuer is step u (the final products
     // P V); once it is done no tensor-core commit is left to arrive on this
     // CTA's barriers.
     if (ok && u > 0 &&
-        !mbar_wait_warp(&step[u % ST], (u / ST) & 1, abort_flag, p.wait_limit_ns)) {
-      if (lane == 0) fail(p.status, abort_flag);
-    }
+        !mbar_wait_warp(&step[u % ST], (u / ST) & 1, abort_flag, p.wait_limit_ns))
+      ok = false;
+    if (!ok && lane == 0) fail(p.status, abort_flag);
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ============================================================ MMA issuer
@@ -624,103 +655,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dq0 = sdesc_sw128(smem_addr(sQ), 16, 1024);
     const uint64_t dk0 = sdesc_sw128(smem_addr(sK), 16, 1024);
     const uint64_t dv0 = sdesc_sw128(smem_addr(sV), C::kAtomBytes, 1024);
-    int u = 0;                    // key steps (ring tiles) issued
-    int nq = 0;                   // Q pairs consumed
-    int pv0 = 0, pv1 = 0;         // products P V issued per Q tile (p_ready phases)
-    int left0 = 0, left1 = 0;     // products still due in the current item
-    int pend0 = -1, pend1 = -1;   // ring tile whose product P V is still to be issued
+    int u = 0;             // key steps (ring tiles) issued
+    int g = 0;             // Q tiles consumed
+    int pv0 = 0, pv1 = 0;  // products P V issued per Q tile (p_half / p_ready phases)
+    // The product O_i += P_i V still to be issued: its ring tile (-1: none),
+    // whether it is the first of its item (it overwrites O) and the last (its
+    // completion is the item's o_done).
+    int pend0 = -1, pend1 = -1;
+    bool first0 = false, first1 = false, last0 = false, last1 = false;
     bool ok = true;
-    // The first product of an item overwrites O (the previous item's O has
-    // been read out by then: it waits for the p_half arrival the softmax
-    // warpgroup makes after its epilogue).
-    bool fresh0 = true, fresh1 = true;
-    // O_i += P_i V for ring tile pend (its V already waited for): the first
-    // half of P (keys 0..63, its p_half arrival already waited for) right
-    // away, the second half once the softmax has published it (p_ready).
-    auto issue_pv = [&](int i, int pend, int& pv, int& left, bool& fresh) -> bool {
+    // O_i += P_i V for ring tile pend (its V and the p_half arrival of its P
+    // already waited for): the first half of P (keys 0..63) right away, the
+    // second half once the softmax has published it (p_ready).
+    auto issue_pv = [&](int i, int& pend, int& pv, bool first, bool last) -> bool {
       const uint64_t dv = dv0 + static_cast<uint64_t>(pend % ST) * kTileDesc;
       const uint32_t tO = tmem + C::kColO + i * D;
       const uint32_t tP = tmem + i * kBN;
-      mma_bf16_ts_w(tO, tP, dv, idesc_o, fresh ? 0u : 1u);
-      fresh = false;
-#pragma unroll
-      for (int kk = 1; kk < kBN / 32; ++kk)
-        mma_bf16_ts_wc<1>(tO, tP + kk * 8, dv + kk * (2048 >> 4), idesc_o);
+      mma_ts_k64_w(tO, tP, dv, idesc_o, first ? 0u : 1u);
       if (!mbar_wait_warp(&p_ready[i], pv & 1, abort_flag, p.wait_limit_ns)) return false;
       tc_fence_after_sync();
-#pragma unroll
-      for (int kk = kBN / 32; kk < kBN / 16; ++kk)
-        mma_bf16_ts_wc<1>(tO, tP + kk * 8, dv + kk * (2048 >> 4), idesc_o);
+      mma_ts_k64_w(tO, tP + 32, dv + 4 * (2048 >> 4), idesc_o, 1u);
       ++pv;
-      if (--left == 0) mma_commit_w(&o_done[i]);
+      if (last) mma_commit_w(&o_done[i]);
+      pend = -1;
       return true;
     };
-    // S_i = Q_i K^T for the key tile in ring slot s.
-    auto issue_s = [&](int i, uint64_t dk) {
-      const uint64_t dq = dq0 + i * kTileDesc;
+    // S_i = Q_i K^T for the key tile with descriptor dk, Q_i in slot qs.
+    auto issue_s = [&](int i, uint64_t dk, int qs) {
+      const uint64_t dq = dq0 + static_cast<uint64_t>(qs) * kTileDesc;
       const uint32_t tS = tmem + i * kBN;
-      mma_bf16_ss_wc<0>(tS, dq, dk, idesc_s);
-#pragma unroll
-      for (int kk = 1; kk < D / 16; ++kk) {
-        const uint64_t koff = ((kk / 4) * C::kAtomBytes + (kk % 4) * 32) >> 4;
-        mma_bf16_ss_wc<1>(tS, dq + koff, dk + koff, idesc_s);
-      }
+      if constexpr (D == 128)
+        mma_ss_k128_w<(C::kAtomBytes >> 4)>(tS, dq, dk, idesc_s);
+      else
+        mma_ss_k64_w(tS, dq, dk, idesc_s);
       mma_commit_w(&s_full[i]);
-    };
-    // The products P V still due for ring tile u - 1 (end of an item).
-    auto flush = [&]() -> bool {
-      if (pend0 < 0 && pend1 < 0) return true;
-      const int sv = (u + ST - 1) % ST;
-      const uint32_t pvv = ((u - 1) / ST) & 1;
-      if (!mbar_wait_warp(&v_full[sv], pvv, abort_flag, p.wait_limit_ns)) return false;
-      if (pend0 >= 0) {
-        if (!mbar_wait_warp(&p_half[0], pv0 & 1, abort_flag, p.wait_limit_ns)) return false;
-        tc_fence_after_sync();
-        if (!issue_pv(0, pend0, pv0, left0, fresh0)) return false;
-        pend0 = -1;
-      }
-      if (pend1 >= 0) {
-        if (!mbar_wait_warp(&p_half[1], pv1 & 1, abort_flag, p.wait_limit_ns)) return false;
-        tc_fence_after_sync();
-        if (!issue_pv(1, pend1, pv1, left1, fresh1)) return false;
-        pend1 = -1;
-      }
-      return true;
     };
     for (int n = 0; ok; ++n) {
       const int k = item_of(n, p.num_items);
       if (k < 0) break;
       Work w;
       if (!decode_work<kPagedKV>(p, k, sinkT, w, false) || w.lastT < 0) continue;
-      if (!flush()) {
-        ok = false;
-        break;
-      }
-      left0 = range_count(w.r0, sinkT);
-      left1 = range_count(w.r1, sinkT);
-      fresh0 = fresh1 = true;
-      if (!mbar_wait_warp(q_full, nq & 1, abort_flag, p.wait_limit_ns)) {
-        ok = false;
-        break;
-      }
-      ++nq;
-      bool first = true;
-      for (int j = 0; j <= w.lastT; ++j) {
+      const int qs0 = g % kQSlots, qs1 = (g + 1) % kQSlots;
+      const uint32_t qp0 = (g / kQSlots) & 1, qp1 = ((g + 1) / kQSlots) & 1;
+      g += kQT;
+      const int count0 = range_count(w.r0, sinkT), count1 = range_count(w.r1, sinkT);
+      int left0 = count0, left1 = count1;
+      for (int j = next_in_pair(w.r0, w.r1, 0, sinkT); j <= w.lastT;
+           j = next_in_pair(w.r0, w.r1, j + 1, sinkT)) {
         const bool a0 = in_range(w.r0, j, sinkT), a1 = in_range(w.r1, j, sinkT);
-        if (!a0 && !a1) continue;
         const int s = u % ST;
         const int sv = (u + ST - 1) % ST;  // V(u - 1)
         const uint32_t pk = (u / ST) & 1, pvv = ((u - 1) / ST) & 1;
         // Needed now: K(u), and for O_0 += P_0 V(u - 1) also V(u - 1) and
-        // P_0.  Tested together (one round trip when all are ready), then
-        // waited on in turn only if one is not.  A barrier not needed is
-        // replaced by q_full in its current, completed phase.
-        const bool need_v = !first && (pend0 >= 0 || pend1 >= 0), need_p0 = !first && pend0 >= 0;
-        const uint32_t qpar = (nq - 1) & 1;
+        // the first half of P_0.  Tested together (one round trip when all
+        // are ready), then waited on in turn only if one is not.  A barrier
+        // not needed is replaced by K(u)'s own.
+        const bool need_v = pend0 >= 0 || pend1 >= 0, need_p0 = pend0 >= 0;
         if (!__all_sync(0xffffffffu,
-                        mbar_test3(&k_full[s], pk, need_v ? &v_full[sv] : q_full,
-                                   need_v ? pvv : qpar, need_p0 ? &p_half[0] : q_full,
-                                   need_p0 ? (pv0 & 1) : qpar) == 7u)) {
+                        mbar_test3(&k_full[s], pk, need_v ? &v_full[sv] : &k_full[s],
+                                   need_v ? pvv : pk, need_p0 ? &p_half[0] : &k_full[s],
+                                   need_p0 ? (pv0 & 1) : pk) == 7u)) {
           if (!mbar_wait_warp(&k_full[s], pk, abort_flag, p.wait_limit_ns) ||
               (need_v && !mbar_wait_warp(&v_full[sv], pvv, abort_flag, p.wait_limit_ns)) ||
               (need_p0 && !mbar_wait_warp(&p_half[0], pv0 & 1, abort_flag, p.wait_limit_ns))) {
@@ -731,15 +725,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint64_t dk = dk0 + static_cast<uint64_t>(s) * kTileDesc;
         // order: O_0 += P_0 V(u-1), S_0(u), O_1 += P_1 V(u-1), S_1(u)
-        if (pend0 >= 0) {
-          if (!issue_pv(0, pend0, pv0, left0, fresh0)) {
-            ok = false;
-            break;
-          }
-          pend0 = -1;
+        if (pend0 >= 0 && !issue_pv(0, pend0, pv0, first0, last0)) {
+          ok = false;
+          break;
         }
         if (a0) {
-          issue_s(0, dk);
+          // the item's first S_0 waits for its Q tile
+          if (left0 == count0) {
+            if (!mbar_wait_warp(&q_full[qs0], qp0, abort_flag, p.wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+          }
+          issue_s(0, dk, qs0);
+          first0 = left0 == count0;
+          last0 = --left0 == 0;
+          if (last0) mma_commit_w(&q_empty[qs0]);
           pend0 = u;
         }
         if (pend1 >= 0) {
@@ -748,69 +750,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after_sync();
-          if (!issue_pv(1, pend1, pv1, left1, fresh1)) {
+          if (!issue_pv(1, pend1, pv1, first1, last1)) {
             ok = false;
             break;
           }
-          pend1 = -1;
         }
         if (a1) {
-          issue_s(1, dk);
+          if (left1 == count1) {
+            if (!mbar_wait_warp(&q_full[qs1], qp1, abort_flag, p.wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+          }
+          issue_s(1, dk, qs1);
+          first1 = left1 == count1;
+          last1 = --left1 == 0;
+          if (last1) mma_commit_w(&q_empty[qs1]);
           pend1 = u;
         }
         mma_commit_w(&step[s]);  // key step u: K(u) and V(u - 1) free once done
         ++u;
-        first = false;
       }
-    }
-    // Final key step: the products of the last tile.
-    if (ok && u > 0) {
-      if (flush())
-        mma_commit_w(&step[u % ST]);
-      else
-        ok = false;
-    }
-    if (!ok && lane == 0) fail(p.status, abort_flag);
-    __syncwarp();
-  } else if (warp == kWarpStore) {
-    // ============================================================ O store warp
-    // Takes the bulk stores of O off the softmax warpgroups: once the four
-    // warps of warpgroup i have taken their turn (and, for a bulk store,
-    // written their rows to the staging tile), this warp issues the tensor
-    // stores, waits until they have read the tile and hands the turn on
-    // (warpgroup 0 then 1, item after item).
-    int nb0 = 0, nb1 = 0;  // epilogues per warpgroup (stage_full phases)
-    bool ok = true;
-    for (int n = 0; ok; ++n) {
-      const int k = item_of(n, p.num_items);
-      if (k < 0) break;
-      Work w;
-      if (!decode_work<kPagedKV>(p, k, sinkT, w, false)) continue;
-#pragma unroll 1
-      for (int i = 0; i < kQT; ++i) {
-        int& nb = i ? nb1 : nb0;
-        if (!mbar_wait_warp(&stage_full[i], nb & 1, abort_flag, p.wait_limit_ns)) {
+      if (!ok) break;
+      // A Q tile with no key tile to see: nothing reads it; hand its slot
+      // back once it has landed.
+      if (count0 == 0) {
+        if (!mbar_wait_warp(&q_full[qs0], qp0, abort_flag, p.wait_limit_ns)) {
           ok = false;
           break;
         }
-        ++nb;
-        if (lane == 0) {
-          if (epilogue_bulk(p, w, i)) {
-#pragma unroll
-            for (int a = 0; a < C::kAtoms; ++a)
-              tma_store_4d(&tmO, sO + a * C::kAtomBytes, a * 64, w.h, w.q_base + w.q0 + i * kBM,
-                           w.b_coord);
-            bulk_commit_group();
-            bulk_wait_read_all();
-          }
-          mbar_arrive(&turn[1 - i]);
+        mma_commit_w(&q_empty[qs0]);
+      }
+      if (count1 == 0) {
+        if (!mbar_wait_warp(&q_full[qs1], qp1, abort_flag, p.wait_limit_ns)) {
+          ok = false;
+          break;
         }
-        __syncwarp();
+        mma_commit_w(&q_empty[qs1]);
       }
     }
+    // Final key step: the products of the last tile.
+    if (ok && (pend0 >= 0 || pend1 >= 0)) {
+      ok = mbar_wait_warp(&v_full[(u + ST - 1) % ST], ((u - 1) / ST) & 1, abort_flag,
+                          p.wait_limit_ns);
+      if (ok && pend0 >= 0) {
+        ok = mbar_wait_warp(&p_half[0], pv0 & 1, abort_flag, p.wait_limit_ns);
+        if (ok) {
+          tc_fence_after_sync();
+          ok = issue_pv(0, pend0, pv0, first0, last0);
+        }
+      }
+      if (ok && pend1 >= 0) {
+        ok = mbar_wait_warp(&p_half[1], pv1 & 1, abort_flag, p.wait_limit_ns);
+        if (ok) {
+          tc_fence_after_sync();
+          ok = issue_pv(1, pend1, pv1, first1, last1);
+        }
+      }
+      if (ok) mma_commit_w(&step[u % ST]);
+    }
     if (!ok && lane == 0) fail(p.status, abort_flag);
-    // The bulk stores of this CTA complete before it exits.
-    if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
   } else {
@@ -825,7 +825,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale2 = p.scale2;
     int t = 0;     // key tiles processed (s_full / p_ready phases)
     int no = 0;    // o_done phases consumed
-    int ne = 0;   // epilogues done (one per item; turn[] phases)
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int k = item_of(n, p.num_items);
@@ -849,8 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float l = 0.f;             // running sum of the fp32 probabilities
       float corr = 0.f;          // running sum of (p - bf16(p)) over each tile's largest p
       int t_item = 0;
-      for (int j = 0; j <= rg.hi; ++j) {
-        if (!in_range(rg, j, sinkT)) continue;
+      for (int j = next_in_range(rg, 0, sinkT); j <= rg.hi; j = next_in_range(rg, j + 1, sinkT)) {
         bool w_ok = mbar_wait(&s_full[i], t & 1, abort_flag, p.wait_limit_ns);
         w_ok = __all_sync(0xffffffffu, w_ok);
         if (!w_ok) {
@@ -880,18 +878,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // half formed.  If a row of the warp does exceed the threshold (rare
         // after the first tile), nothing has been written yet: the warp
         // starts again on the full path below, S being intact.
+        //
+        // The first tile of an item (no maximum in use yet) is speculated
+        // the same way, with the maximum of its first chunk as the guess.
         bool spec_ok = false;
-        if (!edge && !__any_sync(0xffffffffu, m_used == -INFINITY)) {
-          ms = m_used * scale2;
-          const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
+        if (!edge) {
+          const bool first = m_used == -INFINITY;  // uniform: every row starts the item together
           uint32_t ra[32], rb[32], pk0[16], pk1[16];
-          float mxa = -INFINITY;
           tmem_ld_x32(sS + 0, ra);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
           tmem_ld_x32(sS + 32, rb);
-          mxa = max32(ra, mxa);
+          float mxa = max32(ra, -INFINITY);
+          if (first) m_used = mxa;
+          ms = m_used * scale2;
+          const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
           exp32(ra, sc2, nms, sum_a, sum_b, pk0);
           tmem_ld_wait();
 #pragma unroll
@@ -921,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             sum_a = sum_b = 0;  // start again
             mx = -INFINITY;
+            if (first) m_used = -INFINITY;
           }
         }
         // Online-softmax state update from this tile's raw row maximum, and
@@ -964,91 +967,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         };
         if (spec_ok) {
-        } else if (!edge) {
-          // Interior tile, no mask.  Pass 1 reads all of S (one wait) for the
-          // row maximum; pass 2 reads it again chunk by chunk (the next chunk
-          // in flight while one is exponentiated), publishing the first half
-          // of P once chunks 0 and 1 are written.
-          {
-            uint32_t r0[32], r1[32], r2[32], r3[32];
-            tmem_ld_x32(sS + 0, r0);
-            tmem_ld_x32(sS + 32, r1);
-            tmem_ld_x32(sS + 64, r2);
-            tmem_ld_x32(sS + 96, r3);
-            tmem_ld_wait();
+        } else {
+          // First tile of the item, or a tile a boundary crosses (causal
+          // diagonal, window edge, sink keys, ragged tail): all of S in
+          // registers (one wait), the mask on boundary tiles, the row maximum
+          // and the state update, then the exponentials from the registers,
+          // publishing the first half of P once chunks 0 and 1 are written.
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tmem_ld_x32(sS + 0, r0);
+          tmem_ld_x32(sS + 32, r1);
+          tmem_ld_x32(sS + 64, r2);
+          tmem_ld_x32(sS + 96, r3);
+          tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              reg_fence(r0[c]);
-              reg_fence(r1[c]);
-              reg_fence(r2[c]);
-              reg_fence(r3[c]);
-            }
-            mx = max32(r3, max32(r2, max32(r1, max32(r0, mx))));
+          for (int c = 0; c < 32; ++c) {
+            reg_fence(r0[c]);
+            reg_fence(r1[c]);
+            reg_fence(r2[c]);
+            reg_fence(r3[c]);
           }
+          if (edge) {
+            const int kb = j * kBN;
+            const int lim_hi = hi_row - kb;
+            const int lim_lo = (p.window > 0) ? lo_row - kb : kNoLowerBound;
+            const int lim_sink = p.n_sink - kb;
+            mask32(r0, lim_hi, lim_lo, lim_sink);
+            mask32(r1, lim_hi - 32, lim_lo - 32, lim_sink - 32);
+            mask32(r2, lim_hi - 64, lim_lo - 64, lim_sink - 64);
+            mask32(r3, lim_hi - 96, lim_lo - 96, lim_sink - 96);
+          }
+          mx = max32(r3, max32(r2, max32(r1, max32(r0, mx))));
           update_rescale();
           const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
-          uint32_t ra[32], rb[32], pk[16];
-          tmem_ld_x32(sS + 0, ra);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
-          tmem_ld_x32(sS + 32, rb);
-          exp32(ra, sc2, nms, sum_a, sum_b, pk);
+          uint32_t pk[16];
+          exp32(r0, sc2, nms, sum_a, sum_b, pk);
           tmem_st_x16(sS + 0, pk);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) reg_fence(rb[c]);
-          tmem_ld_x32(sS + 64, ra);
-          exp32(rb, sc2, nms, sum_a, sum_b, pk);
+          exp32(r1, sc2, nms, sum_a, sum_b, pk);
           tmem_st_x16(sS + 16, pk);
           tmem_st_wait();
           tc_fence_before_sync();
           mbar_arrive(&p_half[i]);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) reg_fence(ra[c]);
-          tmem_ld_x32(sS + 96, rb);
-          exp32(ra, sc2, nms, sum_a, sum_b, pk);
+          exp32(r2, sc2, nms, sum_a, sum_b, pk);
           tmem_st_x16(sS + 32, pk);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) reg_fence(rb[c]);
-          exp32(rb, sc2, nms, sum_a, sum_b, pk);
+          exp32(r3, sc2, nms, sum_a, sum_b, pk);
           tmem_st_x16(sS + 48, pk);
-        } else {
-          // Boundary tile (causal diagonal, window edge, sink, ragged tail):
-          // the same arithmetic through compact chunk loops, with the mask;
-          // both halves of P are published at the end.
-          const int kb = j * kBN;
-          const int lim_hi = hi_row - kb;
-          const int lim_lo = (p.window > 0) ? lo_row - kb : kNoLowerBound;
-          const int lim_sink = p.n_sink - kb;
-          uint32_t ra[32];
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld_x32(sS + 32 * c, ra);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) reg_fence(ra[e]);
-            mask32(ra, lim_hi - 32 * c, lim_lo - 32 * c, lim_sink - 32 * c);
-            mx = max32(ra, mx);
-          }
-          update_rescale();
-          const uint64_t sc2 = f2(scale2, scale2), nms = f2(-ms, -ms);
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld_x32(sS + 32 * c, ra);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) reg_fence(ra[e]);
-            mask32(ra, lim_hi - 32 * c, lim_lo - 32 * c, lim_sink - 32 * c);
-            uint32_t pk[16];
-            exp32(ra, sc2, nms, sum_a, sum_b, pk);
-            tmem_st_x16(sS + 16 * c, pk);
-          }
-          tmem_st_wait();
-          tc_fence_before_sync();
-          mbar_arrive(&p_half[i]);
         }
         tmem_st_wait();
         tc_fence_before_sync();
@@ -1073,11 +1035,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---------------------------------------------------------------- epilogue
+      // O / l in bf16 straight from tensor memory to the caller's layout
+      // (each thread its own row, 16-byte stores), then the row's LSE.  Every
+      // branch below is uniform over the warp, and the tensor-memory loads
+      // (warp-collective) are made by every lane whatever its row.
       Work w;
       decode_work<kPagedKV>(p, k, sinkT, w, false);
       const int row = w.q0 + i * kBM + r;
       const bool valid = row < w.Lq;
-      bool have_o = t_item > 0;
+      const bool have_o = t_item > 0;
       if (have_o) {
         bool w_ok = mbar_wait(&o_done[i], no & 1, abort_flag, p.wait_limit_ns);
         w_ok = __all_sync(0xffffffffu, w_ok);
@@ -1107,38 +1073,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         inv = e1 / fmaf(l - corr, e1, e2);
         lse_row = mst + logf(fmaf(l, e1, e2));
       }
-      // O goes out through the staging tile and bulk tensor stores (issued by
-      // the store warp), or by direct stores (epilogue_bulk).  Every branch
-      // below is uniform over the warpgroup, and the tensor-memory loads
-      // (warp-collective) are made by every lane whatever its row.
-      const bool bulk = epilogue_bulk(p, w, i);
-      // The staging tile goes to warpgroup 0 then 1 for every item, whether
-      // or not a warpgroup uses it.  Every warp waits for its turn:
-      // warpgroup 0 of item e for warpgroup 1 of item e - 1 to be done with
-      // the tile, warpgroup 1 for warpgroup 0 of item e.  The four warps then
-      // arrive on stage_full[i] (after writing their rows, for a bulk
-      // store), and the store warp hands the turn on once its copy has read
-      // the tile; so a turn is passed only after all four warps have seen
-      // the previous one.
-      const int e_turn = i ? ne : ne - 1;  // phase of turn[i] to wait for
-      ++ne;
-      if (e_turn >= 0) {
-        const bool w_ok =
-            __all_sync(0xffffffffu, mbar_wait(&turn[i], e_turn & 1, abort_flag, p.wait_limit_ns));
-        if (!w_ok) {
-          if (lane == 0) fail(p.status, abort_flag);
-          ok = false;
-          break;
-        }
-      }
-      if (bulk) {
-        // 32 columns at a time (the next chunk's load in flight), scaled by
-        // 1 / l in pairs, packed to bf16 and written as four 16-byte pieces:
-        // chunk k of row r of swizzle atom a sits at position k ^ (r % 8)
-        // (the 128-byte swizzle the tensor store expects).
+      {
         const uint64_t inv2 = f2(inv, inv);
-        auto stage32 = [&](const uint32_t* o, int c) {
-          uint8_t* atom = sO + (c / 2) * C::kAtomBytes + r * 128;
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.o + static_cast<long long>(w.bseq) * p.o_sb +
+            static_cast<long long>(w.q_base + row) * p.o_ss + static_cast<long long>(w.h) * p.o_sh);
+        // 32 columns at a time, the next chunk's load in flight while one is
+        // scaled, packed and stored.
+        auto store32 = [&](const uint32_t* o, int c) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
             uint32_t wv[4];
@@ -1150,9 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        a1);
               wv[e] = seen ? pack_bf16x2(a0, a1) : 0u;
             }
-            const int chunk = (c % 2) * 4 + v4;
-            *reinterpret_cast<uint4*>(atom + ((chunk ^ (r & 7)) * 16)) =
-                make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            if (valid) dst[c * 4 + v4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         };
         uint32_t oa[32], ob[32];
@@ -1167,52 +1107,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) reg_fence(oa[e]);
           if (have_o) tmem_ld_x32(taddr + colO + (c + 1) * 32, ob);
-          stage32(oa, c);
+          store32(oa, c);
           if (have_o) tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) reg_fence(ob[e]);
           if (have_o && c + 2 < D / 32) tmem_ld_x32(taddr + colO + (c + 2) * 32, oa);
-          stage32(ob, c + 1);
+          store32(ob, c + 1);
           if (have_o && c + 2 < D / 32) tmem_ld_wait();
         }
-        // Rows written: make them visible to the bulk copy; the store warp
-        // issues it once all four warps have arrived.
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&stage_full[i]);
-      } else {
-        // Direct stores (varlen tail tile, or no row at all): the tile is not
-        // used; the store warp passes the turn on once all four warps have
-        // taken theirs.
-        if (lane == 0) mbar_arrive(&stage_full[i]);
-        const size_t orow = p.cu_q ? (static_cast<size_t>(w.q_base + row) * p.Hq + w.h) * D
-                                   : ((static_cast<size_t>(w.bseq) * p.Sq + row) * p.Hq + w.h) * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          if (have_o) {
-            tmem_ld_x32(taddr + colO + c * 32, o);
-            tmem_ld_wait();
-          }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) reg_fence(o[e]);
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o + orow);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint32_t wv[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int idx = v4 * 8 + 2 * e;
-                wv[e] = seen ? pack_bf16x2(__uint_as_float(o[idx]) * inv,
-                                           __uint_as_float(o[idx + 1]) * inv)
-                             : 0u;
-              }
-              dst[c * 4 + v4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            }
-          }
-        }
-        __syncwarp();
       }
       if (valid && p.lse != nullptr) {
         const size_t li = p.cu_q ? static_cast<size_t>(w.h) * p.total_q + w.q_base + row
@@ -1290,6 +1192,9 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   if (attr_err != cudaSuccess) return attr_err;
   Params p;
   p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.o_sb = a.o_sb;
+  p.o_ss = a.o_ss;
+  p.o_sh = a.o_sh;
   p.lse = a.lse;
   p.sink = a.sink;
   p.cu_q = a.cu_q;
@@ -1326,11 +1231,9 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   // The paged cache has an instantiation of its own, so that the dense and
   // packed kernels' code is not touched by its page lookups.
   if (a.page_table != nullptr)
-    attn_fwd_kernel<D, true><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK, a.tmV,
-                                                                       a.tmO, p);
+    attn_fwd_kernel<D, true><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK, a.tmV, p);
   else
-    attn_fwd_kernel<D, false><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK, a.tmV,
-                                                                        a.tmO, p);
+    attn_fwd_kernel<D, false><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK, a.tmV, p);
   return cudaGetLastError();
 }
 

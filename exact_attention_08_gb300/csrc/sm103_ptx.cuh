@@ -370,6 +370,80 @@ __device__ __forceinline__ void mma_bf16_ts_wc(uint32_t d_tmem, uint32_t a_tmem,
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "n"(kAcc)
       : "memory");
 }
+// ---------------------------------------------------------------- grouped MMA issue
+// A whole product issued under one elect.sync: the descriptors' start-address
+// fields (bits 0-13, 16-byte units) advance with 32-bit adds on their low
+// words (shared-memory offsets stay below 256 KB, so the field never carries
+// into the next one), which keeps the issuing warp's instruction count per
+// MMA low.  The first K-step overwrites D (or accumulates, for the P V form
+// with acc != 0), the others accumulate.
+//
+// S = A B^T over K = 128 (8 K-steps of 16), both operands K-major with the
+// 128-byte swizzle: K-step kk starts (kk % 4) * 32 bytes into atom kk / 4,
+// atoms kAtom16 x 16 bytes apart.
+template <int kAtom16>
+__device__ __forceinline__ void mma_ss_k128_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 al, ah, bl, bh, x, y;\n\t.reg .b64 da, db;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "mov.b64 {al, ah}, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;\n\t"
+      "add.u32 x, al, 2;\n\tadd.u32 y, bl, 2;\n\tmov.b64 da, {x, ah};\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 x, al, 4;\n\tadd.u32 y, bl, 4;\n\tmov.b64 da, {x, ah};\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 x, al, 6;\n\tadd.u32 y, bl, 6;\n\tmov.b64 da, {x, ah};\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 x, al, %4;\n\tadd.u32 y, bl, %4;\n\tmov.b64 da, {x, ah};\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 x, al, %5;\n\tadd.u32 y, bl, %5;\n\tmov.b64 da, {x, ah};\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 x, al, %6;\n\tadd.u32 y, bl, %6;\n\tmov.b64 da, {x, ah};\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 x, al, %7;\n\tadd.u32 y, bl, %7;\n\tmov.b64 da, {x, ah};\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "n"(kAtom16), "n"(kAtom16 + 2), "n"(kAtom16 + 4),
+      "n"(kAtom16 + 6)
+      : "memory");
+}
+
+// The same over K = 64 (one atom, 4 K-steps).
+__device__ __forceinline__ void mma_ss_k64_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 al, ah, bl, bh, x, y;\n\t.reg .b64 da, db;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "mov.b64 {al, ah}, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;\n\t"
+      "add.u32 x, al, 2;\n\tadd.u32 y, bl, 2;\n\tmov.b64 da, {x, ah};\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 x, al, 4;\n\tadd.u32 y, bl, 4;\n\tmov.b64 da, {x, ah};\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 x, al, 6;\n\tadd.u32 y, bl, 6;\n\tmov.b64 da, {x, ah};\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc)
+      : "memory");
+}
+
+// D += A B over 64 keys (4 K-steps of 16): A from tensor memory (bf16 pairs,
+// 8 columns per K-step), B MN-major in shared memory (2048 bytes, 128 x 16 B,
+// per K-step).  acc == 0 makes the first K-step overwrite D.
+__device__ __forceinline__ void mma_ts_k64_w(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                             uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t.reg .b32 bl, bh, x, y;\n\t.reg .b64 db;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 {bl, bh}, %2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.u32 x, %1, 8;\n\tadd.u32 y, bl, 128;\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x], db, %3, 1;\n\t"
+      "add.u32 x, %1, 16;\n\tadd.u32 y, bl, 256;\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x], db, %3, 1;\n\t"
+      "add.u32 x, %1, 24;\n\tadd.u32 y, bl, 384;\n\tmov.b64 db, {y, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x], db, %3, 1;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
