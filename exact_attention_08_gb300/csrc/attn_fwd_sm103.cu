@@ -16,7 +16,8 @@
 //   warp  8     TMA producer (Q tiles through three slots, the K/V ring);
 //               allocates TMEM
 //   warp  9     MMA issuer (whole warp, one elected lane issues)
-//   warps 10-11 idle (the register split needs whole warpgroups)
+//   warp  10    builds the dense item order of causal packed calls at start
+//   warps 10-11 otherwise idle (the register split needs whole warpgroups)
 // Tensor memory (512 columns): S_i = Q_i K^T at columns [128 i, 128 i + 128)
 // (fp32), O_i at [256 + D i, 256 + D i + D) (fp32).  The softmax writes the
 // probabilities P_i back over the first 64 columns of S_i as packed bf16
@@ -74,6 +75,7 @@ constexpr int kRegsSplit = 2 * 128 * kRegsSoftmax + 128 * kRegsOther;
 static_assert(kRegsSplit <= kThreads * 168, "register split");
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpTable = 10;  // builds the dense item order of packed calls, then idles
 constexpr int kPrefetch = 2;  // key/value tiles warmed in L2 ahead of their load
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -326,18 +328,106 @@ struct Work {
   TileRange r0, r1;
 };
 
+// Causal packed calls (varlen, paged) with up to kTabMaxSeq sequences and
+// kTabMaxLev query pairs per sequence walk a dense item order: only the
+// (sequence, query pair) combinations that hold query rows, level by level
+// from the last query pair down (causal work grows with the pair index), the
+// sequences of a level in decreasing order of their pair count.  In the
+// sparse order, a level of short sequences is mostly empty items, and the
+// persistent CTAs that drew them ended up with less work than the others
+// (measured on 8 sequences of 900-3198 rows: key steps per CTA 112-179
+// against a mean of 147).  One warp builds the table at kernel start.
+constexpr int kTabMaxSeq = 256;
+constexpr int kTabMaxLev = 64;
+
+struct ItemTable {
+  int total;                       // items in the dense order (0: the table is not used)
+  int lev_start[kTabMaxLev + 1];   // dense sequence slots before each level
+  int hist[kTabMaxLev + 1];        // sequences by pair count (scratch of the build)
+  short order[kTabMaxSeq];         // sequences, most query pairs first
+};
+
+// The query rows of packed sequence b, or -1 when its offsets are invalid
+// (the same checks as decode_work).
+template <bool kPagedKV>
+__device__ __forceinline__ int packed_rows(const Params& p, int b) {
+  const int a = p.cu_q[b], e = p.cu_q[b + 1];
+  if (a < 0 || e < a || e > p.total_q || e - a > p.Sq) return -1;
+  if (kPagedKV) {
+    const int lk = p.seqlens_k[b];
+    if (lk < 0 || lk > p.max_pages * kPage) return -1;
+  } else {
+    const int ka = p.cu_k[b], ke = p.cu_k[b + 1];
+    if (ka < 0 || ke < ka) return -1;
+  }
+  return e - a;
+}
+
+// Builds the dense order (one warp).  Sequences with invalid offsets are
+// reported and left out.
+template <bool kPagedKV>
+__device__ __forceinline__ void build_item_table(const Params& p, ItemTable& t, int lane) {
+  const int nlev = p.num_qpairs;
+  for (int l = lane; l <= nlev; l += 32) t.hist[l] = 0;
+  __syncwarp();
+  for (int b = lane; b < p.B; b += 32) {
+    const int rows = packed_rows<kPagedKV>(p, b);
+    if (rows < 0) atomicOr(p.status, kStatusBadInput);
+    const int np = rows <= 0 ? 0 : min((rows + kQT * kBM - 1) / (kQT * kBM), nlev);
+    atomicAdd(&t.hist[np], 1);
+  }
+  __syncwarp();
+  if (lane == 0) {
+    // hist[np] becomes the first slot of the sequences with np pairs (most
+    // pairs first); level qp holds the sequences with more than qp pairs.
+    int run = 0;
+    for (int np = nlev; np >= 0; --np) {
+      const int c = t.hist[np];
+      t.hist[np] = run;
+      run += c;
+    }
+    t.lev_start[0] = 0;
+    for (int l = 0; l < nlev; ++l) {
+      const int qp = nlev - 1 - l;
+      t.lev_start[l + 1] = t.lev_start[l] + t.hist[qp];  // sequences with > qp pairs
+    }
+    t.total = t.lev_start[nlev] * p.Hq;
+  }
+  __syncwarp();
+  for (int b = lane; b < p.B; b += 32) {
+    const int rows = packed_rows<kPagedKV>(p, b);
+    const int np = rows <= 0 ? 0 : min((rows + kQT * kBM - 1) / (kQT * kBM), nlev);
+    t.order[atomicAdd(&t.hist[np], 1)] = static_cast<short>(b);
+  }
+  __syncwarp();
+}
+
 // Item order.  Without causal masking every item is the same work; the
 // query pairs of one (batch, head) are consecutive, so CTAs streaming the
 // same keys and values run together and share them through L2.  With
 // causal masking the work of a pair grows with its index: the longest pairs
-// of every head come first.  Heads of one KV group are adjacent either way.
+// of every head come first (for packed calls through the dense table when
+// there is one).  Heads of one KV group are adjacent either way.
 // Returns false when the item has no query rows or its sequence offsets are
 // invalid (reported once, by the caller that passes report).
-template <bool kPagedKV>
-__device__ __forceinline__ bool decode_work(const Params& p, int k, int sinkT, Work& w,
-                                            bool report) {
+template <bool kPagedKV, bool kTable>
+__device__ __forceinline__ bool decode_work(const Params& p, const ItemTable& tab, int k,
+                                            int sinkT, Work& w, bool report) {
   int qp;
-  if (p.causal) {
+  if (kTable) {
+    const int sl = fdiv(k, p.div_hq);
+    w.h = k - sl * p.Hq;
+    int lo = 0, hi = p.num_qpairs;  // the level l with lev_start[l] <= sl < lev_start[l + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tab.lev_start[mid] <= sl)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    qp = p.num_qpairs - 1 - lo;
+    w.bseq = tab.order[sl - tab.lev_start[lo]];
+  } else if (p.causal) {
     const int x = fdiv(k, p.div_hq), y = fdiv(x, p.div_b);
     w.h = k - x * p.Hq;
     w.bseq = x - y * p.B;
@@ -410,7 +500,7 @@ __device__ __forceinline__ int item_of(int n, int num_items) {
   return k < num_items ? static_cast<int>(k) : -1;
 }
 
-template <int D, bool kPagedKV>
+template <int D, bool kPagedKV, bool kTable>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -436,6 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   __shared__ int abort_flag_s;
   volatile int* abort_flag = &abort_flag_s;
+  __shared__ ItemTable tab;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int sinkT = (p.window > 0 && p.n_sink > 0) ? (p.n_sink + kBN - 1) / kBN : 0;
@@ -465,10 +556,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
+  if (kTable && warp == kWarpTable) build_item_table<kPagedKV>(p, tab, lane);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  const int num_items = kTable ? tab.total : p.num_items;
 
   // The CTA is persistent: every role walks the same item sequence
   // (item_of), skipping the same items, and its ring, barrier-phase and
@@ -560,19 +653,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     for (int n = 0; ok; ++n) {
-      const int k = item_of(n, p.num_items);
+      const int k = item_of(n, num_items);
       if (k < 0) break;
       Work w;
-      if (!decode_work<kPagedKV>(p, k, sinkT, w, lane == 0) || w.lastT < 0) continue;
+      if (!decode_work<kPagedKV, kTable>(p, tab, k, sinkT, w, lane == 0) || w.lastT < 0) continue;
       if (!load_q(w, 0)) {
         ok = false;
         break;
       }
       // Warm L2 with the next item's Q tiles.
       {
-        const int k2 = item_of(n + 1, p.num_items);
+        const int k2 = item_of(n + 1, num_items);
         Work w2;
-        if (k2 >= 0 && decode_work<kPagedKV>(p, k2, sinkT, w2, false) && w2.lastT >= 0) {
+        if (k2 >= 0 && decode_work<kPagedKV, kTable>(p, tab, k2, sinkT, w2, false) && w2.lastT >= 0) {
 #pragma unroll
           for (int i = 0; i < kQT; ++i)
 #pragma unroll
@@ -691,10 +784,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_w(&s_full[i]);
     };
     for (int n = 0; ok; ++n) {
-      const int k = item_of(n, p.num_items);
+      const int k = item_of(n, num_items);
       if (k < 0) break;
       Work w;
-      if (!decode_work<kPagedKV>(p, k, sinkT, w, false) || w.lastT < 0) continue;
+      if (!decode_work<kPagedKV, kTable>(p, tab, k, sinkT, w, false) || w.lastT < 0) continue;
       const int qs0 = g % kQSlots, qs1 = (g + 1) % kQSlots;
       const uint32_t qp0 = (g / kQSlots) & 1, qp1 = ((g + 1) / kQSlots) & 1;
       g += kQT;
@@ -827,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int no = 0;    // o_done phases consumed
     bool ok = true;
     for (int n = 0; ok; ++n) {
-      const int k = item_of(n, p.num_items);
+      const int k = item_of(n, num_items);
       if (k < 0) break;
       // Only what the key loop needs stays live through it; the epilogue
       // decodes the item again.
@@ -836,7 +929,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int hi_row, lo_row;
       {
         Work w;
-        if (!decode_work<kPagedKV>(p, k, sinkT, w, false)) continue;
+        if (!decode_work<kPagedKV, kTable>(p, tab, k, sinkT, w, false)) continue;
         const int row = w.q0 + i * kBM + r;  // sequence-relative query index
         hi_row = p.causal ? min(row + w.off, w.Lk - 1) : w.Lk - 1;
         lo_row = (p.window > 0) ? row + w.off - p.window : kNoLowerBound;
@@ -1040,7 +1133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // branch below is uniform over the warp, and the tensor-memory loads
       // (warp-collective) are made by every lane whatever its row.
       Work w;
-      decode_work<kPagedKV>(p, k, sinkT, w, false);
+      decode_work<kPagedKV, kTable>(p, tab, k, sinkT, w, false);
       const int row = w.q0 + i * kBM + r;
       const bool valid = row < w.Lq;
       const bool have_o = t_item > 0;
@@ -1173,10 +1266,14 @@ __global__ void attn_fill_empty_kernel(__nv_bfloat16* o, size_t o_elems, float* 
 template <int D>
 cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   using C = Cfg<D>;
+  // dynamic shared memory plus the static table and flags of the table
+  // instantiations within the 227 KB a block may have
+  static_assert(C::kSmemBytes + sizeof(ItemTable) + 64 <= 227 * 1024, "shared memory");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    for (auto fn : {attn_fwd_kernel<D, false>, attn_fwd_kernel<D, true>}) {
+    for (auto fn : {attn_fwd_kernel<D, false, false>, attn_fwd_kernel<D, true, false>,
+                    attn_fwd_kernel<D, false, true>, attn_fwd_kernel<D, true, true>}) {
       attr_err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       C::kSmemBytes);
       if (attr_err != cudaSuccess) return;
@@ -1230,10 +1327,24 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   const int grid = static_cast<int>(std::min<long long>(items, std::max(a.num_sms, 1)));
   // The paged cache has an instantiation of its own, so that the dense and
   // packed kernels' code is not touched by its page lookups.
-  if (a.page_table != nullptr)
-    attn_fwd_kernel<D, true><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK, a.tmV, p);
-  else
-    attn_fwd_kernel<D, false><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK, a.tmV, p);
+  // Causal packed calls small enough for the dense item order get the
+  // instantiation that builds and walks it.
+  const bool table = a.cu_q != nullptr && a.causal && a.B <= kTabMaxSeq &&
+                     p.num_qpairs <= kTabMaxLev;
+  if (a.page_table != nullptr) {
+    if (table)
+      attn_fwd_kernel<D, true, true><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK,
+                                                                              a.tmV, p);
+    else
+      attn_fwd_kernel<D, true, false><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK,
+                                                                               a.tmV, p);
+  } else if (table) {
+    attn_fwd_kernel<D, false, true><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK,
+                                                                             a.tmV, p);
+  } else {
+    attn_fwd_kernel<D, false, false><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK,
+                                                                              a.tmV, p);
+  }
   return cudaGetLastError();
 }
 

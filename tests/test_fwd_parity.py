@@ -180,3 +180,38 @@ def test_varlen_repeated_calls_report_ok(ea):
         ea.attn_fwd_ex(q, k, v, cu_q, cu_k, max_seqlen_q=x.max_q, max_seqlen_k=x.max_k, o=o,
                        lse=lse, causal=True, scale=x.scale)
         assert ea.attn_device_status() == ea.ATTN_OK, f"call {rep}"
+
+
+@pytest.mark.parametrize("nseq,lo,hi,seed", [
+    (40, 0, 700, 43),     # many short sequences, some empty: the dense item order
+    (300, 1, 60, 44),     # more sequences than the dense order holds: the sparse order
+])
+def test_varlen_many_sequences(ea, nseq, lo, hi, seed):
+    """Causal packed calls with many sequences of mixed lengths (zero-length
+    ones included) against the oracle, every row."""
+    x = workloads.varlen_inputs(seed, nseq, lo, hi, 4, 2, 128, causal=True)
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    o, lse = ea.attn_fwd_ex(q, k, v, x.cu_q.cuda(), x.cu_k.cuda(), max_seqlen_q=x.max_q,
+                            max_seqlen_k=x.max_k, causal=True, scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    ro, rl = oracle.attn_fwd_varlen(np64(x.q), np64(x.k), np64(x.v), x.cu_q.numpy(),
+                                    x.cu_k.numpy(), x.scale, True)
+    compare(o, lse, ro, rl, f"varlen {nseq} sequences")
+
+
+def test_varlen_bad_offsets_reported(ea):
+    """A sequence whose offsets run backwards is reported as ATTN_ERR_BAD_INPUT
+    and left out; a sequence before it is computed as usual."""
+    x = workloads.varlen_inputs(45, 4, 0, 0, 4, 2, 128, causal=True, lengths=[100, 100, 100, 200])
+    cu = x.cu_q.clone()
+    cu[2] = 350   # sequence 1: 250 rows (> max_seqlen 200), sequence 2 runs backwards
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    o, lse = ea.attn_fwd_ex(q, k, v, cu.cuda(), cu.cuda(), max_seqlen_q=200, max_seqlen_k=200,
+                            causal=True, scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_ERR_BAD_INPUT
+    assert ea.attn_device_status() == ea.ATTN_OK  # cleared by the read
+    ro, rl = oracle.attn_fwd(np64(x.q[None, :100]), np64(x.k[None, :100]), np64(x.v[None, :100]),
+                             x.scale, True)
+    compare(o[None, :100], lse[None, :, :100], ro, rl, "sequence 0 next to a bad one")
