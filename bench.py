@@ -830,6 +830,37 @@ def run_variants(ea, workloads, dev, stream, flush):
         d256["causal" if c else "noncausal"] = {"ms": ms, "tflops": fl / (ms / 1e3) / 1e12}
         del qd, kd, vd, od, ld
     out["prefill_d256_b4h16s2048"] = d256
+    # head dimension 256 on a paged cache: the decode (the decode workload's
+    # shape) and chunked prefill (the chunked-prefill workload's shape)
+    dx = workloads.paged_decode_inputs(5301, 64, 32, 8, 256, 1024, 8192, num_splits=8)
+    dq, dkp, dvp, dpt, dsl = (t.to(dev) for t in (dx.q, dx.k_pages, dx.v_pages, dx.page_table,
+                                                  dx.seqlens))
+    do = torch.empty_like(dq)
+    dl = torch.empty(64, 32, dtype=torch.float32, device=dev)
+    dws = torch.empty(ea.attn_decode_workspace_size(64, 32, 256, 8), dtype=torch.uint8,
+                      device=dev)
+    ms = timed_calls(stream, flush, lambda: ea.attn_decode_paged(
+        dq, dkp, dvp, dpt, dsl, do, dl, num_splits=8, scale=dx.scale, workspace=dws,
+        stream=stream))
+    kvb = decode_kv_bytes(dx.seqlens.tolist(), 8, 256)
+    out["decode_d256_b64hq32hkv8"] = {"ms": ms, "kv_gbs": kvb / (ms / 1e3) / 1e9,
+                                      "kv_bytes": kvb}
+    del dq, dkp, dvp, dpt, dsl, do, dl, dws
+    cx = workloads.paged_prefill_inputs(6301, 8, 32, 8, 256, 2048, 8192, 512, 512)
+    cc = cx.cache
+    cq, ckp, cvp, cpt, ccu, csl = (t.to(dev) for t in (cx.q, cc.k_pages, cc.v_pages,
+                                                       cc.page_table, cx.cu_q, cc.seqlens))
+    co = torch.empty_like(cq)
+    cl = torch.empty(cq.shape[1], cq.shape[0], dtype=torch.float32, device=dev)
+    lqs = (cx.cu_q[1:] - cx.cu_q[:-1]).tolist()
+    c_flops = 4.0 * 256 * 32 * sum(visible_pairs(a, b, True)
+                                   for a, b in zip(lqs, cc.seqlens.tolist()))
+    ms = timed_calls(stream, flush, lambda: ea.attn_fwd_paged(
+        cq, ckp, cvp, cpt, ccu, csl, co, cl, max_seqlen_q=cx.max_q, causal=True,
+        scale=cx.scale, stream=stream))
+    out["chunked_prefill_paged_d256_b8hq32hkv8"] = {"ms": ms, "flops": c_flops,
+                                                    "tflops": c_flops / (ms / 1e3) / 1e12}
+    del cq, ckp, cvp, cpt, ccu, csl, co, cl
     torch.cuda.synchronize(dev)
     return out
 

@@ -354,7 +354,8 @@ ATTN_API int attn_fwd_paged(const void* q, const void* k_pages, const void* v_pa
     return set_error(ATTN_ERR_INVALID_ARG, "bad sizes (B=%d Hq=%d Hkv=%d)", B, Hq, Hkv);
   if (Hq % Hkv != 0)
     return set_error(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
-  if (d != 64 && d != 128) return set_error(ATTN_ERR_UNSUPPORTED, "head dim %d (64 or 128)", d);
+  if (d != 64 && d != 128 && d != 256)
+    return set_error(ATTN_ERR_UNSUPPORTED, "head dim %d (64, 128 or 256)", d);
   if (page_size != 16) return set_error(ATTN_ERR_UNSUPPORTED, "page size %d (16)", page_size);
   if (!(scale > 0.f) || !std::isfinite(scale))
     return set_error(ATTN_ERR_INVALID_ARG, "scale must be finite and positive");
@@ -513,7 +514,8 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
     return set_error(ATTN_ERR_INVALID_ARG, "bad sizes");
   if (Hq % Hkv != 0)
     return set_error(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
-  if (d != 64 && d != 128) return set_error(ATTN_ERR_UNSUPPORTED, "head dim %d (64 or 128)", d);
+  if (d != 64 && d != 128 && d != 256)
+    return set_error(ATTN_ERR_UNSUPPORTED, "head dim %d (64, 128 or 256)", d);
   if (page_size != 16) return set_error(ATTN_ERR_UNSUPPORTED, "page size %d (16)", page_size);
   if (num_splits < 1 || num_splits > 64)
     return set_error(ATTN_ERR_INVALID_ARG, "num_splits %d not in [1, 64]", num_splits);

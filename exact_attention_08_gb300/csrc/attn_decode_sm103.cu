@@ -355,6 +355,241 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
   }
 }
 
+// Head dimension 256.  One accumulator tile of 16 query heads x 256 columns
+// is 128 fp32 registers a thread, too many next to the rest of the state, so
+// the two consumer warps both walk every page of the split: each forms
+// S = Q K^T over the full head dimension (the same numbers in both, so the
+// two online-softmax states stay identical) and keeps its own half of O,
+// columns 128 w .. 128 w + 127.  Q fragments are read from shared memory page
+// by page (64 registers saved).  A ring slot is released once both warps have
+// read it.  Pages in flight per SM: two CTAs x 6 slots x 16 KB.
+constexpr int kStages256 = 6;
+constexpr int kQPitch256 = 256 * 2 + 16;  // bytes per staged query row (16-byte skew)
+
+struct Dec256 {
+  static constexpr int kAtoms = 4;
+  static constexpr int kBoxBytes = kPage * 128;
+  static constexpr int kSliceBytes = kAtoms * kBoxBytes;
+  static constexpr int kStageBytes = 2 * kSliceBytes;
+  static constexpr int kRingBytes = kStages256 * kStageBytes;
+  static constexpr int kOffQ = kRingBytes;
+  static constexpr int kOffBar = kOffQ + kHeadsPerCta * kQPitch256;
+  static constexpr int kSmemBytes = kOffBar + 2 * kStages256 * 8 + 1024;
+};
+
+__global__ void __launch_bounds__(kDecThreads, 2)
+    attn_decode_split256_kernel(const __grid_constant__ CUtensorMap tmK,
+                                const __grid_constant__ CUtensorMap tmV, const DecParams p) {
+  using C = Dec256;
+  constexpr int D = 256;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* empty = full + kStages256;
+  uint8_t* sq = smem + C::kOffQ;
+  __shared__ int abort_flag_s;
+  volatile int* abort_flag = &abort_flag_s;
+
+  const int split = blockIdx.x;
+  const int hkv = blockIdx.y / p.n_hchunks;
+  const int hchunk = blockIdx.y % p.n_hchunks;
+  const int b = blockIdx.z;
+  const int g0 = hchunk * kHeadsPerCta;
+  const int nh = min(kHeadsPerCta, p.G - g0);
+  const int h0 = hkv * p.G + g0;
+
+  int L = p.seqlens[b];
+  if (L < 0 || L > p.max_pages * kPage) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadInput);
+    L = max(0, min(L, p.max_pages * kPage));
+  }
+  const int np = (L + kPage - 1) / kPage;
+  const int pps = (np + p.num_splits - 1) / p.num_splits;
+  const int pg0 = min(split * pps, np);
+  const int pg1 = min(pg0 + pps, np);
+  const int npg = pg1 - pg0;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    abort_flag_s = 0;
+    for (int s = 0; s < kStages256; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
+    }
+    fence_mbar_init();
+  }
+  // The served query heads' rows (16 x 256 bf16, rows past nh zero).
+  {
+    const __nv_bfloat16* qb = p.q + (static_cast<size_t>(b) * p.Hq + h0) * D;
+    for (int idx = threadIdx.x; idx < kHeadsPerCta * (D / 8); idx += kDecThreads) {
+      const int r = idx / (D / 8), c8 = idx % (D / 8);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (r < nh) v = *reinterpret_cast<const uint4*>(qb + static_cast<size_t>(r) * D + c8 * 8);
+      *reinterpret_cast<uint4*>(sq + r * kQPitch256 + c8 * 16) = v;
+    }
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ============================================================ producer
+    if (lane == 0 && npg > 0) {
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      const int* row = p.page_table + static_cast<size_t>(b) * p.max_pages;
+      for (int i = 0; i < npg; ++i) {
+        const int s = i % kStages256;
+        if (!mbar_wait(&empty[s], ((i / kStages256) & 1) ^ 1, abort_flag, p.wait_limit_ns)) {
+          atomicOr(p.status, kStatusTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        int page = row[pg0 + i];
+        if (page < 0 || page >= p.num_pages) {
+          atomicOr(p.status, kStatusBadInput);
+          page = p.num_pages;  // past the pool: the copy reads zeros
+        }
+        uint8_t* st = smem + s * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a) {
+          tma_load_4d(st + a * C::kBoxBytes, &tmK, &full[s], a * 64, hkv, 0, page);
+          tma_load_4d(st + C::kSliceBytes + a * C::kBoxBytes, &tmV, &full[s], a * 64, hkv, 0, page);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ============================================================ consumers
+    const int half = warp - 1;        // the O columns this warp keeps: 128 half ..
+    const int r_lo = lane >> 2;
+    const int cpair = (lane & 3) * 2;
+    const int mi = lane >> 3, rr8 = lane & 7;
+    // ldmatrix rows of the query fragments: matrix mi holds rows 8 (mi & 1) ..,
+    // columns 8 (mi >> 1) .. of each 16 x 16 block.
+    const uint32_t qrow = smem_addr(sq) + (rr8 + ((mi & 1) ? 8 : 0)) * kQPitch256 +
+                          ((mi & 2) ? 16 : 0);
+    float o[D / 16][4];
+#pragma unroll
+    for (int n = 0; n < D / 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    const float scale2 = p.scale2;
+    bool ok = true;
+    for (int i = 0; i < npg; ++i) {
+      const int s = i % kStages256;
+      ok = mbar_wait(&full[s], (i / kStages256) & 1, abort_flag, p.wait_limit_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) {
+          atomicOr(p.status, kStatusTimeout);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      const uint32_t kst = smem_addr(smem + s * C::kStageBytes);
+      const uint32_t vst = kst + C::kSliceBytes;
+      // ---- S[16 heads x 16 tokens] = Q K^T over all 256 columns
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t qa[4];
+        ldsm_x4(qrow + kk * 32, qa[0], qa[1], qa[2], qa[3]);
+        const int tok = rr8 + ((mi & 2) ? 8 : 0);
+        const int e = kk * 16 + ((mi & 1) ? 8 : 0);
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4(kst + (e / 64) * C::kBoxBytes + swz(tok, e % 64), b00, b01, b10, b11);
+        mma16816(sc[0], qa, b00, b01);
+        mma16816(sc[1], qa, b10, b11);
+      }
+      const int tok_base = (pg0 + i) * kPage;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (tok_base + nt * 8 + cpair + (e & 1) >= L) sc[nt][e] = -INFINITY;
+      float mx_lo = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+      float mx_hi = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+      const float ms_lo = (mn_lo == -INFINITY) ? 0.f : mn_lo * scale2;
+      const float ms_hi = (mn_hi == -INFINITY) ? 0.f : mn_hi * scale2;
+      const float a_lo = ex2_approx(fmaf(m_lo, scale2, -ms_lo));
+      const float a_hi = ex2_approx(fmaf(m_hi, scale2, -ms_hi));
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+      uint32_t pa[4];
+      float ps_lo = 0.f, ps_hi = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const float p0 = ex2_approx(fmaf(sc[nt][0], scale2, -ms_lo));
+        const float p1 = ex2_approx(fmaf(sc[nt][1], scale2, -ms_lo));
+        const float p2 = ex2_approx(fmaf(sc[nt][2], scale2, -ms_hi));
+        const float p3 = ex2_approx(fmaf(sc[nt][3], scale2, -ms_hi));
+        ps_lo += p0 + p1;
+        ps_hi += p2 + p3;
+        pa[nt * 2 + 0] = pack_bf16x2(p0, p1);
+        pa[nt * 2 + 1] = pack_bf16x2(p2, p3);
+      }
+      l_lo = l_lo * a_lo + ps_lo;
+      l_hi = l_hi * a_hi + ps_hi;
+      // ---- this warp's half of O = alpha O + P V
+#pragma unroll
+      for (int n = 0; n < D / 16; ++n) {
+        o[n][0] *= a_lo;
+        o[n][1] *= a_lo;
+        o[n][2] *= a_hi;
+        o[n][3] *= a_hi;
+      }
+#pragma unroll
+      for (int n2 = 0; n2 < D / 32; ++n2) {
+        const int tok = rr8 + ((mi & 1) ? 8 : 0);
+        const int e = half * (D / 2) + n2 * 16 + ((mi & 2) ? 8 : 0);
+        uint32_t b0a, b1a, b0b, b1b;
+        ldsm_x4_t(vst + (e / 64) * C::kBoxBytes + swz(tok, e % 64), b0a, b1a, b0b, b1b);
+        mma16816(o[2 * n2], pa, b0a, b1a);
+        mma16816(o[2 * n2 + 1], pa, b0b, b1b);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // ---- the split's normalised half of O and, from warp 1, its LSE
+    if (ok) {
+      l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+      l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+      l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+      l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+      const size_t ws_row0 = (static_cast<size_t>(b) * p.Hq + h0) * p.num_splits + split;
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int g = r_lo + 8 * hr;
+        if (g >= nh) continue;
+        const float l = hr ? l_hi : l_lo, m = hr ? m_hi : m_lo;
+        const bool seen = l > 0.f;
+        const float inv = seen ? 1.f / l : 0.f;
+        const size_t wr = ws_row0 + static_cast<size_t>(g) * p.num_splits;
+        float* dst = p.ws_o + wr * D + half * (D / 2);
+#pragma unroll
+        for (int n = 0; n < D / 16; ++n) {
+          dst[n * 8 + cpair] = o[n][2 * hr] * inv;
+          dst[n * 8 + cpair + 1] = o[n][2 * hr + 1] * inv;
+        }
+        if (half == 0 && (lane & 3) == 0)
+          p.ws_lse[wr] = seen ? fmaf(m, p.scale, logf(l)) : -INFINITY;
+      }
+    }
+  }
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) {
+    // let copies already issued land before the shared memory is released
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2000000ull) {
+    }
+  }
+}
+
 // Merge of the split partials, ascending split order (deterministic).
 template <int D>
 __global__ void __launch_bounds__(D)
@@ -421,11 +656,49 @@ cudaError_t launch_dec(const DecodeLaunch& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+
+cudaError_t launch_dec256(const DecodeLaunch& a, cudaStream_t stream) {
+  using C = Dec256;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attn_decode_split256_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  DecParams p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.page_table = a.page_table;
+  p.seqlens = a.seqlens;
+  p.ws_o = a.ws_o;
+  p.ws_lse = a.ws_lse;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = a.Hq / a.Hkv;
+  p.n_hchunks = (p.G + kHeadsPerCta - 1) / kHeadsPerCta;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
+  p.num_splits = a.num_splits;
+  p.scale = a.scale;
+  p.scale2 = a.scale * kLog2eDec;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.status = a.status;
+  dim3 grid(a.num_splits, a.Hkv * p.n_hchunks, a.B);
+  attn_decode_split256_kernel<<<grid, kDecThreads, C::kSmemBytes, stream>>>(a.tmK, a.tmV, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_decode_combine_kernel<256><<<a.B * a.Hq, 256, 0, stream>>>(
+      a.ws_o, a.ws_lse, static_cast<__nv_bfloat16*>(a.o), a.lse, a.num_splits, a.sink, a.Hq);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_attn_decode(const DecodeLaunch& a, cudaStream_t stream) {
   if (a.d == 128) return launch_dec<128>(a, stream);
   if (a.d == 64) return launch_dec<64>(a, stream);
+  if (a.d == 256) return launch_dec256(a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -21,6 +21,12 @@
 // K is released atom by atom (each atom feeds four of the sixteen K-steps of
 // S), so K(n+1) streams in while S(n) is still running; V is released once
 // O += P V has read it.  O += P V is one N = 256 product per K-step.
+//
+// Keys in a paged cache (the kPaged instantiation, query blocks packed as for
+// varlen): every 128-key tile is eight 16-token pages looked up in the
+// sequence's page-table row, each atom of the tile loaded as eight 16-row
+// boxes from the 4-D map over the page pool (a 16-row box at a 2 KB offset
+// keeps the 128-byte swizzle phase of the atom).
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -58,6 +64,8 @@ constexpr uint32_t kColO = 2 * kR;
 // partial sums stay far from overflow, and the final O / l is unchanged).
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kNoLowerBound = -(1 << 29);
+constexpr int kPage = 16;                // keys per page of a paged cache
+constexpr int kPagesPerTile = kR / kPage;
 
 struct P256 {
   __nv_bfloat16* o;
@@ -65,6 +73,9 @@ struct P256 {
   const float* sink;  // logit sink per query head, or null
   const int* cu_q;    // varlen sequence starts, or null (dense)
   const int* cu_k;
+  const int* page_table;  // paged keys: [B, max_pages] physical pages
+  const int* seqlens_k;   // paged keys: key count of every sequence [B]
+  int max_pages, num_pages;
   long long o_sb, o_ss, o_sh;  // O strides (elements): batch, row, head
   int B, Hq, Hkv, Sq, Skv, total_q, num_qt;
   float scale, scale2;
@@ -85,6 +96,7 @@ struct Tile {
 // CTA order: without a causal mask the Q tiles of one (sequence, head) are
 // adjacent so that they read the same K and V through L2; with one, the
 // last (longest) Q tiles of every head come first.
+template <bool kPaged>
 __device__ __forceinline__ bool decode_tile(const P256& p, Tile& w, bool report) {
   const int per = p.Hq * p.B;
   int x = static_cast<int>(blockIdx.x), qt;
@@ -99,7 +111,22 @@ __device__ __forceinline__ bool decode_tile(const P256& p, Tile& w, bool report)
     w.h = x % p.Hq;
     w.bseq = x / p.Hq;
   }
-  if (p.cu_q != nullptr) {
+  if (kPaged) {
+    // Packed queries against a paged cache: the sequence's keys are its
+    // first seqlens_k[b] cache slots.
+    const int a = p.cu_q[w.bseq], e = p.cu_q[w.bseq + 1];
+    const int lk = p.seqlens_k[w.bseq];
+    if (a < 0 || e < a || e > p.total_q || e - a > p.Sq || lk < 0 ||
+        lk > p.max_pages * kPage) {
+      if (report) atomicOr(p.status, kStatusBadInput);
+      return false;
+    }
+    w.Lq = e - a;
+    w.Lk = lk;
+    w.q_base = a;
+    w.k_base = 0;
+    w.b_coord = 0;
+  } else if (p.cu_q != nullptr) {
     const int a = p.cu_q[w.bseq], e = p.cu_q[w.bseq + 1];
     const int ka = p.cu_k[w.bseq], ke = p.cu_k[w.bseq + 1];
     if (a < 0 || e < a || e > p.total_q || ka < 0 || ke < ka || e - a > p.Sq) {
@@ -181,6 +208,7 @@ __device__ __forceinline__ bool wwait(uint64_t* bar, uint32_t parity, volatile i
   return ok;
 }
 
+template <bool kPaged>
 __global__ void __launch_bounds__(kThr, 1)
     attn_fwd256_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
@@ -206,7 +234,7 @@ __global__ void __launch_bounds__(kThr, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   Tile w;
-  if (!decode_tile(p, w, threadIdx.x == 0)) return;  // uniform over the CTA
+  if (!decode_tile<kPaged>(p, w, threadIdx.x == 0)) return;  // uniform over the CTA
   const int N = w.n_act;
 
   if (threadIdx.x == 0) {
@@ -244,13 +272,44 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
       for (int a = 0; a < kNAtom; ++a)
         tma_load_4d_w(sQ + a * kAtom, &tmQ, q_full, a * 64, w.h, w.q_base + w.q0, w.b_coord);
+      // Paged cache: the physical page of rows 16 pp.. of key tile j, for
+      // lane pp (pages past the sequence's last are replaced by that last
+      // page, whose rows are masked; an index outside the pool is reported
+      // and page 0 read instead).
+      auto page_of = [&](int j) -> int {
+        int phys = 0;
+        if (lane < kPagesPerTile) {
+          const int np = (w.Lk + kPage - 1) / kPage;
+          const int lp = min(j * kPagesPerTile + lane, np - 1);
+          phys = p.page_table[static_cast<size_t>(w.bseq) * p.max_pages + lp];
+          if (phys < 0 || phys >= p.num_pages) {
+            atomicOr(p.status, kStatusBadInput);
+            phys = 0;
+          }
+        }
+        return phys;
+      };
+      // One 64-column atom of key tile j into dst (expected bytes: one atom).
+      auto load_atom = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int a, int j,
+                           int phys) {
+        if constexpr (kPaged) {
+#pragma unroll
+          for (int pp = 0; pp < kPagesPerTile; ++pp)
+            tma_load_4d_w(dst + pp * kPage * 128, map, bar, a * 64, w.hk, 0,
+                          __shfl_sync(0xffffffffu, phys, pp));
+        } else {
+          (void)phys;
+          tma_load_4d_w(dst, map, bar, a * 64, w.hk, w.k_base + j * kR, w.b_coord);
+        }
+      };
       auto load_k = [&](int n) {
-        const int k0 = w.k_base + tile_at(w, n) * kR;
+        const int j = tile_at(w, n);
+        const int phys = kPaged ? page_of(j) : 0;
         for (int a = 0; a < kNAtom; ++a) {
           // atom a is free once S(n - 1) has read it
           if (n > 0 && !wwait(&k_empty[a], (n - 1) & 1, abort_flag, p)) return false;
           mbar_arrive_expect_tx_w(&k_full[a], kAtom);
-          tma_load_4d_w(sK + a * kAtom, &tmK, &k_full[a], a * 64, w.hk, k0, w.b_coord);
+          load_atom(&tmK, sK + a * kAtom, &k_full[a], a, j, phys);
           ++k_cnt[a];
         }
         return true;
@@ -261,11 +320,11 @@ __global__ void __launch_bounds__(kThr, 1)
         // V(n) once O += P(n - 1) V(n - 1) has read V(n - 1).
         if (n + 1 < N && !load_k(n + 1)) break;
         if (n > 0 && !wwait(v_empty, (n - 1) & 1, abort_flag, p)) break;
-        const int k0 = w.k_base + tile_at(w, n) * kR;
+        const int j = tile_at(w, n);
+        const int phys = kPaged ? page_of(j) : 0;
         mbar_arrive_expect_tx_w(v_full, kNAtom * kAtom);
 #pragma unroll
-        for (int a = 0; a < kNAtom; ++a)
-          tma_load_4d_w(sV + a * kAtom, &tmV, v_full, a * 64, w.hk, k0, w.b_coord);
+        for (int a = 0; a < kNAtom; ++a) load_atom(&tmV, sV + a * kAtom, v_full, a, j, phys);
         ++v_loads;
       }
       // Every copy issued lands before the CTA can leave (a load is issued
@@ -506,12 +565,14 @@ __global__ void __launch_bounds__(kThr, 1)
 }  // namespace
 
 cudaError_t launch_attn_fwd256(const FwdLaunch& a, cudaStream_t stream) {
-  if (a.page_table != nullptr || a.d != kD) return cudaErrorInvalidValue;
+  if (a.d != kD) return cudaErrorInvalidValue;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_fwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kSmem);
+    for (auto fn : {attn_fwd256_kernel<false>, attn_fwd256_kernel<true>}) {
+      attr_err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      if (attr_err != cudaSuccess) return;
+    }
   });
   if (attr_err != cudaSuccess) return attr_err;
   P256 p;
@@ -520,6 +581,10 @@ cudaError_t launch_attn_fwd256(const FwdLaunch& a, cudaStream_t stream) {
   p.sink = a.sink;
   p.cu_q = a.cu_q;
   p.cu_k = a.cu_k;
+  p.page_table = a.page_table;
+  p.seqlens_k = a.seqlens_k;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
   p.o_sb = a.o_sb;
   p.o_ss = a.o_ss;
   p.o_sh = a.o_sh;
@@ -540,7 +605,12 @@ cudaError_t launch_attn_fwd256(const FwdLaunch& a, cudaStream_t stream) {
   const long long grid = static_cast<long long>(p.num_qt) * a.Hq * a.B;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  attn_fwd256_kernel<<<static_cast<unsigned>(grid), kThr, kSmem, stream>>>(a.tmQ, a.tmK, a.tmV, p);
+  if (a.page_table != nullptr)
+    attn_fwd256_kernel<true><<<static_cast<unsigned>(grid), kThr, kSmem, stream>>>(a.tmQ, a.tmK,
+                                                                                  a.tmV, p);
+  else
+    attn_fwd256_kernel<false><<<static_cast<unsigned>(grid), kThr, kSmem, stream>>>(a.tmQ, a.tmK,
+                                                                                   a.tmV, p);
   return cudaGetLastError();
 }
 

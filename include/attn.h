@@ -40,11 +40,12 @@
  *     Errors found by a kernel (a bounded wait that ran out, an out-of-range
  *     page index) cannot be returned by the launching call; the kernel
  *     records them in a device-side status word read by attn_device_status.
- *   - Head dimension d: 64, 128 or 256 for the dense, varlen and strided
- *     forward (attn_fwd, attn_fwd_ex, attn_fwd_ex_sink, attn_fwd_strided; at
+ *   - Head dimension d: 64, 128 or 256 for every forward call (attn_fwd,
+ *     attn_fwd_ex, attn_fwd_ex_sink, attn_fwd_strided, attn_fwd_paged; at
  *     d = 256 a CTA takes one 128-row query tile, with two score buffers and
- *     O in tensor memory); 64 or 128 for the paged forward, the decode and the
- *     backward.  The device must be sm_103.
+ *     O in tensor memory) and for the decode (at d = 256 the two consumer
+ *     warps of a split each keep half of O); 64 or 128 for the backward.
+ *     The device must be sm_103.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H

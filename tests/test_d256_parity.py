@@ -132,16 +132,91 @@ def test_logit_sinks(ea):
     _check(ea, x, sink=sink, what="d256 sinks")
 
 
-def test_paged_prefill_rejects_d256(ea):
-    x = workloads.paged_prefill_inputs(220, 2, 4, 2, 128, 0, 0, 0, 0, lengths_k=[64, 32],
-                                       lengths_q=[8, 8])
+PAGED = [
+    # (seed, Hq, Hkv, key counts, query counts, causal, window, n_sink)
+    (220, 4, 2, [300, 17, 1000, 129], [300, 17, 256, 1], True, 0, 0),   # prefill + decode rows
+    (223, 4, 4, [100, 40, 513], [160, 40, 300], True, 0, 0),            # Lq > Lk: masked rows
+    (224, 4, 2, [1500, 300], [400, 300], True, 200, 2),                 # window + sink keys
+    (225, 8, 2, [600, 90], [130, 7], False, 0, 0),                      # non-causal
+]
+
+
+@pytest.mark.parametrize("case", PAGED, ids=[f"seed{c[0]}" for c in PAGED])
+def test_paged_prefill(ea, case):
+    """Query blocks against a paged cache at d = 256 (attn_fwd_paged), against
+    the oracle on the same keys laid out contiguously."""
+    seed, Hq, Hkv, lk, lq, causal, window, n_sink = case
+    x = workloads.paged_prefill_inputs(seed, len(lk), Hq, Hkv, 256, 0, 0, 0, 0, lengths_k=lk,
+                                       lengths_q=lq)
     c = x.cache
-    q = torch.zeros(int(x.cu_q[-1]), 4, 256, dtype=torch.bfloat16, device="cuda")
-    kp = torch.zeros(*c.k_pages.shape[:-1], 256, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(ea.AttnError) as e:
-        ea.attn_fwd_paged(q, kp, kp, c.page_table.cuda(), x.cu_q.cuda(), c.seqlens.cuda(),
-                          max_seqlen_q=x.max_q, scale=0.0625)
-    assert e.value.status == ea.ATTN_ERR_UNSUPPORTED
+    o, lse = ea.attn_fwd_paged(x.q.cuda(), c.k_pages.cuda(), c.v_pages.cuda(),
+                               c.page_table.cuda(), x.cu_q.cuda(), c.seqlens.cuda(),
+                               max_seqlen_q=x.max_q, causal=causal, window=window, n_sink=n_sink,
+                               scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    ro, rl = oracle.attn_fwd_varlen(np64(x.q), np64(c.k_flat), np64(c.v_flat), x.cu_q.numpy(),
+                                    c.cu_kv.to(torch.int32).numpy(), x.scale, causal, window,
+                                    n_sink)
+    compare(o, lse, ro, rl, f"d256 paged prefill seed {seed}")
+    masked = np.isneginf(rl).T
+    if masked.any():
+        assert_masked_rows_zero(o, masked, "d256 paged prefill")
+
+
+def test_paged_prefill_bad_page_index(ea):
+    """A page index outside the pool is reported and never read."""
+    x = workloads.paged_prefill_inputs(226, 2, 4, 2, 256, 0, 0, 0, 0, lengths_k=[200, 64],
+                                       lengths_q=[64, 64])
+    c = x.cache
+    pt = c.page_table.clone()
+    pt[0, 2] = c.k_pages.shape[0] + 5
+    ea.attn_fwd_paged(x.q.cuda(), c.k_pages.cuda(), c.v_pages.cuda(), pt.cuda(), x.cu_q.cuda(),
+                      c.seqlens.cuda(), max_seqlen_q=x.max_q, causal=True, scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_ERR_BAD_INPUT
+    assert ea.attn_device_status() == ea.ATTN_OK
+
+
+@pytest.mark.parametrize("Hq,Hkv,splits", [(8, 2, 1), (8, 2, 3), (32, 8, 8), (4, 4, 5),
+                                           (64, 2, 4)])
+def test_decode(ea, Hq, Hkv, splits):
+    """Paged split-KV decode at d = 256 against the oracle (empty, one-token,
+    page-boundary and long requests; more splits than pages)."""
+    lengths = [1, 15, 16, 17, 300, 0, 64, 1000]
+    x = workloads.paged_decode_inputs(227, len(lengths), Hq, Hkv, 256, 0, 0, lengths=lengths,
+                                      num_splits=splits, extra_pages=7)
+    o, lse = ea.attn_decode_paged(x.q.cuda(), x.k_pages.cuda(), x.v_pages.cuda(),
+                                  x.page_table.cuda(), x.seqlens.cuda(), num_splits=splits,
+                                  scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    k, v = x.contiguous_kv(list(range(len(lengths))))
+    ro, rl = oracle.attn_decode(np64(x.q), np64(k), np64(v), x.seqlens.numpy(), x.scale)
+    compare(o, lse, ro, rl, f"d256 decode Hq={Hq} Hkv={Hkv} S={splits}")
+    assert_masked_rows_zero(o, np.isneginf(rl), "d256 decode empty request")
+
+
+def test_decode_batch(ea):
+    """B=16 requests of 1024-8192 keys, Hq=32, Hkv=8, 8 splits, d = 256, with
+    logit sinks too; every request against the oracle."""
+    x = workloads.paged_decode_inputs(228, 16, 32, 8, 256, 1024, 8192, num_splits=8)
+    q, kp, vp, pt, sl = (t.cuda() for t in (x.q, x.k_pages, x.v_pages, x.page_table, x.seqlens))
+    o, lse = ea.attn_decode_paged(q, kp, vp, pt, sl, num_splits=8, scale=x.scale)
+    sink = workloads.logit_sinks(228, 32)
+    os_, ls_ = ea.attn_decode_paged_sink(q, kp, vp, pt, sl, sink.cuda(), num_splits=8,
+                                         scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    for c in range(0, 16, 4):
+        req = list(range(c, c + 4))
+        k, v = x.contiguous_kv(req)
+        ro, rl = oracle.attn_decode(np64(x.q[req]), np64(k), np64(v), x.seqlens[req].numpy(),
+                                    x.scale)
+        compare(o[c:c + 4], lse[c:c + 4], ro, rl, f"d256 decode requests {c}..{c + 3}")
+        ro, rl = oracle.attn_decode(np64(x.q[req]), np64(k), np64(v), x.seqlens[req].numpy(),
+                                    x.scale, sink=sink.double().numpy())
+        compare(os_[c:c + 4], ls_[c:c + 4], ro, rl, f"d256 decode sinks {c}..{c + 3}")
 
 
 @pytest.mark.parametrize("causal", [False, True])
