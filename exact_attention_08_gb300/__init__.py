@@ -24,7 +24,7 @@ from . import _build
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT",
     "ATTN_ERR_BAD_INPUT", "AttnError", "attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink",
-    "attn_fwd_paged", "attn_fwd_strided", "attn_bwd", "attn_bwd_workspace_size",
+    "attn_fwd_paged", "attn_fwd_strided", "attn_bwd", "attn_bwd_ex", "attn_bwd_workspace_size",
     "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout", "attn_status_string",
     "attn_last_error", "library_path", "lib",
 ]
@@ -60,6 +60,8 @@ def _load() -> ctypes.CDLL:
     L.attn_bwd_workspace_size.argtypes = [i, i, i]
     L.attn_bwd_workspace_size.restype = sz
     L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
+    L.attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f,
+                              i, i, i, vp, sz, vp]
     L.attn_decode_workspace_size.argtypes = [i, i, i, i]
     L.attn_decode_workspace_size.restype = sz
     L.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, sz,
@@ -73,7 +75,7 @@ def _load() -> ctypes.CDLL:
     L.attn_last_error.argtypes = []
     L.attn_last_error.restype = ctypes.c_char_p
     for fn in ("attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink", "attn_fwd_paged", "attn_fwd_strided",
-               "attn_bwd",
+               "attn_bwd", "attn_bwd_ex",
                "attn_decode_paged",
                "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout"):
         getattr(L, fn).restype = ctypes.c_int
@@ -347,6 +349,60 @@ def attn_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, *, causal=False, 
                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                       _stream(stream))
     _check(rc, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_ex(q, k, v, o, lse, dout, cu_seqlens_q=None, cu_seqlens_k=None, dq=None, dk=None,
+                dv=None, *, max_seqlen_q=None, max_seqlen_k=None, causal=False, window=0,
+                n_sink=0, scale=None, workspace=None, stream=None):
+    """Gradients of attn_fwd_ex (sink keys, sliding window, packed sequences).
+    With cu_seqlens (int32 CUDA tensors [nseq+1]): q, o, dout [Tq,Hq,d], k/v
+    [Tk,Hkv,d], lse [Hq,Tq]; without: the dense layout of attn_bwd."""
+    torch = _torch()
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _need(t, n, torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    varlen = cu_seqlens_q is not None
+    if varlen:
+        _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, dev)
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, dev)
+        Tq, Hq, d = q.shape
+        Tk, Hkv, dk_ = k.shape
+        if max_seqlen_q is None or max_seqlen_k is None:
+            raise ValueError("max_seqlen_q and max_seqlen_k are required with cu_seqlens")
+        B, sq, sk = cu_seqlens_q.numel() - 1, int(max_seqlen_q), int(max_seqlen_k)
+        lse_shape = (Hq, Tq)
+    else:
+        B, sq, Hq, d = q.shape
+        Bk, sk, Hkv, dk_ = k.shape
+        if Bk != B:
+            raise ValueError("q/k batch sizes disagree")
+        Tq = Tk = 0
+        lse_shape = (B, Hq, sq)
+    if dk_ != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q/k/v shapes disagree")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("o and dout must be shaped like q")
+    if tuple(lse.shape) != lse_shape:
+        raise ValueError(f"lse must be {list(lse_shape)}")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n, ref in ((dq, "dq", q), (dk, "dk", k), (dv, "dv", v)):
+        _need(t, n, torch.bfloat16, dev)
+        if tuple(t.shape) != tuple(ref.shape):
+            raise ValueError(f"{n} has the wrong shape")
+    need = attn_bwd_workspace_size(B, Hq, sq)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib.attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                         _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q) if varlen else None,
+                         _ptr(cu_seqlens_k) if varlen else None, B, Hq, Hkv, sq, sk, Tq, Tk, d,
+                         scale, int(bool(causal)), int(window), int(n_sink), _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_bwd_ex")
     return dq, dk, dv
 
 

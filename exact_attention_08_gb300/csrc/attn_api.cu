@@ -425,23 +425,37 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Sq) {
   return bwd_workspace_bytes(B, Hq, Sq);
 }
 
-ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                      const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
-                      int Sq, int Skv, int d, float scale, int causal, void* workspace,
-                      size_t workspace_bytes, void* stream) {
+ATTN_API int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                         const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                         int Hkv, int max_Sq, int max_Skv, int total_q, int total_k, int d,
+                         float scale, int causal, int window, int n_sink, void* workspace,
+                         size_t workspace_bytes, void* stream) {
   t_last_error.clear();
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv < 0)
+  const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
+  if (varlen && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr))
+    return set_error(ATTN_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k go together");
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || max_Sq < 0 || max_Skv < 0)
     return set_error(ATTN_ERR_INVALID_ARG, "negative or zero size (B=%d Hq=%d Hkv=%d)", B, Hq, Hkv);
+  if (varlen && (total_q < 0 || total_k < 0))
+    return set_error(ATTN_ERR_INVALID_ARG, "negative total_q / total_k");
   if (Hq % Hkv != 0)
     return set_error(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
   if (d != 64 && d != 128) return set_error(ATTN_ERR_UNSUPPORTED, "head dim %d (64 or 128)", d);
   if (!(scale > 0.f) || !std::isfinite(scale))
     return set_error(ATTN_ERR_INVALID_ARG, "scale must be finite and positive");
   if (causal != 0 && causal != 1) return set_error(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (window < 0) window = 0;
+  if (window > 0 && !causal)
+    return set_error(ATTN_ERR_INVALID_ARG, "a sliding window requires causal");
+  if (n_sink < 0 || (n_sink > 0 && window == 0))
+    return set_error(ATTN_ERR_INVALID_ARG, "sink keys require a window");
   if (B == 0) return ATTN_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t kv_bytes = static_cast<size_t>(B) * Skv * Hkv * d * 2;
-  if (Sq == 0) {  // no query: dK = dV = 0
+  const long long rows_q = varlen ? total_q : static_cast<long long>(B) * max_Sq;
+  const long long rows_k = varlen ? total_k : static_cast<long long>(B) * max_Skv;
+  const size_t kv_bytes = static_cast<size_t>(rows_k) * Hkv * d * 2;
+  if (rows_q == 0 || max_Sq == 0) {  // no query: dK = dV = 0
     if (kv_bytes == 0) return ATTN_OK;
     if (!dk || !dv) return set_error(ATTN_ERR_INVALID_ARG, "dk and dv must be set");
     cudaError_t e = cudaMemsetAsync(dk, 0, kv_bytes, st);
@@ -450,13 +464,15 @@ ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o
   }
   if (!q || !o || !lse || !dout || !dq || !workspace)
     return set_error(ATTN_ERR_INVALID_ARG, "null pointer");
-  if (Skv > 0 && (!k || !v || !dk || !dv))
+  if (rows_k > 0 && (!k || !v || !dk || !dv))
     return set_error(ATTN_ERR_INVALID_ARG, "k, v, dk and dv must be set");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u))
+      (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
     return set_error(ATTN_ERR_INVALID_ARG, "tensors must be 16-byte aligned (lse 4-byte)");
-  const size_t need = bwd_workspace_bytes(B, Hq, Sq);
+  const size_t need = bwd_workspace_bytes(B, Hq, max_Sq);
   if (workspace_bytes < need)
     return set_error(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
                      need);
@@ -471,26 +487,44 @@ ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.total_q = varlen ? total_q : 0;
+  a.total_k = varlen ? total_k : 0;
   const size_t rows = need / (2 * sizeof(float));
   a.ws_lse2 = static_cast<float*>(workspace);
   a.ws_d = static_cast<float*>(workspace) + rows;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
-  a.Sq = Sq;
-  a.Skv = Skv;
+  a.Sq = max_Sq;
+  a.Skv = max_Skv;
   a.d = d;
   a.scale = scale;
   a.causal = causal;
+  a.window = window;
+  a.n_sink = n_sink;
   a.status = ds->status;
-  if ((rc = make_map(&a.tmQ, q, d, Hq, Sq, B, 128, "q")) != ATTN_OK) return rc;
-  if ((rc = make_map(&a.tmDO, dout, d, Hq, Sq, B, 128, "dout")) != ATTN_OK) return rc;
-  if (Skv > 0) {
-    if ((rc = make_map(&a.tmK, k, d, Hkv, Skv, B, 128, "k")) != ATTN_OK) return rc;
-    if ((rc = make_map(&a.tmV, v, d, Hkv, Skv, B, 128, "v")) != ATTN_OK) return rc;
+  // Dense tensors are 4-D maps (d, H, S, B); packed ones (d, H, total, 1).
+  const uint64_t sq = varlen ? static_cast<uint64_t>(total_q) : static_cast<uint64_t>(max_Sq);
+  const uint64_t sk = varlen ? static_cast<uint64_t>(total_k) : static_cast<uint64_t>(max_Skv);
+  const uint64_t nb = varlen ? 1u : static_cast<uint64_t>(B);
+  if ((rc = make_map(&a.tmQ, q, d, Hq, sq, nb, 128, "q")) != ATTN_OK) return rc;
+  if ((rc = make_map(&a.tmDO, dout, d, Hq, sq, nb, 128, "dout")) != ATTN_OK) return rc;
+  if (rows_k > 0 && max_Skv > 0) {
+    if ((rc = make_map(&a.tmK, k, d, Hkv, sk, nb, 128, "k")) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.tmV, v, d, Hkv, sk, nb, 128, "v")) != ATTN_OK) return rc;
   }
   cudaError_t e = launch_attn_bwd(a, st);
   return e == cudaSuccess ? ATTN_OK : cuda_error(e, "attn_bwd launch");
+}
+
+ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                      int Sq, int Skv, int d, float scale, int causal, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  return attn_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, nullptr, nullptr, B, Hq, Hkv, Sq, Skv, 0,
+                     0, d, scale, causal, 0, 0, workspace, workspace_bytes, stream);
 }
 
 ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits) {

@@ -35,6 +35,14 @@
 //   dV += P^T dO, dK += dS^T Q   (A from tensor memory, B MN-major)
 //   S = Q K^T, dP = dO V^T, dQ += dS K.
 // P and dS enter the second products as bf16, like P in the forward.
+//
+// Masks are the forward's: causal aligned to the end of each sequence's keys,
+// a sliding window of W keys with n_sink sink keys visible to every query
+// that may see them causally, packed (varlen) sequences through cu_seqlens
+// ("TileLang tutorial, ch.15", sections 3.4, 5.2 and 5.3).  The dK/dV kernel
+// walks the query tiles that see its key tile (one contiguous range: the
+// window bounds it above unless the tile holds sink keys); the dQ kernel
+// walks the sink tiles, then its window of key tiles.
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -89,20 +97,58 @@ struct BwdCfg {
 };
 
 struct BwdParams {
-  const __nv_bfloat16* dout;  // [B, Sq, Hq, d] (row statistics only)
+  const __nv_bfloat16* dout;  // [B, Sq, Hq, d] or packed [total_q, Hq, d] (row statistics only)
   const __nv_bfloat16* o;
-  const float* lse;          // [B, Hq, Sq], natural log
+  const float* lse;          // [B, Hq, Sq] or packed [Hq, total_q], natural log
+  const int* cu_q;           // packed sequences: [B + 1] query offsets, or null (dense)
+  const int* cu_k;           // packed sequences: [B + 1] key offsets
   float* lse2;               // [B, Hq, Sqp] workspace: -LSE * log2(e), -inf on pad rows
   float* dvec;               // [B, Hq, Sqp] workspace: -rowsum(dO * O)
   __nv_bfloat16* dq;         // [B, Sq, Hq, d]
   __nv_bfloat16* dk;         // [B, Skv, Hkv, d]
   __nv_bfloat16* dv;
-  int B, Hq, Hkv, Sq, Skv, Sqp, d;
+  int B, Hq, Hkv, Sq, Skv, Sqp, d;  // Sq, Skv: the longest sequence when packed
+  int total_q, total_k;             // packed token counts
   float scale, scale2;
-  int causal;
+  int causal, window, n_sink;
   uint64_t wait_limit_ns;
   int* status;
 };
+
+// One sequence's geometry: lengths, first rows in the tensors (for
+// addressing outputs), and the TMA coordinates of its first rows.
+struct SeqGeo {
+  int Lq, Lk, q_base, k_base, b_coord;
+  long long q_row0, k_row0;
+};
+
+// False (and reported when `report`) for packed offsets out of range.
+__device__ __forceinline__ bool seq_geo(const BwdParams& p, int b, SeqGeo& g, bool report) {
+  if (p.cu_q != nullptr) {
+    const int a = p.cu_q[b], e = p.cu_q[b + 1], ka = p.cu_k[b], ke = p.cu_k[b + 1];
+    if (a < 0 || e < a || e > p.total_q || e - a > p.Sq || ka < 0 || ke < ka ||
+        ke > p.total_k || ke - ka > p.Skv) {
+      if (report) atomicOr(p.status, kStatusBadInput);
+      return false;
+    }
+    g.Lq = e - a;
+    g.Lk = ke - ka;
+    g.q_base = a;
+    g.k_base = ka;
+    g.b_coord = 0;
+    g.q_row0 = a;
+    g.k_row0 = ka;
+  } else {
+    g.Lq = p.Sq;
+    g.Lk = p.Skv;
+    g.q_base = 0;
+    g.k_base = 0;
+    g.b_coord = b;
+    g.q_row0 = static_cast<long long>(b) * p.Sq;
+    g.k_row0 = static_cast<long long>(b) * p.Skv;
+  }
+  return true;
+}
 
 __device__ __forceinline__ void reg_fence_b(uint32_t& r) { asm volatile("" : "+r"(r)); }
 
@@ -172,12 +218,15 @@ __global__ void attn_bwd_rowstat_kernel(BwdParams p) {
     const long long rw = rw0 + sub;
     float acc = 0.f, l2 = INFINITY;
     int i = 0;
+    bool row_ok = false;
     if (rw < nrow) {
       i = static_cast<int>(rw % p.Sqp);
       const long long bh = rw / p.Sqp;
       const int h = static_cast<int>(bh % p.Hq), b = static_cast<int>(bh / p.Hq);
-      if (i < p.Sq) {
-        const size_t base = ((static_cast<size_t>(b) * p.Sq + i) * p.Hq + h) * p.d;
+      SeqGeo g;
+      row_ok = seq_geo(p, b, g, i == 0 && h == 0 && l8 == 0) && i < g.Lq;
+      if (row_ok) {
+        const size_t base = ((static_cast<size_t>(g.q_row0) + i) * p.Hq + h) * p.d;
         for (int t = l8 * 8; t < p.d; t += 64) {  // eight bf16 (16 bytes) per lane
           const uint4 g = *reinterpret_cast<const uint4*>(p.dout + base + t);
           const uint4 o = *reinterpret_cast<const uint4*>(p.o + base + t);
@@ -189,14 +238,16 @@ __global__ void attn_bwd_rowstat_kernel(BwdParams p) {
                        __uint_as_float(ow[e] & 0xffff0000u), acc);
           }
         }
-        const float l = p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Sq + i];
+        const float l = p.cu_q != nullptr
+                            ? p.lse[static_cast<size_t>(h) * p.total_q + g.q_row0 + i]
+                            : p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Sq + i];
         l2 = (l == -INFINITY) ? INFINITY : l * kLog2eB;
       }
     }
 #pragma unroll
     for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (l8 == 0 && rw < nrow) {
-      p.dvec[rw] = (i < p.Sq) ? -acc : 0.f;  // stored negated: added, not subtracted
+      p.dvec[rw] = row_ok ? -acc : 0.f;  // stored negated: added, not subtracted
       p.lse2[rw] = -l2;
     }
   }
@@ -255,15 +306,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // mask (where key tile 0 has the most query tiles) the longest come first.
   const int kt = blockIdx.x / (p.B * p.Hkv), hk = (blockIdx.x / p.B) % p.Hkv, b = blockIdx.x % p.B;
   const int G = p.Hq / p.Hkv;
-  const int nqt = p.Sqp / kB;
-  const int off = p.Skv - p.Sq;
   const int k0 = kt * kB;
-  int qt_lo = 0;
+  SeqGeo sg;
+  // A key tile past its sequence's keys has nothing to write (uniform exit).
+  if (!seq_geo(p, b, sg, false) || k0 >= sg.Lk) return;
+  const int nqt = (sg.Lq + kB - 1) / kB;
+  const int off = sg.Lk - sg.Lq;
+  // The query tiles that see a key of the tile: from the first query that
+  // sees key k0 (causal) to the last that sees key k0 + 127 (window; a tile
+  // holding sink keys is seen to the end).
+  int qt_lo = 0, qt_hi = nqt - 1;
   if (p.causal) {
     const int qmin = k0 - off;  // first query that sees key k0
     qt_lo = qmin <= 0 ? 0 : qmin / kB;
   }
-  const int nq = nqt > qt_lo ? nqt - qt_lo : 0;
+  if (p.window > 0 && k0 >= p.n_sink) {
+    const int qmax = k0 + kB - 1 - off + p.window - 1;  // last query that sees key k0 + 127
+    qt_hi = qmax < 0 ? -1 : min(qt_hi, qmax / kB);
+  }
+  const int nq = qt_hi >= qt_lo ? qt_hi - qt_lo + 1 : 0;
   const int ntiles = G * nq;  // (query head, query tile) pairs, head-major
 
   if (threadIdx.x == 0) {
@@ -296,8 +357,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_arrive_expect_tx_w(kv_full, 2 * C::kTile);
 #pragma unroll
     for (int a = 0; a < C::kAtoms; ++a) {
-      tma_load_4d_w(sK + a * C::kAtomBytes, &tmK, kv_full, a * 64, hk, k0, b);
-      tma_load_4d_w(sV + a * C::kAtomBytes, &tmV, kv_full, a * 64, hk, k0, b);
+      tma_load_4d_w(sK + a * C::kAtomBytes, &tmK, kv_full, a * 64, hk, sg.k_base + k0,
+                    sg.b_coord);
+      tma_load_4d_w(sV + a * C::kAtomBytes, &tmV, kv_full, a * 64, hk, sg.k_base + k0,
+                    sg.b_coord);
     }
     int issued = 0;
     for (int t = 0; t < ntiles; ++t) {
@@ -308,9 +371,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx_w(&q_full[s], 2 * C::kTile + 2 * C::kVec);
 #pragma unroll
       for (int a = 0; a < C::kAtoms; ++a) {
-        tma_load_4d_w(st + a * C::kAtomBytes, &tmQ, &q_full[s], a * 64, h, qt * kB, b);
-        tma_load_4d_w(st + C::kTile + a * C::kAtomBytes, &tmDO, &q_full[s], a * 64, h, qt * kB,
-                      b);
+        tma_load_4d_w(st + a * C::kAtomBytes, &tmQ, &q_full[s], a * 64, h,
+                      sg.q_base + qt * kB, sg.b_coord);
+        tma_load_4d_w(st + C::kTile + a * C::kAtomBytes, &tmDO, &q_full[s], a * 64, h,
+                      sg.q_base + qt * kB, sg.b_coord);
       }
       const size_t vrow = (static_cast<size_t>(b) * p.Hq + h) * p.Sqp + static_cast<size_t>(qt) * kB;
       bulk_load_1d_w(st + 2 * C::kTile, p.lse2 + vrow, C::kVec, &q_full[s]);
@@ -414,8 +478,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // this warp's 64 entries of the two row vectors (-LSE2, -D)
       const uint32_t nl2_addr = smem_addr(stage(s) + 2 * C::kTile) + 4 * 64 * wh;
       const uint32_t nd2_addr = nl2_addr + 4 * kB;
-      // column c (query qt*128 + c) is visible to this key row iff c >= cmin
-      const int cmin = p.causal ? k_idx - off - qt * kB : -(1 << 30);
+      // column c (query qt*128 + c) is visible to this key row iff
+      // cmin <= c <= cmax: causal from below, the window from above (not for
+      // sink keys); key rows past the sequence see nothing
+      int cmin = p.causal ? k_idx - off - qt * kB : -(1 << 30);
+      int cmax = (p.window > 0 && k_idx >= p.n_sink) ? k_idx - off + p.window - 1 - qt * kB
+                                                      : (1 << 30);
+      if (k_idx >= sg.Lk) cmin = 1 << 30;
       // P^T of this warp's 64 columns: written to tensor memory for dV and
       // kept in registers (bf16 pairs) for dS^T, because S^T of the next
       // tile replaces it.
@@ -446,10 +515,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pf[2 * e] = ex2_approx(x0);
             pf[2 * e + 1] = ex2_approx(x1);
           }
-          if (cmin > 32 * c4) {
+          if (cmin > 32 * c4 || cmax < 32 * c4 + 31) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (32 * c4 + e < cmin) pf[e] = 0.f;
+              if (32 * c4 + e < cmin || 32 * c4 + e > cmax) pf[e] = 0.f;
           }
           pack32(pf, pkeep + 16 * j);
           tmem_st_x16(taddr + 64 * wh + 16 * j, pkeep + 16 * j);
@@ -497,8 +566,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok && warp_wait(done, 0, abort_flag, p)) {
       tc_fence_after_sync();
-      const bool valid = k_idx < p.Skv;
-      const size_t orow = ((static_cast<size_t>(b) * p.Skv + k_idx) * p.Hkv + hk) * D;
+      const bool valid = k_idx < sg.Lk;
+      const size_t orow = ((static_cast<size_t>(sg.k_row0) + k_idx) * p.Hkv + hk) * D;
       constexpr int kHalfChunks = D / 64;  // 32-column chunks in a column half
 #pragma unroll 1
       for (int g = 0; g < 2; ++g) {  // 0: dV, 1: dK (times scale)
@@ -569,13 +638,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int h = (blockIdx.x / p.B) % p.Hq, b = blockIdx.x % p.B;
   const int hk = h / (p.Hq / p.Hkv);
   const int q0 = qt * kB;
-  const int off = p.Skv - p.Sq;
-  int nkt = (p.Skv + kB - 1) / kB;
+  SeqGeo sg;
+  // A query tile past its sequence's queries has nothing to write.
+  if (!seq_geo(p, b, sg, false) || q0 >= sg.Lq) return;
+  const int off = sg.Lk - sg.Lq;
+  // The key tiles the tile's rows see: the sink tiles, then the window's
+  // tiles from the first key above the first row's window bound up to the
+  // last key any row sees (causal bound, end of the keys).
+  int jhi = (sg.Lk - 1) / kB;
   if (p.causal) {
-    const int qlast = min(q0 + kB - 1, p.Sq - 1);
-    const int kmax = min(p.Skv - 1, qlast + off);  // last key any row of the tile sees
-    nkt = kmax >= 0 ? kmax / kB + 1 : 0;
+    const int qlast = min(q0 + kB - 1, sg.Lq - 1);
+    const int kmax = min(sg.Lk - 1, qlast + off);  // last key any row of the tile sees
+    jhi = kmax >= 0 ? kmax / kB : -1;
   }
+  if (sg.Lk <= 0) jhi = -1;
+  int jlo = 0, sinkT = 0;
+  if (p.window > 0) {
+    const int lo = q0 + off - p.window;  // keys above lo are in the first row's window
+    jlo = lo < 0 ? 0 : (lo + 1) / kB;
+    sinkT = (p.n_sink + kB - 1) / kB;
+  }
+  const int ns = min(sinkT, jhi + 1);
+  const int nkt = jhi < 0 ? 0 : ns + max(0, jhi - max(jlo, sinkT) + 1);
+  // the n-th key tile walked: sink tiles first, then the window's range
+  auto tile_at = [&](int n) { return n < ns ? n : max(jlo, sinkT) + (n - ns); };
 
   if (threadIdx.x == 0) {
     mbar_init(qd_full, 1);
@@ -608,8 +694,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_arrive_expect_tx_w(qd_full, 2 * C::kTile);
 #pragma unroll
     for (int a = 0; a < C::kAtoms; ++a) {
-      tma_load_4d_w(sQ + a * C::kAtomBytes, &tmQ, qd_full, a * 64, h, q0, b);
-      tma_load_4d_w(sDO + a * C::kAtomBytes, &tmDO, qd_full, a * 64, h, q0, b);
+      tma_load_4d_w(sQ + a * C::kAtomBytes, &tmQ, qd_full, a * 64, h, sg.q_base + q0, sg.b_coord);
+      tma_load_4d_w(sDO + a * C::kAtomBytes, &tmDO, qd_full, a * 64, h, sg.q_base + q0,
+                    sg.b_coord);
     }
     int issued = 0;
     for (int t = 0; t < nkt; ++t) {
@@ -619,9 +706,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx_w(&kv_full[s], 2 * C::kTile);
 #pragma unroll
       for (int a = 0; a < C::kAtoms; ++a) {
-        tma_load_4d_w(st + a * C::kAtomBytes, &tmK, &kv_full[s], a * 64, hk, t * kB, b);
-        tma_load_4d_w(st + C::kTile + a * C::kAtomBytes, &tmV, &kv_full[s], a * 64, hk, t * kB,
-                      b);
+        const int kr = sg.k_base + tile_at(t) * kB;
+        tma_load_4d_w(st + a * C::kAtomBytes, &tmK, &kv_full[s], a * 64, hk, kr, sg.b_coord);
+        tma_load_4d_w(st + C::kTile + a * C::kAtomBytes, &tmV, &kv_full[s], a * 64, hk, kr,
+                      sg.b_coord);
       }
       issued = t + 1;
     }
@@ -704,9 +792,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      // column c (key t*128 + c) is visible to this row iff c <= cmax
-      int cmax = p.Skv - 1 - t * kB;
-      if (p.causal) cmax = min(cmax, q_idx + off - t * kB);
+      // column c (key j*128 + c) is visible to this row iff c <= cmax (the
+      // key tail, causal) and, with a window, c > cmin or the key is a sink
+      const int j = tile_at(t);
+      int cmax = sg.Lk - 1 - j * kB;
+      if (p.causal) cmax = min(cmax, q_idx + off - j * kB);
+      const int cmin = p.window > 0 ? q_idx + off - p.window - j * kB : -(1 << 30);
+      const int csink = p.n_sink - j * kB;  // columns below are sink keys
       uint64_t pp[32];  // P in fp32 pairs
       {
         uint32_t ra[64];
@@ -748,10 +840,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 nd2);
             pf2_split(pf2_mul(pp[16 * j + e], g2), pf[2 * e], pf[2 * e + 1]);
           }
-          if (cmax < 32 * c4 + 31) {  // a chunk the diagonal or the key tail crosses
+          if (cmax < 32 * c4 + 31 || (cmin >= 32 * c4 && csink < 32 * c4 + 32)) {
+            // a chunk the diagonal, the key tail or the window's edge crosses
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (32 * c4 + e > cmax) pf[e] = 0.f;
+            for (int e = 0; e < 32; ++e) {
+              const int c = 32 * c4 + e;
+              if (c > cmax || (c <= cmin && c >= csink)) pf[e] = 0.f;
+            }
           }
           pack32(pf, pk);
           tmem_st_x16(taddr + kB + 64 * wh + 16 * j, pk);
@@ -763,8 +858,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok && warp_wait(done, 0, abort_flag, p)) {
       tc_fence_after_sync();
-      const bool valid = q_idx < p.Sq;
-      __nv_bfloat16* dst = p.dq + ((static_cast<size_t>(b) * p.Sq + q_idx) * p.Hq + h) * D;
+      const bool valid = q_idx < sg.Lq;
+      __nv_bfloat16* dst = p.dq + ((static_cast<size_t>(sg.q_row0) + q_idx) * p.Hq + h) * D;
       constexpr int kHalfChunks = D / 64;
 #pragma unroll 1
       for (int c = wh * kHalfChunks; c < (wh + 1) * kHalfChunks; ++c) {
@@ -813,6 +908,12 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t stream) {
   p.dout = static_cast<const __nv_bfloat16*>(a.dout);
   p.o = static_cast<const __nv_bfloat16*>(a.o);
   p.lse = a.lse;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.total_q = a.total_q;
+  p.total_k = a.total_k;
+  p.window = a.window;
+  p.n_sink = a.n_sink;
   p.lse2 = a.ws_lse2;
   p.dvec = a.ws_d;
   p.dq = static_cast<__nv_bfloat16*>(a.dq);

@@ -56,17 +56,20 @@ struct DecodeLaunch {
 
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmDO;  // 4-D maps (d, H, S, B), 64 x 1 x 128 x 1 boxes
-  const void* o;                    // bf16 forward output [B, Sq, Hq, d]
+  const void* o;                    // bf16 forward output [B, Sq, Hq, d] or [total_q, Hq, d]
   const void* dout;                 // bf16 gradient of O, same layout
-  const float* lse;                 // forward LSE [B, Hq, Sq] (natural log)
-  void* dq;                         // bf16 [B, Sq, Hq, d]
-  void* dk;                         // bf16 [B, Skv, Hkv, d]
+  const float* lse;                 // forward LSE [B, Hq, Sq] or [Hq, total_q] (natural log)
+  void* dq;                         // bf16, the layout of q
+  void* dk;                         // bf16 [B, Skv, Hkv, d] or [total_k, Hkv, d]
   void* dv;
   float* ws_lse2;                   // [B, Hq, Sqp] fp32 workspace
   float* ws_d;                      // [B, Hq, Sqp] fp32 workspace
-  int B, Hq, Hkv, Sq, Skv, d;
+  const int* cu_q;                  // packed sequences: [B + 1] offsets, or null (dense)
+  const int* cu_k;
+  int total_q, total_k;             // packed token counts
+  int B, Hq, Hkv, Sq, Skv, d;       // Sq, Skv: the longest sequence when packed
   float scale;
-  int causal;
+  int causal, window, n_sink;
   int* status;
 };
 

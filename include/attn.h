@@ -197,8 +197,9 @@ ATTN_API int attn_fwd_paged(const void* q, const void* k_pages, const void* v_pa
 ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Sq);
 
 /*
- * Backward pass of attn_fwd (dense BSHD, causal or not, GQA; no window,
- * sink keys or logit sink): from q, k, v, the forward's o and lse and the
+ * Backward pass of attn_fwd (dense BSHD, causal or not, GQA; attn_bwd_ex
+ * adds sink keys, the window and packed sequences): from q, k, v, the
+ * forward's o and lse and the
  * gradient dout of o, writes
  *   dq [B, Sq, Hq, d], dk, dv [B, Skv, Hkv, d]   (bf16, device, caller-owned)
  * with dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO, P = exp(scale Q K^T -
@@ -217,6 +218,29 @@ ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o
                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
                       int B, int Hq, int Hkv, int Sq, int Skv, int d, float scale, int causal,
                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward pass of attn_fwd_ex: the gradients of attn_bwd, with the same
+ * masks as the forward (sink keys, sliding window, packed sequences;
+ * "TileLang tutorial, ch.15", sections 3.4, 5.2 and 5.3).
+ *   cu_seqlens_q, cu_seqlens_k: NULL for the dense layout of attn_bwd; else
+ *   int32 [B + 1] offsets of B packed sequences as in attn_fwd_ex, with q, o,
+ *   dout, dq [total_q, Hq, d], k, v, dk, dv [total_k, Hkv, d] and lse
+ *   [Hq, total_q]; max_Sq / max_Skv bound every sequence's lengths (the dense
+ *   sizes when not packed).  A packed sequence with offsets out of range is
+ *   left out and reported as ATTN_ERR_BAD_INPUT (attn_device_status).
+ *   window, n_sink: as in attn_fwd_ex (window > 0 requires causal, n_sink > 0
+ *   requires a window).
+ *   workspace: at least attn_bwd_workspace_size(B, Hq, max_Sq) bytes.
+ *   Keys no query sees get dk = dv = 0; queries that see no key get dq = 0.
+ * Errors as attn_bwd.
+ */
+ATTN_API int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                         const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                         int Hkv, int max_Sq, int max_Skv, int total_q, int total_k, int d,
+                         float scale, int causal, int window, int n_sink, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 /*
  * Bytes of device workspace attn_decode_paged needs for these sizes (split

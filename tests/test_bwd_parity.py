@@ -124,3 +124,89 @@ def test_full_length(ea, causal):
     x = workloads.dense_inputs(113 + int(causal), 1, 4, 4, 2048, 2048, 128, causal)
     errs = _compare(ea, x, 163 + int(causal), f"S=2048 causal={causal}")
     print("bwd rel L2 / max:", errs)
+
+
+# ------------------------------------------------------------------ sink keys, window, packed
+
+WINDOW_CASES = [
+    # (seed, B, Hq, Hkv, Sq, Skv, d, window, n_sink)
+    (121, 1, 2, 2, 700, 700, 128, 200, 1),      # window + one sink key
+    (122, 1, 4, 2, 600, 900, 128, 100, 3),      # Sq < Skv, GQA
+    (123, 1, 2, 2, 1500, 1500, 64, 300, 130),   # sinks spanning two key tiles, d=64
+    (124, 1, 2, 2, 500, 300, 128, 64, 2),       # Sq > Skv: rows with no key
+    (125, 2, 2, 2, 400, 400, 128, 128, 0),      # window alone, tile-aligned
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES, ids=[f"seed{c[0]}" for c in WINDOW_CASES])
+def test_window_and_sink_keys(ea, case):
+    """Causal sliding window with sink keys (attn_bwd_ex) against the oracle."""
+    seed, B, Hq, Hkv, Sq, Skv, d, window, n_sink = case
+    x = workloads.dense_inputs(seed, B, Hq, Hkv, Sq, Skv, d, True, window, n_sink)
+    g = workloads.grad_output(seed + 50, x.q.shape)
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    o, lse = ea.attn_fwd_ex(q, k, v, causal=True, window=window, n_sink=n_sink, scale=x.scale)
+    dq, dk, dv = ea.attn_bwd_ex(q, k, v, o, lse, g.cuda(), causal=True, window=window,
+                                n_sink=n_sink, scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    rq, rk, rv = oracle.attn_bwd(np64(x.q), np64(x.k), np64(x.v), np64(g), x.scale, True, window,
+                                 n_sink)
+    for a, b, n in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        _check(a, b, f"window seed {seed} {n}")
+
+
+VARLEN_CASES = [
+    # (seed, query lengths, key lengths (None: the same), Hq, Hkv, causal, window, n_sink)
+    (131, [300, 1, 129, 700, 256], None, 8, 2, True, 0, 0),
+    (132, [200, 5, 129], [400, 5, 700], 4, 4, True, 0, 0),     # cached prefixes (Sq < Skv)
+    (133, [150, 64, 300], [100, 64, 1], 4, 2, True, 0, 0),     # Sq > Skv: rows with no key
+    (134, [200, 513, 64], [200, 300, 1], 4, 2, False, 0, 0),
+    (135, [900, 333], None, 4, 2, True, 100, 2),               # window + sink keys
+]
+
+
+@pytest.mark.parametrize("case", VARLEN_CASES, ids=[f"seed{c[0]}" for c in VARLEN_CASES])
+def test_varlen(ea, case):
+    """Packed sequences (cu_seqlens) against the oracle, sequence by sequence."""
+    seed, lq, lk, Hq, Hkv, causal, window, n_sink = case
+    x = workloads.varlen_inputs(seed, len(lq), 0, 0, Hq, Hkv, 128, causal, window, n_sink,
+                                lengths=lq, klengths=lk)
+    g = workloads.grad_output(seed + 50, x.q.shape)
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    cq, ck = x.cu_q.cuda(), x.cu_k.cuda()
+    o, lse = ea.attn_fwd_ex(q, k, v, cq, ck, max_seqlen_q=x.max_q, max_seqlen_k=x.max_k,
+                            causal=causal, window=window, n_sink=n_sink, scale=x.scale)
+    dq, dk, dv = ea.attn_bwd_ex(q, k, v, o, lse, g.cuda(), cq, ck, max_seqlen_q=x.max_q,
+                                max_seqlen_k=x.max_k, causal=causal, window=window,
+                                n_sink=n_sink, scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    cu_q, cu_k = x.cu_q.tolist(), x.cu_k.tolist()
+    rq = np.zeros(x.q.shape)
+    rk = np.zeros(x.k.shape)
+    rv = np.zeros(x.v.shape)
+    for s in range(len(lq)):
+        a, e, ka, ke = cu_q[s], cu_q[s + 1], cu_k[s], cu_k[s + 1]
+        sq, sk, sv = oracle.attn_bwd(np64(x.q[None, a:e]), np64(x.k[None, ka:ke]),
+                                     np64(x.v[None, ka:ke]), np64(g[None, a:e]), x.scale,
+                                     causal, window, n_sink)
+        rq[a:e], rk[ka:ke], rv[ka:ke] = sq[0], sk[0], sv[0]
+    for a_, b_, n in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        _check(a_, b_, f"varlen seed {seed} {n}")
+
+
+def test_varlen_matches_dense(ea):
+    """One packed sequence gives the same bits as the dense call."""
+    x = workloads.dense_inputs(136, 1, 4, 2, 500, 500, 128, True)
+    g = workloads.grad_output(186, x.q.shape).cuda()
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    o, lse = ea.attn_fwd(q, k, v, causal=True, scale=x.scale)
+    dense = ea.attn_bwd(q, k, v, o, lse, g, causal=True, scale=x.scale)
+    cu = torch.tensor([0, 500], dtype=torch.int32, device="cuda")
+    packed = ea.attn_bwd_ex(q[0], k[0], v[0], o[0], lse[0].contiguous(), g[0], cu, cu,
+                            max_seqlen_q=500, max_seqlen_k=500, causal=True, scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    for a, b in zip(dense, packed):
+        assert torch.equal(a[0].view(torch.int16), b.view(torch.int16))
