@@ -302,9 +302,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = &abort_s;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  // Blocks go out in index order: key tile outermost, so that under a causal
-  // mask (where key tile 0 has the most query tiles) the longest come first.
-  const int kt = blockIdx.x / (p.B * p.Hkv), hk = (blockIdx.x / p.B) % p.Hkv, b = blockIdx.x % p.B;
+  // Blocks go out in index order.  Under a causal mask the key tile is
+  // outermost, so that the longest (key tile 0 has the most query tiles) come
+  // first; without one every block is the same work and the key tiles of one
+  // (batch, key head) are adjacent, so the blocks running together read the
+  // same query and output-gradient tiles through L2.
+  const int nkt_all = (p.Skv + kB - 1) / kB;
+  int kt, hk, b;
+  if (p.causal) {
+    kt = blockIdx.x / (p.B * p.Hkv);
+    hk = (blockIdx.x / p.B) % p.Hkv;
+    b = blockIdx.x % p.B;
+  } else {
+    kt = blockIdx.x % nkt_all;
+    hk = (blockIdx.x / nkt_all) % p.Hkv;
+    b = blockIdx.x / (nkt_all * p.Hkv);
+  }
   const int G = p.Hq / p.Hkv;
   const int k0 = kt * kB;
   SeqGeo sg;
@@ -632,10 +645,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = &abort_s;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  // Query tile outermost, the last (under a causal mask the longest) first.
+  // Under a causal mask the query tile is outermost, the last (longest)
+  // first; without one the query tiles of one (batch, head) are adjacent, so
+  // the blocks running together read the same key and value tiles.
   const int nqt_all = p.Sqp / kB;
-  const int qt = nqt_all - 1 - static_cast<int>(blockIdx.x / (p.B * p.Hq));
-  const int h = (blockIdx.x / p.B) % p.Hq, b = blockIdx.x % p.B;
+  int qt, h, b;
+  if (p.causal) {
+    qt = nqt_all - 1 - static_cast<int>(blockIdx.x / (p.B * p.Hq));
+    h = (blockIdx.x / p.B) % p.Hq;
+    b = blockIdx.x % p.B;
+  } else {
+    qt = blockIdx.x % nqt_all;
+    h = (blockIdx.x / nqt_all) % p.Hq;
+    b = blockIdx.x / (nqt_all * p.Hq);
+  }
   const int hk = h / (p.Hq / p.Hkv);
   const int q0 = qt * kB;
   SeqGeo sg;
