@@ -61,7 +61,8 @@ def _load():
                                                       i, i, _D, _D]
             lib.oracle_decode_split.argtypes = [_D, _D, _D, _I, _D, _D, i, i, i, i, i, d, i, i]
             lib.oracle_combine.argtypes = [_D, _D, _D, _D, ctypes.c_long, i, i, _D]
-            lib.oracle_attn_bwd.argtypes = [_D, _D, _D, _D, _D, _D, _D, i, i, i, i, i, i, d, i, i, i]
+            lib.oracle_attn_bwd.argtypes = [_D, _D, _D, _D, _D, _D, _D, i, i, i, i, i, i, d, i, i, i,
+                                            _D, _D]
             lib.oracle_num_threads.argtypes = []
             lib.oracle_set_num_threads.argtypes = [i]
             for f in ("oracle_attn_fwd", "oracle_attn_fwd_varlen", "oracle_attn_decode",
@@ -214,17 +215,22 @@ def combine(o_part, lse_part, sink=None):
     return o.reshape(*lead, d), lse.reshape(*lead)
 
 
-def attn_bwd(q, k, v, dout, scale, causal=False, window=0, n_sink=0):
+def attn_bwd(q, k, v, dout, scale, causal=False, window=0, n_sink=0, sink=None):
     """Gradients of the dense forward for output gradient dout [B,Sq,Hq,d];
-    returns (dq [B,Sq,Hq,d], dk [B,Skv,Hkv,d], dv [B,Skv,Hkv,d])."""
+    returns (dq [B,Sq,Hq,d], dk [B,Skv,Hkv,d], dv [B,Skv,Hkv,d]), and with a
+    logit sink per query head (sink [Hq]) also dsink [Hq]."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     B, Sq, Hq, d = q.shape
     _, Skv, Hkv, _ = k.shape
     dq = np.empty_like(q)
     dk = np.empty_like(k)
     dv = np.empty_like(v)
+    sk, psk = _sink(sink, Hq, "attn_bwd")
+    dsink = np.zeros(Hq, np.float64) if sink is not None else None
     rc = _load().oracle_attn_bwd(_pd(q), _pd(k), _pd(v), _pd(dout), _pd(dq), _pd(dk), _pd(dv), B,
                                  Hq, Hkv, Sq, Skv, d, float(scale), int(bool(causal)), int(window),
-                                 int(n_sink))
+                                 int(n_sink), psk, None if dsink is None else _pd(dsink))
     _check(rc, "attn_bwd")
-    return dq, dk, dv
+    if sink is None:
+        return dq, dk, dv
+    return dq, dk, dv, dsink

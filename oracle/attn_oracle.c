@@ -428,15 +428,26 @@ ORACLE_API int oracle_combine(const double *o_part, const double *lse_part, doub
  * Rows that see no key contribute nothing (their dQ is 0).  dK and dV of a
  * key/value head sum over the Hq/Hkv query heads that read it, in ascending
  * head, then row order.  dq [B,Sq,Hq,d], dk/dv [B,Skv,Hkv,d].
+ * sink: NULL, or the logit sink of every query head [Hq]: one more softmax
+ * column with no value row (the forward's reading), so P_ij is normalised
+ * over the keys and the sink; its own gradient is
+ *     dsink_h = sum over rows i of head h of  -P_i,sink D_i
+ * (dS of the sink column, whose dP is 0), summed over the batch in ascending
+ * order into dsink [Hq].
  */
 ORACLE_API int oracle_attn_bwd(const double *q, const double *k, const double *v,
                                const double *dout, double *dq, double *dk, double *dv, int B,
                                int Hq, int Hkv, int Sq, int Skv, int d, double scale, int causal,
-                               int window, int n_sink)
+                               int window, int n_sink, const double *sink, double *dsink)
 {
     if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return 1;
+    if (sink && !dsink) return 1;
     const int groups = Hq / Hkv;
     int bad = 0;
+    /* per (batch, head) sink gradients, summed in ascending batch order below */
+    double *dsink_part = sink ? (double *)calloc((size_t)(B > 0 ? B : 1) * Hq, sizeof(double))
+                              : NULL;
+    if (sink && !dsink_part) return 2;
 #pragma omp parallel
     {
         double *p = (double *)malloc(sizeof(double) * (Skv > 0 ? Skv : 1));
@@ -461,7 +472,8 @@ ORACLE_API int oracle_attn_bwd(const double *q, const double *k, const double *v
                         const double *gi = dout + (((b * Sq + i) * Hq) + h) * d;
                         double *dqi = dq + (((b * Sq + i) * Hq) + h) * d;
                         for (int t = 0; t < d; ++t) dqi[t] = 0.0;
-                        double m = -INFINITY;
+                        const double sg = sink ? sink[h] : -INFINITY;
+                        double m = sg; /* the sink's column takes part in the row maximum */
                         for (long j = 0; j < Skv; ++j) {
                             if (!visible(i, j, Sq, Skv, causal, window, n_sink)) {
                                 p[j] = -INFINITY;
@@ -472,8 +484,8 @@ ORACLE_API int oracle_attn_bwd(const double *q, const double *k, const double *v
                             p[j] = scale * dot;
                             if (p[j] > m) m = p[j];
                         }
-                        if (m == -INFINITY) continue; /* no visible key */
-                        double sum = 0.0;
+                        if (m == -INFINITY) continue; /* no visible key and no sink */
+                        double sum = (sg == -INFINITY) ? 0.0 : exp(sg - m);
                         for (long j = 0; j < Skv; ++j) {
                             p[j] = (p[j] == -INFINITY) ? 0.0 : exp(p[j] - m);
                             sum += p[j];
@@ -495,12 +507,21 @@ ORACLE_API int oracle_attn_bwd(const double *q, const double *k, const double *v
                                 dkb[j * kvs + t] += scale * ds * qi[t];
                             }
                         }
+                        if (sg != -INFINITY) dsink_part[b * Hq + h] -= exp(sg - m) / sum * D;
                     }
                 }
             }
         }
         free(p);
         free(dp);
+    }
+    if (sink) {
+        for (int h = 0; h < Hq; ++h) {
+            double acc = 0.0;
+            for (int b = 0; b < B; ++b) acc += dsink_part[(long)b * Hq + h];
+            dsink[h] = acc;
+        }
+        free(dsink_part);
     }
     return bad ? 2 : 0;
 }
