@@ -24,7 +24,8 @@ from . import _build
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT",
     "ATTN_ERR_BAD_INPUT", "AttnError", "attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink",
-    "attn_fwd_paged", "attn_fwd_strided", "attn_bwd", "attn_bwd_ex", "attn_bwd_workspace_size",
+    "attn_fwd_paged", "attn_fwd_strided", "attn_bwd", "attn_bwd_ex", "attn_bwd_ex_sink",
+    "attn_bwd_workspace_size",
     "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout", "attn_status_string",
     "attn_last_error", "library_path", "lib",
 ]
@@ -62,6 +63,8 @@ def _load() -> ctypes.CDLL:
     L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
     L.attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f,
                               i, i, i, vp, sz, vp]
+    L.attn_bwd_ex_sink.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
+                                   i, f, i, i, i, vp, vp, vp, sz, vp]
     L.attn_decode_workspace_size.argtypes = [i, i, i, i]
     L.attn_decode_workspace_size.restype = sz
     L.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, sz,
@@ -75,7 +78,7 @@ def _load() -> ctypes.CDLL:
     L.attn_last_error.argtypes = []
     L.attn_last_error.restype = ctypes.c_char_p
     for fn in ("attn_fwd", "attn_fwd_ex", "attn_fwd_ex_sink", "attn_fwd_paged", "attn_fwd_strided",
-               "attn_bwd", "attn_bwd_ex",
+               "attn_bwd", "attn_bwd_ex", "attn_bwd_ex_sink",
                "attn_decode_paged",
                "attn_decode_paged_sink", "attn_device_status", "attn_check_wait_timeout"):
         getattr(L, fn).restype = ctypes.c_int
@@ -358,6 +361,32 @@ def attn_bwd_ex(q, k, v, o, lse, dout, cu_seqlens_q=None, cu_seqlens_k=None, dq=
     """Gradients of attn_fwd_ex (sink keys, sliding window, packed sequences).
     With cu_seqlens (int32 CUDA tensors [nseq+1]): q, o, dout [Tq,Hq,d], k/v
     [Tk,Hkv,d], lse [Hq,Tq]; without: the dense layout of attn_bwd."""
+    return _bwd_ex(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, dq, dk, dv, None, None,
+                   max_seqlen_q, max_seqlen_k, causal, window, n_sink, scale, workspace, stream)
+
+
+def attn_bwd_ex_sink(q, k, v, o, lse, dout, sink_logit, cu_seqlens_q=None, cu_seqlens_k=None,
+                     dq=None, dk=None, dv=None, dsink=None, *, max_seqlen_q=None,
+                     max_seqlen_k=None, causal=False, window=0, n_sink=0, scale=None,
+                     workspace=None, stream=None):
+    """Gradients of attn_fwd_ex_sink: (dq, dk, dv, dsink), dsink fp32 [Hq]
+    the gradient of the logit sink.  lse is the forward's (sink included)."""
+    torch = _torch()
+    _need(sink_logit, "sink_logit", torch.float32, q.device)
+    Hq = q.shape[-2]
+    if sink_logit.numel() != Hq:
+        raise ValueError(f"sink_logit must hold Hq={Hq} values")
+    dsink = torch.empty(Hq, dtype=torch.float32, device=q.device) if dsink is None else dsink
+    _need(dsink, "dsink", torch.float32, q.device)
+    if dsink.numel() != Hq:
+        raise ValueError(f"dsink must hold Hq={Hq} values")
+    return _bwd_ex(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, dq, dk, dv,
+                   sink_logit.contiguous(), dsink, max_seqlen_q, max_seqlen_k, causal, window,
+                   n_sink, scale, workspace, stream)
+
+
+def _bwd_ex(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, dq, dk, dv, sink_logit, dsink,
+            max_seqlen_q, max_seqlen_k, causal, window, n_sink, scale, workspace, stream):
     torch = _torch()
     dev = q.device
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
@@ -397,13 +426,16 @@ def attn_bwd_ex(q, k, v, o, lse, dout, cu_seqlens_q=None, cu_seqlens_k=None, dq=
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    rc = lib.attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
-                         _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q) if varlen else None,
-                         _ptr(cu_seqlens_k) if varlen else None, B, Hq, Hkv, sq, sk, Tq, Tk, d,
-                         scale, int(bool(causal)), int(window), int(n_sink), _ptr(workspace),
-                         workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(rc, "attn_bwd_ex")
-    return dq, dk, dv
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+            _ptr(dv), _ptr(cu_seqlens_q) if varlen else None,
+            _ptr(cu_seqlens_k) if varlen else None, B, Hq, Hkv, sq, sk, Tq, Tk, d, scale,
+            int(bool(causal)), int(window), int(n_sink))
+    tail = (_ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if sink_logit is None:
+        _check(lib.attn_bwd_ex(*args, *tail), "attn_bwd_ex")
+        return dq, dk, dv
+    _check(lib.attn_bwd_ex_sink(*args, _ptr(sink_logit), _ptr(dsink), *tail), "attn_bwd_ex_sink")
+    return dq, dk, dv, dsink
 
 
 def attn_decode_workspace_size(B: int, Hq: int, d: int, num_splits: int) -> int:

@@ -425,13 +425,23 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Sq) {
   return bwd_workspace_bytes(B, Hq, Sq);
 }
 
-ATTN_API int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
-                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                         const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
-                         int Hkv, int max_Sq, int max_Skv, int total_q, int total_k, int d,
-                         float scale, int causal, int window, int n_sink, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Every backward entry point.  sink / dsink: the logit sink per query head
+// and its gradient [Hq], or both null.
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+             const int* cu_seqlens_k, int B, int Hq, int Hkv, int max_Sq, int max_Skv,
+             int total_q, int total_k, int d, float scale, int causal, int window, int n_sink,
+             const float* sink, float* dsink, void* workspace, size_t workspace_bytes,
+             void* stream) {
   t_last_error.clear();
+  if ((sink == nullptr) != (dsink == nullptr))
+    return set_error(ATTN_ERR_INVALID_ARG, "sink_logit and dsink go together");
+  if ((reinterpret_cast<uintptr_t>(sink) & 3u) || (reinterpret_cast<uintptr_t>(dsink) & 3u))
+    return set_error(ATTN_ERR_INVALID_ARG, "misaligned sink pointer");
   const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
   if (varlen && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr))
     return set_error(ATTN_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k go together");
@@ -450,18 +460,21 @@ ATTN_API int attn_bwd_ex(const void* q, const void* k, const void* v, const void
     return set_error(ATTN_ERR_INVALID_ARG, "a sliding window requires causal");
   if (n_sink < 0 || (n_sink > 0 && window == 0))
     return set_error(ATTN_ERR_INVALID_ARG, "sink keys require a window");
-  if (B == 0) return ATTN_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const long long rows_q = varlen ? total_q : static_cast<long long>(B) * max_Sq;
-  const long long rows_k = varlen ? total_k : static_cast<long long>(B) * max_Skv;
-  const size_t kv_bytes = static_cast<size_t>(rows_k) * Hkv * d * 2;
-  if (rows_q == 0 || max_Sq == 0) {  // no query: dK = dV = 0
-    if (kv_bytes == 0) return ATTN_OK;
-    if (!dk || !dv) return set_error(ATTN_ERR_INVALID_ARG, "dk and dv must be set");
-    cudaError_t e = cudaMemsetAsync(dk, 0, kv_bytes, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kv_bytes, st);
+  if (B == 0 || max_Sq == 0 || (varlen && total_q == 0)) {
+    // no query: dK = dV = 0 and a zero sink gradient
+    const long long rows_k0 = varlen ? total_k : static_cast<long long>(B) * max_Skv;
+    const size_t kv_bytes0 = static_cast<size_t>(rows_k0) * Hkv * d * 2;
+    cudaError_t e = cudaSuccess;
+    if (kv_bytes0 > 0) {
+      if (!dk || !dv) return set_error(ATTN_ERR_INVALID_ARG, "dk and dv must be set");
+      e = cudaMemsetAsync(dk, 0, kv_bytes0, st);
+      if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kv_bytes0, st);
+    }
+    if (e == cudaSuccess && dsink) e = cudaMemsetAsync(dsink, 0, sizeof(float) * Hq, st);
     return e == cudaSuccess ? ATTN_OK : cuda_error(e, "zeroing dk/dv");
   }
+  const long long rows_k = varlen ? total_k : static_cast<long long>(B) * max_Skv;
   if (!q || !o || !lse || !dout || !dq || !workspace)
     return set_error(ATTN_ERR_INVALID_ARG, "null pointer");
   if (rows_k > 0 && (!k || !v || !dk || !dv))
@@ -489,6 +502,8 @@ ATTN_API int attn_bwd_ex(const void* q, const void* k, const void* v, const void
   a.dv = dv;
   a.cu_q = cu_seqlens_q;
   a.cu_k = cu_seqlens_k;
+  a.sink = sink;
+  a.dsink = dsink;
   a.total_q = varlen ? total_q : 0;
   a.total_k = varlen ? total_k : 0;
   const size_t rows = need / (2 * sizeof(float));
@@ -517,6 +532,34 @@ ATTN_API int attn_bwd_ex(const void* q, const void* k, const void* v, const void
   }
   cudaError_t e = launch_attn_bwd(a, st);
   return e == cudaSuccess ? ATTN_OK : cuda_error(e, "attn_bwd launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+ATTN_API int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                         const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                         int Hkv, int max_Sq, int max_Skv, int total_q, int total_k, int d,
+                         float scale, int causal, int window, int n_sink, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv,
+                  max_Sq, max_Skv, total_q, total_k, d, scale, causal, window, n_sink, nullptr,
+                  nullptr, workspace, workspace_bytes, stream);
+}
+
+ATTN_API int attn_bwd_ex_sink(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                              int Hkv, int max_Sq, int max_Skv, int total_q, int total_k, int d,
+                              float scale, int causal, int window, int n_sink,
+                              const float* sink_logit, float* dsink, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!sink_logit || !dsink) return set_error(ATTN_ERR_INVALID_ARG, "sink_logit and dsink needed");
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv,
+                  max_Sq, max_Skv, total_q, total_k, d, scale, causal, window, n_sink,
+                  sink_logit, dsink, workspace, workspace_bytes, stream);
 }
 
 ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

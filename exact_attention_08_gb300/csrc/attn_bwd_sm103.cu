@@ -253,6 +253,38 @@ __global__ void attn_bwd_rowstat_kernel(BwdParams p) {
   }
 }
 
+// Gradient of the logit sink of query head h (blockIdx.x): with the sink as
+// one more softmax column without a value row, dS of that column is
+// P_sink (0 - D) per row, so dsink_h = -sum_rows exp(sink_h - LSE) D over the
+// rows of the head.  The workspace holds -LSE log2(e) and -D per row (pad
+// rows and rows without a key: -inf, 0).  Each thread sums a fixed set of
+// rows and the block adds the partial sums in a fixed tree, so the result
+// does not depend on scheduling.
+constexpr int kSinkThreads = 256;
+__global__ void __launch_bounds__(kSinkThreads)
+    attn_bwd_dsink_kernel(const float* __restrict__ lse2, const float* __restrict__ dvec,
+                          const float* __restrict__ sink, float* __restrict__ dsink, int B, int Hq,
+                          int Sqp) {
+  __shared__ float part[kSinkThreads];
+  const int h = blockIdx.x;
+  const float s2 = sink[h] * kLog2eB;  // -inf: no sink, a zero gradient
+  float acc = 0.f;
+  const long long rows = static_cast<long long>(B) * Sqp;
+  for (long long r = threadIdx.x; r < rows; r += kSinkThreads) {
+    const long long b = r / Sqp, i = r % Sqp;
+    const size_t w = (static_cast<size_t>(b) * Hq + h) * Sqp + i;
+    const float x = s2 + lse2[w];
+    if (x > -INFINITY) acc = fmaf(exp2f(x), dvec[w], acc);  // P_sink (-D)
+  }
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int n = kSinkThreads / 2; n > 0; n >>= 1) {
+    if (threadIdx.x < n) part[threadIdx.x] += part[threadIdx.x + n];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) dsink[h] = part[0];
+}
+
 // Packs 32 fp32 values into 16 bf16 pairs (element 2e in the low half).
 __device__ __forceinline__ void pack32(const float* f, uint32_t* pk) {
 #pragma unroll
@@ -965,7 +997,13 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t stream) {
   }
   dim3 g2((p.Sqp / kB) * a.Hq * a.B);
   attn_bwd_dq_kernel<D><<<g2, kBwdThreads, C::kLaunchQ, stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO, p);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.sink != nullptr) {
+    attn_bwd_dsink_kernel<<<a.Hq, kSinkThreads, 0, stream>>>(p.lse2, p.dvec, a.sink, a.dsink, a.B,
+                                                             a.Hq, p.Sqp);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace

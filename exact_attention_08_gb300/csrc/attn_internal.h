@@ -66,6 +66,8 @@ struct BwdLaunch {
   float* ws_d;                      // [B, Hq, Sqp] fp32 workspace
   const int* cu_q;                  // packed sequences: [B + 1] offsets, or null (dense)
   const int* cu_k;
+  const float* sink;                // logit sink per query head [Hq], or null
+  float* dsink;                     // its gradient [Hq] (written when sink is set)
   int total_q, total_k;             // packed token counts
   int B, Hq, Hkv, Sq, Skv, d;       // Sq, Skv: the longest sequence when packed
   float scale;

@@ -243,6 +243,28 @@ ATTN_API int attn_bwd_ex(const void* q, const void* k, const void* v, const void
                          size_t workspace_bytes, void* stream);
 
 /*
+ * Backward pass of attn_fwd_ex_sink: attn_bwd_ex's gradients plus that of
+ * the logit sink ("TileLang tutorial, ch.15", section 4.6, the sink as one
+ * more softmax column without a value row).
+ *   lse: the forward's LSE, which includes the sink term; with it the
+ *   dq, dk, dv of attn_bwd_ex are those of the sink-augmented softmax.
+ *   sink_logit: DEVICE fp32 [Hq], the forward's sigma (-inf: none).
+ *   dsink: DEVICE fp32 [Hq] (out): dL/dsigma_h = -sum over the rows of head h
+ *     (every sequence) of P_sink * rowsum(dO * O), P_sink = e^(sigma_h - LSE).
+ *     Each head is summed by one block in a fixed order, so repeated calls
+ *     give identical bits.  No query: dsink = 0.
+ * Both sink pointers must be set (ATTN_ERR_INVALID_ARG otherwise); the other
+ * arguments and errors are those of attn_bwd_ex.
+ */
+ATTN_API int attn_bwd_ex_sink(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                              int Hkv, int max_Sq, int max_Skv, int total_q, int total_k, int d,
+                              float scale, int causal, int window, int n_sink,
+                              const float* sink_logit, float* dsink, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace attn_decode_paged needs for these sizes (split
  * partial outputs and log-sum-exps, fp32).  0 on invalid sizes.
  */

@@ -130,3 +130,20 @@ def test_argument_errors_of_the_newer_entry_points_without_gpu():
     assert L.attn_decode_paged(p16, p16, p16, p16, p16, p16, None, 2, 8, 2, 192, 16, 4, 10, 8, 0.1,
                                p16, 1 << 20, None) == ea.ATTN_ERR_UNSUPPORTED
     assert "192" in ea.attn_last_error()
+
+
+def test_backward_sink_argument_errors_without_gpu():
+    """attn_bwd_ex_sink wants both sink pointers, 4-byte aligned; both checks
+    answer before any CUDA call."""
+    import exact_attention_08_gb300 as ea
+    L = ea.lib
+    buf = ctypes.create_string_buffer(256)
+    p = ctypes.cast(buf, ctypes.c_void_p).value
+    p16 = (p + 15) & ~15
+    args = (p16, p16, p16, p16, p16, p16, p16, p16, p16, None, None, 1, 2, 2, 8, 8, 0, 0, 128,
+            0.1, 0, 0, 0)
+    tail = (p16, 1 << 20, None)
+    assert L.attn_bwd_ex_sink(*args, p16, None, *tail) == ea.ATTN_ERR_INVALID_ARG
+    assert L.attn_bwd_ex_sink(*args, None, p16, *tail) == ea.ATTN_ERR_INVALID_ARG
+    assert L.attn_bwd_ex_sink(*args, p16 + 2, p16, *tail) == ea.ATTN_ERR_INVALID_ARG
+    assert "sink" in ea.attn_last_error()

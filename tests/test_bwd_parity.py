@@ -210,3 +210,122 @@ def test_varlen_matches_dense(ea):
     assert ea.attn_device_status() == ea.ATTN_OK
     for a, b in zip(dense, packed):
         assert torch.equal(a[0].view(torch.int16), b.view(torch.int16))
+
+
+def _dsink_bound(o, lse, g, sink):
+    """Per-head tolerance on the sink gradient, from the arithmetic: the
+    kernel forms D = rowsum(dO * O) from the bf16 O, each element with an
+    independent relative rounding of at most 2^-9, so the error of
+    sum_rows P_sink D has a standard deviation of about
+    2^-9 / sqrt(3) * sqrt(sum_rows P_sink^2 sum_t (dO_t O_t)^2); the bound
+    takes 8 of those (about 14 sigma) plus 1e-3 of sum_rows P_sink |D| for the
+    fp32 LSE that P_sink is rebuilt from (dense [B,Sq,Hq,d] / [B,Hq,Sq] fp64
+    arrays from the oracle)."""
+    p = np.exp(np.asarray(sink, np.float64)[None, :, None] - lse)        # [B, Hq, Sq]
+    p = np.where(np.isfinite(p), p, 0.0)
+    go = (g * o).transpose(0, 2, 1, 3)                                    # [B, Hq, Sq, d]
+    rnd = np.sqrt(np.sum(p ** 2 * np.sum(go ** 2, axis=-1), axis=(0, 2)))
+    lsee = np.sum(p * np.abs(go.sum(axis=-1)), axis=(0, 2))
+    return 8.0 * 2.0 ** -9 * rnd + 1e-3 * lsee + 1e-6
+
+
+def _check_dsink(got, ref, bound, what):
+    got = got.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite"
+    err = np.abs(got - ref)
+    assert np.all(err <= bound), f"{what}: errors {err} above {bound}"
+
+
+SINK_CASES = [
+    # (seed, B, Hq, Hkv, Sq, Skv, d, causal, window, n_sink, extreme sinks)
+    (141, 2, 4, 2, 300, 300, 128, True, 0, 0, True),    # -inf, +100, -30 and a plain sink
+    (142, 1, 4, 4, 400, 700, 64, False, 0, 0, False),   # non-causal, d=64
+    (143, 1, 4, 2, 600, 600, 128, True, 128, 2, False),  # window + sink keys
+    (144, 1, 2, 2, 500, 300, 128, True, 0, 0, False),   # Sq > Skv: rows with no key
+]
+
+
+@pytest.mark.parametrize("case", SINK_CASES, ids=[f"seed{c[0]}" for c in SINK_CASES])
+def test_logit_sink(ea, case):
+    """attn_bwd_ex_sink: dq, dk, dv and the sink's gradient against the
+    oracle's backward with the same logit sink."""
+    seed, B, Hq, Hkv, Sq, Skv, d, causal, window, n_sink, extremes = case
+    x = workloads.dense_inputs(seed, B, Hq, Hkv, Sq, Skv, d, causal, window, n_sink)
+    g = workloads.grad_output(seed + 50, x.q.shape)
+    sink = workloads.logit_sinks(seed + 70, Hq, extremes=extremes)
+    q, k, v, sg = x.q.cuda(), x.k.cuda(), x.v.cuda(), sink.cuda()
+    o, lse = ea.attn_fwd_ex_sink(q, k, v, sg, causal=causal, window=window, n_sink=n_sink,
+                                 scale=x.scale)
+    dq, dk, dv, ds = ea.attn_bwd_ex_sink(q, k, v, o, lse, g.cuda(), sg, causal=causal,
+                                         window=window, n_sink=n_sink, scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    rq, rk, rv, rs = oracle.attn_bwd(np64(x.q), np64(x.k), np64(x.v), np64(g), x.scale, causal,
+                                     window, n_sink, sink=sink.double().numpy())
+    for a, b, n in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        _check(a, b, f"sink seed {seed} {n}")
+    ro, rl = oracle.attn_fwd(np64(x.q), np64(x.k), np64(x.v), x.scale, causal, window, n_sink,
+                             sink=sink.double().numpy())
+    _check_dsink(ds, rs, _dsink_bound(ro, rl, np64(g), sink.numpy()), f"sink seed {seed} dsink")
+    if extremes:
+        assert ds[0].item() == 0.0  # sigma = -inf: no sink, no gradient
+    # a fixed summation order: the same bits again
+    again = ea.attn_bwd_ex_sink(q, k, v, o, lse, g.cuda(), sg, causal=causal, window=window,
+                                n_sink=n_sink, scale=x.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(again[3], ds)
+    assert torch.equal(again[0].view(torch.int16), dq.view(torch.int16))
+
+
+def test_logit_sink_varlen(ea):
+    """Packed sequences with a logit sink: the sink's gradient sums every
+    sequence's rows of the head."""
+    lq, lk = [300, 1, 129, 500], [300, 40, 129, 200]
+    Hq, Hkv = 4, 2
+    x = workloads.varlen_inputs(145, len(lq), 0, 0, Hq, Hkv, 128, True, lengths=lq, klengths=lk)
+    g = workloads.grad_output(195, x.q.shape)
+    sink = workloads.logit_sinks(215, Hq)
+    q, k, v, sg = x.q.cuda(), x.k.cuda(), x.v.cuda(), sink.cuda()
+    cq, ck = x.cu_q.cuda(), x.cu_k.cuda()
+    o, lse = ea.attn_fwd_ex_sink(q, k, v, sg, cq, ck, max_seqlen_q=x.max_q, max_seqlen_k=x.max_k,
+                                 causal=True, scale=x.scale)
+    dq, dk, dv, ds = ea.attn_bwd_ex_sink(q, k, v, o, lse, g.cuda(), sg, cq, ck,
+                                         max_seqlen_q=x.max_q, max_seqlen_k=x.max_k, causal=True,
+                                         scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    cu_q, cu_k = x.cu_q.tolist(), x.cu_k.tolist()
+    rq, rk, rv = np.zeros(x.q.shape), np.zeros(x.k.shape), np.zeros(x.v.shape)
+    rs = np.zeros(Hq)
+    os_, ls_, gs_ = [], [], []
+    sk = sink.double().numpy()
+    for s in range(len(lq)):
+        a, e, ka, ke = cu_q[s], cu_q[s + 1], cu_k[s], cu_k[s + 1]
+        qs, ks, vs, gs = (np64(x.q[None, a:e]), np64(x.k[None, ka:ke]), np64(x.v[None, ka:ke]),
+                          np64(g[None, a:e]))
+        sq, skk, sv, sds = oracle.attn_bwd(qs, ks, vs, gs, x.scale, True, sink=sk)
+        rq[a:e], rk[ka:ke], rv[ka:ke] = sq[0], skk[0], sv[0]
+        rs += sds
+        ro, rl = oracle.attn_fwd(qs, ks, vs, x.scale, True, sink=sk)
+        os_.append(ro[0])
+        ls_.append(rl[0])
+        gs_.append(gs[0])
+    for a_, b_, n in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        _check(a_, b_, f"varlen sink {n}")
+    # the packed rows as one batch row: [1, Tq, Hq, d] and [1, Hq, Tq]
+    bound = _dsink_bound(np.concatenate(os_)[None], np.concatenate(ls_, axis=1)[None],
+                         np.concatenate(gs_)[None], sk)
+    _check_dsink(ds, rs, bound, "varlen sink dsink")
+
+
+def test_logit_sink_without_queries(ea):
+    """No query row: dk = dv = 0 and a zero sink gradient."""
+    q = torch.zeros(1, 0, 2, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.randn(1, 5, 2, 128, device="cuda").to(torch.bfloat16)
+    lse = torch.zeros(1, 2, 0, device="cuda")
+    sg = torch.tensor([1.0, 2.0], device="cuda")
+    ds = torch.full((2,), 7.0, device="cuda")
+    dq, dk, dv, ds = ea.attn_bwd_ex_sink(q, k, k, q, lse, q, sg, dsink=ds, causal=True)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
+    assert torch.count_nonzero(ds) == 0
