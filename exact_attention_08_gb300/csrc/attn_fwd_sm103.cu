@@ -75,7 +75,11 @@ constexpr int kRegsSplit = 2 * 128 * kRegsSoftmax + 128 * kRegsOther;
 static_assert(kRegsSplit <= kThreads * 168, "register split");
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
-constexpr int kWarpTable = 10;  // builds the dense item order of packed calls, then idles
+constexpr int kWarpTable = 10;  // builds the dense item order of packed calls, then locates items
+// Item records in flight between the locating warp and the roles, and the
+// arrivals that free one: the producer and MMA warps, the eight softmax warps.
+constexpr int kRecSlots = 4;
+constexpr int kRecReaders = 10;
 constexpr int kPrefetch = 2;  // key/value tiles warmed in L2 ahead of their load
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -94,8 +98,8 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   // q_full[3], q_empty[3], k_full[S], v_full[S], step[S], s_full[2], p_half[2], p_ready[2],
-  // o_done[2], drain
-  static constexpr int kNumBars = 2 * kQSlots + 3 * kStages + 4 * kQT + 1;
+  // o_done[2], drain, rec_full[R], rec_empty[R]
+  static constexpr int kNumBars = 2 * kQSlots + 3 * kStages + 4 * kQT + 1 + 2 * kRecSlots;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static constexpr uint32_t kTmemCols = 512;
@@ -130,6 +134,7 @@ __device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
 struct Params {
   __nv_bfloat16* o;
   long long o_sb, o_ss, o_sh;  // O strides (elements): batch, row, head; d contiguous
+  int o_v8;                    // every O row starts on 32 bytes: 32-byte stores
   float* lse;
   const float* sink;  // logit sink per query head [Hq], or null
   const int* cu_q;
@@ -348,7 +353,7 @@ struct ItemTable {
 };
 
 // The query rows of packed sequence b, or -1 when its offsets are invalid
-// (the same checks as decode_work).
+// (the same checks as locate_item).
 template <bool kPagedKV>
 __device__ __forceinline__ int packed_rows(const Params& p, int b) {
   const int a = p.cu_q[b], e = p.cu_q[b + 1];
@@ -408,15 +413,23 @@ __device__ __forceinline__ void build_item_table(const Params& p, ItemTable& t, 
 // causal masking the work of a pair grows with its index: the longest pairs
 // of every head come first (for packed calls through the dense table when
 // there is one).  Heads of one KV group are adjacent either way.
-// Returns false when the item has no query rows or its sequence offsets are
-// invalid (reported once, by the caller that passes report).
+//
+// An item's record: what locating it takes the item table or global memory
+// for (the sequence offsets); work_of derives the rest.  live = 0 marks the
+// end of a CTA's items.
+struct ItemRec {
+  int bseq, h, q0, Lq, Lk, q_base, k_base, live;
+};
+
+// Locates item k.  Returns false when it has no query rows or its sequence
+// offsets are invalid (reported when report is set).
 template <bool kPagedKV, bool kTable>
-__device__ __forceinline__ bool decode_work(const Params& p, const ItemTable& tab, int k,
-                                            int sinkT, Work& w, bool report) {
+__device__ __forceinline__ bool locate_item(const Params& p, const ItemTable& tab, int k,
+                                            ItemRec& r, bool report) {
   int qp;
   if (kTable) {
     const int sl = fdiv(k, p.div_hq);
-    w.h = k - sl * p.Hq;
+    r.h = k - sl * p.Hq;
     int lo = 0, hi = p.num_qpairs;  // the level l with lev_start[l] <= sl < lev_start[l + 1]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -426,53 +439,64 @@ __device__ __forceinline__ bool decode_work(const Params& p, const ItemTable& ta
         hi = mid;
     }
     qp = p.num_qpairs - 1 - lo;
-    w.bseq = tab.order[sl - tab.lev_start[lo]];
+    r.bseq = tab.order[sl - tab.lev_start[lo]];
   } else if (p.causal) {
     const int x = fdiv(k, p.div_hq), y = fdiv(x, p.div_b);
-    w.h = k - x * p.Hq;
-    w.bseq = x - y * p.B;
+    r.h = k - x * p.Hq;
+    r.bseq = x - y * p.B;
     qp = p.num_qpairs - 1 - y;
   } else {
     const int x = fdiv(k, p.div_qp), y = fdiv(x, p.div_hq);
     qp = k - x * p.num_qpairs;
-    w.h = x - y * p.Hq;
-    w.bseq = y;
+    r.h = x - y * p.Hq;
+    r.bseq = y;
   }
   if (kPagedKV) {
     // Packed queries against a paged cache: the sequence's keys are its
     // first seqlens_k[b] cache slots, reached through its page-table row.
-    const int a = p.cu_q[w.bseq], e = p.cu_q[w.bseq + 1];
-    const int lk = p.seqlens_k[w.bseq];
+    const int a = p.cu_q[r.bseq], e = p.cu_q[r.bseq + 1];
+    const int lk = p.seqlens_k[r.bseq];
     if (a < 0 || e < a || e > p.total_q || e - a > p.Sq || lk < 0 || lk > p.max_pages * kPage) {
       if (report) atomicOr(p.status, kStatusBadInput);
       return false;
     }
-    w.Lq = e - a;
-    w.Lk = lk;
-    w.q_base = a;
-    w.k_base = 0;
-    w.b_coord = 0;
+    r.Lq = e - a;
+    r.Lk = lk;
+    r.q_base = a;
+    r.k_base = 0;
   } else if (p.cu_q != nullptr) {
-    const int a = p.cu_q[w.bseq], e = p.cu_q[w.bseq + 1];
-    const int ka = p.cu_k[w.bseq], ke = p.cu_k[w.bseq + 1];
+    const int a = p.cu_q[r.bseq], e = p.cu_q[r.bseq + 1];
+    const int ka = p.cu_k[r.bseq], ke = p.cu_k[r.bseq + 1];
     if (a < 0 || e < a || e > p.total_q || ka < 0 || ke < ka || e - a > p.Sq) {
       if (report) atomicOr(p.status, kStatusBadInput);
       return false;
     }
-    w.Lq = e - a;
-    w.Lk = ke - ka;
-    w.q_base = a;
-    w.k_base = ka;
-    w.b_coord = 0;
+    r.Lq = e - a;
+    r.Lk = ke - ka;
+    r.q_base = a;
+    r.k_base = ka;
   } else {
-    w.Lq = p.Sq;
-    w.Lk = p.Skv;
-    w.q_base = 0;
-    w.k_base = 0;
-    w.b_coord = w.bseq;
+    r.Lq = p.Sq;
+    r.Lk = p.Skv;
+    r.q_base = 0;
+    r.k_base = 0;
   }
-  w.q0 = qp * (kQT * kBM);
-  if (w.q0 >= w.Lq) return false;
+  r.q0 = qp * (kQT * kBM);
+  r.live = 1;
+  return r.q0 < r.Lq;
+}
+
+// Coordinates, masks and active key-tile ranges of a located item.
+template <bool kPagedKV>
+__device__ __forceinline__ void work_of(const Params& p, const ItemRec& r, Work& w) {
+  w.bseq = r.bseq;
+  w.h = r.h;
+  w.q0 = r.q0;
+  w.Lq = r.Lq;
+  w.Lk = r.Lk;
+  w.q_base = r.q_base;
+  w.k_base = r.k_base;
+  w.b_coord = (kPagedKV || p.cu_q != nullptr) ? 0 : r.bseq;
   w.off = w.Lk - w.Lq;
   w.hk = fdiv(w.h, p.div_group);
   w.m0 = make_mask(w.q0, w.Lq, w.Lk, w.off, p.causal, p.window);
@@ -480,8 +504,6 @@ __device__ __forceinline__ bool decode_work(const Params& p, const ItemTable& ta
   w.r0 = tile_range(w.m0, w.Lk, p.window);
   w.r1 = tile_range(w.m1, w.Lk, p.window);
   w.lastT = max(w.r0.hi, w.r1.hi);  // last key tile any row touches (-1: none)
-  (void)sinkT;
-  return true;
 }
 
 // Number of active key tiles of a range.
@@ -523,10 +545,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_ready = p_half + kQT;  // [2]: all of P_i written
   uint64_t* o_done = p_ready + kQT;
   uint64_t* drain = o_done + kQT;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* rec_full = drain + 1;              // [kRecSlots]: item record written
+  uint64_t* rec_empty = rec_full + kRecSlots;  // [kRecSlots]: every role is done with it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rec_empty + kRecSlots);
   __shared__ int abort_flag_s;
   volatile int* abort_flag = &abort_flag_s;
   __shared__ ItemTable tab;
+  __shared__ ItemRec recs[kRecSlots];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int sinkT = (p.window > 0 && p.n_sink > 0) ? (p.n_sink + kBN - 1) / kBN : 0;
@@ -550,6 +575,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_done[i], 1);
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < kRecSlots; ++s) {
+      mbar_init(&rec_full[s], 1);
+      mbar_init(&rec_empty[s], kRecReaders);
+    }
     fence_mbar_init();
   }
   if (warp == kWarpLoad) {
@@ -562,10 +591,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const int num_items = kTable ? tab.total : p.num_items;
+  // Record c of this CTA's item sequence, for a whole warp (false when the
+  // wait gave up); the caller frees it with release_item once it is done.
+  auto take_item = [&](int c, ItemRec& r) -> bool {
+    if (!mbar_wait_warp(&rec_full[c % kRecSlots], (c / kRecSlots) & 1, abort_flag,
+                        p.wait_limit_ns))
+      return false;
+    r = recs[c % kRecSlots];
+    return true;
+  };
+  auto release_item = [&](int c) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rec_empty[c % kRecSlots]);
+  };
 
-  // The CTA is persistent: every role walks the same item sequence
-  // (item_of), skipping the same items, and its ring, barrier-phase and
-  // step counters carry over from one item to the next.
+  // The CTA is persistent: one warp locates its items (item_of, then the
+  // table or the sequence offsets) ahead of the others and hands them over
+  // as records in a ring of kRecSlots; every role takes the same records in
+  // the same order, and its ring, barrier-phase and step counters carry over
+  // from one item to the next.
   //
   // Q tiles.  The g-th Q tile this CTA loads (two per item with key tiles,
   // tile 0 then tile 1) goes to slot g % 3; the slot is refilled once every
@@ -652,25 +696,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       }
     };
-    for (int n = 0; ok; ++n) {
-      const int k = item_of(n, num_items);
-      if (k < 0) break;
+    for (int c = 0; ok; ++c) {
       Work w;
-      if (!decode_work<kPagedKV, kTable>(p, tab, k, sinkT, w, lane == 0) || w.lastT < 0) continue;
+      {
+        ItemRec r;
+        if (!take_item(c, r)) {
+          ok = false;
+          break;
+        }
+        if (!r.live) break;
+        work_of<kPagedKV>(p, r, w);
+        release_item(c);
+      }
+      if (w.lastT < 0) continue;
       if (!load_q(w, 0)) {
         ok = false;
         break;
       }
-      // Warm L2 with the next item's Q tiles.
-      {
-        const int k2 = item_of(n + 1, num_items);
-        Work w2;
-        if (k2 >= 0 && decode_work<kPagedKV, kTable>(p, tab, k2, sinkT, w2, false) && w2.lastT >= 0) {
+      // Warm L2 with the next item's Q tiles, if its record is out already.
+      if (__all_sync(0xffffffffu, mbar_test(&rec_full[(c + 1) % kRecSlots],
+                                            ((c + 1) / kRecSlots) & 1))) {
+        const ItemRec r2 = recs[(c + 1) % kRecSlots];
+        if (r2.live) {
+          const int bc = (kPagedKV || p.cu_q != nullptr) ? 0 : r2.bseq;
 #pragma unroll
           for (int i = 0; i < kQT; ++i)
 #pragma unroll
             for (int a = 0; a < C::kAtoms; ++a)
-              tma_prefetch_4d_w(&tmQ, a * 64, w2.h, w2.q_base + w2.q0 + i * kBM, w2.b_coord);
+              tma_prefetch_4d_w(&tmQ, a * 64, r2.h, r2.q_base + r2.q0 + i * kBM, bc);
         }
       }
       bool q1 = false;  // Q tile 1 loaded (after the item's first K tile)
@@ -783,11 +836,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_ss_k64_w(tS, dq, dk, idesc_s);
       mma_commit_w(&s_full[i]);
     };
-    for (int n = 0; ok; ++n) {
-      const int k = item_of(n, num_items);
-      if (k < 0) break;
+    for (int c = 0; ok; ++c) {
       Work w;
-      if (!decode_work<kPagedKV, kTable>(p, tab, k, sinkT, w, false) || w.lastT < 0) continue;
+      {
+        ItemRec r;
+        if (!take_item(c, r)) {
+          ok = false;
+          break;
+        }
+        if (!r.live) break;
+        work_of<kPagedKV>(p, r, w);
+        release_item(c);
+      }
+      if (w.lastT < 0) continue;
       const int qs0 = g % kQSlots, qs1 = (g + 1) % kQSlots;
       const uint32_t qp0 = (g / kQSlots) & 1, qp1 = ((g + 1) / kQSlots) & 1;
       g += kQT;
@@ -905,6 +966,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) fail(p.status, abort_flag);
     __syncwarp();
+  } else if (warp == kWarpTable) {
+    // ============================================================ item locator
+    // Walks this CTA's items ahead of the other roles: one record per item
+    // with query rows (items with invalid sequence offsets are reported here
+    // and left out), then one with live = 0.  A slot is rewritten once all
+    // kRecReaders warps have freed it, so the locator runs up to kRecSlots
+    // items ahead of the slowest role and its table search and offset loads
+    // stay off their item changes.
+    bool ok = true;
+    int c = 0;
+    for (int n = 0; ok; ++n) {
+      const int k = item_of(n, num_items);
+      ItemRec r = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (k >= 0 && !locate_item<kPagedKV, kTable>(p, tab, k, r, lane == 0)) continue;
+      const int rs = c % kRecSlots;
+      if (c >= kRecSlots &&
+          !mbar_wait_warp(&rec_empty[rs], ((c / kRecSlots) - 1) & 1, abort_flag, p.wait_limit_ns)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        recs[rs] = r;
+        mbar_arrive(&rec_full[rs]);
+      }
+      __syncwarp();
+      ++c;
+      if (k < 0) break;
+    }
+    if (!ok && lane == 0) fail(p.status, abort_flag);
+    __syncwarp();
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax) : "memory");
@@ -919,17 +1010,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     int t = 0;     // key tiles processed (s_full / p_ready phases)
     int no = 0;    // o_done phases consumed
     bool ok = true;
-    for (int n = 0; ok; ++n) {
-      const int k = item_of(n, num_items);
-      if (k < 0) break;
+    for (int c = 0; ok; ++c) {
       // Only what the key loop needs stays live through it; the epilogue
-      // decodes the item again.
+      // reads the item's record again (this warp frees it after that).
       TileMask m;
       TileRange rg;
       int hi_row, lo_row;
       {
+        ItemRec rec;
+        if (!take_item(c, rec)) {
+          if (lane == 0) fail(p.status, abort_flag);
+          ok = false;
+          break;
+        }
+        if (!rec.live) break;
         Work w;
-        if (!decode_work<kPagedKV, kTable>(p, tab, k, sinkT, w, false)) continue;
+        work_of<kPagedKV>(p, rec, w);
         const int row = w.q0 + i * kBM + r;  // sequence-relative query index
         hi_row = p.causal ? min(row + w.off, w.Lk - 1) : w.Lk - 1;
         lo_row = (p.window > 0) ? row + w.off - p.window : kNoLowerBound;
@@ -1133,7 +1229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // branch below is uniform over the warp, and the tensor-memory loads
       // (warp-collective) are made by every lane whatever its row.
       Work w;
-      decode_work<kPagedKV, kTable>(p, tab, k, sinkT, w, false);
+      work_of<kPagedKV>(p, recs[c % kRecSlots], w);
       const int row = w.q0 + i * kBM + r;
       const bool valid = row < w.Lq;
       const bool have_o = t_item > 0;
@@ -1173,19 +1269,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             static_cast<long long>(w.q_base + row) * p.o_ss + static_cast<long long>(w.h) * p.o_sh);
         // 32 columns at a time, the next chunk's load in flight while one is
         // scaled, packed and stored.
+        // Each thread stores its own row, so one store instruction touches
+        // 32 rows; 32-byte stores halve the instructions (and the requests
+        // the L1 processes) against 16-byte ones.
         auto store32 = [&](const uint32_t* o, int c) {
+          uint32_t wv[16];
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint32_t wv[4];
+          for (int e = 0; e < 16; ++e) {
+            float a0, a1;
+            f2_split(f2_mul(f2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2), a0,
+                     a1);
+            wv[e] = seen ? pack_bf16x2(a0, a1) : 0u;
+          }
+          if (valid) {
+            if (p.o_v8) {
+              st_global_v8(dst + c * 4, wv);
+              st_global_v8(dst + c * 4 + 2, wv + 8);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int idx = v4 * 8 + 2 * e;
-              float a0, a1;
-              f2_split(f2_mul(f2(__uint_as_float(o[idx]), __uint_as_float(o[idx + 1])), inv2), a0,
-                       a1);
-              wv[e] = seen ? pack_bf16x2(a0, a1) : 0u;
+              for (int v4 = 0; v4 < 4; ++v4)
+                dst[c * 4 + v4] = make_uint4(wv[4 * v4], wv[4 * v4 + 1], wv[4 * v4 + 2], wv[4 * v4 + 3]);
             }
-            if (valid) dst[c * 4 + v4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         };
         uint32_t oa[32], ob[32];
@@ -1217,6 +1321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The next item's first product into O must wait until O has been read:
       // it waits for this warpgroup's next p_half arrival, made after this.
       tc_fence_before_sync();
+      release_item(c);
     }
   }
 
@@ -1266,9 +1371,11 @@ __global__ void attn_fill_empty_kernel(__nv_bfloat16* o, size_t o_elems, float* 
 template <int D>
 cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   using C = Cfg<D>;
-  // dynamic shared memory plus the static table and flags of the table
-  // instantiations within the 227 KB a block may have
-  static_assert(C::kSmemBytes + sizeof(ItemTable) + 64 <= 227 * 1024, "shared memory");
+  // dynamic shared memory plus the static table, item records and flags
+  // within the 227 KB a block may have
+  static_assert(C::kSmemBytes + sizeof(ItemTable) + kRecSlots * sizeof(ItemRec) + 64 <=
+                    227 * 1024,
+                "shared memory");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -1292,6 +1399,8 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   p.o_sb = a.o_sb;
   p.o_ss = a.o_ss;
   p.o_sh = a.o_sh;
+  p.o_v8 = (reinterpret_cast<uintptr_t>(a.o) % 32 == 0) && a.o_sb % 16 == 0 && a.o_ss % 16 == 0 &&
+           a.o_sh % 16 == 0;
   p.lse = a.lse;
   p.sink = a.sink;
   p.cu_q = a.cu_q;

@@ -131,11 +131,31 @@ __device__ __forceinline__ uint32_t mbar_test3(uint64_t* a, uint32_t pa, uint64_
   return ra | rb | rc;
 }
 
+// Non-blocking test of one barrier phase.
+__device__ __forceinline__ uint32_t mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P1;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, P1;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok;
+}
+
 // Warp-collective form of mbar_wait: every lane of a converged warp calls it
 // and all get the same answer (false if any lane gave up).
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
                                                const volatile int* abort_flag, uint64_t limit_ns) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, limit_ns));
+}
+
+// 32-byte global store (sm_100 and later); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 // ---------------------------------------------------------------- TMA
