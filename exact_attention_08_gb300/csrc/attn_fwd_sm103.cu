@@ -414,18 +414,17 @@ __device__ __forceinline__ void build_item_table(const Params& p, ItemTable& t, 
 // of every head come first (for packed calls through the dense table when
 // there is one).  Heads of one KV group are adjacent either way.
 //
-// An item's record: what locating it takes the item table or global memory
-// for (the sequence offsets); work_of derives the rest.  live = 0 marks the
-// end of a CTA's items.
-struct ItemRec {
-  int bseq, h, q0, Lq, Lk, q_base, k_base, live;
+// What locating an item takes the item table or global memory (the
+// sequence offsets) for; work_of derives the rest.
+struct ItemLoc {
+  int bseq, h, q0, Lq, Lk, q_base, k_base;
 };
 
 // Locates item k.  Returns false when it has no query rows or its sequence
 // offsets are invalid (reported when report is set).
 template <bool kPagedKV, bool kTable>
 __device__ __forceinline__ bool locate_item(const Params& p, const ItemTable& tab, int k,
-                                            ItemRec& r, bool report) {
+                                            ItemLoc& r, bool report) {
   int qp;
   if (kTable) {
     const int sl = fdiv(k, p.div_hq);
@@ -482,13 +481,12 @@ __device__ __forceinline__ bool locate_item(const Params& p, const ItemTable& ta
     r.k_base = 0;
   }
   r.q0 = qp * (kQT * kBM);
-  r.live = 1;
   return r.q0 < r.Lq;
 }
 
 // Coordinates, masks and active key-tile ranges of a located item.
 template <bool kPagedKV>
-__device__ __forceinline__ void work_of(const Params& p, const ItemRec& r, Work& w) {
+__device__ __forceinline__ void work_of(const Params& p, const ItemLoc& r, Work& w) {
   w.bseq = r.bseq;
   w.h = r.h;
   w.q0 = r.q0;
@@ -511,6 +509,15 @@ __device__ __forceinline__ int range_count(const TileRange& r, int sinkT) {
   if (r.hi < 0) return 0;
   return min(sinkT, r.hi + 1) + max(0, r.hi - max(r.lo, sinkT) + 1);
 }
+
+// An item as the locating warp hands it to the other roles: its decoding
+// and the active key-tile counts of its two Q tiles.  live = 0 marks the end
+// of a CTA's items.
+struct ItemRec {
+  Work w;
+  int count0, count1;
+  int live;
+};
 
 // The n-th item of this CTA: items are dealt out in bands of gridDim.x, every
 // other band in reverse CTA order, so that with the longest items first the
@@ -591,14 +598,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const int num_items = kTable ? tab.total : p.num_items;
-  // Record c of this CTA's item sequence, for a whole warp (false when the
-  // wait gave up); the caller frees it with release_item once it is done.
-  auto take_item = [&](int c, ItemRec& r) -> bool {
-    if (!mbar_wait_warp(&rec_full[c % kRecSlots], (c / kRecSlots) & 1, abort_flag,
-                        p.wait_limit_ns))
-      return false;
-    r = recs[c % kRecSlots];
-    return true;
+  // Waits, for a whole warp, until record c of this CTA's item sequence is
+  // out (false when the wait gave up); the caller reads recs[c % kRecSlots]
+  // and frees it with release_item once it is done.
+  auto take_item = [&](int c) -> bool {
+    return mbar_wait_warp(&rec_full[c % kRecSlots], (c / kRecSlots) & 1, abort_flag,
+                          p.wait_limit_ns);
   };
   auto release_item = [&](int c) {
     __syncwarp();
@@ -699,13 +704,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; ok; ++c) {
       Work w;
       {
-        ItemRec r;
-        if (!take_item(c, r)) {
+        if (!take_item(c)) {
           ok = false;
           break;
         }
+        const ItemRec& r = recs[c % kRecSlots];
         if (!r.live) break;
-        work_of<kPagedKV>(p, r, w);
+        w = r.w;
         release_item(c);
       }
       if (w.lastT < 0) continue;
@@ -716,14 +721,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Warm L2 with the next item's Q tiles, if its record is out already.
       if (__all_sync(0xffffffffu, mbar_test(&rec_full[(c + 1) % kRecSlots],
                                             ((c + 1) / kRecSlots) & 1))) {
-        const ItemRec r2 = recs[(c + 1) % kRecSlots];
-        if (r2.live) {
-          const int bc = (kPagedKV || p.cu_q != nullptr) ? 0 : r2.bseq;
+        const ItemRec& r2 = recs[(c + 1) % kRecSlots];
+        if (r2.live && r2.w.lastT >= 0) {
 #pragma unroll
           for (int i = 0; i < kQT; ++i)
 #pragma unroll
             for (int a = 0; a < C::kAtoms; ++a)
-              tma_prefetch_4d_w(&tmQ, a * 64, r2.h, r2.q_base + r2.q0 + i * kBM, bc);
+              tma_prefetch_4d_w(&tmQ, a * 64, r2.w.h, r2.w.q_base + r2.w.q0 + i * kBM,
+                                r2.w.b_coord);
         }
       }
       bool q1 = false;  // Q tile 1 loaded (after the item's first K tile)
@@ -838,21 +843,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int c = 0; ok; ++c) {
       Work w;
+      int count0, count1;
       {
-        ItemRec r;
-        if (!take_item(c, r)) {
+        if (!take_item(c)) {
           ok = false;
           break;
         }
+        const ItemRec& r = recs[c % kRecSlots];
         if (!r.live) break;
-        work_of<kPagedKV>(p, r, w);
+        w = r.w;
+        count0 = r.count0;
+        count1 = r.count1;
         release_item(c);
       }
       if (w.lastT < 0) continue;
       const int qs0 = g % kQSlots, qs1 = (g + 1) % kQSlots;
       const uint32_t qp0 = (g / kQSlots) & 1, qp1 = ((g + 1) / kQSlots) & 1;
       g += kQT;
-      const int count0 = range_count(w.r0, sinkT), count1 = range_count(w.r1, sinkT);
       int left0 = count0, left1 = count1;
       for (int j = next_in_pair(w.r0, w.r1, 0, sinkT); j <= w.lastT;
            j = next_in_pair(w.r0, w.r1, j + 1, sinkT)) {
@@ -978,8 +985,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int c = 0;
     for (int n = 0; ok; ++n) {
       const int k = item_of(n, num_items);
-      ItemRec r = {0, 0, 0, 0, 0, 0, 0, 0};
-      if (k >= 0 && !locate_item<kPagedKV, kTable>(p, tab, k, r, lane == 0)) continue;
+      ItemLoc loc = {0, 0, 0, 0, 0, 0, 0};
+      if (k >= 0 && !locate_item<kPagedKV, kTable>(p, tab, k, loc, lane == 0)) continue;
+      ItemRec r;
+      work_of<kPagedKV>(p, loc, r.w);
+      r.count0 = range_count(r.w.r0, sinkT);
+      r.count1 = range_count(r.w.r1, sinkT);
+      r.live = k >= 0;
       const int rs = c % kRecSlots;
       if (c >= kRecSlots &&
           !mbar_wait_warp(&rec_empty[rs], ((c / kRecSlots) - 1) & 1, abort_flag, p.wait_limit_ns)) {
@@ -1017,15 +1029,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileRange rg;
       int hi_row, lo_row;
       {
-        ItemRec rec;
-        if (!take_item(c, rec)) {
+        if (!take_item(c)) {
           if (lane == 0) fail(p.status, abort_flag);
           ok = false;
           break;
         }
+        const ItemRec& rec = recs[c % kRecSlots];
         if (!rec.live) break;
-        Work w;
-        work_of<kPagedKV>(p, rec, w);
+        const Work& w = rec.w;
         const int row = w.q0 + i * kBM + r;  // sequence-relative query index
         hi_row = p.causal ? min(row + w.off, w.Lk - 1) : w.Lk - 1;
         lo_row = (p.window > 0) ? row + w.off - p.window : kNoLowerBound;
@@ -1228,8 +1239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (each thread its own row, 16-byte stores), then the row's LSE.  Every
       // branch below is uniform over the warp, and the tensor-memory loads
       // (warp-collective) are made by every lane whatever its row.
-      Work w;
-      work_of<kPagedKV>(p, recs[c % kRecSlots], w);
+      const Work& w = recs[c % kRecSlots].w;
       const int row = w.q0 + i * kBM + r;
       const bool valid = row < w.Lq;
       const bool have_o = t_item > 0;
