@@ -209,6 +209,7 @@ __device__ __forceinline__ void bwd_fail(int* status, volatile int* abort_flag) 
 // O_t (fp32) and LSE2 = LSE log2(e), both stored negated (the kernels add
 // them); rows past Sq (to the tile boundary) and rows whose LSE is -inf (no
 // key) get -LSE2 = -inf and D = 0, so every P built from them is 0.
+template <int D>
 __global__ void attn_bwd_rowstat_kernel(BwdParams p) {
   const int lane = threadIdx.x % 32, sub = lane / 8, l8 = lane % 8;
   const long long nrow = static_cast<long long>(p.B) * p.Hq * p.Sqp;
@@ -226,11 +227,23 @@ __global__ void attn_bwd_rowstat_kernel(BwdParams p) {
       SeqGeo g;
       row_ok = seq_geo(p, b, g, i == 0 && h == 0 && l8 == 0) && i < g.Lq;
       if (row_ok) {
-        const size_t base = ((static_cast<size_t>(g.q_row0) + i) * p.Hq + h) * p.d;
-        for (int t = l8 * 8; t < p.d; t += 64) {  // eight bf16 (16 bytes) per lane
-          const uint4 g = *reinterpret_cast<const uint4*>(p.dout + base + t);
-          const uint4 o = *reinterpret_cast<const uint4*>(p.o + base + t);
-          const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, ow[4] = {o.x, o.y, o.z, o.w};
+        const size_t base = ((static_cast<size_t>(g.q_row0) + i) * p.Hq + h) * D;
+        const float l = p.cu_q != nullptr
+                            ? p.lse[static_cast<size_t>(h) * p.total_q + g.q_row0 + i]
+                            : p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Sq + i];
+        // eight bf16 (16 bytes) per lane and load, every load of the row in
+        // flight before the first product
+        constexpr int kLd = D / 64;
+        uint4 gv[kLd], ov[kLd];
+#pragma unroll
+        for (int c = 0; c < kLd; ++c) {
+          gv[c] = *reinterpret_cast<const uint4*>(p.dout + base + l8 * 8 + c * 64);
+          ov[c] = *reinterpret_cast<const uint4*>(p.o + base + l8 * 8 + c * 64);
+        }
+#pragma unroll
+        for (int c = 0; c < kLd; ++c) {
+          const uint32_t gw[4] = {gv[c].x, gv[c].y, gv[c].z, gv[c].w};
+          const uint32_t ow[4] = {ov[c].x, ov[c].y, ov[c].z, ov[c].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             acc = fmaf(__uint_as_float(gw[e] << 16), __uint_as_float(ow[e] << 16), acc);
@@ -238,9 +251,6 @@ __global__ void attn_bwd_rowstat_kernel(BwdParams p) {
                        __uint_as_float(ow[e] & 0xffff0000u), acc);
           }
         }
-        const float l = p.cu_q != nullptr
-                            ? p.lse[static_cast<size_t>(h) * p.total_q + g.q_row0 + i]
-                            : p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Sq + i];
         l2 = (l == -INFINITY) ? INFINITY : l * kLog2eB;
       }
     }
@@ -986,7 +996,7 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t stream) {
   p.causal = a.causal;
   p.wait_limit_ns = kWaitLimitNs;
   p.status = a.status;
-  attn_bwd_rowstat_kernel<<<1216, 256, 0, stream>>>(p);
+  attn_bwd_rowstat_kernel<D><<<1216, 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.Skv > 0) {

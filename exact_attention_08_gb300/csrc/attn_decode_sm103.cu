@@ -596,6 +596,9 @@ __global__ void __launch_bounds__(D)
     attn_decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
                                __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                                int num_splits, const float* __restrict__ sink, int Hq) {
+  // Launched as a programmatic dependent of the split kernel: its launch
+  // overlaps the split's tail, and this waits for the split's results.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const size_t row = blockIdx.x;  // b * Hq + h
   const float* ls = ws_lse + row * num_splits;
   // A logit sink joins the merge as one more denominator term with no output
@@ -617,6 +620,26 @@ __global__ void __launch_bounds__(D)
   }
   o[row * D + t] = __float2bfloat16(acc / wsum);
   if (lse && t == 0) lse[row] = M + logf(wsum);
+}
+
+// The merge, launched so that it may start while the split kernel drains
+// (programmatic stream serialization; the kernel's griddepcontrol.wait
+// keeps its reads after the split's writes).
+template <int D>
+cudaError_t launch_combine(const DecodeLaunch& a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B * a.Hq);
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_decode_combine_kernel<D>,
+                            static_cast<const float*>(a.ws_o), static_cast<const float*>(a.ws_lse),
+                            static_cast<__nv_bfloat16*>(a.o), a.lse, a.num_splits, a.sink, a.Hq);
 }
 
 template <int D>
@@ -651,9 +674,8 @@ cudaError_t launch_dec(const DecodeLaunch& a, cudaStream_t stream) {
   attn_decode_split_kernel<D><<<grid, kDecThreads, C::kSmemBytes, stream>>>(a.tmK, a.tmV, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_decode_combine_kernel<D><<<a.B * a.Hq, D, 0, stream>>>(
-      a.ws_o, a.ws_lse, static_cast<__nv_bfloat16*>(a.o), a.lse, a.num_splits, a.sink, a.Hq);
-  return cudaGetLastError();
+  e = launch_combine<D>(a, stream);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 
@@ -688,9 +710,8 @@ cudaError_t launch_dec256(const DecodeLaunch& a, cudaStream_t stream) {
   attn_decode_split256_kernel<<<grid, kDecThreads, C::kSmemBytes, stream>>>(a.tmK, a.tmV, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_decode_combine_kernel<256><<<a.B * a.Hq, 256, 0, stream>>>(
-      a.ws_o, a.ws_lse, static_cast<__nv_bfloat16*>(a.o), a.lse, a.num_splits, a.sink, a.Hq);
-  return cudaGetLastError();
+  e = launch_combine<256>(a, stream);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -200,6 +200,47 @@ def test_varlen_many_sequences(ea, nseq, lo, hi, seed):
     compare(o, lse, ro, rl, f"varlen {nseq} sequences")
 
 
+def test_varlen_long_sequence(ea):
+    """A packed causal call whose longest sequence has more than 64 query
+    pairs (the sparse item order), beside short ones: sampled rows of the
+    long sequence, every row of the others."""
+    lq = [17000, 300, 1]
+    x = workloads.varlen_inputs(46, len(lq), 0, 0, 2, 1, 128, causal=True, lengths=lq)
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    o, lse = ea.attn_fwd_ex(q, k, v, x.cu_q.cuda(), x.cu_k.cuda(), max_seqlen_q=x.max_q,
+                            max_seqlen_k=x.max_k, causal=True, scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    cu = x.cu_q.tolist()
+    for s_, rows in ((0, sample_rows(lq[0], seed=46)), (1, None), (2, None)):
+        a, e = cu[s_], cu[s_ + 1]
+        ro, rl = oracle.attn_fwd(np64(x.q[None, a:e]), np64(x.k[None, a:e]),
+                                 np64(x.v[None, a:e]), x.scale, True, rows=rows)
+        idx = torch.as_tensor(a + (np.arange(e - a) if rows is None else np.asarray(rows)),
+                              device=o.device)
+        compare(o[None, idx], lse[None, :, idx], ro, rl, f"varlen long, sequence {s_}")
+
+
+def test_varlen_sequences_without_keys(ea):
+    """Causal packed sequences with no keys at all between ones with keys
+    (items with query rows and no key tile, in the dense item order): O = 0
+    and LSE = -inf there, the others as the oracle."""
+    lq, lk = [200, 300, 150, 90], [0, 300, 0, 120]
+    x = workloads.varlen_inputs(47, len(lq), 0, 0, 4, 2, 128, causal=True, lengths=lq,
+                                klengths=lk)
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    o, lse = ea.attn_fwd_ex(q, k, v, x.cu_q.cuda(), x.cu_k.cuda(), max_seqlen_q=x.max_q,
+                            max_seqlen_k=x.max_k, causal=True, scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    ro, rl = oracle.attn_fwd_varlen(np64(x.q), np64(x.k), np64(x.v), x.cu_q.numpy(),
+                                    x.cu_k.numpy(), x.scale, True)
+    compare(o, lse, ro, rl, "varlen, sequences without keys")
+    masked = np.isneginf(rl).T
+    assert masked[:200].all() and masked[500:650].all()
+    assert_masked_rows_zero(o, masked, "varlen, sequences without keys")
+
+
 def test_varlen_bad_offsets_reported(ea):
     """A sequence whose offsets run backwards is reported as ATTN_ERR_BAD_INPUT
     and left out; a sequence before it is computed as usual."""
