@@ -13,6 +13,12 @@
 //   shared memory  Q (4 atoms of 128 rows x 64 columns, 64 KB), K (4 atoms),
 //                  V (4 atoms), barriers: 192 KB + 1 KB
 //
+// The grid is persistent: one CTA per SM walks its share of the Q tiles
+// (items dealt in bands of gridDim.x, every other band in reverse order),
+// and every role's barrier phases run on over the CTA's whole sequence of
+// key tiles.  Q, like K, is released atom by atom after the last S of an
+// item, so the next item's Q and K stream in while that S still runs.
+//
 // Warps: 0-3 softmax (thread r owns query row q0 + r, lanes of its quarter of
 // tensor memory), 4 TMA producer, 5 MMA issuer.  Per key tile n the issuer
 // runs S(n+1) = Q K(n+1)^T into the other S buffer, then O += P(n) V(n) as soon
@@ -33,6 +39,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -53,9 +60,9 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kNAtom * kAtom;
 constexpr int kOffV = 2 * kNAtom * kAtom;
 constexpr int kOffBar = 3 * kNAtom * kAtom;
-// q_full, k_full[4], k_empty[4], v_full, v_empty, s_full[2], p_ready[2],
-// o_done[2], drain, and the tensor-memory address slot
-constexpr int kNumBars = 1 + kNAtom + kNAtom + 1 + 1 + 2 + 2 + 2 + 1;
+// q_full[4], q_empty[4], k_full[4], k_empty[4], v_full, v_empty, s_full[2],
+// p_ready[2], o_done[2], drain, and the tensor-memory address slot
+constexpr int kNumBars = 4 * kNAtom + 1 + 1 + 2 + 2 + 2 + 1;
 constexpr int kSmem = kOffBar + (kNumBars + 1) * 8 + 1024;
 static_assert(kSmem <= 227 * 1024, "shared memory");
 constexpr uint32_t kColO = 2 * kR;
@@ -77,7 +84,8 @@ struct P256 {
   const int* seqlens_k;   // paged keys: key count of every sequence [B]
   int max_pages, num_pages;
   long long o_sb, o_ss, o_sh;  // O strides (elements): batch, row, head
-  int B, Hq, Hkv, Sq, Skv, total_q, num_qt;
+  int o_v8;                    // every O row starts on 32 bytes: 32-byte stores
+  int B, Hq, Hkv, Sq, Skv, total_q, num_qt, num_items;
   float scale, scale2;
   int causal, window, n_sink;
   uint64_t wait_limit_ns;
@@ -93,13 +101,13 @@ struct Tile {
   int jlo, jhi, sinkT, n_act;
 };
 
-// CTA order: without a causal mask the Q tiles of one (sequence, head) are
+// Item order: without a causal mask the Q tiles of one (sequence, head) are
 // adjacent so that they read the same K and V through L2; with one, the
 // last (longest) Q tiles of every head come first.
 template <bool kPaged>
-__device__ __forceinline__ bool decode_tile(const P256& p, Tile& w, bool report) {
+__device__ __forceinline__ bool decode_tile(const P256& p, int item, Tile& w, bool report) {
   const int per = p.Hq * p.B;
-  int x = static_cast<int>(blockIdx.x), qt;
+  int x = item, qt;
   if (p.causal) {
     qt = p.num_qt - 1 - x / per;
     x %= per;
@@ -174,6 +182,15 @@ __device__ __forceinline__ bool decode_tile(const P256& p, Tile& w, bool report)
   return true;
 }
 
+// The n-th item of this CTA, or -1 past the last: bands of gridDim.x items,
+// every other band dealt in reverse CTA order.
+__device__ __forceinline__ int item_at(int n, int num_items) {
+  const int G = gridDim.x;
+  const int pos = (n & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const long long k = static_cast<long long>(n) * G + pos;
+  return k < num_items ? static_cast<int>(k) : -1;
+}
+
 // The n-th active key tile (sink tiles first, then the window's range).
 __device__ __forceinline__ int tile_at(const Tile& w, int n) {
   const int ns = min(w.sinkT, w.jhi + 1);
@@ -219,8 +236,9 @@ __global__ void __launch_bounds__(kThr, 1)
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;               // [4] K atom a of the current key tile landed
+  uint64_t* q_full = bars;                   // [4] Q atom a of the current item landed
+  uint64_t* q_empty = q_full + kNAtom;       // [4] the item's last S has read Q atom a
+  uint64_t* k_full = q_empty + kNAtom;       // [4] K atom a of the current key tile landed
   uint64_t* k_empty = k_full + kNAtom;       // [4] S has read K atom a
   uint64_t* v_full = k_empty + kNAtom;       // V tile landed
   uint64_t* v_empty = v_full + 1;            // O += P V has read V
@@ -233,13 +251,10 @@ __global__ void __launch_bounds__(kThr, 1)
   volatile int* abort_flag = &abort_s;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  Tile w;
-  if (!decode_tile<kPaged>(p, w, threadIdx.x == 0)) return;  // uniform over the CTA
-  const int N = w.n_act;
-
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
     for (int a = 0; a < kNAtom; ++a) {
+      mbar_init(&q_full[a], 1);
+      mbar_init(&q_empty[a], 1);
       mbar_init(&k_full[a], 1);
       mbar_init(&k_empty[a], 1);
     }
@@ -263,15 +278,21 @@ __global__ void __launch_bounds__(kThr, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // Counters over the CTA's whole sequence: key tiles (one S, one P V each)
+  // and items with key tiles (one Q load each).  Items without a visible key
+  // (n_act = 0) only have an epilogue.
   if (warp == kWarpProducer) {
     // ============================================================ TMA producer
     int k_cnt[kNAtom] = {0, 0, 0, 0};  // loads issued into each K atom
     int v_loads = 0;                   // V tiles whose loads were issued
-    if (N > 0) {
-      mbar_arrive_expect_tx_w(q_full, kNAtom * kAtom);
-#pragma unroll
-      for (int a = 0; a < kNAtom; ++a)
-        tma_load_4d_w(sQ + a * kAtom, &tmQ, q_full, a * 64, w.h, w.q_base + w.q0, w.b_coord);
+    int q_loads = 0;                   // items whose Q was loaded
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      const int item = item_at(it, p.num_items);
+      if (item < 0) break;
+      Tile w;
+      if (!decode_tile<kPaged>(p, item, w, lane == 0) || w.n_act == 0) continue;
+      const int N = w.n_act;
       // Paged cache: the physical page of rows 16 pp.. of key tile j, for
       // lane pp (pages past the sequence's last are replaced by that last
       // page, whose rows are masked; an index outside the pool is reported
@@ -302,24 +323,41 @@ __global__ void __launch_bounds__(kThr, 1)
           tma_load_4d_w(dst, map, bar, a * 64, w.hk, w.k_base + j * kR, w.b_coord);
         }
       };
+      // Key tile n of the item; for n = 0 the item's Q atoms go first, each
+      // once the previous item's last S has read it.
       auto load_k = [&](int n) {
         const int j = tile_at(w, n);
         const int phys = kPaged ? page_of(j) : 0;
         for (int a = 0; a < kNAtom; ++a) {
-          // atom a is free once S(n - 1) has read it
-          if (n > 0 && !wwait(&k_empty[a], (n - 1) & 1, abort_flag, p)) return false;
+          if (n == 0) {
+            if (q_loads > 0 && !wwait(&q_empty[a], (q_loads - 1) & 1, abort_flag, p))
+              return false;
+            mbar_arrive_expect_tx_w(&q_full[a], kAtom);
+            tma_load_4d_w(sQ + a * kAtom, &tmQ, &q_full[a], a * 64, w.h, w.q_base + w.q0,
+                          w.b_coord);
+          }
+          // atom a is free once the S before has read it
+          if (k_cnt[a] > 0 && !wwait(&k_empty[a], (k_cnt[a] - 1) & 1, abort_flag, p))
+            return false;
           mbar_arrive_expect_tx_w(&k_full[a], kAtom);
           load_atom(&tmK, sK + a * kAtom, &k_full[a], a, j, phys);
           ++k_cnt[a];
         }
+        if (n == 0) ++q_loads;
         return true;
       };
-      bool ok = load_k(0);
+      ok = load_k(0);
       for (int n = 0; ok && n < N; ++n) {
         // K runs one key tile ahead of V: K(n + 1) as S(n) releases its atoms,
-        // V(n) once O += P(n - 1) V(n - 1) has read V(n - 1).
-        if (n + 1 < N && !load_k(n + 1)) break;
-        if (n > 0 && !wwait(v_empty, (n - 1) & 1, abort_flag, p)) break;
+        // V(n) once the P V before has read the V before.
+        if (n + 1 < N && !load_k(n + 1)) {
+          ok = false;
+          break;
+        }
+        if (v_loads > 0 && !wwait(v_empty, (v_loads - 1) & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
         const int j = tile_at(w, n);
         const int phys = kPaged ? page_of(j) : 0;
         mbar_arrive_expect_tx_w(v_full, kNAtom * kAtom);
@@ -327,14 +365,15 @@ __global__ void __launch_bounds__(kThr, 1)
         for (int a = 0; a < kNAtom; ++a) load_atom(&tmV, sV + a * kAtom, v_full, a, j, phys);
         ++v_loads;
       }
-      // Every copy issued lands before the CTA can leave (a load is issued
-      // only after the previous one into the same buffer has been consumed,
-      // so waiting for the last phase of each barrier covers them all).
-      mbar_wait(q_full, 0, nullptr, p.wait_limit_ns);
-      for (int a = 0; a < kNAtom; ++a)
-        if (k_cnt[a] > 0) mbar_wait(&k_full[a], (k_cnt[a] - 1) & 1, nullptr, p.wait_limit_ns);
-      if (v_loads > 0) mbar_wait(v_full, (v_loads - 1) & 1, nullptr, p.wait_limit_ns);
     }
+    // Every copy issued lands before the CTA can leave (a load is issued
+    // only after the previous one into the same buffer has been consumed,
+    // so waiting for the last phase of each barrier covers them all).
+    for (int a = 0; a < kNAtom; ++a) {
+      if (q_loads > 0) mbar_wait(&q_full[a], (q_loads - 1) & 1, nullptr, p.wait_limit_ns);
+      if (k_cnt[a] > 0) mbar_wait(&k_full[a], (k_cnt[a] - 1) & 1, nullptr, p.wait_limit_ns);
+    }
+    if (v_loads > 0) mbar_wait(v_full, (v_loads - 1) & 1, nullptr, p.wait_limit_ns);
   } else if (warp == kWarpIssuer) {
     // ============================================================ MMA issuer
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, kR, false);
@@ -342,13 +381,19 @@ __global__ void __launch_bounds__(kThr, 1)
     const uint64_t dq = sdesc_sw128(smem_addr(sQ), 16, 1024);
     const uint64_t dk = sdesc_sw128(smem_addr(sK), 16, 1024);
     const uint64_t dv = sdesc_sw128(smem_addr(sV), kAtom, 1024);
-    // S(n) = Q K(n)^T into buffer n % 2: K-steps 4a .. 4a+3 read atom a of Q
-    // and K; atom a of K is released as soon as its four steps are done.
-    auto issue_s = [&](int n) -> bool {
-      const uint32_t tS = tmem + (n & 1) * kR;
+    int g = 0;   // key tiles of earlier items
+    int qi = 0;  // items with key tiles before this one
+    // S of key tile g + n = Q K^T into buffer (g + n) % 2: K-steps 4a .. 4a+3
+    // read atom a of Q and K; atom a of K is released as soon as its four
+    // steps are done, and after the item's last S atom a of Q too.
+    auto issue_s = [&](int n, bool last) -> bool {
+      const int t = g + n;
+      const uint32_t tS = tmem + (t & 1) * kR;
 #pragma unroll 1
       for (int a = 0; a < kNAtom; ++a) {
-        if (!wwait(&k_full[a], n & 1, abort_flag, p)) return false;
+        if ((n == 0 && !wwait(&q_full[a], qi & 1, abort_flag, p)) ||
+            !wwait(&k_full[a], t & 1, abort_flag, p))
+          return false;
         tc_fence_after_sync();
 #pragma unroll
         for (int s4 = 0; s4 < 4; ++s4) {
@@ -356,202 +401,232 @@ __global__ void __launch_bounds__(kThr, 1)
           mma_bf16_ss_w(tS, dq + ko, dk + ko, idesc_s, (a > 0 || s4 > 0) ? 1u : 0u);
         }
         mma_commit_w(&k_empty[a]);
+        if (last) mma_commit_w(&q_empty[a]);
       }
-      mma_commit_w(&s_full[n & 1]);
+      mma_commit_w(&s_full[t & 1]);
       return true;
     };
-    bool ok = N > 0 && wwait(q_full, 0, abort_flag, p);
-    if (ok) {
-      tc_fence_after_sync();
-      ok = issue_s(0);
-    }
-    for (int n = 0; ok && n < N; ++n) {
-      if (n + 1 < N && !issue_s(n + 1)) break;
-      // O += P(n) V(n): A = P(n) (bf16 pairs, key-step kk at column 8 kk of
-      // S(n)'s buffer), B = V read along d (N = 256, one product per step).
-      if (!wwait(&p_ready[n & 1], (n >> 1) & 1, abort_flag, p) ||
-          !wwait(v_full, n & 1, abort_flag, p))
-        break;
-      tc_fence_after_sync();
-      const uint32_t tP = tmem + (n & 1) * kR;
-#pragma unroll
-      for (int kk = 0; kk < kR / 16; ++kk)
-        mma_bf16_ts_w(tmem + kColO, tP + 8 * kk, dv + kk * (2048 >> 4), idesc_o,
-                      (n > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_w(v_empty);
-      mma_commit_w(&o_done[n & 1]);
-    }
-    // Every product issued has completed before tensor memory is released.
-    mma_commit_w(drain);
-    mbar_wait(drain, 0, nullptr, p.wait_limit_ns);
-  } else {
-    // ============================================================ softmax warps 0-3
-    const int r = warp * 32 + lane;
-    const int q = w.q0 + r;  // sequence-relative query row
-    const bool valid = q < w.Lq;
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int hi = p.causal ? min(q + w.off, w.Lk - 1) : w.Lk - 1;
-    const int lo = p.window > 0 ? q + w.off - p.window : kNoLowerBound;
-    float m_run = -INFINITY;   // running maximum of the raw scores
-    float m_used = -INFINITY;  // maximum the exponentials are taken against
-    float l = 0.f;             // sum of the exponentials (against m_used)
-    // O is formed from bf16-rounded P while l sums the fp32 values; when one
-    // key dominates a row that rounding error does not cancel, so the
-    // difference p - bf16(p) of every tile's largest p is taken out of the
-    // normaliser of O (not of the log-sum-exp).
-    float corr = 0.f;
     bool ok = true;
-    for (int n = 0; n < N; ++n) {
-      const int j = tile_at(w, n);
-      if (!wwait(&s_full[n & 1], (n >> 1) & 1, abort_flag, p)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const uint32_t tS = taddr + (n & 1) * kR;
-      uint32_t s[kR];
-#pragma unroll
-      for (int c = 0; c < kR / 32; ++c) tmem_ld_x32(tS + 32 * c, s + 32 * c);
-      tmem_wait_ld256();
-#pragma unroll
-      for (int e = 0; e < kR; ++e) reg_fence256(s[e]);
-      if (!interior(w, j, p.window, p.n_sink)) {
-        // key k = j*128 + c is visible iff k <= hi and (k > lo or k < n_sink)
-        const int ka = j * kR;
-#pragma unroll
-        for (int c = 0; c < kR; ++c) {
-          const int k = ka + c;
-          if (!(k <= hi && (k > lo || k < p.n_sink))) s[c] = __float_as_uint(-INFINITY);
+    for (int it = 0; ok; ++it) {
+      const int item = item_at(it, p.num_items);
+      if (item < 0) break;
+      Tile w;
+      if (!decode_tile<kPaged>(p, item, w, false) || w.n_act == 0) continue;
+      const int N = w.n_act;
+      ok = issue_s(0, N == 1);
+      for (int n = 0; ok && n < N; ++n) {
+        if (n + 1 < N && !issue_s(n + 1, n + 2 == N)) {
+          ok = false;
+          break;
         }
-      }
-      float mx8[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) mx8[t] = __uint_as_float(s[t]);
-#pragma unroll
-      for (int c = 8; c < kR; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
-      const float tmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      m_run = fmaxf(m_run, tmax);
-      // Lazy rescale: move the reference maximum only when the scores have
-      // outgrown it by 2^8; O (already holding earlier tiles) is then scaled
-      // by 2^((m_used - m_run) scale2) once O += P V of the previous tile is
-      // done.  The tensor-memory accesses are warp-collective: a warp rescales
-      // if any of its rows must (the others multiply by 1).
-      const bool first = (m_used == -INFINITY);
-      const bool grow = first ? (m_run != -INFINITY) : ((m_run - m_used) * p.scale2 > kRescaleLog2);
-      const bool resc = grow && !first;
-      if (__any_sync(0xffffffffu, resc)) {
-        if (!wwait(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort_flag, p)) {
+        // O += P V of key tile t: A = P (bf16 pairs, key-step kk at column
+        // 8 kk of S(t)'s buffer), B = V read along d (N = 256, one product
+        // per step).  The item's first overwrites O: the epilogue before it
+        // has read O out before the p_ready arrival waited for here.
+        const int t = g + n;
+        if (!wwait(&p_ready[t & 1], (t >> 1) & 1, abort_flag, p) ||
+            !wwait(v_full, t & 1, abort_flag, p)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const float alpha = resc ? ex2_approx((m_used - m_run) * p.scale2) : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < kD / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld_x32(taddr + kColO + 32 * c, o);
-          tmem_wait_ld256();
+        const uint32_t tP = tmem + (t & 1) * kR;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st_x32(taddr + kColO + 32 * c, o);
-        }
-        tmem_st_wait();
-        l *= alpha;
-        corr *= alpha;
+        for (int kk = 0; kk < kR / 16; ++kk)
+          mma_bf16_ts_w(tmem + kColO, tP + 8 * kk, dv + kk * (2048 >> 4), idesc_o,
+                        (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_w(v_empty);
+        mma_commit_w(&o_done[t & 1]);
       }
-      if (grow) m_used = m_run;
-      // P = 2^(S scale2 - m_used scale2) as bf16 pairs over the first 64
-      // columns of the buffer (key-step kk of O += P V at column 8 kk); a row
-      // that has seen no key yet has m_used = -inf and every P = 0.
-      const float nms = first && !grow ? 0.f : -m_used * p.scale2;
-      float sum0 = 0.f, sum1 = 0.f;
-      uint32_t pk[kR / 2];
-#pragma unroll
-      for (int e = 0; e < kR / 2; ++e) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * e]), p.scale2, nms));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * e + 1]), p.scale2, nms));
-        if (e & 1)
-          sum1 += p0 + p1;
-        else
-          sum0 += p0 + p1;
-        pk[e] = pack_bf16x2(p0, p1);
-      }
-      l += sum0 + sum1;
-      {  // the tile's largest p, with the arithmetic used for it above
-        const float ptop = ex2_approx(fmaf(tmax, p.scale2, nms));
-        corr += ptop - __uint_as_float(pack_bf16x2(0.f, ptop) & 0xffff0000u);
-      }
-      tmem_st_x32(tS, pk);
-      tmem_st_x32(tS + 32, pk + 32);
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&p_ready[n & 1]);
+      g += N;
+      ++qi;
     }
-    // ---------------------------------------------------------------- epilogue
-    if (ok) {
-      const bool have_o = N > 0;
-      if (have_o) {
-        if (!wwait(&o_done[(N - 1) & 1], ((N - 1) >> 1) & 1, abort_flag, p))
+    // Every product issued has completed before tensor memory is released.
+    mma_commit_w(drain);
+    mbar_wait(drain, 0, nullptr, p.wait_limit_ns);
+  } else if (warp < 4) {
+    // ============================================================ softmax warps 0-3
+    const int r = warp * 32 + lane;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    int g = 0;  // key tiles of earlier items
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      const int item = item_at(it, p.num_items);
+      if (item < 0) break;
+      Tile w;
+      if (!decode_tile<kPaged>(p, item, w, false)) continue;
+      const int N = w.n_act;
+      const int q = w.q0 + r;  // sequence-relative query row
+      const bool valid = q < w.Lq;
+      const int hi = p.causal ? min(q + w.off, w.Lk - 1) : w.Lk - 1;
+      const int lo = p.window > 0 ? q + w.off - p.window : kNoLowerBound;
+      float m_run = -INFINITY;   // running maximum of the raw scores
+      float m_used = -INFINITY;  // maximum the exponentials are taken against
+      float l = 0.f;             // sum of the exponentials (against m_used)
+      // O is formed from bf16-rounded P while l sums the fp32 values; when one
+      // key dominates a row that rounding error does not cancel, so the
+      // difference p - bf16(p) of every tile's largest p is taken out of the
+      // normaliser of O (not of the log-sum-exp).
+      float corr = 0.f;
+      for (int n = 0; n < N; ++n) {
+        const int j = tile_at(w, n);
+        const int t = g + n;
+        if (!wwait(&s_full[t & 1], (t >> 1) & 1, abort_flag, p)) {
           ok = false;
-        else
-          tc_fence_after_sync();
-      }
-      if (ok) {
-        // O / l, or with a logit sink sigma of this head one more term of
-        // the denominator taken against m* = max(sigma, m scale) ("TileLang
-        // tutorial, ch.15", section 4.6); a row that saw no key gets O = 0.
-        const bool seen = have_o && l > 0.f;
-        const float sg = p.sink ? p.sink[w.h] : -INFINITY;
-        float inv, lse_row;
-        if (sg == -INFINITY) {
-          inv = seen ? 1.f / (l - corr) : 0.f;
-          lse_row = seen ? fmaf(m_used, p.scale, logf(l)) : -INFINITY;
-        } else {
-          const float am = seen ? m_used * p.scale : -INFINITY;
-          const float mst = fmaxf(am, sg);
-          const float e1 = seen ? expf(am - mst) : 0.f;
-          const float e2 = expf(sg - mst);
-          inv = e1 / fmaf(l - corr, e1, e2);
-          lse_row = mst + logf(fmaf(l, e1, e2));
+          break;
         }
-        const size_t orow =
-            (p.cu_q ? static_cast<size_t>(w.q_base + q) * p.o_ss
-                    : static_cast<size_t>(w.bseq) * p.o_sb + static_cast<size_t>(q) * p.o_ss) +
-            static_cast<size_t>(w.h) * p.o_sh;
-#pragma unroll 1
-        for (int c = 0; c < kD / 32; ++c) {
-          uint32_t o[32];
+        tc_fence_after_sync();
+        const uint32_t tS = taddr + (t & 1) * kR;
+        uint32_t s[kR];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-          if (have_o) {
+        for (int c = 0; c < kR / 32; ++c) tmem_ld_x32(tS + 32 * c, s + 32 * c);
+        tmem_wait_ld256();
+#pragma unroll
+        for (int e = 0; e < kR; ++e) reg_fence256(s[e]);
+        if (!interior(w, j, p.window, p.n_sink)) {
+          // key k = j*128 + c is visible iff k <= hi and (k > lo or k < n_sink)
+          const int ka = j * kR;
+#pragma unroll
+          for (int c = 0; c < kR; ++c) {
+            const int k = ka + c;
+            if (!(k <= hi && (k > lo || k < p.n_sink))) s[c] = __float_as_uint(-INFINITY);
+          }
+        }
+        float mx8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(s[e]);
+#pragma unroll
+        for (int c = 8; c < kR; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
+        const float tmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        m_run = fmaxf(m_run, tmax);
+        // Lazy rescale: move the reference maximum only when the scores have
+        // outgrown it by 2^8; O (already holding earlier tiles) is then scaled
+        // by 2^((m_used - m_run) scale2) once O += P V of the previous tile is
+        // done.  The tensor-memory accesses are warp-collective: a warp
+        // rescales if any of its rows must (the others multiply by 1).
+        const bool first = (m_used == -INFINITY);
+        const bool grow =
+            first ? (m_run != -INFINITY) : ((m_run - m_used) * p.scale2 > kRescaleLog2);
+        const bool resc = grow && !first;
+        if (__any_sync(0xffffffffu, resc)) {
+          if (!wwait(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, p)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const float alpha = resc ? ex2_approx((m_used - m_run) * p.scale2) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < kD / 32; ++c) {
+            uint32_t o[32];
             tmem_ld_x32(taddr + kColO + 32 * c, o);
             tmem_wait_ld256();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st_x32(taddr + kColO + 32 * c, o);
           }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) reg_fence256(o[e]);
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o + orow + 32 * c);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint32_t wv[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int idx = v4 * 8 + 2 * e;
-                wv[e] = seen ? pack_bf16x2(__uint_as_float(o[idx]) * inv,
-                                           __uint_as_float(o[idx + 1]) * inv)
-                             : 0u;
-              }
-              dst[v4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            }
-          }
+          tmem_st_wait();
+          l *= alpha;
+          corr *= alpha;
         }
-        if (valid && p.lse != nullptr) {
-          const size_t li = p.cu_q ? static_cast<size_t>(w.h) * p.total_q + w.q_base + q
-                                   : (static_cast<size_t>(w.bseq) * p.Hq + w.h) * p.Sq + q;
-          p.lse[li] = lse_row;
+        if (grow) m_used = m_run;
+        // P = 2^(S scale2 - m_used scale2) as bf16 pairs over the first 64
+        // columns of the buffer (key-step kk of O += P V at column 8 kk); a
+        // row that has seen no key yet has m_used = -inf and every P = 0.
+        const float nms = first && !grow ? 0.f : -m_used * p.scale2;
+        float sum0 = 0.f, sum1 = 0.f;
+        uint32_t pk[kR / 2];
+#pragma unroll
+        for (int e = 0; e < kR / 2; ++e) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * e]), p.scale2, nms));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * e + 1]), p.scale2, nms));
+          if (e & 1)
+            sum1 += p0 + p1;
+          else
+            sum0 += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        l += sum0 + sum1;
+        {  // the tile's largest p, with the arithmetic used for it above
+          const float ptop = ex2_approx(fmaf(tmax, p.scale2, nms));
+          corr += ptop - __uint_as_float(pack_bf16x2(0.f, ptop) & 0xffff0000u);
+        }
+        tmem_st_x32(tS, pk);
+        tmem_st_x32(tS + 32, pk + 32);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&p_ready[t & 1]);
+      }
+      if (!ok) break;
+      // -------------------------------------------------------------- epilogue
+      const bool have_o = N > 0;
+      if (have_o) {
+        const int t = g + N - 1;
+        if (!wwait(&o_done[t & 1], (t >> 1) & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+      }
+      g += N;
+      // O / l, or with a logit sink sigma of this head one more term of the
+      // denominator taken against m* = max(sigma, m scale) ("TileLang
+      // tutorial, ch.15", section 4.6); a row that saw no key gets O = 0.
+      const bool seen = have_o && l > 0.f;
+      const float sg = p.sink ? p.sink[w.h] : -INFINITY;
+      float inv, lse_row;
+      if (sg == -INFINITY) {
+        inv = seen ? 1.f / (l - corr) : 0.f;
+        lse_row = seen ? fmaf(m_used, p.scale, logf(l)) : -INFINITY;
+      } else {
+        const float am = seen ? m_used * p.scale : -INFINITY;
+        const float mst = fmaxf(am, sg);
+        const float e1 = seen ? expf(am - mst) : 0.f;
+        const float e2 = expf(sg - mst);
+        inv = e1 / fmaf(l - corr, e1, e2);
+        lse_row = mst + logf(fmaf(l, e1, e2));
+      }
+      const size_t orow =
+          (p.cu_q ? static_cast<size_t>(w.q_base + q) * p.o_ss
+                  : static_cast<size_t>(w.bseq) * p.o_sb + static_cast<size_t>(q) * p.o_ss) +
+          static_cast<size_t>(w.h) * p.o_sh;
+#pragma unroll 1
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t o[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+        if (have_o) {
+          tmem_ld_x32(taddr + kColO + 32 * c, o);
+          tmem_wait_ld256();
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) reg_fence256(o[e]);
+        if (valid) {
+          uint32_t wv[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            wv[e] = seen ? pack_bf16x2(__uint_as_float(o[2 * e]) * inv,
+                                       __uint_as_float(o[2 * e + 1]) * inv)
+                         : 0u;
+          uint4* dst = reinterpret_cast<uint4*>(p.o + orow + 32 * c);
+          if (p.o_v8) {
+            st_global_v8(dst, wv);
+            st_global_v8(dst + 2, wv + 8);
+          } else {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(wv[4 * v4], wv[4 * v4 + 1], wv[4 * v4 + 2], wv[4 * v4 + 3]);
+          }
         }
       }
+      if (valid && p.lse != nullptr) {
+        const size_t li = p.cu_q ? static_cast<size_t>(w.h) * p.total_q + w.q_base + q
+                                 : (static_cast<size_t>(w.bseq) * p.Hq + w.h) * p.Sq + q;
+        p.lse[li] = lse_row;
+      }
+      // The next item's first O += P V waits for this warp's next p_ready
+      // arrival, made after the reads of O above.
+      tc_fence_before_sync();
     }
   }
 
@@ -588,6 +663,8 @@ cudaError_t launch_attn_fwd256(const FwdLaunch& a, cudaStream_t stream) {
   p.o_sb = a.o_sb;
   p.o_ss = a.o_ss;
   p.o_sh = a.o_sh;
+  p.o_v8 = (reinterpret_cast<uintptr_t>(a.o) % 32 == 0) && a.o_sb % 16 == 0 && a.o_ss % 16 == 0 &&
+           a.o_sh % 16 == 0;
   p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
@@ -602,9 +679,18 @@ cudaError_t launch_attn_fwd256(const FwdLaunch& a, cudaStream_t stream) {
   p.n_sink = a.n_sink;
   p.wait_limit_ns = kWaitLimitNs;
   p.status = a.status;
-  const long long grid = static_cast<long long>(p.num_qt) * a.Hq * a.B;
-  if (grid <= 0) return cudaSuccess;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const long long items = static_cast<long long>(p.num_qt) * a.Hq * a.B;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  p.num_items = static_cast<int>(items);
+  // Dense calls: persistent, one CTA per SM (each holds all 512 tensor-
+  // memory columns), the equal-length items dealt in bands.  Packed and
+  // paged calls: one CTA per item, so that the hardware hands the next item
+  // to whichever SM frees first (item costs follow the sequence lengths,
+  // which a fixed dealing balances badly: 1.54 ms persistent against 1.22 ms
+  // on a paged batch of 2,048-8,192 cached keys).
+  const bool packed = a.cu_q != nullptr || a.page_table != nullptr;
+  const long long grid = packed ? items : std::min<long long>(items, std::max(a.num_sms, 1));
   if (a.page_table != nullptr)
     attn_fwd256_kernel<true><<<static_cast<unsigned>(grid), kThr, kSmem, stream>>>(a.tmQ, a.tmK,
                                                                                   a.tmV, p);
