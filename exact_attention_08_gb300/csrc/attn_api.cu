@@ -520,6 +520,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   a.window = window;
   a.n_sink = n_sink;
   a.status = ds->status;
+  a.num_sms = ds->num_sms;
   // Dense tensors are 4-D maps (d, H, S, B); packed ones (d, H, total, 1).
   const uint64_t sq = varlen ? static_cast<uint64_t>(total_q) : static_cast<uint64_t>(max_Sq);
   const uint64_t sk = varlen ? static_cast<uint64_t>(total_k) : static_cast<uint64_t>(max_Skv);

@@ -11,9 +11,13 @@
 //   dS = P * (dP - D),   dQ = scale dS K,   dK = scale dS^T Q.
 // Every gradient is accumulated in fp32 in tensor memory over its whole
 // reduction and written once, so the results do not depend on scheduling
-// (no atomics): dK and dV by one CTA per key tile, looping over every query
-// tile of every query head that reads the key head; dQ by one CTA per query
-// tile, looping over the key tiles.
+// (no atomics): dK and dV of a key tile by one CTA, looping over every
+// query tile of every query head that reads the key head; dQ of a query tile
+// by one CTA, looping over the key tiles.  For dense calls both grids are
+// persistent (one CTA per SM walking its share of the tiles, every barrier
+// phase carried over from one tile to the next, the next tile's loads and
+// first products overlapping the last one's output), for packed calls one
+// CTA per tile.
 //
 // Kernels:
 //   attn_bwd_rowstat_kernel  D and LSE in base 2 per query row, padded to
@@ -49,6 +53,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -316,8 +321,66 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok;
 }
 
-// dK and dV of one key tile (128 keys) of key head hk: one CTA per
-// (key tile, key head, batch).
+// The n-th item of this CTA, or -1 past the last: bands of gridDim.x items,
+// every other band dealt in reverse CTA order.  With one CTA per item (the
+// grid as large as the item count) every CTA takes its own item only.
+__device__ __forceinline__ int bwd_item_at(int n, int num_items) {
+  const int G = gridDim.x;
+  const int pos = (n & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const long long k = static_cast<long long>(n) * G + pos;
+  return k < num_items ? static_cast<int>(k) : -1;
+}
+
+// One key tile of the dK/dV kernel: which, and the query tiles that see it.
+struct KvItem {
+  int kt, hk, b, k0, qt_lo, nq, ntiles;
+  SeqGeo sg;
+};
+
+// Item order.  Under a causal mask the key tile is outermost, so that the
+// longest (key tile 0 has the most query tiles) come first; without one
+// every item is the same work and the key tiles of one (batch, key head) are
+// adjacent, so the CTAs running together read the same query and
+// output-gradient tiles through L2.  False for a key tile past its
+// sequence's keys (nothing to write).
+__device__ __forceinline__ bool kv_item(const BwdParams& p, int item, KvItem& it) {
+  const int nkt_all = (p.Skv + kB - 1) / kB;
+  if (p.causal) {
+    it.kt = item / (p.B * p.Hkv);
+    it.hk = (item / p.B) % p.Hkv;
+    it.b = item % p.B;
+  } else {
+    it.kt = item % nkt_all;
+    it.hk = (item / nkt_all) % p.Hkv;
+    it.b = item / (nkt_all * p.Hkv);
+  }
+  it.k0 = it.kt * kB;
+  if (!seq_geo(p, it.b, it.sg, false) || it.k0 >= it.sg.Lk) return false;
+  const int nqt = (it.sg.Lq + kB - 1) / kB;
+  const int off = it.sg.Lk - it.sg.Lq;
+  // The query tiles that see a key of the tile: from the first query that
+  // sees key k0 (causal) to the last that sees key k0 + 127 (window; a tile
+  // holding sink keys is seen to the end).
+  int qt_lo = 0, qt_hi = nqt - 1;
+  if (p.causal) {
+    const int qmin = it.k0 - off;  // first query that sees key k0
+    qt_lo = qmin <= 0 ? 0 : qmin / kB;
+  }
+  if (p.window > 0 && it.k0 >= p.n_sink) {
+    const int qmax = it.k0 + kB - 1 - off + p.window - 1;  // last query that sees key k0 + 127
+    qt_hi = qmax < 0 ? -1 : min(qt_hi, qmax / kB);
+  }
+  it.qt_lo = qt_lo;
+  it.nq = qt_hi >= qt_lo ? qt_hi - qt_lo + 1 : 0;
+  it.ntiles = (p.Hq / p.Hkv) * it.nq;  // (query head, query tile) pairs, head-major
+  return true;
+}
+
+// dK and dV of key tiles (128 keys) of a key head: items (key tile, key head,
+// batch), the grid persistent for dense calls (one CTA per SM walking its
+// items, every barrier phase carried over the CTA's whole sequence of query
+// tiles) and one CTA per item for packed ones (item costs follow the
+// sequence lengths).
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -336,54 +399,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* sa_full = bars + 5;   // S^T is in tensor memory
   uint64_t* sb_full = bars + 6;   // dP^T is in tensor memory
   uint64_t* pa_ready = bars + 7;  // P^T written (one arrival per compute thread)
-  uint64_t* pb_ready = bars + 11; // dS^T written (one arrival per compute thread)
-  uint64_t* done = bars + 8;      // every product of the CTA is done
+  uint64_t* done = bars + 8;      // every product of the item is done
   uint64_t* drain = bars + 9;
+  uint64_t* kv_empty = bars + 10; // the item's last products reading K and V are done
+  uint64_t* pb_ready = bars + 11; // dS^T written (one arrival per compute thread)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
   __shared__ int abort_s;
   volatile int* abort_flag = &abort_s;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-  // Blocks go out in index order.  Under a causal mask the key tile is
-  // outermost, so that the longest (key tile 0 has the most query tiles) come
-  // first; without one every block is the same work and the key tiles of one
-  // (batch, key head) are adjacent, so the blocks running together read the
-  // same query and output-gradient tiles through L2.
-  const int nkt_all = (p.Skv + kB - 1) / kB;
-  int kt, hk, b;
-  if (p.causal) {
-    kt = blockIdx.x / (p.B * p.Hkv);
-    hk = (blockIdx.x / p.B) % p.Hkv;
-    b = blockIdx.x % p.B;
-  } else {
-    kt = blockIdx.x % nkt_all;
-    hk = (blockIdx.x / nkt_all) % p.Hkv;
-    b = blockIdx.x / (nkt_all * p.Hkv);
-  }
   const int G = p.Hq / p.Hkv;
-  const int k0 = kt * kB;
-  SeqGeo sg;
-  // A key tile past its sequence's keys has nothing to write (uniform exit).
-  if (!seq_geo(p, b, sg, false) || k0 >= sg.Lk) return;
-  const int nqt = (sg.Lq + kB - 1) / kB;
-  const int off = sg.Lk - sg.Lq;
-  // The query tiles that see a key of the tile: from the first query that
-  // sees key k0 (causal) to the last that sees key k0 + 127 (window; a tile
-  // holding sink keys is seen to the end).
-  int qt_lo = 0, qt_hi = nqt - 1;
-  if (p.causal) {
-    const int qmin = k0 - off;  // first query that sees key k0
-    qt_lo = qmin <= 0 ? 0 : qmin / kB;
-  }
-  if (p.window > 0 && k0 >= p.n_sink) {
-    const int qmax = k0 + kB - 1 - off + p.window - 1;  // last query that sees key k0 + 127
-    qt_hi = qmax < 0 ? -1 : min(qt_hi, qmax / kB);
-  }
-  const int nq = qt_hi >= qt_lo ? qt_hi - qt_lo + 1 : 0;
-  const int ntiles = G * nq;  // (query head, query tile) pairs, head-major
+  const int num_items = ((p.Skv + kB - 1) / kB) * p.Hkv * p.B;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_free[s], 1);
@@ -407,37 +436,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   auto stage = [&](int s) { return smem + C::kOffStage + s * C::kStageBytes; };
 
+  // Counters over the CTA's items: query tiles (one stage load, one set of
+  // products each) and items with query tiles (one K / V load each).  Items
+  // without a query tile only write zeros.
   if (warp == kWarpProd) {
     // ================================================================ producer
-    mbar_arrive_expect_tx_w(kv_full, 2 * C::kTile);
-#pragma unroll
-    for (int a = 0; a < C::kAtoms; ++a) {
-      tma_load_4d_w(sK + a * C::kAtomBytes, &tmK, kv_full, a * 64, hk, sg.k_base + k0,
-                    sg.b_coord);
-      tma_load_4d_w(sV + a * C::kAtomBytes, &tmV, kv_full, a * 64, hk, sg.k_base + k0,
-                    sg.b_coord);
-    }
-    int issued = 0;
-    for (int t = 0; t < ntiles; ++t) {
-      const int s = t & 1;
-      if (t >= 2 && !warp_wait(&q_free[s], ((t >> 1) - 1) & 1, abort_flag, p)) break;
-      const int h = hk * G + t / nq, qt = qt_lo + t % nq;
-      uint8_t* st = stage(s);
-      mbar_arrive_expect_tx_w(&q_full[s], 2 * C::kTile + 2 * C::kVec);
+    int kv_loads = 0, issued = 0;
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int item = bwd_item_at(n, num_items);
+      if (item < 0) break;
+      KvItem it;
+      if (!kv_item(p, item, it) || it.ntiles == 0) continue;
+      // K and V are single-buffered: the previous item's last S^T and dP^T
+      // must be done with them
+      if (kv_loads > 0 && !warp_wait(kv_empty, (kv_loads - 1) & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx_w(kv_full, 2 * C::kTile);
 #pragma unroll
       for (int a = 0; a < C::kAtoms; ++a) {
-        tma_load_4d_w(st + a * C::kAtomBytes, &tmQ, &q_full[s], a * 64, h,
-                      sg.q_base + qt * kB, sg.b_coord);
-        tma_load_4d_w(st + C::kTile + a * C::kAtomBytes, &tmDO, &q_full[s], a * 64, h,
-                      sg.q_base + qt * kB, sg.b_coord);
+        tma_load_4d_w(sK + a * C::kAtomBytes, &tmK, kv_full, a * 64, it.hk,
+                      it.sg.k_base + it.k0, it.sg.b_coord);
+        tma_load_4d_w(sV + a * C::kAtomBytes, &tmV, kv_full, a * 64, it.hk,
+                      it.sg.k_base + it.k0, it.sg.b_coord);
       }
-      const size_t vrow = (static_cast<size_t>(b) * p.Hq + h) * p.Sqp + static_cast<size_t>(qt) * kB;
-      bulk_load_1d_w(st + 2 * C::kTile, p.lse2 + vrow, C::kVec, &q_full[s]);
-      bulk_load_1d_w(st + 2 * C::kTile + C::kVec, p.dvec + vrow, C::kVec, &q_full[s]);
-      issued = t + 1;
+      ++kv_loads;
+      for (int t = 0; t < it.ntiles; ++t) {
+        const int s = issued & 1;
+        if (issued >= 2 && !warp_wait(&q_free[s], ((issued >> 1) - 1) & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        const int h = it.hk * G + t / it.nq, qt = it.qt_lo + t % it.nq;
+        uint8_t* st = stage(s);
+        mbar_arrive_expect_tx_w(&q_full[s], 2 * C::kTile + 2 * C::kVec);
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a) {
+          tma_load_4d_w(st + a * C::kAtomBytes, &tmQ, &q_full[s], a * 64, h,
+                        it.sg.q_base + qt * kB, it.sg.b_coord);
+          tma_load_4d_w(st + C::kTile + a * C::kAtomBytes, &tmDO, &q_full[s], a * 64, h,
+                        it.sg.q_base + qt * kB, it.sg.b_coord);
+        }
+        const size_t vrow =
+            (static_cast<size_t>(it.b) * p.Hq + h) * p.Sqp + static_cast<size_t>(qt) * kB;
+        bulk_load_1d_w(st + 2 * C::kTile, p.lse2 + vrow, C::kVec, &q_full[s]);
+        bulk_load_1d_w(st + 2 * C::kTile + C::kVec, p.dvec + vrow, C::kVec, &q_full[s]);
+        ++issued;
+      }
     }
     // Let every copy issued land before the CTA can leave.
-    warp_wait(kv_full, 0, nullptr, p);
+    if (kv_loads > 0) warp_wait(kv_full, (kv_loads - 1) & 1, nullptr, p);
     for (int s = 0; s < 2; ++s) {
       const int n_s = (issued - s + 1) / 2;  // loads issued into stage s
       if (n_s > 0) warp_wait(&q_full[s], (n_s - 1) & 1, nullptr, p);
@@ -447,12 +497,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // Per query tile t the pipe runs dP^T(t), dV(t), S^T(t+1), dK(t): S^T of
     // the next tile overwrites P^T(t) once dV(t) has read it, while the
     // compute warps form dS^T(t) from P^T kept in their registers; dP^T(t+1)
-    // overwrites dS^T(t) once dK(t) has read it.
+    // overwrites dS^T(t) once dK(t) has read it.  An item's first dV and dK
+    // overwrite the accumulators: they wait for the P^T / dS^T arrivals the
+    // compute warps make after reading the previous item's dK and dV out.
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, kB, false);
     constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, true);
     const uint64_t dk = sdesc_sw128(smem_addr(sK), 16, 1024);
     const uint64_t dvk = sdesc_sw128(smem_addr(sV), 16, 1024);
     const uint32_t tS = tmem, tP = tmem + kB, tDV = tmem + 2 * kB, tDK = tmem + 2 * kB + D;
+    int T = 0;    // query tiles of earlier items
+    int kvi = 0;  // items with query tiles before this one
     auto issue_st = [&](int t) -> bool {  // S^T(t) = K Q(t)^T
       const int s = t & 1;
       if (!warp_wait(&q_full[s], (t >> 1) & 1, abort_flag, p)) return false;
@@ -466,49 +520,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit_w(sa_full);
       return true;
     };
-    bool ok = warp_wait(kv_full, 0, abort_flag, p);
-    if (ok) tc_fence_after_sync();
-    if (ok && ntiles > 0) ok = issue_st(0);
-    for (int t = 0; ok && t < ntiles; ++t) {
-      const int s = t & 1;
-      const uint32_t st = smem_addr(stage(s));
-      const uint64_t ddok = sdesc_sw128(st + C::kTile, 16, 1024);
-      // dP^T(t) = V dO(t)^T
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int item = bwd_item_at(n, num_items);
+      if (item < 0) break;
+      KvItem it;
+      if (!kv_item(p, item, it) || it.ntiles == 0) continue;
+      const int nt = it.ntiles;
+      ok = warp_wait(kv_full, kvi & 1, abort_flag, p);
+      if (ok) tc_fence_after_sync();
+      if (ok) ok = issue_st(T);
+      for (int t = 0; ok && t < nt; ++t) {
+        const int u = T + t;  // query tile over the CTA's items
+        const int s = u & 1;
+        const uint32_t st = smem_addr(stage(s));
+        const uint64_t ddok = sdesc_sw128(st + C::kTile, 16, 1024);
+        // dP^T(t) = V dO(t)^T
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
-        mma_bf16_ss_w(tP, dvk + ko, ddok + ko, idesc_s, kk > 0 ? 1u : 0u);
-      }
-      mma_commit_w(sb_full);
-      // dV += P^T dO(t) (A from tensor memory, K = queries; B read along d)
-      if (!warp_wait(pa_ready, t & 1, abort_flag, p)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const uint64_t dqm = sdesc_sw128(st, C::kAtomBytes, 1024);
-      const uint64_t ddom = sdesc_sw128(st + C::kTile, C::kAtomBytes, 1024);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
+          mma_bf16_ss_w(tP, dvk + ko, ddok + ko, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_w(sb_full);
+        // the item's last products reading K (its last S^T, issued before)
+        // and V: the producer may load the next item's K and V
+        if (t + 1 == nt) mma_commit_w(kv_empty);
+        // dV += P^T dO(t) (A from tensor memory, K = queries; B read along d)
+        if (!warp_wait(pa_ready, u & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t dqm = sdesc_sw128(st, C::kAtomBytes, 1024);
+        const uint64_t ddom = sdesc_sw128(st + C::kTile, C::kAtomBytes, 1024);
 #pragma unroll
-      for (int kk = 0; kk < kB / 16; ++kk)
-        mma_bf16_ts_w(tDV, tS + packed_col(kk), ddom + kk * (2048 >> 4), idesc_g,
-                      (t > 0 || kk > 0) ? 1u : 0u);
-      if (t + 1 < ntiles && !issue_st(t + 1)) {
-        ok = false;
-        break;
-      }
-      // dK += dS^T Q(t)
-      if (!warp_wait(pb_ready, t & 1, abort_flag, p)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
+        for (int kk = 0; kk < kB / 16; ++kk)
+          mma_bf16_ts_w(tDV, tS + packed_col(kk), ddom + kk * (2048 >> 4), idesc_g,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+        if (t + 1 < nt && !issue_st(u + 1)) {
+          ok = false;
+          break;
+        }
+        // dK += dS^T Q(t)
+        if (!warp_wait(pb_ready, u & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
 #pragma unroll
-      for (int kk = 0; kk < kB / 16; ++kk)
-        mma_bf16_ts_w(tDK, tP + packed_col(kk), dqm + kk * (2048 >> 4), idesc_g,
-                      (t > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_w(&q_free[s]);
+        for (int kk = 0; kk < kB / 16; ++kk)
+          mma_bf16_ts_w(tDK, tP + packed_col(kk), dqm + kk * (2048 >> 4), idesc_g,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_w(&q_free[s]);
+      }
+      if (ok) mma_commit_w(done);
+      T += nt;
+      ++kvi;
     }
-    mma_commit_w(done);
     // Every product issued has finished before tensor memory is released.
     mma_commit_w(drain);
     warp_wait(drain, 0, nullptr, p);
@@ -516,113 +584,130 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ================================================================ compute warps
     const int wq = warp & 3, wh = warp >> 2;  // lane quarter, column half
     const int r = wq * 32 + lane;
-    const int k_idx = k0 + r;
     const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint64_t sc2 = pf2(p.scale2, p.scale2);
+    int T = 0;    // query tiles of earlier items
+    int kvi = 0;  // items with query tiles before this one
     bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
-      const int s = t & 1;
-      // the stage's row vectors came by bulk copy: observe their barrier too
-      if (!warp_wait(sa_full, t & 1, abort_flag, p) ||
-          !warp_wait(&q_full[s], (t >> 1) & 1, abort_flag, p)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const int qt = qt_lo + t % nq;
-      // this warp's 64 entries of the two row vectors (-LSE2, -D)
-      const uint32_t nl2_addr = smem_addr(stage(s) + 2 * C::kTile) + 4 * 64 * wh;
-      const uint32_t nd2_addr = nl2_addr + 4 * kB;
-      // column c (query qt*128 + c) is visible to this key row iff
-      // cmin <= c <= cmax: causal from below, the window from above (not for
-      // sink keys); key rows past the sequence see nothing
-      int cmin = p.causal ? k_idx - off - qt * kB : -(1 << 30);
-      int cmax = (p.window > 0 && k_idx >= p.n_sink) ? k_idx - off + p.window - 1 - qt * kB
-                                                      : (1 << 30);
-      if (k_idx >= sg.Lk) cmin = 1 << 30;
-      // P^T of this warp's 64 columns: written to tensor memory for dV and
-      // kept in registers (bf16 pairs) for dS^T, because S^T of the next
-      // tile replaces it.
-      uint32_t pkeep[32];
-      {
-        uint32_t ra[64];
-        uint64_t nl2[16];
-        tmem_ld_x32(taddr + 64 * wh, ra);
-        tmem_ld_x32(taddr + 64 * wh + 32, ra + 32);
-        lds_chunk(nl2_addr, nl2);
-        tmem_ld_wait_b();
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int c4 = 2 * wh + j;
-          float pf[32];
-          // x = S scale2 - LSE2 in pairs (the vector holds -LSE2); the mask
-          // is applied only to a chunk the diagonal crosses
-          if (j == 1) lds_chunk(nl2_addr + 128, nl2);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            reg_fence_b(ra[32 * j + 2 * e]);
-            reg_fence_b(ra[32 * j + 2 * e + 1]);
-            const uint64_t x2 = pf2_fma(
-                pf2(__uint_as_float(ra[32 * j + 2 * e]), __uint_as_float(ra[32 * j + 2 * e + 1])),
-                sc2, nl2[e]);
-            float x0, x1;
-            pf2_split(x2, x0, x1);
-            pf[2 * e] = ex2_approx(x0);
-            pf[2 * e + 1] = ex2_approx(x1);
-          }
-          if (cmin > 32 * c4 || cmax < 32 * c4 + 31) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (32 * c4 + e < cmin || 32 * c4 + e > cmax) pf[e] = 0.f;
-          }
-          pack32(pf, pkeep + 16 * j);
-          tmem_st_x16(taddr + 64 * wh + 16 * j, pkeep + 16 * j);
+    for (int n = 0; ok; ++n) {
+      const int item = bwd_item_at(n, num_items);
+      if (item < 0) break;
+      KvItem it;
+      if (!kv_item(p, item, it)) continue;
+      const int nt = it.ntiles;
+      const int k_idx = it.k0 + r;
+      const int off = it.sg.Lk - it.sg.Lq;
+      for (int t = 0; t < nt; ++t) {
+        const int u = T + t;
+        const int s = u & 1;
+        // the stage's row vectors came by bulk copy: observe their barrier too
+        if (!warp_wait(sa_full, u & 1, abort_flag, p) ||
+            !warp_wait(&q_full[s], (u >> 1) & 1, abort_flag, p)) {
+          ok = false;
+          break;
         }
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(pa_ready);
-      // dS^T = P^T (dP^T - D), from the bf16 P^T
-      if (!warp_wait(sb_full, t & 1, abort_flag, p)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      {
-        uint32_t ra[64];
-        uint64_t nd2[16];  // -D in pairs
-        tmem_ld_x32(taddr + kB + 64 * wh, ra);
-        tmem_ld_x32(taddr + kB + 64 * wh + 32, ra + 32);
-        lds_chunk(nd2_addr, nd2);
-        tmem_ld_wait_b();
+        tc_fence_after_sync();
+        const int qt = it.qt_lo + t % it.nq;
+        // this warp's 64 entries of the two row vectors (-LSE2, -D)
+        const uint32_t nl2_addr = smem_addr(stage(s) + 2 * C::kTile) + 4 * 64 * wh;
+        const uint32_t nd2_addr = nl2_addr + 4 * kB;
+        // column c (query qt*128 + c) is visible to this key row iff
+        // cmin <= c <= cmax: causal from below, the window from above (not for
+        // sink keys); key rows past the sequence see nothing
+        int cmin = p.causal ? k_idx - off - qt * kB : -(1 << 30);
+        int cmax = (p.window > 0 && k_idx >= p.n_sink) ? k_idx - off + p.window - 1 - qt * kB
+                                                        : (1 << 30);
+        if (k_idx >= it.sg.Lk) cmin = 1 << 30;
+        // P^T of this warp's 64 columns: written to tensor memory for dV and
+        // kept in registers (bf16 pairs) for dS^T, because S^T of the next
+        // tile replaces it.
+        uint32_t pkeep[32];
+        {
+          uint32_t ra[64];
+          uint64_t nl2[16];
+          tmem_ld_x32(taddr + 64 * wh, ra);
+          tmem_ld_x32(taddr + 64 * wh + 32, ra + 32);
+          lds_chunk(nl2_addr, nl2);
+          tmem_ld_wait_b();
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float pf[32];
-          uint32_t pk[16];
-          if (j == 1) lds_chunk(nd2_addr + 128, nd2);
+          for (int j = 0; j < 2; ++j) {
+            const int c4 = 2 * wh + j;
+            float pf[32];
+            // x = S scale2 - LSE2 in pairs (the vector holds -LSE2); the mask
+            // is applied only to a chunk the diagonal crosses
+            if (j == 1) lds_chunk(nl2_addr + 128, nl2);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            reg_fence_b(ra[32 * j + 2 * e]);
-            reg_fence_b(ra[32 * j + 2 * e + 1]);
-            const uint32_t w = pkeep[16 * j + e];
-            const uint64_t p2 = pf2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-            const uint64_t g2 = pf2_add(
-                pf2(__uint_as_float(ra[32 * j + 2 * e]), __uint_as_float(ra[32 * j + 2 * e + 1])),
-                nd2[e]);
-            pf2_split(pf2_mul(p2, g2), pf[2 * e], pf[2 * e + 1]);
+            for (int e = 0; e < 16; ++e) {
+              reg_fence_b(ra[32 * j + 2 * e]);
+              reg_fence_b(ra[32 * j + 2 * e + 1]);
+              const uint64_t x2 = pf2_fma(pf2(__uint_as_float(ra[32 * j + 2 * e]),
+                                              __uint_as_float(ra[32 * j + 2 * e + 1])),
+                                          sc2, nl2[e]);
+              float x0, x1;
+              pf2_split(x2, x0, x1);
+              pf[2 * e] = ex2_approx(x0);
+              pf[2 * e + 1] = ex2_approx(x1);
+            }
+            if (cmin > 32 * c4 || cmax < 32 * c4 + 31) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (32 * c4 + e < cmin || 32 * c4 + e > cmax) pf[e] = 0.f;
+            }
+            pack32(pf, pkeep + 16 * j);
+            tmem_st_x16(taddr + 64 * wh + 16 * j, pkeep + 16 * j);
           }
-          pack32(pf, pk);
-          tmem_st_x16(taddr + kB + 64 * wh + 16 * j, pk);
         }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(pa_ready);
+        // dS^T = P^T (dP^T - D), from the bf16 P^T
+        if (!warp_wait(sb_full, u & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        {
+          uint32_t ra[64];
+          uint64_t nd2[16];  // -D in pairs
+          tmem_ld_x32(taddr + kB + 64 * wh, ra);
+          tmem_ld_x32(taddr + kB + 64 * wh + 32, ra + 32);
+          lds_chunk(nd2_addr, nd2);
+          tmem_ld_wait_b();
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float pf[32];
+            uint32_t pk[16];
+            if (j == 1) lds_chunk(nd2_addr + 128, nd2);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              reg_fence_b(ra[32 * j + 2 * e]);
+              reg_fence_b(ra[32 * j + 2 * e + 1]);
+              const uint32_t w = pkeep[16 * j + e];
+              const uint64_t p2 = pf2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+              const uint64_t g2 = pf2_add(pf2(__uint_as_float(ra[32 * j + 2 * e]),
+                                              __uint_as_float(ra[32 * j + 2 * e + 1])),
+                                          nd2[e]);
+              pf2_split(pf2_mul(p2, g2), pf[2 * e], pf[2 * e + 1]);
+            }
+            pack32(pf, pk);
+            tmem_st_x16(taddr + kB + 64 * wh + 16 * j, pk);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(pb_ready);
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(pb_ready);
-    }
-    if (ok && warp_wait(done, 0, abort_flag, p)) {
-      tc_fence_after_sync();
-      const bool valid = k_idx < sg.Lk;
-      const size_t orow = ((static_cast<size_t>(sg.k_row0) + k_idx) * p.Hkv + hk) * D;
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (nt > 0) {
+        if (!warp_wait(done, kvi & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+      }
+      const bool valid = k_idx < it.sg.Lk;
+      const size_t orow = ((static_cast<size_t>(it.sg.k_row0) + k_idx) * p.Hkv + it.hk) * D;
       constexpr int kHalfChunks = D / 64;  // 32-column chunks in a column half
 #pragma unroll 1
       for (int g = 0; g < 2; ++g) {  // 0: dV, 1: dK (times scale)
@@ -631,7 +716,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll 1
         for (int c = wh * kHalfChunks; c < (wh + 1) * kHalfChunks; ++c) {
           uint32_t ra[32];
-          if (ntiles > 0) {
+          if (nt > 0) {
             tmem_ld_x32(taddr + 2 * kB + g * D + 32 * c, ra);
             tmem_ld_wait_b();
           }
@@ -639,7 +724,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             reg_fence_b(ra[e]);
-            f[e] = ntiles > 0 ? __uint_as_float(ra[e]) * mul : 0.f;
+            f[e] = nt > 0 ? __uint_as_float(ra[e]) * mul : 0.f;
           }
           uint32_t pk[16];
           pack32(f, pk);
@@ -651,6 +736,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       }
+      // The next item's first dV and dK wait for this warp's next arrivals,
+      // made after the reads of the accumulators above.
+      tc_fence_before_sync();
+      T += nt;
+      if (nt > 0) ++kvi;
     }
   }
   tc_fence_before_sync();
@@ -659,8 +749,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// dQ of one query tile (128 rows) of query head h: one CTA per
-// (query tile, query head, batch), looping over the visible key tiles.
+// One query tile of the dQ kernel: which, and the key tiles its rows see.
+struct QItem {
+  int qt, h, b, hk, q0, jlo, jhi, sinkT, ns, nkt;
+  SeqGeo sg;
+  // the n-th key tile walked: sink tiles first, then the window's range
+  __device__ __forceinline__ int tile_at(int n) const {
+    return n < ns ? n : max(jlo, sinkT) + (n - ns);
+  }
+};
+
+// Item order.  Under a causal mask the query tile is outermost, the last
+// (longest) first; without one the query tiles of one (batch, head) are
+// adjacent, so the CTAs running together read the same key and value tiles.
+// False for a query tile past its sequence's queries (nothing to write).
+__device__ __forceinline__ bool q_item(const BwdParams& p, int item, QItem& it) {
+  const int nqt_all = p.Sqp / kB;
+  if (p.causal) {
+    it.qt = nqt_all - 1 - item / (p.B * p.Hq);
+    it.h = (item / p.B) % p.Hq;
+    it.b = item % p.B;
+  } else {
+    it.qt = item % nqt_all;
+    it.h = (item / nqt_all) % p.Hq;
+    it.b = item / (nqt_all * p.Hq);
+  }
+  it.hk = it.h / (p.Hq / p.Hkv);
+  it.q0 = it.qt * kB;
+  if (!seq_geo(p, it.b, it.sg, false) || it.q0 >= it.sg.Lq) return false;
+  const int off = it.sg.Lk - it.sg.Lq;
+  // The key tiles the tile's rows see: the sink tiles, then the window's
+  // tiles from the first key above the first row's window bound up to the
+  // last key any row sees (causal bound, end of the keys).
+  int jhi = (it.sg.Lk - 1) / kB;
+  if (p.causal) {
+    const int qlast = min(it.q0 + kB - 1, it.sg.Lq - 1);
+    const int kmax = min(it.sg.Lk - 1, qlast + off);  // last key any row of the tile sees
+    jhi = kmax >= 0 ? kmax / kB : -1;
+  }
+  if (it.sg.Lk <= 0) jhi = -1;
+  int jlo = 0, sinkT = 0;
+  if (p.window > 0) {
+    const int lo = it.q0 + off - p.window;  // keys above lo are in the first row's window
+    jlo = lo < 0 ? 0 : (lo + 1) / kB;
+    sinkT = (p.n_sink + kB - 1) / kB;
+  }
+  it.jlo = jlo;
+  it.jhi = jhi;
+  it.sinkT = sinkT;
+  it.ns = min(sinkT, jhi + 1);
+  it.nkt = jhi < 0 ? 0 : it.ns + max(0, jhi - max(jlo, sinkT) + 1);
+  return true;
+}
+
+// dQ of query tiles (128 rows) of a query head: items (query tile, query
+// head, batch), persistent for dense calls and one CTA per item for packed
+// ones, as in the dK/dV kernel.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -673,68 +817,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sDO = smem + C::kOffDO;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBarQ);
-  uint64_t* qd_full = bars;      // Q and dO landed
-  uint64_t* kv_full = bars + 1;  // [2] K and V of a key tile landed
-  uint64_t* kv_free = bars + 3;  // [2] the products reading that stage are done
-  uint64_t* sa_full = bars + 5;  // S of a key tile is in tensor memory
-  uint64_t* p_ready = bars + 6;  // dS written (one arrival per compute thread)
-  uint64_t* sb_full = bars + 9;  // dP is in tensor memory
-  uint64_t* done = bars + 7;
-  uint64_t* drain = bars + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* qd_full = bars;       // Q and dO landed
+  uint64_t* kv_full = bars + 1;   // [2] K and V of a key tile landed
+  uint64_t* kv_free = bars + 3;   // [2] the products reading that stage are done
+  // [2] S of a key tile is in tensor memory, one barrier per S buffer: S of
+  // the next tile is issued before dS of this one is formed, so with one
+  // barrier for both it could complete twice before a waiter looks (across
+  // an item change, while the compute warps write dQ out)
+  uint64_t* sa_full = bars + 5;
+  uint64_t* p_ready = bars + 7;   // dS written (one arrival per compute thread)
+  uint64_t* done = bars + 8;      // every product of the item is done
+  uint64_t* drain = bars + 9;
+  uint64_t* sb_full = bars + 10;  // dP is in tensor memory
+  uint64_t* qd_empty = bars + 11; // the item's last products reading Q and dO are done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
   static_assert(2 * kB + D + kB <= 512, "two S buffers, dP and dQ in tensor memory");
   __shared__ int abort_s;
   volatile int* abort_flag = &abort_s;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-  // Under a causal mask the query tile is outermost, the last (longest)
-  // first; without one the query tiles of one (batch, head) are adjacent, so
-  // the blocks running together read the same key and value tiles.
-  const int nqt_all = p.Sqp / kB;
-  int qt, h, b;
-  if (p.causal) {
-    qt = nqt_all - 1 - static_cast<int>(blockIdx.x / (p.B * p.Hq));
-    h = (blockIdx.x / p.B) % p.Hq;
-    b = blockIdx.x % p.B;
-  } else {
-    qt = blockIdx.x % nqt_all;
-    h = (blockIdx.x / nqt_all) % p.Hq;
-    b = blockIdx.x / (nqt_all * p.Hq);
-  }
-  const int hk = h / (p.Hq / p.Hkv);
-  const int q0 = qt * kB;
-  SeqGeo sg;
-  // A query tile past its sequence's queries has nothing to write.
-  if (!seq_geo(p, b, sg, false) || q0 >= sg.Lq) return;
-  const int off = sg.Lk - sg.Lq;
-  // The key tiles the tile's rows see: the sink tiles, then the window's
-  // tiles from the first key above the first row's window bound up to the
-  // last key any row sees (causal bound, end of the keys).
-  int jhi = (sg.Lk - 1) / kB;
-  if (p.causal) {
-    const int qlast = min(q0 + kB - 1, sg.Lq - 1);
-    const int kmax = min(sg.Lk - 1, qlast + off);  // last key any row of the tile sees
-    jhi = kmax >= 0 ? kmax / kB : -1;
-  }
-  if (sg.Lk <= 0) jhi = -1;
-  int jlo = 0, sinkT = 0;
-  if (p.window > 0) {
-    const int lo = q0 + off - p.window;  // keys above lo are in the first row's window
-    jlo = lo < 0 ? 0 : (lo + 1) / kB;
-    sinkT = (p.n_sink + kB - 1) / kB;
-  }
-  const int ns = min(sinkT, jhi + 1);
-  const int nkt = jhi < 0 ? 0 : ns + max(0, jhi - max(jlo, sinkT) + 1);
-  // the n-th key tile walked: sink tiles first, then the window's range
-  auto tile_at = [&](int n) { return n < ns ? n : max(jlo, sinkT) + (n - ns); };
+  const int num_items = (p.Sqp / kB) * p.Hq * p.B;
 
   if (threadIdx.x == 0) {
     mbar_init(qd_full, 1);
+    mbar_init(qd_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_free[s], 1);
+      mbar_init(&sa_full[s], 1);
     }
-    mbar_init(sa_full, 1);
     mbar_init(sb_full, 1);
     mbar_init(p_ready, kComputeThreads);
     mbar_init(done, 1);
@@ -751,34 +861,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   auto stage = [&](int s) { return smem + C::kOffKV + s * 2 * C::kTile; };
-  // S of key tile t in one of two buffers: columns [0,128) or [384,512)
-  auto s_col = [&](int t) { return (t & 1) ? 3u * kB : 0u; };
+  // S of key tile u (counted over the CTA's items) in one of two buffers:
+  // columns [0,128) or [384,512)
+  auto s_col = [&](int u) { return (u & 1) ? 3u * kB : 0u; };
 
+  // Counters over the CTA's items: key tiles (one stage load, one set of
+  // products each) and items with key tiles (one Q / dO load each).
   if (warp == kWarpProd) {
     // ================================================================ producer
-    mbar_arrive_expect_tx_w(qd_full, 2 * C::kTile);
-#pragma unroll
-    for (int a = 0; a < C::kAtoms; ++a) {
-      tma_load_4d_w(sQ + a * C::kAtomBytes, &tmQ, qd_full, a * 64, h, sg.q_base + q0, sg.b_coord);
-      tma_load_4d_w(sDO + a * C::kAtomBytes, &tmDO, qd_full, a * 64, h, sg.q_base + q0,
-                    sg.b_coord);
-    }
-    int issued = 0;
-    for (int t = 0; t < nkt; ++t) {
-      const int s = t & 1;
-      if (t >= 2 && !warp_wait(&kv_free[s], ((t >> 1) - 1) & 1, abort_flag, p)) break;
-      uint8_t* st = stage(s);
-      mbar_arrive_expect_tx_w(&kv_full[s], 2 * C::kTile);
+    int qd_loads = 0, issued = 0;
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int item = bwd_item_at(n, num_items);
+      if (item < 0) break;
+      QItem it;
+      if (!q_item(p, item, it) || it.nkt == 0) continue;
+      // Q and dO are single-buffered: the previous item's last S and dP must
+      // be done with them
+      if (qd_loads > 0 && !warp_wait(qd_empty, (qd_loads - 1) & 1, abort_flag, p)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx_w(qd_full, 2 * C::kTile);
 #pragma unroll
       for (int a = 0; a < C::kAtoms; ++a) {
-        const int kr = sg.k_base + tile_at(t) * kB;
-        tma_load_4d_w(st + a * C::kAtomBytes, &tmK, &kv_full[s], a * 64, hk, kr, sg.b_coord);
-        tma_load_4d_w(st + C::kTile + a * C::kAtomBytes, &tmV, &kv_full[s], a * 64, hk, kr,
-                      sg.b_coord);
+        tma_load_4d_w(sQ + a * C::kAtomBytes, &tmQ, qd_full, a * 64, it.h,
+                      it.sg.q_base + it.q0, it.sg.b_coord);
+        tma_load_4d_w(sDO + a * C::kAtomBytes, &tmDO, qd_full, a * 64, it.h,
+                      it.sg.q_base + it.q0, it.sg.b_coord);
       }
-      issued = t + 1;
+      ++qd_loads;
+      for (int t = 0; t < it.nkt; ++t) {
+        const int s = issued & 1;
+        if (issued >= 2 && !warp_wait(&kv_free[s], ((issued >> 1) - 1) & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = stage(s);
+        mbar_arrive_expect_tx_w(&kv_full[s], 2 * C::kTile);
+        const int kr = it.sg.k_base + it.tile_at(t) * kB;
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a) {
+          tma_load_4d_w(st + a * C::kAtomBytes, &tmK, &kv_full[s], a * 64, it.hk, kr,
+                        it.sg.b_coord);
+          tma_load_4d_w(st + C::kTile + a * C::kAtomBytes, &tmV, &kv_full[s], a * 64, it.hk, kr,
+                        it.sg.b_coord);
+        }
+        ++issued;
+      }
     }
-    warp_wait(qd_full, 0, nullptr, p);
+    if (qd_loads > 0) warp_wait(qd_full, (qd_loads - 1) & 1, nullptr, p);
     for (int s = 0; s < 2; ++s) {
       const int n_s = (issued - s + 1) / 2;
       if (n_s > 0) warp_wait(&kv_full[s], (n_s - 1) & 1, nullptr, p);
@@ -786,150 +918,188 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kWarpIssue) {
     // ================================================================ MMA issuer
     // Per key tile t the pipe runs dP(t), S(t+1), dQ(t): S of the next tile
-    // goes to the other S buffer while the compute warps form dS(t).
+    // goes to the other S buffer while the compute warps form dS(t).  An
+    // item's first dQ overwrites the accumulator: it waits for the dS arrival
+    // the compute warps make after reading the previous item's dQ out.
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, kB, false);
     constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, true);
     const uint64_t dq = sdesc_sw128(smem_addr(sQ), 16, 1024);
     const uint64_t ddo = sdesc_sw128(smem_addr(sDO), 16, 1024);
     const uint32_t tP = tmem + kB, tDQ = tmem + 2 * kB;
-    auto issue_s = [&](int t) -> bool {  // S(t) = Q K(t)^T
-      const int s = t & 1;
-      if (!warp_wait(&kv_full[s], (t >> 1) & 1, abort_flag, p)) return false;
+    int U = 0;    // key tiles of earlier items
+    int qdi = 0;  // items with key tiles before this one
+    auto issue_s = [&](int u) -> bool {  // S(u) = Q K(u)^T
+      const int s = u & 1;
+      if (!warp_wait(&kv_full[s], (u >> 1) & 1, abort_flag, p)) return false;
       tc_fence_after_sync();
       const uint64_t dkk = sdesc_sw128(smem_addr(stage(s)), 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
-        mma_bf16_ss_w(tmem + s_col(t), dq + ko, dkk + ko, idesc_s, kk > 0 ? 1u : 0u);
+        mma_bf16_ss_w(tmem + s_col(u), dq + ko, dkk + ko, idesc_s, kk > 0 ? 1u : 0u);
       }
-      mma_commit_w(sa_full);
+      mma_commit_w(&sa_full[u & 1]);
       return true;
     };
-    bool ok = warp_wait(qd_full, 0, abort_flag, p);
-    if (ok) tc_fence_after_sync();
-    if (ok && nkt > 0) ok = issue_s(0);
-    for (int t = 0; ok && t < nkt; ++t) {
-      const int s = t & 1;
-      const uint32_t st = smem_addr(stage(s));
-      const uint64_t dvk = sdesc_sw128(st + C::kTile, 16, 1024);
-      // dP(t) = dO V(t)^T (M = queries, N = keys, K = d)
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int item = bwd_item_at(n, num_items);
+      if (item < 0) break;
+      QItem it;
+      if (!q_item(p, item, it) || it.nkt == 0) continue;
+      const int nt = it.nkt;
+      ok = warp_wait(qd_full, qdi & 1, abort_flag, p);
+      if (ok) tc_fence_after_sync();
+      if (ok) ok = issue_s(U);
+      for (int t = 0; ok && t < nt; ++t) {
+        const int u = U + t;
+        const int s = u & 1;
+        const uint32_t st = smem_addr(stage(s));
+        const uint64_t dvk = sdesc_sw128(st + C::kTile, 16, 1024);
+        // dP(t) = dO V(t)^T (M = queries, N = keys, K = d)
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
-        mma_bf16_ss_w(tP, ddo + ko, dvk + ko, idesc_s, kk > 0 ? 1u : 0u);
-      }
-      mma_commit_w(sb_full);
-      if (t + 1 < nkt && !issue_s(t + 1)) {
-        ok = false;
-        break;
-      }
-      if (!warp_wait(p_ready, t & 1, abort_flag, p)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      // dQ += dS K(t) (A = dS from tensor memory, K = keys; B = K(t) read along d)
-      const uint64_t dkm = sdesc_sw128(st, C::kAtomBytes, 1024);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
+          mma_bf16_ss_w(tP, ddo + ko, dvk + ko, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_w(sb_full);
+        // the item's last products reading Q (its last S, issued before) and
+        // dO: the producer may load the next item's Q and dO
+        if (t + 1 == nt) mma_commit_w(qd_empty);
+        if (t + 1 < nt && !issue_s(u + 1)) {
+          ok = false;
+          break;
+        }
+        if (!warp_wait(p_ready, u & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        // dQ += dS K(t) (A = dS from tensor memory, K = keys; B = K(t) read along d)
+        const uint64_t dkm = sdesc_sw128(st, C::kAtomBytes, 1024);
 #pragma unroll
-      for (int kk = 0; kk < kB / 16; ++kk)
-        mma_bf16_ts_w(tDQ, tP + packed_col(kk), dkm + kk * (2048 >> 4), idesc_g,
-                      (t > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_w(&kv_free[s]);
+        for (int kk = 0; kk < kB / 16; ++kk)
+          mma_bf16_ts_w(tDQ, tP + packed_col(kk), dkm + kk * (2048 >> 4), idesc_g,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_w(&kv_free[s]);
+      }
+      if (ok) mma_commit_w(done);
+      U += nt;
+      ++qdi;
     }
-    mma_commit_w(done);
     mma_commit_w(drain);
     warp_wait(drain, 0, nullptr, p);
   } else if (warp < kComputeWarps) {
     // ================================================================ compute warps
     const int wq = warp & 3, wh = warp >> 2;  // lane quarter, column half
     const int r = wq * 32 + lane;
-    const int q_idx = q0 + r;
     const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const size_t vrow = (static_cast<size_t>(b) * p.Hq + h) * p.Sqp + q_idx;
-    const float nlse2 = p.lse2[vrow];  // -LSE2; -inf past Sq: every P of the row is 0
-    const float ndval = p.dvec[vrow];  // -D
-    const uint64_t sc2 = pf2(p.scale2, p.scale2), nl2 = pf2(nlse2, nlse2), nd2 = pf2(ndval, ndval);
+    const uint64_t sc2 = pf2(p.scale2, p.scale2);
+    int U = 0;    // key tiles of earlier items
+    int qdi = 0;  // items with key tiles before this one
     bool ok = true;
-    for (int t = 0; t < nkt; ++t) {
-      // P of this warp's 64 columns from S(t), while dQ(t-1) and dP(t) run
-      if (!warp_wait(sa_full, t & 1, abort_flag, p)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      // column c (key j*128 + c) is visible to this row iff c <= cmax (the
-      // key tail, causal) and, with a window, c > cmin or the key is a sink
-      const int j = tile_at(t);
-      int cmax = sg.Lk - 1 - j * kB;
-      if (p.causal) cmax = min(cmax, q_idx + off - j * kB);
-      const int cmin = p.window > 0 ? q_idx + off - p.window - j * kB : -(1 << 30);
-      const int csink = p.n_sink - j * kB;  // columns below are sink keys
-      uint64_t pp[32];  // P in fp32 pairs
-      {
-        uint32_t ra[64];
-        tmem_ld_x32(taddr + s_col(t) + 64 * wh, ra);
-        tmem_ld_x32(taddr + s_col(t) + 64 * wh + 32, ra + 32);
-        tmem_ld_wait_b();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          reg_fence_b(ra[2 * e]);
-          reg_fence_b(ra[2 * e + 1]);
-          float x0, x1;
-          pf2_split(pf2_fma(pf2(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])), sc2, nl2),
-                    x0, x1);
-          pp[e] = pf2(ex2_approx(x0), ex2_approx(x1));
+    for (int n = 0; ok; ++n) {
+      const int item = bwd_item_at(n, num_items);
+      if (item < 0) break;
+      QItem it;
+      if (!q_item(p, item, it)) continue;
+      const int nt = it.nkt;
+      const int off = it.sg.Lk - it.sg.Lq;
+      const int q_idx = it.q0 + r;
+      const size_t vrow = (static_cast<size_t>(it.b) * p.Hq + it.h) * p.Sqp + q_idx;
+      const float nlse2 = p.lse2[vrow];  // -LSE2; -inf past Sq: every P of the row is 0
+      const float ndval = p.dvec[vrow];  // -D
+      const uint64_t nl2 = pf2(nlse2, nlse2), nd2 = pf2(ndval, ndval);
+      for (int t = 0; t < nt; ++t) {
+        const int u = U + t;
+        // P of this warp's 64 columns from S(t), while dQ(t-1) and dP(t) run
+        if (!warp_wait(&sa_full[u & 1], (u >> 1) & 1, abort_flag, p)) {
+          ok = false;
+          break;
         }
-      }
-      // dS = P (dP - D) once dP(t) is in tensor memory
-      if (!warp_wait(sb_full, t & 1, abort_flag, p)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      {
-        uint32_t rb[64];
-        tmem_ld_x32(taddr + kB + 64 * wh, rb);
-        tmem_ld_x32(taddr + kB + 64 * wh + 32, rb + 32);
-        tmem_ld_wait_b();
+        tc_fence_after_sync();
+        // column c (key j*128 + c) is visible to this row iff c <= cmax (the
+        // key tail, causal) and, with a window, c > cmin or the key is a sink
+        const int j = it.tile_at(t);
+        int cmax = it.sg.Lk - 1 - j * kB;
+        if (p.causal) cmax = min(cmax, q_idx + off - j * kB);
+        const int cmin = p.window > 0 ? q_idx + off - p.window - j * kB : -(1 << 30);
+        const int csink = p.n_sink - j * kB;  // columns below are sink keys
+        uint64_t pp[32];  // P in fp32 pairs
+        {
+          uint32_t ra[64];
+          tmem_ld_x32(taddr + s_col(u) + 64 * wh, ra);
+          tmem_ld_x32(taddr + s_col(u) + 64 * wh + 32, ra + 32);
+          tmem_ld_wait_b();
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int c4 = 2 * wh + j;
-          float pf[32];
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            reg_fence_b(rb[32 * j + 2 * e]);
-            reg_fence_b(rb[32 * j + 2 * e + 1]);
-            const uint64_t g2 = pf2_add(
-                pf2(__uint_as_float(rb[32 * j + 2 * e]), __uint_as_float(rb[32 * j + 2 * e + 1])),
-                nd2);
-            pf2_split(pf2_mul(pp[16 * j + e], g2), pf[2 * e], pf[2 * e + 1]);
+          for (int e = 0; e < 32; ++e) {
+            reg_fence_b(ra[2 * e]);
+            reg_fence_b(ra[2 * e + 1]);
+            float x0, x1;
+            pf2_split(pf2_fma(pf2(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])),
+                              sc2, nl2),
+                      x0, x1);
+            pp[e] = pf2(ex2_approx(x0), ex2_approx(x1));
           }
-          if (cmax < 32 * c4 + 31 || (cmin >= 32 * c4 && csink < 32 * c4 + 32)) {
-            // a chunk the diagonal, the key tail or the window's edge crosses
+        }
+        // dS = P (dP - D) once dP(t) is in tensor memory
+        if (!warp_wait(sb_full, u & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        {
+          uint32_t rb[64];
+          tmem_ld_x32(taddr + kB + 64 * wh, rb);
+          tmem_ld_x32(taddr + kB + 64 * wh + 32, rb + 32);
+          tmem_ld_wait_b();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int c = 32 * c4 + e;
-              if (c > cmax || (c <= cmin && c >= csink)) pf[e] = 0.f;
+          for (int jj = 0; jj < 2; ++jj) {
+            const int c4 = 2 * wh + jj;
+            float pf[32];
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              reg_fence_b(rb[32 * jj + 2 * e]);
+              reg_fence_b(rb[32 * jj + 2 * e + 1]);
+              const uint64_t g2 = pf2_add(pf2(__uint_as_float(rb[32 * jj + 2 * e]),
+                                              __uint_as_float(rb[32 * jj + 2 * e + 1])),
+                                          nd2);
+              pf2_split(pf2_mul(pp[16 * jj + e], g2), pf[2 * e], pf[2 * e + 1]);
             }
+            if (cmax < 32 * c4 + 31 || (cmin >= 32 * c4 && csink < 32 * c4 + 32)) {
+              // a chunk the diagonal, the key tail or the window's edge crosses
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const int c = 32 * c4 + e;
+                if (c > cmax || (c <= cmin && c >= csink)) pf[e] = 0.f;
+              }
+            }
+            pack32(pf, pk);
+            tmem_st_x16(taddr + kB + 64 * wh + 16 * jj, pk);
           }
-          pack32(pf, pk);
-          tmem_st_x16(taddr + kB + 64 * wh + 16 * j, pk);
         }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(p_ready);
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(p_ready);
-    }
-    if (ok && warp_wait(done, 0, abort_flag, p)) {
-      tc_fence_after_sync();
-      const bool valid = q_idx < sg.Lq;
-      __nv_bfloat16* dst = p.dq + ((static_cast<size_t>(sg.q_row0) + q_idx) * p.Hq + h) * D;
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (nt > 0) {
+        if (!warp_wait(done, qdi & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+      }
+      const bool valid = q_idx < it.sg.Lq;
+      __nv_bfloat16* dst =
+          p.dq + ((static_cast<size_t>(it.sg.q_row0) + q_idx) * p.Hq + it.h) * D;
       constexpr int kHalfChunks = D / 64;
 #pragma unroll 1
       for (int c = wh * kHalfChunks; c < (wh + 1) * kHalfChunks; ++c) {
         uint32_t ra[32];
-        if (nkt > 0) {
+        if (nt > 0) {
           tmem_ld_x32(taddr + 2 * kB + 32 * c, ra);
           tmem_ld_wait_b();
         }
@@ -937,7 +1107,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           reg_fence_b(ra[e]);
-          f[e] = nkt > 0 ? __uint_as_float(ra[e]) * p.scale : 0.f;
+          f[e] = nt > 0 ? __uint_as_float(ra[e]) * p.scale : 0.f;
         }
         uint32_t pk[16];
         pack32(f, pk);
@@ -948,6 +1118,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
         }
       }
+      // The next item's first dQ waits for this warp's next arrival, made
+      // after the reads of the accumulator above.
+      tc_fence_before_sync();
+      U += nt;
+      if (nt > 0) ++qdi;
     }
   }
   tc_fence_before_sync();
@@ -999,14 +1174,24 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t stream) {
   attn_bwd_rowstat_kernel<D><<<1216, 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // Dense calls: persistent grids (one CTA per SM; every item is about the
+  // same work, or ordered longest first under a causal mask).  Packed calls:
+  // one CTA per item, so that the hardware hands the next item to whichever
+  // SM frees first (item costs follow the sequence lengths).
+  const bool packed = a.cu_q != nullptr;
+  auto grid_of = [&](long long items) {
+    return static_cast<unsigned>(packed ? items
+                                        : std::min<long long>(items, std::max(a.num_sms, 1)));
+  };
   if (a.Skv > 0) {
-    dim3 g1(((a.Skv + kB - 1) / kB) * a.Hkv * a.B);
-    attn_bwd_dkdv_kernel<D><<<g1, kBwdThreads, C::kLaunchKV, stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO,
-                                                                     p);
+    const long long n1 = static_cast<long long>((a.Skv + kB - 1) / kB) * a.Hkv * a.B;
+    attn_bwd_dkdv_kernel<D><<<grid_of(n1), kBwdThreads, C::kLaunchKV, stream>>>(
+        a.tmQ, a.tmK, a.tmV, a.tmDO, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  dim3 g2((p.Sqp / kB) * a.Hq * a.B);
-  attn_bwd_dq_kernel<D><<<g2, kBwdThreads, C::kLaunchQ, stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO, p);
+  const long long n2 = static_cast<long long>(p.Sqp / kB) * a.Hq * a.B;
+  attn_bwd_dq_kernel<D><<<grid_of(n2), kBwdThreads, C::kLaunchQ, stream>>>(a.tmQ, a.tmK, a.tmV,
+                                                                          a.tmDO, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.sink != nullptr) {
     attn_bwd_dsink_kernel<<<a.Hq, kSinkThreads, 0, stream>>>(p.lse2, p.dvec, a.sink, a.dsink, a.B,

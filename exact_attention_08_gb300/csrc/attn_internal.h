@@ -73,6 +73,7 @@ struct BwdLaunch {
   float scale;
   int causal, window, n_sink;
   int* status;
+  int num_sms;  // SMs of the device (the persistent grids)
 };
 
 // Bytes of workspace the backward needs (two fp32 row vectors per query row,
