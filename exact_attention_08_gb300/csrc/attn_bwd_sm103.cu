@@ -112,6 +112,7 @@ struct BwdParams {
   __nv_bfloat16* dq;         // [B, Sq, Hq, d]
   __nv_bfloat16* dk;         // [B, Skv, Hkv, d]
   __nv_bfloat16* dv;
+  int v8;                    // dq, dk and dv start on 32 bytes: 32-byte stores
   int B, Hq, Hkv, Sq, Skv, Sqp, d;  // Sq, Skv: the longest sequence when packed
   int total_q, total_k;             // packed token counts
   float scale, scale2;
@@ -306,6 +307,22 @@ __device__ __forceinline__ void pack32(const float* f, uint32_t* pk) {
   for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
 }
 
+// 32 bf16 (16 pairs) of one row to global memory: two 32-byte stores when
+// the row is 32-byte aligned (each thread stores its own row, so a store
+// instruction touches 32 rows and fewer, wider ones cost the L1 less), else
+// four 16-byte stores.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t* pk, int v8) {
+  if (v8) {
+    st_global_v8(dst, pk);
+    st_global_v8(dst + 16, pk + 8);
+  } else {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int v4 = 0; v4 < 4; ++v4)
+      d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+  }
+}
+
 // K-step kk of a K-major SW128 operand: 32 bytes along a row inside a
 // 128-byte atom, then the next atom column.
 template <int kAtomBytes>
@@ -463,6 +480,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       it.sg.k_base + it.k0, it.sg.b_coord);
       }
       ++kv_loads;
+      // Warm L2 with the next item's K and V: they are single-buffered, so
+      // their load waits for this item's last products and is then on the
+      // way to the next item's first S^T.
+      {
+        KvItem nx;
+        const int nitem = bwd_item_at(n + 1, num_items);
+        if (nitem >= 0 && kv_item(p, nitem, nx) && nx.ntiles > 0) {
+#pragma unroll
+          for (int a = 0; a < C::kAtoms; ++a) {
+            tma_prefetch_4d_w(&tmK, a * 64, nx.hk, nx.sg.k_base + nx.k0, nx.sg.b_coord);
+            tma_prefetch_4d_w(&tmV, a * 64, nx.hk, nx.sg.k_base + nx.k0, nx.sg.b_coord);
+          }
+        }
+      }
       for (int t = 0; t < it.ntiles; ++t) {
         const int s = issued & 1;
         if (issued >= 2 && !warp_wait(&q_free[s], ((issued >> 1) - 1) & 1, abort_flag, p)) {
@@ -728,12 +759,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           uint32_t pk[16];
           pack32(f, pk);
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-          }
+          if (valid) store_row32(dst + 32 * c, pk, p.v8);
         }
       }
       // The next item's first dV and dK wait for this warp's next arrivals,
@@ -891,6 +917,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       it.sg.q_base + it.q0, it.sg.b_coord);
       }
       ++qd_loads;
+      // Warm L2 with the next item's Q and dO (single-buffered, as K and V
+      // in the dK/dV kernel).
+      {
+        QItem nx;
+        const int nitem = bwd_item_at(n + 1, num_items);
+        if (nitem >= 0 && q_item(p, nitem, nx) && nx.nkt > 0) {
+#pragma unroll
+          for (int a = 0; a < C::kAtoms; ++a) {
+            tma_prefetch_4d_w(&tmQ, a * 64, nx.h, nx.sg.q_base + nx.q0, nx.sg.b_coord);
+            tma_prefetch_4d_w(&tmDO, a * 64, nx.h, nx.sg.q_base + nx.q0, nx.sg.b_coord);
+          }
+        }
+      }
       for (int t = 0; t < it.nkt; ++t) {
         const int s = issued & 1;
         if (issued >= 2 && !warp_wait(&kv_free[s], ((issued >> 1) - 1) & 1, abort_flag, p)) {
@@ -1111,12 +1150,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         uint32_t pk[16];
         pack32(f, pk);
-        if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-        }
+        if (valid) store_row32(dst + 32 * c, pk, p.v8);
       }
       // The next item's first dQ waits for this warp's next arrival, made
       // after the reads of the accumulator above.
@@ -1159,6 +1193,8 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t stream) {
   p.dq = static_cast<__nv_bfloat16*>(a.dq);
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.v8 = (reinterpret_cast<uintptr_t>(a.dq) | reinterpret_cast<uintptr_t>(a.dk) |
+          reinterpret_cast<uintptr_t>(a.dv)) % 32 == 0;
   p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
