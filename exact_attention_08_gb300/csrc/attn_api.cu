@@ -574,7 +574,8 @@ ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o
 ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
   if (B < 0 || Hq <= 0 || d <= 0 || num_splits <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * num_splits;
-  return rows * d * sizeof(float) + rows * sizeof(float);
+  // split outputs, split log-sum-exps, the request order
+  return rows * d * sizeof(float) + rows * sizeof(float) + static_cast<size_t>(B) * sizeof(int);
 }
 
 }  // extern "C"
@@ -630,6 +631,7 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   a.seqlens = seqlens;
   a.ws_o = static_cast<float*>(workspace);
   a.ws_lse = static_cast<float*>(workspace) + rows * d;
+  a.order = reinterpret_cast<int*>(a.ws_lse + rows);
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;

@@ -28,7 +28,10 @@
 // (three warps, a 48 KB ring at d = 128) run four to an SM, so that one CTA's
 // ramp-up and drain overlap the others' streaming: 192 KB of pages in flight
 // per SM (measured against two CTAs of five warps and a 64 KB ring: 0.845
-// against 0.745 of the copy bandwidth).
+// against 0.745 of the copy bandwidth).  A one-block kernel first orders the
+// requests longest first, and the split kernel takes its request from that
+// order, so that the short requests' CTAs fill the end of the grid instead
+// of a long one running alone there.
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -67,12 +70,73 @@ struct DecCfg {
   static constexpr int kSmemBytes = kOffBar + 2 * kStagesDec * 8 + 1024;
 };
 
+// Requests longest first: a counting sort of the batch on its page counts
+// (descending; when there are more page counts than buckets, buckets of
+// equal width), one block.  The split kernel takes its request from this
+// order, so the hardware hands out the longest requests' CTAs first and the
+// short ones fill the end (the same result whatever the order: every CTA
+// computes its own split, and the merge order is fixed).
+constexpr int kOrderBuckets = 4096;
+constexpr int kOrderThreads = 1024;
+__global__ void __launch_bounds__(kOrderThreads)
+    attn_decode_order_kernel(const int* __restrict__ seqlens, int B, int max_pages, int* order) {
+  __shared__ int cnt[kOrderBuckets];
+  __shared__ int wsum[kOrderThreads / 32];
+  const int t = threadIdx.x;
+  const int nb = min(max_pages + 1, kOrderBuckets);
+  for (int i = t; i < kOrderBuckets; i += kOrderThreads) cnt[i] = 0;
+  __syncthreads();
+  auto bucket = [&](int b) {  // bucket 0: the most pages
+    const int L = seqlens[b];
+    const int np = L <= 0 ? 0 : min((L + 15) / 16, max_pages);
+    const long long k = static_cast<long long>(max_pages - np) * nb / (max_pages + 1);
+    return static_cast<int>(k < nb - 1 ? k : nb - 1);
+  };
+  for (int b = t; b < B; b += kOrderThreads) atomicAdd(&cnt[bucket(b)], 1);
+  __syncthreads();
+  // Exclusive scan of the counts: four buckets a thread, then across lanes
+  // and warps.
+  constexpr int kPer = kOrderBuckets / kOrderThreads;
+  int local[kPer], run = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    local[j] = run;
+    run += cnt[t * kPer + j];
+  }
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if ((t & 31) >= o) incl += v;
+  }
+  if ((t & 31) == 31) wsum[t >> 5] = incl;
+  __syncthreads();
+  if (t < 32) {
+    const int v = wsum[t];
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (t >= o) x += y;
+    }
+    wsum[t] = x - v;
+  }
+  __syncthreads();
+  const int base = wsum[t >> 5] + (incl - run);
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) cnt[t * kPer + j] = base + local[j];
+  __syncthreads();
+  for (int b = t; b < B; b += kOrderThreads) order[atomicAdd(&cnt[bucket(b)], 1)] = b;
+}
+
 struct DecParams {
   const __nv_bfloat16* q;
   const int* page_table;
   const int* seqlens;
   float* ws_o;
   float* ws_lse;
+  const int* order;  // [B] requests longest first (the grid's z order)
   int B, Hq, Hkv, G, n_hchunks, max_pages, num_pages, num_splits;
   float scale, scale2;
   uint64_t wait_limit_ns;
@@ -124,7 +188,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
   const int split = blockIdx.x;
   const int hkv = blockIdx.y / p.n_hchunks;
   const int hchunk = blockIdx.y % p.n_hchunks;
-  const int b = blockIdx.z;
+  // Launched as a programmatic dependent of the order kernel: the launch
+  // overlaps it, and this waits for its result.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = p.order[blockIdx.z];
   const int g0 = hchunk * kHeadsPerCta;                  // first group member served
   const int nh = min(kHeadsPerCta, p.G - g0);            // query heads served
   const int h0 = hkv * p.G + g0;                         // first query head served
@@ -394,7 +461,10 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   const int split = blockIdx.x;
   const int hkv = blockIdx.y / p.n_hchunks;
   const int hchunk = blockIdx.y % p.n_hchunks;
-  const int b = blockIdx.z;
+  // Launched as a programmatic dependent of the order kernel: the launch
+  // overlaps it, and this waits for its result.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = p.order[blockIdx.z];
   const int g0 = hchunk * kHeadsPerCta;
   const int nh = min(kHeadsPerCta, p.G - g0);
   const int h0 = hkv * p.G + g0;
@@ -642,6 +712,26 @@ cudaError_t launch_combine(const DecodeLaunch& a, cudaStream_t stream) {
                             static_cast<__nv_bfloat16*>(a.o), a.lse, a.num_splits, a.sink, a.Hq);
 }
 
+// The request order, then the split kernel as its programmatic dependent.
+template <typename Kernel>
+cudaError_t launch_ordered(const DecodeLaunch& a, Kernel kernel, dim3 grid, size_t smem,
+                           const DecParams& p, cudaStream_t stream) {
+  attn_decode_order_kernel<<<1, kOrderThreads, 0, stream>>>(a.seqlens, a.B, a.max_pages, a.order);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a.tmK, a.tmV, p);
+}
+
 template <int D>
 cudaError_t launch_dec(const DecodeLaunch& a, cudaStream_t stream) {
   using C = DecCfg<D>;
@@ -671,8 +761,10 @@ cudaError_t launch_dec(const DecodeLaunch& a, cudaStream_t stream) {
   p.wait_limit_ns = kWaitLimitNs;
   p.status = a.status;
   dim3 grid(a.num_splits, a.Hkv * p.n_hchunks, a.B);
-  attn_decode_split_kernel<D><<<grid, kDecThreads, C::kSmemBytes, stream>>>(a.tmK, a.tmV, p);
-  cudaError_t e = cudaGetLastError();
+  p.order = a.order;
+  cudaError_t e =
+      launch_ordered(a, attn_decode_split_kernel<D>, grid, C::kSmemBytes, p, stream);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = launch_combine<D>(a, stream);
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -707,8 +799,9 @@ cudaError_t launch_dec256(const DecodeLaunch& a, cudaStream_t stream) {
   p.wait_limit_ns = kWaitLimitNs;
   p.status = a.status;
   dim3 grid(a.num_splits, a.Hkv * p.n_hchunks, a.B);
-  attn_decode_split256_kernel<<<grid, kDecThreads, C::kSmemBytes, stream>>>(a.tmK, a.tmV, p);
-  cudaError_t e = cudaGetLastError();
+  p.order = a.order;
+  cudaError_t e = launch_ordered(a, attn_decode_split256_kernel, grid, C::kSmemBytes, p, stream);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = launch_combine<256>(a, stream);
   return e != cudaSuccess ? e : cudaGetLastError();

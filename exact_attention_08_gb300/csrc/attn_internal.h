@@ -49,6 +49,7 @@ struct DecodeLaunch {
   const int* seqlens;
   float* ws_o;    // [B, Hq, S, d] fp32 split outputs (normalised)
   float* ws_lse;  // [B, Hq, S] fp32 split log-sum-exps (natural log)
+  int* order;     // [B] workspace: the requests longest first
   int B, Hq, Hkv, d, page, max_pages, num_pages, num_splits;
   float scale;
   int* status;

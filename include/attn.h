@@ -266,7 +266,8 @@ ATTN_API int attn_bwd_ex_sink(const void* q, const void* k, const void* v, const
 
 /*
  * Bytes of device workspace attn_decode_paged needs for these sizes (split
- * partial outputs and log-sum-exps, fp32).  0 on invalid sizes.
+ * partial outputs and log-sum-exps, fp32, and the batch's requests ordered
+ * longest first, int32 [B]).  0 on invalid sizes.
  */
 ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits);
 

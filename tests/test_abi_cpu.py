@@ -73,7 +73,8 @@ def test_decode_argument_errors_without_gpu():
     L = ea.lib
     buf = ctypes.create_string_buffer(64)
     p16 = (ctypes.cast(buf, ctypes.c_void_p).value + 15) & ~15
-    assert L.attn_decode_workspace_size(64, 32, 128, 8) == 64 * 32 * 8 * (128 + 1) * 4
+    # split outputs and log-sum-exps (fp32), the request order (int32)
+    assert L.attn_decode_workspace_size(64, 32, 128, 8) == 64 * 32 * 8 * (128 + 1) * 4 + 64 * 4
     assert L.attn_decode_workspace_size(-1, 32, 128, 8) == 0
     args = [p16, p16, p16, p16, p16, p16, None, 2, 8, 2, 128, 16, 4, 10, 8, 0.1, p16, 1 << 20, None]
     bad = list(args)
