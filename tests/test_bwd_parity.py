@@ -329,3 +329,39 @@ def test_logit_sink_without_queries(ea):
     torch.cuda.synchronize()
     assert torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
     assert torch.count_nonzero(ds) == 0
+
+
+PERSISTENT_CASES = [
+    # (seed, B, Hq, Hkv, Sq, Skv, causal, window, n_sink): more key tiles and
+    # query tiles than SMs, so every CTA of the persistent grids walks
+    # several items, some of which have no tile to process
+    (151, 4, 8, 8, 1500, 1024, True, 0, 0),     # Sq > Skv: query tiles with no key
+    (152, 4, 8, 4, 300, 2048, True, 100, 2),    # key tiles no query sees (window)
+]
+
+
+@pytest.mark.parametrize("case", PERSISTENT_CASES, ids=[f"seed{c[0]}" for c in PERSISTENT_CASES])
+def test_persistent_items(ea, case):
+    """Dense calls large enough that the persistent dK/dV and dQ grids give
+    each CTA several items, empty ones among them, against the oracle."""
+    seed, B, Hq, Hkv, Sq, Skv, causal, window, n_sink = case
+    x = workloads.dense_inputs(seed, B, Hq, Hkv, Sq, Skv, 128, causal, window, n_sink)
+    g = workloads.grad_output(seed + 50, x.q.shape)
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    o, lse = ea.attn_fwd_ex(q, k, v, causal=causal, window=window, n_sink=n_sink, scale=x.scale)
+    dq, dk, dv = ea.attn_bwd_ex(q, k, v, o, lse, g.cuda(), causal=causal, window=window,
+                                n_sink=n_sink, scale=x.scale)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    rq, rk, rv = oracle.attn_bwd(np64(x.q), np64(x.k), np64(x.v), np64(g), x.scale, causal, window,
+                                 n_sink)
+    for a, b, n in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        _check(a, b, f"persistent seed {seed} {n}")
+    # exact zeros where nothing is seen: query rows before the first key,
+    # keys no query's window reaches
+    if Sq > Skv:
+        assert torch.count_nonzero(dq[:, :Sq - Skv]) == 0
+    if window > 0:
+        first_seen = Skv - Sq - window + 1  # the first window key of query 0
+        assert torch.count_nonzero(dk[:, n_sink:first_seen]) == 0
+        assert torch.count_nonzero(dv[:, n_sink:first_seen]) == 0
