@@ -227,3 +227,12 @@ def test_full_size_sampled(ea, causal):
     err = _check(ea, x, rows=sample_rows(2048), what=f"d256 full c={causal}")
     print(f"d256 full causal={causal}: max |dO| {err[0]:.2e}, max |dLSE| {err[1]:.2e}, "
           f"{err[2]} elements with |O| >= 4")
+
+
+def test_persistent_items_without_keys(ea):
+    """More Q tiles than SMs with Sq > Skv (causal): the persistent grid's CTAs
+    walk items whose rows see no key (O = 0, LSE = -inf) between ones that
+    do; sampled rows against the oracle, the masked rows checked bit for bit."""
+    x = workloads.dense_inputs(229, 2, 16, 8, 1200, 600, 256, True)
+    rows = sample_rows(1200, seed=229)
+    _check(ea, x, rows=rows, what="d256 persistent, rows without keys")
