@@ -1309,7 +1309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_x32(taddr + colO, oa);
           tmem_ld_wait();
         }
-#pragma unroll
+        // Not unrolled: the epilogue runs once per item, and as straight-line
+        // code it missed the instruction cache chunk after chunk (measured:
+        // rolled, the window call 102.7 -> 100.4 us, GQA causal 194.5 -> 192.0).
+#pragma unroll 1
         for (int c = 0; c < D / 32; c += 2) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) reg_fence(oa[e]);
