@@ -297,16 +297,22 @@ __global__ void __launch_bounds__(kThr, 1)
       // lane pp (pages past the sequence's last are replaced by that last
       // page, whose rows are masked; an index outside the pool is reported
       // and page 0 read instead).
-      auto page_of = [&](int j) -> int {
+      // Each tile's pages are read from the page table two tiles ahead of
+      // its loads (lookup) and checked when used (checked); the K and V
+      // loads of a tile share them.
+      auto lookup = [&](int n) -> int {
         int phys = 0;
-        if (lane < kPagesPerTile) {
+        if (kPaged && n < N && lane < kPagesPerTile) {
           const int np = (w.Lk + kPage - 1) / kPage;
-          const int lp = min(j * kPagesPerTile + lane, np - 1);
+          const int lp = min(tile_at(w, n) * kPagesPerTile + lane, np - 1);
           phys = p.page_table[static_cast<size_t>(w.bseq) * p.max_pages + lp];
-          if (phys < 0 || phys >= p.num_pages) {
-            atomicOr(p.status, kStatusBadInput);
-            phys = 0;
-          }
+        }
+        return phys;
+      };
+      auto checked = [&](int phys) -> int {
+        if (kPaged && lane < kPagesPerTile && (phys < 0 || phys >= p.num_pages)) {
+          atomicOr(p.status, kStatusBadInput);
+          phys = 0;
         }
         return phys;
       };
@@ -325,9 +331,8 @@ __global__ void __launch_bounds__(kThr, 1)
       };
       // Key tile n of the item; for n = 0 the item's Q atoms go first, each
       // once the previous item's last S has read it.
-      auto load_k = [&](int n) {
+      auto load_k = [&](int n, int phys) {
         const int j = tile_at(w, n);
-        const int phys = kPaged ? page_of(j) : 0;
         for (int a = 0; a < kNAtom; ++a) {
           if (n == 0) {
             if (q_loads > 0 && !wwait(&q_empty[a], (q_loads - 1) & 1, abort_flag, p))
@@ -346,24 +351,32 @@ __global__ void __launch_bounds__(kThr, 1)
         if (n == 0) ++q_loads;
         return true;
       };
-      ok = load_k(0);
+      int ph0 = checked(lookup(0));  // pages of tile n (V(n) still to load)
+      int ph1 = lookup(1);            // tile n + 1, in flight
+      ok = load_k(0, ph0);
       for (int n = 0; ok && n < N; ++n) {
         // K runs one key tile ahead of V: K(n + 1) as S(n) releases its atoms,
         // V(n) once the P V before has read the V before.
-        if (n + 1 < N && !load_k(n + 1)) {
-          ok = false;
-          break;
+        const int ph2 = lookup(n + 2);
+        if (n + 1 < N) {
+          ph1 = checked(ph1);
+          if (!load_k(n + 1, ph1)) {
+            ok = false;
+            break;
+          }
         }
         if (v_loads > 0 && !wwait(v_empty, (v_loads - 1) & 1, abort_flag, p)) {
           ok = false;
           break;
         }
         const int j = tile_at(w, n);
-        const int phys = kPaged ? page_of(j) : 0;
+        const int phys = ph0;
         mbar_arrive_expect_tx_w(v_full, kNAtom * kAtom);
 #pragma unroll
         for (int a = 0; a < kNAtom; ++a) load_atom(&tmV, sV + a * kAtom, v_full, a, j, phys);
         ++v_loads;
+        ph0 = ph1;
+        ph1 = ph2;
       }
     }
     // Every copy issued lands before the CTA can leave (a load is issued
