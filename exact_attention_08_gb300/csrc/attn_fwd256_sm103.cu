@@ -108,7 +108,20 @@ template <bool kPaged>
 __device__ __forceinline__ bool decode_tile(const P256& p, int item, Tile& w, bool report) {
   const int per = p.Hq * p.B;
   int x = item, qt;
-  if (p.causal) {
+  if (kPaged) {
+    // Query blocks against a paged cache read far more keys than they have
+    // queries: the items that share a sequence's key head (its query tiles
+    // and the query heads of the group) are adjacent, so that the CTAs
+    // running together read its keys and values once from HBM (taking the
+    // query tiles longest first across all heads instead re-read them 3.5x).
+    const int G = p.Hq / p.Hkv;
+    const int hg = x % G;
+    x /= G;
+    qt = p.num_qt - 1 - x % p.num_qt;
+    x /= p.num_qt;
+    w.h = (x % p.Hkv) * G + hg;
+    w.bseq = x / p.Hkv;
+  } else if (p.causal) {
     qt = p.num_qt - 1 - x / per;
     x %= per;
     w.h = x % p.Hq;
@@ -320,10 +333,11 @@ __global__ void __launch_bounds__(kThr, 1)
       auto load_atom = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int a, int j,
                            int phys) {
         if constexpr (kPaged) {
-#pragma unroll
-          for (int pp = 0; pp < kPagesPerTile; ++pp)
-            tma_load_4d_w(dst + pp * kPage * 128, map, bar, a * 64, w.hk, 0,
-                          __shfl_sync(0xffffffffu, phys, pp));
+          // lane pp issues the box of its own page: one warp instruction
+          // starts the copies of all eight pages of the atom
+          if (lane < kPagesPerTile)
+            tma_load_4d(dst + lane * kPage * 128, map, bar, a * 64, w.hk, 0, phys);
+          __syncwarp();
         } else {
           (void)phys;
           tma_load_4d_w(dst, map, bar, a * 64, w.hk, w.k_base + j * kR, w.b_coord);

@@ -696,13 +696,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         w.b_coord);
         return;
       } else {
+        // lane pp issues the boxes of its own page: one warp instruction
+        // starts the copies of all eight pages of an atom
+        if (lane < kPagesPerTile) {
 #pragma unroll
-      for (int pp = 0; pp < kPagesPerTile; ++pp) {
-        const int pg = __shfl_sync(0xffffffffu, phys, pp);
-#pragma unroll
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_4d_w(dst + a * C::kAtomBytes + pp * kPage * 128, map, bar, a * 64, w.hk, 0, pg);
-      }
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_4d(dst + a * C::kAtomBytes + lane * kPage * 128, map, bar, a * 64, w.hk, 0,
+                        phys);
+        }
+        __syncwarp();
       }
     };
     for (int c = 0; ok; ++c) {
