@@ -224,14 +224,16 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       const int* row = p.page_table + static_cast<size_t>(b) * p.max_pages;
+      int page_next = row[pg0];  // each page index read one page ahead of its loads
       for (int i = 0; i < npg; ++i) {
         const int s = i % kStagesDec;
+        int page = page_next;
+        if (i + 1 < npg) page_next = row[pg0 + i + 1];
         if (!mbar_wait(&empty[s], ((i / kStagesDec) & 1) ^ 1, abort_flag, p.wait_limit_ns)) {
           atomicOr(p.status, kStatusTimeout);
           *abort_flag = 1;
           break;
         }
-        int page = row[pg0 + i];
         if (page < 0 || page >= p.num_pages) {
           atomicOr(p.status, kStatusBadInput);
           page = p.num_pages;  // past the pool: the copy reads zeros
@@ -507,14 +509,16 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       const int* row = p.page_table + static_cast<size_t>(b) * p.max_pages;
+      int page_next = row[pg0];  // each page index read one page ahead of its loads
       for (int i = 0; i < npg; ++i) {
         const int s = i % kStages256;
+        int page = page_next;
+        if (i + 1 < npg) page_next = row[pg0 + i + 1];
         if (!mbar_wait(&empty[s], ((i / kStages256) & 1) ^ 1, abort_flag, p.wait_limit_ns)) {
           atomicOr(p.status, kStatusTimeout);
           *abort_flag = 1;
           break;
         }
-        int page = row[pg0 + i];
         if (page < 0 || page >= p.num_pages) {
           atomicOr(p.status, kStatusBadInput);
           page = p.num_pages;  // past the pool: the copy reads zeros
