@@ -344,6 +344,12 @@ struct Work {
 // against a mean of 147).  One warp builds the table at kernel start.
 constexpr int kTabMaxSeq = 256;
 constexpr int kTabMaxLev = 64;
+// Query blocks against a paged cache (chunked prefill, speculative decoding)
+// read far more keys than they have queries, so an item's cost follows its
+// sequence's key count rather than its query pair: batches of up to
+// kTabSortMax sequences are ordered by key count instead (longest first,
+// each sequence's query pairs last first, its heads adjacent).
+constexpr int kTabSortMax = 64;
 
 struct ItemTable {
   int total;                       // items in the dense order (0: the table is not used)
@@ -372,6 +378,50 @@ __device__ __forceinline__ int packed_rows(const Params& p, int b) {
 // reported and left out.
 template <bool kPagedKV>
 __device__ __forceinline__ void build_item_table(const Params& p, ItemTable& t, int lane) {
+  if (kPagedKV && p.B <= kTabSortMax) {
+    // by key tiles, ties by sequence index: hist[b] the key tiles of b and
+    // lev_start[b + 1] its pairs, then order[rank] = b, hist[rank] its
+    // pairs, and lev_start the running slot counts
+    const int nlev = p.num_qpairs;
+    int rk[2], npb[2];
+    for (int i = 0; i < 2; ++i) {
+      const int b = lane + 32 * i;
+      if (b < p.B) {
+        const int rows = packed_rows<kPagedKV>(p, b);
+        if (rows < 0) atomicOr(p.status, kStatusBadInput);
+        npb[i] = rows <= 0 ? 0 : min((rows + kQT * kBM - 1) / (kQT * kBM), nlev);
+        t.hist[b] = rows < 0 ? 0 : (p.seqlens_k[b] + kBN - 1) / kBN;
+      }
+    }
+    __syncwarp();
+    for (int i = 0; i < 2; ++i) {
+      const int b = lane + 32 * i;
+      rk[i] = 0;
+      if (b < p.B) {
+        const int kb = t.hist[b];
+        for (int c = 0; c < p.B; ++c) {
+          const int kc = t.hist[c];
+          rk[i] += (kc > kb || (kc == kb && c < b)) ? 1 : 0;
+        }
+      }
+    }
+    __syncwarp();
+    for (int i = 0; i < 2; ++i) {
+      const int b = lane + 32 * i;
+      if (b < p.B) {
+        t.order[rk[i]] = static_cast<short>(b);
+        t.hist[rk[i]] = npb[i];
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      t.lev_start[0] = 0;
+      for (int r = 0; r < p.B; ++r) t.lev_start[r + 1] = t.lev_start[r] + t.hist[r];
+      t.total = t.lev_start[p.B] * p.Hq;
+    }
+    __syncwarp();
+    return;
+  }
   const int nlev = p.num_qpairs;
   for (int l = lane; l <= nlev; l += 32) t.hist[l] = 0;
   __syncwarp();
@@ -426,7 +476,22 @@ template <bool kPagedKV, bool kTable>
 __device__ __forceinline__ bool locate_item(const Params& p, const ItemTable& tab, int k,
                                             ItemLoc& r, bool report) {
   int qp;
-  if (kTable) {
+  if (kTable && kPagedKV && p.B <= kTabSortMax) {
+    // the sequence rank r with lev_start[r] <= sl < lev_start[r + 1], its
+    // query pairs last first
+    const int sl = fdiv(k, p.div_hq);
+    r.h = k - sl * p.Hq;
+    int lo = 0, hi = p.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tab.lev_start[mid] <= sl)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    qp = tab.lev_start[lo + 1] - 1 - sl;
+    r.bseq = tab.order[lo];
+  } else if (kTable) {
     const int sl = fdiv(k, p.div_hq);
     r.h = k - sl * p.Hq;
     int lo = 0, hi = p.num_qpairs;  // the level l with lev_start[l] <= sl < lev_start[l + 1]
