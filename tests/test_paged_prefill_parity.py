@@ -122,3 +122,20 @@ def test_chunked_prefill_full_size(ea):
         idx = torch.as_tensor(cu_q[b] + rows, dtype=torch.long, device=o.device)
         compare(o.index_select(0, idx)[None], lse.index_select(1, idx)[None], ro, rl,
                 f"chunked prefill sequence {b}")
+
+
+@pytest.mark.parametrize("nseq,seed", [(50, 87), (80, 88)])
+def test_many_sequences(ea, nseq, seed):
+    """Causal query blocks of 0-300 rows against caches of 0-1,500 keys: 50
+    sequences (dealt by key count, two per lane of the ordering warp) and 80
+    (past that bound: dealt by query pair), empty blocks and caches among
+    them, against the oracle."""
+    r = np.random.default_rng(seed)
+    lk = r.integers(0, 1500, nseq).tolist()
+    lq = [int(min(q, k)) for q, k in zip(r.integers(0, 300, nseq), lk)]
+    x = workloads.paged_prefill_inputs(seed, nseq, 4, 2, 128, 0, 0, 0, 0, lengths_k=lk,
+                                       lengths_q=lq)
+    o, lse = _run(ea, x)
+    assert ea.attn_device_status() == ea.ATTN_OK
+    ro, rl = _oracle(x)
+    compare(o, lse, ro, rl, f"paged prefill, {nseq} sequences")
