@@ -1,7 +1,8 @@
 """Builds libattn_gb300.so in-tree with nvcc for sm_103a.
 
-Three translation units (host ABI, prefill kernel, decode kernels) compile in
-parallel, then link into one shared library next to this file.  The CUDA
+The translation units (host ABI, the forward kernels at d <= 128 and at
+d = 256, the decode kernels, the backward kernels at d <= 128 and at d = 256)
+compile in parallel, then link into one shared library next to this file.  The CUDA
 runtime is linked statically; the driver's tensor-map encoder is resolved at
 run time, so the library needs no link-time libcuda.
 """
@@ -17,8 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libattn_gb300.so")
 SOURCES = ["attn_api.cu", "attn_fwd_sm103.cu", "attn_fwd256_sm103.cu", "attn_decode_sm103.cu",
-           "attn_bwd_sm103.cu"]
-HEADERS = ["sm103_ptx.cuh", "attn_internal.h"]
+           "attn_bwd_sm103.cu", "attn_bwd256_sm103.cu"]
+HEADERS = ["sm103_ptx.cuh", "attn_internal.h", "attn_bwd_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "-I", CSRC, "-I", INCLUDE]

@@ -451,7 +451,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
     return set_error(ATTN_ERR_INVALID_ARG, "negative total_q / total_k");
   if (Hq % Hkv != 0)
     return set_error(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
-  if (d != 64 && d != 128) return set_error(ATTN_ERR_UNSUPPORTED, "head dim %d (64 or 128)", d);
+  if (d != 64 && d != 128 && d != 256)
+    return set_error(ATTN_ERR_UNSUPPORTED, "head dim %d (64, 128 or 256)", d);
   if (!(scale > 0.f) || !std::isfinite(scale))
     return set_error(ATTN_ERR_INVALID_ARG, "scale must be finite and positive");
   if (causal != 0 && causal != 1) return set_error(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
@@ -494,6 +495,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   if (rc != ATTN_OK) return rc;
   BwdLaunch a;
   std::memset(&a, 0, sizeof(a));
+  a.v = v;
   a.o = o;
   a.dout = dout;
   a.lse = lse;
@@ -522,14 +524,16 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   a.status = ds->status;
   a.num_sms = ds->num_sms;
   // Dense tensors are 4-D maps (d, H, S, B); packed ones (d, H, total, 1).
+  // The d = 256 kernels stream 64-row tiles.
   const uint64_t sq = varlen ? static_cast<uint64_t>(total_q) : static_cast<uint64_t>(max_Sq);
   const uint64_t sk = varlen ? static_cast<uint64_t>(total_k) : static_cast<uint64_t>(max_Skv);
   const uint64_t nb = varlen ? 1u : static_cast<uint64_t>(B);
-  if ((rc = make_map(&a.tmQ, q, d, Hq, sq, nb, 128, "q")) != ATTN_OK) return rc;
-  if ((rc = make_map(&a.tmDO, dout, d, Hq, sq, nb, 128, "dout")) != ATTN_OK) return rc;
+  const uint32_t box = d == 256 ? 64 : 128;
+  if ((rc = make_map(&a.tmQ, q, d, Hq, sq, nb, box, "q")) != ATTN_OK) return rc;
+  if ((rc = make_map(&a.tmDO, dout, d, Hq, sq, nb, box, "dout")) != ATTN_OK) return rc;
   if (rows_k > 0 && max_Skv > 0) {
-    if ((rc = make_map(&a.tmK, k, d, Hkv, sk, nb, 128, "k")) != ATTN_OK) return rc;
-    if ((rc = make_map(&a.tmV, v, d, Hkv, sk, nb, 128, "v")) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.tmK, k, d, Hkv, sk, nb, box, "k")) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.tmV, v, d, Hkv, sk, nb, box, "v")) != ATTN_OK) return rc;
   }
   cudaError_t e = launch_attn_bwd(a, st);
   return e == cudaSuccess ? ATTN_OK : cuda_error(e, "attn_bwd launch");
@@ -719,6 +723,7 @@ ATTN_API int attn_device_status(void* stream) {
   if (e != cudaSuccess) return cuda_error(e, "clearing the status word");
   if (word & kStatusTimeout) return ATTN_ERR_TIMEOUT;
   if (word & kStatusBadInput) return ATTN_ERR_BAD_INPUT;
+  if (word & kStatusLayout) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
 

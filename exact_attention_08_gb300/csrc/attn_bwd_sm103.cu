@@ -47,8 +47,7 @@
 // walks the query tiles that see its key tile (one contiguous range: the
 // window bounds it above unless the tile holds sink keys); the dQ kernel
 // walks the sink tiles, then its window of key tiles.
-#include "attn_internal.h"
-#include "sm103_ptx.cuh"
+#include "attn_bwd_common.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -62,17 +61,6 @@ namespace attn {
 namespace {
 
 using namespace ptx;
-
-constexpr int kB = 128;          // rows of every tile (keys or queries)
-// Warps 0-7 compute, 8 producer, 9 MMA.  Compute warp w reads tensor-memory
-// lanes 32 (w % 4) .. +31 (its sub-partition's quarter) and the column half
-// w / 4 of every 128-column tile, so each sub-partition runs two of them.
-constexpr int kComputeWarps = 8;
-constexpr int kBwdThreads = 32 * (kComputeWarps + 2);
-constexpr int kWarpProd = kComputeWarps;
-constexpr int kWarpIssue = kComputeWarps + 1;
-constexpr int kComputeThreads = 32 * kComputeWarps;
-constexpr float kLog2eB = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
@@ -100,116 +88,6 @@ struct BwdCfg {
   static constexpr int kLaunchKV = kSmemKV > kOneCta ? kSmemKV : kOneCta;
   static constexpr int kLaunchQ = kSmemQ > kOneCta ? kSmemQ : kOneCta;
 };
-
-struct BwdParams {
-  const __nv_bfloat16* dout;  // [B, Sq, Hq, d] or packed [total_q, Hq, d] (row statistics only)
-  const __nv_bfloat16* o;
-  const float* lse;          // [B, Hq, Sq] or packed [Hq, total_q], natural log
-  const int* cu_q;           // packed sequences: [B + 1] query offsets, or null (dense)
-  const int* cu_k;           // packed sequences: [B + 1] key offsets
-  float* lse2;               // [B, Hq, Sqp] workspace: -LSE * log2(e), -inf on pad rows
-  float* dvec;               // [B, Hq, Sqp] workspace: -rowsum(dO * O)
-  __nv_bfloat16* dq;         // [B, Sq, Hq, d]
-  __nv_bfloat16* dk;         // [B, Skv, Hkv, d]
-  __nv_bfloat16* dv;
-  int v8;                    // dq, dk and dv start on 32 bytes: 32-byte stores
-  int B, Hq, Hkv, Sq, Skv, Sqp, d;  // Sq, Skv: the longest sequence when packed
-  int total_q, total_k;             // packed token counts
-  float scale, scale2;
-  int causal, window, n_sink;
-  uint64_t wait_limit_ns;
-  int* status;
-};
-
-// One sequence's geometry: lengths, first rows in the tensors (for
-// addressing outputs), and the TMA coordinates of its first rows.
-struct SeqGeo {
-  int Lq, Lk, q_base, k_base, b_coord;
-  long long q_row0, k_row0;
-};
-
-// False (and reported when `report`) for packed offsets out of range.
-__device__ __forceinline__ bool seq_geo(const BwdParams& p, int b, SeqGeo& g, bool report) {
-  if (p.cu_q != nullptr) {
-    const int a = p.cu_q[b], e = p.cu_q[b + 1], ka = p.cu_k[b], ke = p.cu_k[b + 1];
-    if (a < 0 || e < a || e > p.total_q || e - a > p.Sq || ka < 0 || ke < ka ||
-        ke > p.total_k || ke - ka > p.Skv) {
-      if (report) atomicOr(p.status, kStatusBadInput);
-      return false;
-    }
-    g.Lq = e - a;
-    g.Lk = ke - ka;
-    g.q_base = a;
-    g.k_base = ka;
-    g.b_coord = 0;
-    g.q_row0 = a;
-    g.k_row0 = ka;
-  } else {
-    g.Lq = p.Sq;
-    g.Lk = p.Skv;
-    g.q_base = 0;
-    g.k_base = 0;
-    g.b_coord = b;
-    g.q_row0 = static_cast<long long>(b) * p.Sq;
-    g.k_row0 = static_cast<long long>(b) * p.Skv;
-  }
-  return true;
-}
-
-__device__ __forceinline__ void reg_fence_b(uint32_t& r) { asm volatile("" : "+r"(r)); }
-
-__device__ __forceinline__ uint64_t pf2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void pf2_split(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t pf2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t pf2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t pf2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-
-// Four consecutive floats of shared memory as two pairs (one 16-byte load).
-// Volatile, so it stays after the barrier wait that makes the data valid.
-__device__ __forceinline__ void lds_pairs2(uint32_t addr, uint64_t& a, uint64_t& b) {
-  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
-}
-// One 32-column chunk of a row vector: 16 pairs.
-__device__ __forceinline__ void lds_chunk(uint32_t addr, uint64_t* v) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) lds_pairs2(addr + 16 * i, v[2 * i], v[2 * i + 1]);
-}
-
-__device__ __forceinline__ void tmem_ld_wait_b() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// A 128-column fp32 tile rewritten in place as bf16 pairs: the 32-column
-// chunk c goes to 16 columns at 64 (c / 2) + 16 (c % 2), inside the column
-// half that holds its source, so the warp that reads a half is the only one
-// that writes it.  K-step kk (16 columns of the tile) of an MMA that takes
-// the packed tile as its A operand starts at packed_col(kk).
-__device__ __forceinline__ uint32_t packed_col(int kk) {
-  return static_cast<uint32_t>(64 * (kk / 4) + 8 * (kk % 4));
-}
-
-__device__ __forceinline__ void bwd_fail(int* status, volatile int* abort_flag) {
-  atomicOr(status, kStatusTimeout);
-  if (abort_flag) *abort_flag = 1;
-}
 
 // Eight lanes per query row (four rows per warp at a time): D = sum_t dO_t
 // O_t (fp32) and LSE2 = LSE log2(e), both stored negated (the kernels add
@@ -301,52 +179,6 @@ __global__ void __launch_bounds__(kSinkThreads)
   if (threadIdx.x == 0) dsink[h] = part[0];
 }
 
-// Packs 32 fp32 values into 16 bf16 pairs (element 2e in the low half).
-__device__ __forceinline__ void pack32(const float* f, uint32_t* pk) {
-#pragma unroll
-  for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
-}
-
-// 32 bf16 (16 pairs) of one row to global memory: two 32-byte stores when
-// the row is 32-byte aligned (each thread stores its own row, so a store
-// instruction touches 32 rows and fewer, wider ones cost the L1 less), else
-// four 16-byte stores.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t* pk, int v8) {
-  if (v8) {
-    st_global_v8(dst, pk);
-    st_global_v8(dst + 16, pk + 8);
-  } else {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int v4 = 0; v4 < 4; ++v4)
-      d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-  }
-}
-
-// K-step kk of a K-major SW128 operand: 32 bytes along a row inside a
-// 128-byte atom, then the next atom column.
-template <int kAtomBytes>
-__device__ __forceinline__ uint64_t kmajor_step(int kk) {
-  return static_cast<uint64_t>(((kk / 4) * kAtomBytes + (kk % 4) * 32) >> 4);
-}
-
-// Bounded wait by every lane of the warp; on failure the status is set once.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          const BwdParams& p) {
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.wait_limit_ns));
-  if (!ok && (threadIdx.x % 32) == 0) bwd_fail(p.status, abort_flag);
-  return ok;
-}
-
-// The n-th item of this CTA, or -1 past the last: bands of gridDim.x items,
-// every other band dealt in reverse CTA order.  With one CTA per item (the
-// grid as large as the item count) every CTA takes its own item only.
-__device__ __forceinline__ int bwd_item_at(int n, int num_items) {
-  const int G = gridDim.x;
-  const int pos = (n & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-  const long long k = static_cast<long long>(n) * G + pos;
-  return k < num_items ? static_cast<int>(k) : -1;
-}
 
 // One key tile of the dK/dV kernel: which, and the query tiles that see it.
 struct KvItem {
@@ -1165,8 +997,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// The dK/dV and dQ kernels of head dimension 64 or 128.
 template <int D>
-cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t stream) {
+cudaError_t launch_bwd_grads(const BwdParams& p, const BwdLaunch& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  cudaError_t e;
+  // Dense calls: persistent grids (one CTA per SM; every item is about the
+  // same work, or ordered longest first under a causal mask).  Packed calls:
+  // one CTA per item, so that the hardware hands the next item to whichever
+  // SM frees first (item costs follow the sequence lengths).
+  const bool packed = a.cu_q != nullptr;
+  auto grid_of = [&](long long items) {
+    return static_cast<unsigned>(packed ? items
+                                        : std::min<long long>(items, std::max(a.num_sms, 1)));
+  };
+  if (a.Skv > 0) {
+    const long long n1 = static_cast<long long>((a.Skv + kB - 1) / kB) * a.Hkv * a.B;
+    attn_bwd_dkdv_kernel<D><<<grid_of(n1), kBwdThreads, C::kLaunchKV, stream>>>(
+        a.tmQ, a.tmK, a.tmV, a.tmDO, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const long long n2 = static_cast<long long>(p.Sqp / kB) * a.Hq * a.B;
+  attn_bwd_dq_kernel<D><<<grid_of(n2), kBwdThreads, C::kLaunchQ, stream>>>(a.tmQ, a.tmK, a.tmV,
+                                                                          a.tmDO, p);
+  return cudaGetLastError();
+}
+
+
+template <int D>
+cudaError_t set_bwd_attributes() {
   using C = BwdCfg<D>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -1177,10 +1036,21 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t stream) {
       attr_err = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchQ);
   });
-  if (attr_err != cudaSuccess) return attr_err;
+  return attr_err;
+}
+
+// Row statistics, then the gradient kernels of head dimension D (d = 256:
+// attn_bwd256_sm103.cu), then the logit sink's gradient.
+template <int D>
+cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t stream) {
+  if constexpr (D != 256) {
+    const cudaError_t attr_err = set_bwd_attributes<D>();
+    if (attr_err != cudaSuccess) return attr_err;
+  }
   BwdParams p;
   p.dout = static_cast<const __nv_bfloat16*>(a.dout);
   p.o = static_cast<const __nv_bfloat16*>(a.o);
+  p.v = static_cast<const __nv_bfloat16*>(a.v);
   p.lse = a.lse;
   p.cu_q = a.cu_q;
   p.cu_k = a.cu_k;
@@ -1210,25 +1080,11 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t stream) {
   attn_bwd_rowstat_kernel<D><<<1216, 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // Dense calls: persistent grids (one CTA per SM; every item is about the
-  // same work, or ordered longest first under a causal mask).  Packed calls:
-  // one CTA per item, so that the hardware hands the next item to whichever
-  // SM frees first (item costs follow the sequence lengths).
-  const bool packed = a.cu_q != nullptr;
-  auto grid_of = [&](long long items) {
-    return static_cast<unsigned>(packed ? items
-                                        : std::min<long long>(items, std::max(a.num_sms, 1)));
-  };
-  if (a.Skv > 0) {
-    const long long n1 = static_cast<long long>((a.Skv + kB - 1) / kB) * a.Hkv * a.B;
-    attn_bwd_dkdv_kernel<D><<<grid_of(n1), kBwdThreads, C::kLaunchKV, stream>>>(
-        a.tmQ, a.tmK, a.tmV, a.tmDO, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if constexpr (D == 256) {
+    if ((e = launch_bwd256(p, a, stream)) != cudaSuccess) return e;
+  } else {
+    if ((e = launch_bwd_grads<D>(p, a, stream)) != cudaSuccess) return e;
   }
-  const long long n2 = static_cast<long long>(p.Sqp / kB) * a.Hq * a.B;
-  attn_bwd_dq_kernel<D><<<grid_of(n2), kBwdThreads, C::kLaunchQ, stream>>>(a.tmQ, a.tmK, a.tmV,
-                                                                          a.tmDO, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.sink != nullptr) {
     attn_bwd_dsink_kernel<<<a.Hq, kSinkThreads, 0, stream>>>(p.lse2, p.dvec, a.sink, a.dsink, a.B,
                                                              a.Hq, p.Sqp);
@@ -1247,6 +1103,7 @@ size_t bwd_workspace_bytes(int B, int Hq, int Sq) {
 cudaError_t launch_attn_bwd(const BwdLaunch& a, cudaStream_t stream) {
   if (a.d == 128) return launch_bwd_d<128>(a, stream);
   if (a.d == 64) return launch_bwd_d<64>(a, stream);
+  if (a.d == 256) return launch_bwd_d<256>(a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -13,6 +13,7 @@ namespace attn {
 enum : int {
   kStatusTimeout = 1,   // a bounded wait ran out
   kStatusBadInput = 2,  // out-of-range device data (page index, cu_seqlens)
+  kStatusLayout = 4,    // a kernel's shared-memory window was not where its layout needs it
 };
 
 // Default limit of every bounded wait in the production kernels.
@@ -57,6 +58,8 @@ struct DecodeLaunch {
 
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmDO;  // 4-D maps (d, H, S, B), 64 x 1 x 128 x 1 boxes
+                                    // (64 x 1 x 64 x 1 at d = 256)
+  const void* v;                    // bf16 values [B, Skv, Hkv, d] or [total_k, Hkv, d]
   const void* o;                    // bf16 forward output [B, Sq, Hq, d] or [total_q, Hq, d]
   const void* dout;                 // bf16 gradient of O, same layout
   const float* lse;                 // forward LSE [B, Hq, Sq] or [Hq, total_q] (natural log)

@@ -121,11 +121,11 @@ def test_argument_errors_of_the_newer_entry_points_without_gpu():
     assert L.attn_bwd(p16, p16, p16, p16, p16, p16, p16, p16, p16, 1, 2, 2, 300, 8, 128, 0.1, 0,
                       p16, 16, None) == ea.ATTN_ERR_INVALID_ARG
     assert ea.attn_bwd_workspace_size(1, 2, 300) == 2 * 2 * 384 * 4
-    # d = 256 runs in every forward call and the decode; the backward rejects
-    # it before any launch, and so does every call for other head dimensions
-    assert L.attn_bwd(p16, p16, p16, p16, p16, p16, p16, p16, p16, 1, 2, 2, 8, 8, 256, 0.1, 0,
+    # d = 64, 128 and 256 run in every call; other head dimensions are
+    # rejected before any launch
+    assert L.attn_bwd(p16, p16, p16, p16, p16, p16, p16, p16, p16, 1, 2, 2, 8, 8, 192, 0.1, 0,
                       p16, 1 << 20, None) == ea.ATTN_ERR_UNSUPPORTED
-    assert "256" in ea.attn_last_error()
+    assert "192" in ea.attn_last_error()
     assert L.attn_fwd_paged(p16, p16, p16, p16, p16, p16, p16, None, 1, 2, 2, 8, 8, 96, 16, 4,
                             4, 0.1, 1, 0, 0, None, None) == ea.ATTN_ERR_UNSUPPORTED
     assert L.attn_decode_paged(p16, p16, p16, p16, p16, p16, None, 2, 8, 2, 192, 16, 4, 10, 8, 0.1,
