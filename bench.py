@@ -817,8 +817,8 @@ def run_variants(ea, workloads, dev, stream, flush):
         bw["causal" if c else "noncausal"] = {"ms": ms, "tflops": fl / (ms / 1e3) / 1e12}
     bw["note"] = "FLOPs 2.5x the forward's (five products)"
     out["backward_b4h16s2048d128"] = bw
-    # head dimension 256
-    d256 = {}
+    # head dimension 256: the forward, then the backward of its output
+    d256, b256 = {}, {}
     for c in (False, True):
         xd = workloads.dense_inputs(7101 + int(c), 4, 16, 16, 2048, 2048, 256, c)
         qd, kd, vd = xd.q.to(dev), xd.k.to(dev), xd.v.to(dev)
@@ -828,8 +828,17 @@ def run_variants(ea, workloads, dev, stream, flush):
             qd, kd, vd, od, ld, causal=c, scale=xd.scale, stream=stream))
         fl = prefill_flops(4, 16, 2048, 2048, 256, c)
         d256["causal" if c else "noncausal"] = {"ms": ms, "tflops": fl / (ms / 1e3) / 1e12}
-        del qd, kd, vd, od, ld
+        gd = workloads.grad_output(7111 + int(c), qd.shape).to(dev)
+        gq, gk, gv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        ms = timed_calls(stream, flush, lambda: ea.attn_bwd(
+            qd, kd, vd, od, ld, gd, gq, gk, gv, causal=c, scale=xd.scale, workspace=bws,
+            stream=stream), n=10)
+        b256["causal" if c else "noncausal"] = {"ms": ms, "tflops": 2.5 * fl / (ms / 1e3) / 1e12}
+        del qd, kd, vd, od, ld, gd, gq, gk, gv
     out["prefill_d256_b4h16s2048"] = d256
+    b256["note"] = ("FLOPs 2.5x the forward's (five products); dV, dK and dQ from three "
+                    "launches, each recomputing the scores")
+    out["backward_d256_b4h16s2048"] = b256
     # head dimension 256 on a paged cache: the decode (the decode workload's
     # shape) and chunked prefill (the chunked-prefill workload's shape)
     dx = workloads.paged_decode_inputs(5301, 64, 32, 8, 256, 1024, 8192, num_splits=8)

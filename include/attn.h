@@ -43,9 +43,10 @@
  *   - Head dimension d: 64, 128 or 256 for every forward call (attn_fwd,
  *     attn_fwd_ex, attn_fwd_ex_sink, attn_fwd_strided, attn_fwd_paged; at
  *     d = 256 a CTA takes one 128-row query tile, with two score buffers and
- *     O in tensor memory) and for the decode (at d = 256 the two consumer
- *     warps of a split each keep half of O); 64 or 128 for the backward.
- *     The device must be sm_103.
+ *     O in tensor memory), for the decode (at d = 256 the two consumer
+ *     warps of a split each keep half of O) and for the backward (at
+ *     d = 256 dV, dK and dQ come from three launches that stream 64-row
+ *     tiles).  The device must be sm_103.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
@@ -212,7 +213,7 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Sq);
  *   lse: the forward's [B, Hq, Sq] output (rows with -inf, which saw no key,
  *   get dq = 0 and contribute nothing).  workspace: device buffer of at least
  *   attn_bwd_workspace_size(B, Hq, Sq) bytes, overwritten.  Sq == 0 zeroes
- *   dk and dv; Skv == 0 zeroes dq.  d must be 64 or 128.
+ *   dk and dv; Skv == 0 zeroes dq.  d must be 64, 128 or 256.
  */
 ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o,
                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
@@ -348,8 +349,10 @@ ATTN_API int attn_decode_paged_noalloc(const void* q, const void* k_pages, const
 
 /*
  * Synchronises `stream`, then returns and clears the device-side status word
- * of the current device (ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_BAD_INPUT), or
- * ATTN_ERR_CUDA if the synchronisation itself failed.
+ * of the current device (ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_BAD_INPUT, or
+ * ATTN_ERR_UNSUPPORTED when a kernel found its dynamic shared memory off the
+ * 1024-byte boundary its layout assumes and wrote nothing), or ATTN_ERR_CUDA
+ * if the synchronisation itself failed.
  */
 ATTN_API int attn_device_status(void* stream);
 
