@@ -68,19 +68,27 @@ struct BwdCfg {
   static constexpr int kAtoms = D / 64;          // 128-byte swizzle atoms per row
   static constexpr int kAtomBytes = kB * 128;    // one atom column of a tile
   static constexpr int kVec = kB * 4;            // one fp32 row vector of a tile
-  // dK/dV kernel: K, V resident; two stages of (Q, dO, LSE2, D)
-  static constexpr int kStageBytes = 2 * kTile + 2 * kVec;
+  // dK/dV kernel: K, V resident; Q tiles in three slots (read by S^T early
+  // and by dK late in a query tile's products), dO tiles with the tile's two
+  // row vectors (-LSE2, -D) in two.  No alignment slack: the kernel checks
+  // that the dynamic shared memory starts on 1024 bytes (it does on this GPU,
+  // with no static shared memory) and reports otherwise.
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTile;
-  static constexpr int kOffStage = 2 * kTile;
-  static constexpr int kOffBarKV = kOffStage + 2 * kStageBytes;
-  static constexpr int kSmemKV = kOffBarKV + 16 * 8 + 1024;
-  // dQ kernel: Q, dO resident; two stages of (K, V)
+  static constexpr int kOffQs = 2 * kTile;
+  static constexpr int kDSlot = kTile + 2 * kVec;
+  static constexpr int kOffDs = kOffQs + 3 * kTile;
+  static constexpr int kOffBarKV = kOffDs + 2 * kDSlot;
+  static constexpr int kSmemKV = kOffBarKV + 24 * 8;
+  static_assert(kDSlot % 1024 == 0, "dO slots on the swizzle atom");
+  // dQ kernel: Q, dO resident; K tiles in three slots (read by S early and
+  // by dQ late in a key tile's products), V tiles in two (read by dP only)
   static constexpr int kOffQ = 0;
   static constexpr int kOffDO = kTile;
-  static constexpr int kOffKV = 2 * kTile;
-  static constexpr int kOffBarQ = kOffKV + 2 * 2 * kTile;
-  static constexpr int kSmemQ = kOffBarQ + 16 * 8 + 1024;
+  static constexpr int kOffKs = 2 * kTile;
+  static constexpr int kOffVs = kOffKs + 3 * kTile;
+  static constexpr int kOffBarQ = kOffVs + 2 * kTile;
+  static constexpr int kSmemQ = kOffBarQ + 24 * 8 + 1024;
   static_assert(kSmemKV <= 227 * 1024 && kSmemQ <= 227 * 1024, "shared memory");
   // Each CTA allocates all 512 tensor-memory columns: ask for enough shared
   // memory that a second CTA never shares the SM (its allocation would wait).
@@ -238,23 +246,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          const __grid_constant__ CUtensorMap tmDO, BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_align1024(smem_raw);
+  // The layout fills shared memory with no room to round the window up to
+  // the swizzle atom: a window off the boundary is reported, not used.
+  if (smem_addr(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusLayout);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBarKV);
   uint64_t* kv_full = bars;       // K and V tiles landed
-  uint64_t* q_full = bars + 1;    // [2] Q, dO, LSE2, D of a query tile landed
-  uint64_t* q_free = bars + 3;    // [2] the products reading that stage are done
-  uint64_t* sa_full = bars + 5;   // S^T is in tensor memory
-  uint64_t* sb_full = bars + 6;   // dP^T is in tensor memory
-  uint64_t* pa_ready = bars + 7;  // P^T written (one arrival per compute thread)
-  uint64_t* done = bars + 8;      // every product of the item is done
-  uint64_t* drain = bars + 9;
-  uint64_t* kv_empty = bars + 10; // the item's last products reading K and V are done
-  uint64_t* pb_ready = bars + 11; // dS^T written (one arrival per compute thread)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
-  __shared__ int abort_s;
-  volatile int* abort_flag = &abort_s;
+  uint64_t* q_full = bars + 1;    // [3] Q of a query tile landed
+  uint64_t* q_free = bars + 4;    // [3] S^T and dK of that tile are done
+  uint64_t* d_full = bars + 7;    // [2] dO, -LSE2, -D of a query tile landed
+  uint64_t* d_free = bars + 9;    // [2] dP^T, dV and dK of that tile are done
+  uint64_t* sa_full = bars + 11;  // S^T is in tensor memory
+  uint64_t* sb_full = bars + 12;  // dP^T is in tensor memory
+  uint64_t* pa_ready = bars + 13; // P^T written (one arrival per compute thread)
+  uint64_t* pb_ready = bars + 14; // dS^T written (one arrival per compute thread)
+  uint64_t* done = bars + 15;     // every product of the item is done
+  uint64_t* drain = bars + 16;
+  uint64_t* kv_empty = bars + 17; // the item's last products reading K and V are done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  // in the layout too: no static shared memory ahead of the window
+  int* abort_s = reinterpret_cast<int*>(bars + 19);
+  volatile int* abort_flag = abort_s;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int G = p.Hq / p.Hkv;
   const int num_items = ((p.Skv + kB - 1) / kB) * p.Hkv * p.B;
@@ -262,9 +279,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_free[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&d_full[s], 1);
+      mbar_init(&d_free[s], 1);
     }
     mbar_init(sa_full, 1);
     mbar_init(sb_full, 1);
@@ -273,7 +294,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(done, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
-    abort_s = 0;
+    *abort_s = 0;
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, 512);
@@ -283,14 +304,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  auto stage = [&](int s) { return smem + C::kOffStage + s * C::kStageBytes; };
+  auto qslot = [&](int u) { return smem + C::kOffQs + (u % 3) * C::kTile; };   // Q of query tile u
+  auto dslot = [&](int u) { return smem + C::kOffDs + (u & 1) * C::kDSlot; };  // dO, vectors of tile u
 
-  // Counters over the CTA's items: query tiles (one stage load, one set of
-  // products each) and items with query tiles (one K / V load each).  Items
+  // Counters over the CTA's items: query tiles (one Q and one dO load, one
+  // set of products each) and items with query tiles (one K / V load each).  Items
   // without a query tile only write zeros.
   if (warp == kWarpProd) {
     // ================================================================ producer
-    int kv_loads = 0, issued = 0;
+    int kv_loads = 0, issued = 0, q_loads = 0;  // issued: dO loads (and query tiles)
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int item = bwd_item_at(n, num_items);
@@ -326,34 +348,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       }
+      // Q of query tile u goes to slot u % 3 once S^T and dK of tile u - 3
+      // are done, dO and the row vectors to slot u % 2 once tile u - 2 is
+      // done: both loads run more than a query tile ahead of their first
+      // product.
       for (int t = 0; t < it.ntiles; ++t) {
-        const int s = issued & 1;
-        if (issued >= 2 && !warp_wait(&q_free[s], ((issued >> 1) - 1) & 1, abort_flag, p)) {
+        const int u = issued;
+        const int h = it.hk * G + t / it.nq, qt = it.qt_lo + t % it.nq;
+        if (u >= 3 && !warp_wait(&q_free[u % 3], ((u / 3) - 1) & 1, abort_flag, p)) {
           ok = false;
           break;
         }
-        const int h = it.hk * G + t / it.nq, qt = it.qt_lo + t % it.nq;
-        uint8_t* st = stage(s);
-        mbar_arrive_expect_tx_w(&q_full[s], 2 * C::kTile + 2 * C::kVec);
+        mbar_arrive_expect_tx_w(&q_full[u % 3], C::kTile);
 #pragma unroll
-        for (int a = 0; a < C::kAtoms; ++a) {
-          tma_load_4d_w(st + a * C::kAtomBytes, &tmQ, &q_full[s], a * 64, h,
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_4d_w(qslot(u) + a * C::kAtomBytes, &tmQ, &q_full[u % 3], a * 64, h,
                         it.sg.q_base + qt * kB, it.sg.b_coord);
-          tma_load_4d_w(st + C::kTile + a * C::kAtomBytes, &tmDO, &q_full[s], a * 64, h,
-                        it.sg.q_base + qt * kB, it.sg.b_coord);
+        ++q_loads;
+        if (u >= 2 && !warp_wait(&d_free[u & 1], ((u >> 1) - 1) & 1, abort_flag, p)) {
+          ok = false;
+          break;
         }
+        uint8_t* ds = dslot(u);
+        mbar_arrive_expect_tx_w(&d_full[u & 1], C::kTile + 2 * C::kVec);
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_4d_w(ds + a * C::kAtomBytes, &tmDO, &d_full[u & 1], a * 64, h,
+                        it.sg.q_base + qt * kB, it.sg.b_coord);
         const size_t vrow =
             (static_cast<size_t>(it.b) * p.Hq + h) * p.Sqp + static_cast<size_t>(qt) * kB;
-        bulk_load_1d_w(st + 2 * C::kTile, p.lse2 + vrow, C::kVec, &q_full[s]);
-        bulk_load_1d_w(st + 2 * C::kTile + C::kVec, p.dvec + vrow, C::kVec, &q_full[s]);
+        bulk_load_1d_w(ds + C::kTile, p.lse2 + vrow, C::kVec, &d_full[u & 1]);
+        bulk_load_1d_w(ds + C::kTile + C::kVec, p.dvec + vrow, C::kVec, &d_full[u & 1]);
         ++issued;
       }
     }
     // Let every copy issued land before the CTA can leave.
     if (kv_loads > 0) warp_wait(kv_full, (kv_loads - 1) & 1, nullptr, p);
-    for (int s = 0; s < 2; ++s) {
-      const int n_s = (issued - s + 1) / 2;  // loads issued into stage s
+    for (int s = 0; s < 3; ++s) {
+      const int n_s = (q_loads - s + 2) / 3;  // loads issued into Q slot s
       if (n_s > 0) warp_wait(&q_full[s], (n_s - 1) & 1, nullptr, p);
+    }
+    for (int s = 0; s < 2; ++s) {
+      const int n_s = (issued - s + 1) / 2;  // loads issued into dO slot s
+      if (n_s > 0) warp_wait(&d_full[s], (n_s - 1) & 1, nullptr, p);
     }
   } else if (warp == kWarpIssue) {
     // ================================================================ MMA issuer
@@ -370,11 +407,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tS = tmem, tP = tmem + kB, tDV = tmem + 2 * kB, tDK = tmem + 2 * kB + D;
     int T = 0;    // query tiles of earlier items
     int kvi = 0;  // items with query tiles before this one
-    auto issue_st = [&](int t) -> bool {  // S^T(t) = K Q(t)^T
-      const int s = t & 1;
-      if (!warp_wait(&q_full[s], (t >> 1) & 1, abort_flag, p)) return false;
+    auto issue_st = [&](int u) -> bool {  // S^T(u) = K Q(u)^T
+      if (!warp_wait(&q_full[u % 3], (u / 3) & 1, abort_flag, p)) return false;
       tc_fence_after_sync();
-      const uint64_t dqk = sdesc_sw128(smem_addr(stage(s)), 16, 1024);
+      const uint64_t dqk = sdesc_sw128(smem_addr(qslot(u)), 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
@@ -395,9 +431,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) ok = issue_st(T);
       for (int t = 0; ok && t < nt; ++t) {
         const int u = T + t;  // query tile over the CTA's items
-        const int s = u & 1;
-        const uint32_t st = smem_addr(stage(s));
-        const uint64_t ddok = sdesc_sw128(st + C::kTile, 16, 1024);
+        if (!warp_wait(&d_full[u & 1], (u >> 1) & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t dst_ = smem_addr(dslot(u));
+        const uint64_t ddok = sdesc_sw128(dst_, 16, 1024);
         // dP^T(t) = V dO(t)^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -414,8 +454,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint64_t dqm = sdesc_sw128(st, C::kAtomBytes, 1024);
-        const uint64_t ddom = sdesc_sw128(st + C::kTile, C::kAtomBytes, 1024);
+        const uint64_t dqm = sdesc_sw128(smem_addr(qslot(u)), C::kAtomBytes, 1024);
+        const uint64_t ddom = sdesc_sw128(dst_, C::kAtomBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kB / 16; ++kk)
           mma_bf16_ts_w(tDV, tS + packed_col(kk), ddom + kk * (2048 >> 4), idesc_g,
@@ -434,7 +474,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int kk = 0; kk < kB / 16; ++kk)
           mma_bf16_ts_w(tDK, tP + packed_col(kk), dqm + kk * (2048 >> 4), idesc_g,
                         (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_w(&q_free[s]);
+        // the tile's last products: its Q slot, and its dO slot (whose row
+        // vectors the compute warps read before publishing dS^T)
+        mma_commit_w(&q_free[u % 3]);
+        mma_commit_w(&d_free[u & 1]);
       }
       if (ok) mma_commit_w(done);
       T += nt;
@@ -462,17 +505,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int off = it.sg.Lk - it.sg.Lq;
       for (int t = 0; t < nt; ++t) {
         const int u = T + t;
-        const int s = u & 1;
-        // the stage's row vectors came by bulk copy: observe their barrier too
+        // the row vectors came by bulk copy with dO: observe that barrier too
         if (!warp_wait(sa_full, u & 1, abort_flag, p) ||
-            !warp_wait(&q_full[s], (u >> 1) & 1, abort_flag, p)) {
+            !warp_wait(&d_full[u & 1], (u >> 1) & 1, abort_flag, p)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const int qt = it.qt_lo + t % it.nq;
         // this warp's 64 entries of the two row vectors (-LSE2, -D)
-        const uint32_t nl2_addr = smem_addr(stage(s) + 2 * C::kTile) + 4 * 64 * wh;
+        const uint32_t nl2_addr = smem_addr(dslot(u) + C::kTile) + 4 * 64 * wh;
         const uint32_t nd2_addr = nl2_addr + 4 * kB;
         // column c (query qt*128 + c) is visible to this key row iff
         // cmin <= c <= cmax: causal from below, the window from above (not for
@@ -676,8 +718,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sDO = smem + C::kOffDO;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBarQ);
   uint64_t* qd_full = bars;       // Q and dO landed
-  uint64_t* kv_full = bars + 1;   // [2] K and V of a key tile landed
-  uint64_t* kv_free = bars + 3;   // [2] the products reading that stage are done
+  uint64_t* k_full = bars + 1;    // [3] K of a key tile landed
+  uint64_t* k_free = bars + 13;   // [3] S and dQ of that tile are done
+  uint64_t* v_full = bars + 16;   // [2] V of a key tile landed
+  uint64_t* v_free = bars + 18;   // [2] dP of that tile is done
   // [2] S of a key tile is in tensor memory, one barrier per S buffer: S of
   // the next tile is issued before dS of this one is formed, so with one
   // barrier for both it could complete twice before a waiter looks (across
@@ -698,9 +742,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(qd_full, 1);
     mbar_init(qd_empty, 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_free[s], 1);
+    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_free[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_free[s], 1);
       mbar_init(&sa_full[s], 1);
     }
     mbar_init(sb_full, 1);
@@ -718,7 +766,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  auto stage = [&](int s) { return smem + C::kOffKV + s * 2 * C::kTile; };
+  auto kslot = [&](int u) { return smem + C::kOffKs + (u % 3) * C::kTile; };  // K of key tile u
+  auto vslot = [&](int u) { return smem + C::kOffVs + (u & 1) * C::kTile; };  // V of key tile u
   // S of key tile u (counted over the CTA's items) in one of two buffers:
   // columns [0,128) or [384,512)
   auto s_col = [&](int u) { return (u & 1) ? 3u * kB : 0u; };
@@ -727,7 +776,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // products each) and items with key tiles (one Q / dO load each).
   if (warp == kWarpProd) {
     // ================================================================ producer
-    int qd_loads = 0, issued = 0;
+    int qd_loads = 0, issued = 0, k_loads = 0;  // issued: V loads (and key tiles)
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int item = bwd_item_at(n, num_items);
@@ -762,29 +811,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       }
+      // K of key tile u goes to slot u % 3 once S and dQ of tile u - 3 are
+      // done, V to slot u % 2 once dP of tile u - 2 is: both loads run more
+      // than a key tile ahead of their first product.
       for (int t = 0; t < it.nkt; ++t) {
-        const int s = issued & 1;
-        if (issued >= 2 && !warp_wait(&kv_free[s], ((issued >> 1) - 1) & 1, abort_flag, p)) {
+        const int u = issued;
+        if (u >= 3 && !warp_wait(&k_free[u % 3], ((u / 3) - 1) & 1, abort_flag, p)) {
           ok = false;
           break;
         }
-        uint8_t* st = stage(s);
-        mbar_arrive_expect_tx_w(&kv_full[s], 2 * C::kTile);
         const int kr = it.sg.k_base + it.tile_at(t) * kB;
+        mbar_arrive_expect_tx_w(&k_full[u % 3], C::kTile);
 #pragma unroll
-        for (int a = 0; a < C::kAtoms; ++a) {
-          tma_load_4d_w(st + a * C::kAtomBytes, &tmK, &kv_full[s], a * 64, it.hk, kr,
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_4d_w(kslot(u) + a * C::kAtomBytes, &tmK, &k_full[u % 3], a * 64, it.hk, kr,
                         it.sg.b_coord);
-          tma_load_4d_w(st + C::kTile + a * C::kAtomBytes, &tmV, &kv_full[s], a * 64, it.hk, kr,
-                        it.sg.b_coord);
+        ++k_loads;
+        if (u >= 2 && !warp_wait(&v_free[u & 1], ((u >> 1) - 1) & 1, abort_flag, p)) {
+          ok = false;
+          break;
         }
+        mbar_arrive_expect_tx_w(&v_full[u & 1], C::kTile);
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_4d_w(vslot(u) + a * C::kAtomBytes, &tmV, &v_full[u & 1], a * 64, it.hk, kr,
+                        it.sg.b_coord);
         ++issued;
       }
     }
     if (qd_loads > 0) warp_wait(qd_full, (qd_loads - 1) & 1, nullptr, p);
+    for (int s = 0; s < 3; ++s) {
+      const int n_s = (k_loads - s + 2) / 3;
+      if (n_s > 0) warp_wait(&k_full[s], (n_s - 1) & 1, nullptr, p);
+    }
     for (int s = 0; s < 2; ++s) {
       const int n_s = (issued - s + 1) / 2;
-      if (n_s > 0) warp_wait(&kv_full[s], (n_s - 1) & 1, nullptr, p);
+      if (n_s > 0) warp_wait(&v_full[s], (n_s - 1) & 1, nullptr, p);
     }
   } else if (warp == kWarpIssue) {
     // ================================================================ MMA issuer
@@ -800,10 +862,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int U = 0;    // key tiles of earlier items
     int qdi = 0;  // items with key tiles before this one
     auto issue_s = [&](int u) -> bool {  // S(u) = Q K(u)^T
-      const int s = u & 1;
-      if (!warp_wait(&kv_full[s], (u >> 1) & 1, abort_flag, p)) return false;
+      if (!warp_wait(&k_full[u % 3], (u / 3) & 1, abort_flag, p)) return false;
       tc_fence_after_sync();
-      const uint64_t dkk = sdesc_sw128(smem_addr(stage(s)), 16, 1024);
+      const uint64_t dkk = sdesc_sw128(smem_addr(kslot(u)), 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
@@ -824,9 +885,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) ok = issue_s(U);
       for (int t = 0; ok && t < nt; ++t) {
         const int u = U + t;
-        const int s = u & 1;
-        const uint32_t st = smem_addr(stage(s));
-        const uint64_t dvk = sdesc_sw128(st + C::kTile, 16, 1024);
+        if (!warp_wait(&v_full[u & 1], (u >> 1) & 1, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t dvk = sdesc_sw128(smem_addr(vslot(u)), 16, 1024);
         // dP(t) = dO V(t)^T (M = queries, N = keys, K = d)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -834,6 +898,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_bf16_ss_w(tP, ddo + ko, dvk + ko, idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit_w(sb_full);
+        mma_commit_w(&v_free[u & 1]);
         // the item's last products reading Q (its last S, issued before) and
         // dO: the producer may load the next item's Q and dO
         if (t + 1 == nt) mma_commit_w(qd_empty);
@@ -847,12 +912,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         tc_fence_after_sync();
         // dQ += dS K(t) (A = dS from tensor memory, K = keys; B = K(t) read along d)
-        const uint64_t dkm = sdesc_sw128(st, C::kAtomBytes, 1024);
+        const uint64_t dkm = sdesc_sw128(smem_addr(kslot(u)), C::kAtomBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kB / 16; ++kk)
           mma_bf16_ts_w(tDQ, tP + packed_col(kk), dkm + kk * (2048 >> 4), idesc_g,
                         (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_w(&kv_free[s]);
+        mma_commit_w(&k_free[u % 3]);
       }
       if (ok) mma_commit_w(done);
       U += nt;
