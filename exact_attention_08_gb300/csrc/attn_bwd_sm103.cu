@@ -26,12 +26,14 @@
 //   attn_bwd_dkdv_kernel<D>  warps 0-7: S^T -> P^T, dP^T -> dS^T (warps w
 //                            and w+4 share key row 32 (w % 4) + lane and
 //                            split the 128 query columns in halves); warp 8:
-//                            TMA producer (K, V once; Q, dO and the two row
-//                            vectors per query tile, two stages); warp 9:
+//                            TMA producer (K, V once; Q per query tile in
+//                            three slots, dO and the two row vectors in
+//                            two); warp 9:
 //                            MMA issuer.  Tensor memory: S^T [0,128),
 //                            dP^T [128,256), dV [256,256+D), dK [256+D,..).
 //   attn_bwd_dq_kernel<D>    the same roles over key tiles for one query
-//                            tile: S [0,128) and [384,512) alternately,
+//                            tile (K in three slots, V in two): S [0,128)
+//                            and [384,512) alternately,
 //                            dP [128,256), dQ [256,256+D); P is formed from
 //                            S(t) while dQ(t-1) and dP(t) run.
 // Products (tcgen05, kind::f16, M=128, fp32 in tensor memory):
@@ -772,8 +774,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // columns [0,128) or [384,512)
   auto s_col = [&](int u) { return (u & 1) ? 3u * kB : 0u; };
 
-  // Counters over the CTA's items: key tiles (one stage load, one set of
-  // products each) and items with key tiles (one Q / dO load each).
+  // Counters over the CTA's items: key tiles (one K and one V load, one set
+  // of products each) and items with key tiles (one Q / dO load each).
   if (warp == kWarpProd) {
     // ================================================================ producer
     int qd_loads = 0, issued = 0, k_loads = 0;  // issued: V loads (and key tiles)
