@@ -724,18 +724,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* k_free = bars + 13;   // [3] S and dQ of that tile are done
   uint64_t* v_full = bars + 16;   // [2] V of a key tile landed
   uint64_t* v_free = bars + 18;   // [2] dP of that tile is done
-  // [2] S of a key tile is in tensor memory, one barrier per S buffer: S of
-  // the next tile is issued before dS of this one is formed, so with one
-  // barrier for both it could complete twice before a waiter looks (across
-  // an item change, while the compute warps write dQ out)
-  uint64_t* sa_full = bars + 5;
-  uint64_t* p_ready = bars + 7;   // dS written (one arrival per compute thread)
+  uint64_t* sa_full = bars + 5;   // S of a key tile is in tensor memory
+  uint64_t* st_read = bars + 6;   // S read out (one arrival per compute warp)
+  // [2] dP of a key tile is in its buffer / dS written over it (one arrival
+  // per compute thread), one barrier per buffer: dP of the next tile is
+  // issued before dS of this one is formed, so with one barrier for both
+  // buffers a phase could complete twice before a waiter looks
+  uint64_t* sb_full = bars + 22;
+  uint64_t* p_ready = bars + 20;
   uint64_t* done = bars + 8;      // every product of the item is done
   uint64_t* drain = bars + 9;
-  uint64_t* sb_full = bars + 10;  // dP is in tensor memory
   uint64_t* qd_empty = bars + 11; // the item's last products reading Q and dO are done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
-  static_assert(2 * kB + D + kB <= 512, "two S buffers, dP and dQ in tensor memory");
+  static_assert(2 * kB + D + kB <= 512, "S, two dP buffers and dQ in tensor memory");
   __shared__ int abort_s;
   volatile int* abort_flag = &abort_s;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -751,10 +752,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_free[s], 1);
-      mbar_init(&sa_full[s], 1);
+      mbar_init(&sb_full[s], 1);
+      mbar_init(&p_ready[s], kComputeThreads);
     }
-    mbar_init(sb_full, 1);
-    mbar_init(p_ready, kComputeThreads);
+    mbar_init(sa_full, 1);
+    mbar_init(st_read, kComputeWarps);
     mbar_init(done, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -770,9 +772,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   auto kslot = [&](int u) { return smem + C::kOffKs + (u % 3) * C::kTile; };  // K of key tile u
   auto vslot = [&](int u) { return smem + C::kOffVs + (u & 1) * C::kTile; };  // V of key tile u
-  // S of key tile u (counted over the CTA's items) in one of two buffers:
-  // columns [0,128) or [384,512)
-  auto s_col = [&](int u) { return (u & 1) ? 3u * kB : 0u; };
+  // Tensor memory: S [0,128); dP of key tile u (counted over the CTA's
+  // items), then dS over it, in one of two buffers: [128,256) or [384,512);
+  // dQ [256,256+D).
+  auto dp_col = [&](int u) { return (u & 1) ? 3u * kB : 1u * kB; };
 
   // Counters over the CTA's items: key tiles (one K and one V load, one set
   // of products each) and items with key tiles (one Q / dO load each).
@@ -852,27 +855,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpIssue) {
     // ================================================================ MMA issuer
-    // Per key tile t the pipe runs dP(t), S(t+1), dQ(t): S of the next tile
-    // goes to the other S buffer while the compute warps form dS(t).  An
-    // item's first dQ overwrites the accumulator: it waits for the dS arrival
-    // the compute warps make after reading the previous item's dQ out.
+    // Per key tile t the pipe runs S(t+1), dP(t+1), dQ(t): S of the next
+    // tile overwrites S(t) as soon as the compute warps have read it out,
+    // and dP(t+1) goes to the other dP buffer, so neither waits for dS(t);
+    // dP(t+2) overwrites dS(t) after dQ(t) has read it.  An item's first dQ
+    // overwrites the accumulator: it waits for the dS arrival the compute
+    // warps make after reading the previous item's dQ out.
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, kB, false);
     constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, true);
     const uint64_t dq = sdesc_sw128(smem_addr(sQ), 16, 1024);
     const uint64_t ddo = sdesc_sw128(smem_addr(sDO), 16, 1024);
-    const uint32_t tP = tmem + kB, tDQ = tmem + 2 * kB;
+    const uint32_t tDQ = tmem + 2 * kB;
     int U = 0;    // key tiles of earlier items
     int qdi = 0;  // items with key tiles before this one
-    auto issue_s = [&](int u) -> bool {  // S(u) = Q K(u)^T
+    auto issue_s = [&](int u) -> bool {  // S(u) = Q K(u)^T, over S(u-1) once read out
+      if (u > 0 && !warp_wait(st_read, (u - 1) & 1, abort_flag, p)) return false;
       if (!warp_wait(&k_full[u % 3], (u / 3) & 1, abort_flag, p)) return false;
       tc_fence_after_sync();
       const uint64_t dkk = sdesc_sw128(smem_addr(kslot(u)), 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
-        mma_bf16_ss_w(tmem + s_col(u), dq + ko, dkk + ko, idesc_s, kk > 0 ? 1u : 0u);
+        mma_bf16_ss_w(tmem, dq + ko, dkk + ko, idesc_s, kk > 0 ? 1u : 0u);
       }
-      mma_commit_w(&sa_full[u & 1]);
+      mma_commit_w(sa_full);
+      return true;
+    };
+    auto issue_dp = [&](int u) -> bool {  // dP(u) = dO V(u)^T (M = queries, N = keys, K = d)
+      if (!warp_wait(&v_full[u & 1], (u >> 1) & 1, abort_flag, p)) return false;
+      tc_fence_after_sync();
+      const uint64_t dvk = sdesc_sw128(smem_addr(vslot(u)), 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
+        mma_bf16_ss_w(tmem + dp_col(u), ddo + ko, dvk + ko, idesc_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(&sb_full[u & 1]);
+      mma_commit_w(&v_free[u & 1]);
       return true;
     };
     bool ok = true;
@@ -884,31 +903,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int nt = it.nkt;
       ok = warp_wait(qd_full, qdi & 1, abort_flag, p);
       if (ok) tc_fence_after_sync();
-      if (ok) ok = issue_s(U);
+      if (ok) ok = issue_s(U) && issue_dp(U);
       for (int t = 0; ok && t < nt; ++t) {
         const int u = U + t;
-        if (!warp_wait(&v_full[u & 1], (u >> 1) & 1, abort_flag, p)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint64_t dvk = sdesc_sw128(smem_addr(vslot(u)), 16, 1024);
-        // dP(t) = dO V(t)^T (M = queries, N = keys, K = d)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ko = kmajor_step<C::kAtomBytes>(kk);
-          mma_bf16_ss_w(tP, ddo + ko, dvk + ko, idesc_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit_w(sb_full);
-        mma_commit_w(&v_free[u & 1]);
-        // the item's last products reading Q (its last S, issued before) and
-        // dO: the producer may load the next item's Q and dO
+        // the item's last products reading Q and dO (its last S and dP, issued
+        // before): the producer may load the next item's Q and dO
         if (t + 1 == nt) mma_commit_w(qd_empty);
-        if (t + 1 < nt && !issue_s(u + 1)) {
+        if (t + 1 < nt && !(issue_s(u + 1) && issue_dp(u + 1))) {
           ok = false;
           break;
         }
-        if (!warp_wait(p_ready, u & 1, abort_flag, p)) {
+        if (!warp_wait(&p_ready[u & 1], (u >> 1) & 1, abort_flag, p)) {
           ok = false;
           break;
         }
@@ -917,7 +922,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t dkm = sdesc_sw128(smem_addr(kslot(u)), C::kAtomBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kB / 16; ++kk)
-          mma_bf16_ts_w(tDQ, tP + packed_col(kk), dkm + kk * (2048 >> 4), idesc_g,
+          mma_bf16_ts_w(tDQ, tmem + dp_col(u) + packed_col(kk), dkm + kk * (2048 >> 4), idesc_g,
                         (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit_w(&k_free[u % 3]);
       }
@@ -950,8 +955,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t nl2 = pf2(nlse2, nlse2), nd2 = pf2(ndval, ndval);
       for (int t = 0; t < nt; ++t) {
         const int u = U + t;
-        // P of this warp's 64 columns from S(t), while dQ(t-1) and dP(t) run
-        if (!warp_wait(&sa_full[u & 1], (u >> 1) & 1, abort_flag, p)) {
+        // P of this warp's 64 columns from S(t), while dQ(t-1) and S(t+1) run
+        if (!warp_wait(sa_full, u & 1, abort_flag, p)) {
           ok = false;
           break;
         }
@@ -966,9 +971,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint64_t pp[32];  // P in fp32 pairs
         {
           uint32_t ra[64];
-          tmem_ld_x32(taddr + s_col(u) + 64 * wh, ra);
-          tmem_ld_x32(taddr + s_col(u) + 64 * wh + 32, ra + 32);
+          tmem_ld_x32(taddr + 64 * wh, ra);
+          tmem_ld_x32(taddr + 64 * wh + 32, ra + 32);
           tmem_ld_wait_b();
+          // S(t) is in registers: S(t+1) may replace it
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(st_read);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             reg_fence_b(ra[2 * e]);
@@ -981,15 +990,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
         // dS = P (dP - D) once dP(t) is in tensor memory
-        if (!warp_wait(sb_full, u & 1, abort_flag, p)) {
+        if (!warp_wait(&sb_full[u & 1], (u >> 1) & 1, abort_flag, p)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         {
           uint32_t rb[64];
-          tmem_ld_x32(taddr + kB + 64 * wh, rb);
-          tmem_ld_x32(taddr + kB + 64 * wh + 32, rb + 32);
+          tmem_ld_x32(taddr + dp_col(u) + 64 * wh, rb);
+          tmem_ld_x32(taddr + dp_col(u) + 64 * wh + 32, rb + 32);
           tmem_ld_wait_b();
 #pragma unroll
           for (int jj = 0; jj < 2; ++jj) {
@@ -1014,12 +1023,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               }
             }
             pack32(pf, pk);
-            tmem_st_x16(taddr + kB + 64 * wh + 16 * jj, pk);
+            tmem_st_x16(taddr + dp_col(u) + 64 * wh + 16 * jj, pk);
           }
         }
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(p_ready);
+        mbar_arrive(&p_ready[u & 1]);
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
