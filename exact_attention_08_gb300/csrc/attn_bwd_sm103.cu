@@ -28,14 +28,15 @@
 //                            split the 128 query columns in halves); warp 8:
 //                            TMA producer (K, V once; Q per query tile in
 //                            three slots, dO and the two row vectors in
-//                            two); warp 9:
-//                            MMA issuer.  Tensor memory: S^T [0,128),
-//                            dP^T [128,256), dV [256,256+D), dK [256+D,..).
+//                            two); warp 9: MMA issuer.  Tensor memory:
+//                            S^T [0,128), dP^T [128,256), dV [256,256+D),
+//                            dK [256+D,..).
 //   attn_bwd_dq_kernel<D>    the same roles over key tiles for one query
-//                            tile (K in three slots, V in two): S [0,128)
-//                            and [384,512) alternately,
-//                            dP [128,256), dQ [256,256+D); P is formed from
-//                            S(t) while dQ(t-1) and dP(t) run.
+//                            tile (K in three slots, V in two): S [0,128),
+//                            released once read out; dP (then dS) in
+//                            [128,256) and [384,512) alternately; dQ
+//                            [256,256+D).  S and dP of the next tile run
+//                            while dS of this one is formed.
 // Products (tcgen05, kind::f16, M=128, fp32 in tensor memory):
 //   S^T = K Q^T, dP^T = V dO^T   (both operands K-major in shared memory)
 //   dV += P^T dO, dK += dS^T Q   (A from tensor memory, B MN-major)
