@@ -126,6 +126,15 @@ def test_full_length(ea, causal):
     print("bwd rel L2 / max:", errs)
 
 
+def test_long_causal(ea):
+    """S = 8192 causal on two heads (the long-sequence shape): 64 key tiles a
+    head, so every CTA of the persistent grids walks one long item through
+    the operand rings (every element compared)."""
+    x = workloads.dense_inputs(115, 1, 2, 2, 8192, 8192, 128, True)
+    errs = _compare(ea, x, 165, "S=8192 causal")
+    print("bwd S=8192 rel L2 / max:", errs)
+
+
 # ------------------------------------------------------------------ sink keys, window, packed
 
 WINDOW_CASES = [
