@@ -76,6 +76,17 @@ def test_bad_page_index_is_reported(ea):
     compare(o[:1], lse[:1], ro, rl, "good request next to a bad one")
 
 
+def test_long_requests(ea):
+    """Requests of 30,000-65,536 tokens (about 2,000-4,100 pages each, 8
+    splits of about 250-500 pages) through the workspace decode."""
+    x = workloads.paged_decode_inputs(5801, 4, 32, 8, 128, 30000, 65536, num_splits=8)
+    o, lse = run_decode(ea, x)
+    assert ea.attn_device_status() == ea.ATTN_OK
+    ro, rl = oracle_decode(x, list(range(4)))
+    e = compare(o, lse, ro, rl, "long requests")
+    print("decode long requests errors", e)
+
+
 def test_full_size(ea):
     x = workloads.paged_decode()
     ws = torch.empty(ea.attn_decode_workspace_size(64, 32, 128, 8), dtype=torch.uint8,

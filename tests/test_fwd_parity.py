@@ -137,6 +137,15 @@ def test_long_causal_full_size(ea, window):
           f"{err[2]} elements with |O| >= 4")
 
 
+def test_very_long_causal(ea):
+    """S = 32768 causal on two heads: items of up to 256 key tiles (the K/V
+    ring, the tile counts and the item order far past the workloads'
+    lengths), rows sampled in every tile."""
+    x = workloads.dense_inputs(58, 1, 2, 2, 32768, 32768, 128, True)
+    err = check_dense(ea, x, rows=sample_rows(32768), what="S=32768 causal")
+    print(f"S=32768 causal: max |dO| {err[0]:.2e}, max |dLSE| {err[1]:.2e}")
+
+
 def test_gqa_full_size(ea):
     x = workloads.gqa_causal()
     err = check_dense(ea, x, rows=sample_rows(4096), what="gqa")
