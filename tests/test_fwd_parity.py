@@ -137,6 +137,13 @@ def test_long_causal_full_size(ea, window):
           f"{err[2]} elements with |O| >= 4")
 
 
+def test_many_short_sequences(ea):
+    """64 batch entries of 100 rows, GQA 4:1, causal: one partial Q tile per
+    (batch, head), 512 items through the persistent grid."""
+    x = workloads.dense_inputs(59, 64, 8, 2, 100, 100, 128, True)
+    check_dense(ea, x, what="64 x 100 causal")
+
+
 def test_very_long_causal(ea):
     """S = 32768 causal on two heads: items of up to 256 key tiles (the K/V
     ring, the tile counts and the item order far past the workloads'
