@@ -120,9 +120,9 @@ def test_prefill_full_size_with_sinks(ea, causal):
     _check(ea, x, sink, rows=sample_rows(2048, seed=5), what=f"full size, causal={causal}")
 
 
-@pytest.mark.parametrize("num_splits", [1, 8])
-def test_decode_with_sinks(ea, num_splits):
-    d = workloads.paged_decode_inputs(71, 6, 8, 2, 128, 1, 900, num_splits=num_splits,
+@pytest.mark.parametrize("num_splits,hd", [(1, 128), (8, 128), (3, 256), (8, 64)])
+def test_decode_with_sinks(ea, num_splits, hd):
+    d = workloads.paged_decode_inputs(71, 6, 8, 2, hd, 1, 900, num_splits=num_splits,
                                       lengths=[900, 0, 1, 17, 256, 640])
     sink = workloads.logit_sinks(71, 8, lo=0.0, hi=8.0, extremes=True)
     o, lse = ea.attn_decode_paged_sink(d.q.cuda(), d.k_pages.cuda(), d.v_pages.cuda(),
@@ -134,7 +134,7 @@ def test_decode_with_sinks(ea, num_splits):
     k, v = d.contiguous_kv(req)
     ro, rl = oracle.attn_decode(np64(d.q), np64(k), np64(v), d.seqlens.numpy(), d.scale,
                                 sink=sink.double().numpy())
-    compare(o, lse, ro, rl, f"decode with sinks, splits={num_splits}")
+    compare(o, lse, ro, rl, f"decode with sinks, splits={num_splits}, d={hd}")
     # request 1 has no key: O = 0, LSE = sink
     assert torch.all(o[1].view(torch.int16) == 0)
     assert torch.equal(lse[1], sink.cuda())
