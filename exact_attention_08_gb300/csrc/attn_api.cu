@@ -271,18 +271,6 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
   a.o_sb = varlen ? 0 : str[3][0];
   a.o_ss = varlen ? static_cast<long long>(Hq) * d : str[3][1];
   a.o_sh = varlen ? d : str[3][2];
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.q_sb = varlen ? 0 : str[0][0];
-  a.q_ss = varlen ? static_cast<long long>(Hq) * d : str[0][1];
-  a.q_sh = varlen ? d : str[0][2];
-  a.k_sb = varlen ? 0 : str[1][0];
-  a.k_ss = varlen ? static_cast<long long>(Hkv) * d : str[1][1];
-  a.k_sh = varlen ? d : str[1][2];
-  a.v_sb = varlen ? 0 : str[2][0];
-  a.v_ss = varlen ? static_cast<long long>(Hkv) * d : str[2][1];
-  a.v_sh = varlen ? d : str[2][2];
   if (rows_k == 0) {
     cudaError_t e = launch_attn_fill_empty(a, st);
     return e == cudaSuccess ? ATTN_OK : cuda_error(e, "fill launch");

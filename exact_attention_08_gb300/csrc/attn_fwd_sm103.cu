@@ -86,9 +86,6 @@ constexpr float kRescaleLog2 = 8.0f;
 // Lower visibility bound when there is no window: far below every key index,
 // yet chunk offsets (at most a few hundred) can be subtracted without overflow.
 constexpr int kNoLowerBound = -(1 << 29);
-// Up to this many sink keys are scored in the epilogue (when the inputs are
-// addressable directly) instead of as key tiles of their own.
-constexpr int kSinkEpi = 8;
 
 template <int D>
 struct Cfg {
@@ -136,11 +133,6 @@ __device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
 
 struct Params {
   __nv_bfloat16* o;
-  const __nv_bfloat16* q;  // inputs, read directly for the sink keys scored in the epilogue
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
-  long long q_sb, q_ss, q_sh, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh;
-  int sink_epi;  // the n_sink (<= kSinkEpi) sink keys are merged in the epilogue
   long long o_sb, o_ss, o_sh;  // O strides (elements): batch, row, head; d contiguous
   int o_v8;                    // every O row starts on 32 bytes: 32-byte stores
   float* lse;
@@ -602,7 +594,7 @@ __device__ __forceinline__ int item_of(int n, int num_items) {
   return k < num_items ? static_cast<int>(k) : -1;
 }
 
-template <int D, bool kPagedKV, bool kTable, bool kSinkE>
+template <int D, bool kPagedKV, bool kTable>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -634,10 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ ItemRec recs[kRecSlots];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // With sink_epi the key loop is a plain window: the sink keys a row's
-  // window leaves out join in the epilogue.
-  const int n_sink_loop = kSinkE ? 0 : p.n_sink;
-  const int sinkT = (p.window > 0 && n_sink_loop > 0) ? (n_sink_loop + kBN - 1) / kBN : 0;
+  const int sinkT = (p.window > 0 && p.n_sink > 0) ? (p.n_sink + kBN - 1) / kBN : 0;
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
@@ -1153,7 +1142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const bool edge = !tile_interior(m, j, p.window, n_sink_loop);
+        const bool edge = !tile_interior(m, j, p.window, p.n_sink);
         const uint32_t sS = taddr + colS;
         uint64_t sum_a = 0, sum_b = 0;  // bit pattern 0 is (+0.f, +0.f)
         float mx = -INFINITY;
@@ -1286,7 +1275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kb = j * kBN;
             const int lim_hi = hi_row - kb;
             const int lim_lo = (p.window > 0) ? lo_row - kb : kNoLowerBound;
-            const int lim_sink = n_sink_loop - kb;
+            const int lim_sink = p.n_sink - kb;
             mask32(r0, lim_hi, lim_lo, lim_sink);
             mask32(r1, lim_hi - 32, lim_lo - 32, lim_sink - 32);
             mask32(r2, lim_hi - 64, lim_lo - 64, lim_sink - 64);
@@ -1339,69 +1328,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = w.q0 + i * kBM + r;
       const bool valid = row < w.Lq;
       const bool have_o = t_item > 0;
-      // Sink keys outside this row's window (and causally visible): scored
-      // against the row's Q (read from the input) and merged into the running
-      // maximum and sum as one more group of keys; O from tensor memory is
-      // rescaled by o_mul and gains sum_j psink_j V_j in the stores below.
-      // A row that sees a sink key also sees keys of its window, so have_o.
-      // Done while the item's last products still run (before o_done).
-      float o_mul = 1.f;
-      float psink[kSinkEpi];
-#pragma unroll
-      for (int j = 0; j < kSinkEpi; ++j) psink[j] = 0.f;
-      bool any_sink = false;
-      if constexpr (kSinkE) {
-        const int vis_hi = min(min(row + w.off - p.window, row + w.off), w.Lk - 1);
-        float sj[kSinkEpi];
-        float smax = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kSinkEpi; ++j) sj[j] = -INFINITY;
-        if (valid && have_o && vis_hi >= 0) {
-          const uint4* qr = reinterpret_cast<const uint4*>(
-              p.q + w.bseq * p.q_sb + static_cast<long long>(w.q_base + row) * p.q_ss +
-              static_cast<long long>(w.h) * p.q_sh);
-          uint4 qv[D / 8];
-#pragma unroll
-          for (int c = 0; c < D / 8; ++c) qv[c] = qr[c];
-#pragma unroll
-          for (int j = 0; j < kSinkEpi; ++j) {
-            if (j < p.n_sink && j <= vis_hi) {
-              const uint4* kr = reinterpret_cast<const uint4*>(
-                  p.k + w.bseq * p.k_sb + static_cast<long long>(w.k_base + j) * p.k_ss +
-                  static_cast<long long>(w.hk) * p.k_sh);
-              float acc = 0.f;
-#pragma unroll
-              for (int c = 0; c < D / 8; ++c) {
-                const uint4 kv = kr[c];
-                const uint32_t qw[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
-                const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  acc = fmaf(__uint_as_float(qw[e] << 16), __uint_as_float(kw[e] << 16), acc);
-                  acc = fmaf(__uint_as_float(qw[e] & 0xffff0000u),
-                             __uint_as_float(kw[e] & 0xffff0000u), acc);
-                }
-              }
-              sj[j] = acc;
-              smax = fmaxf(smax, acc);
-            }
-          }
-        }
-        if (smax > -INFINITY) {
-          const float m_new = fmaxf(m_used, smax);
-          o_mul = exp2f((m_used - m_new) * scale2);
-          l *= o_mul;
-          corr *= o_mul;
-#pragma unroll
-          for (int j = 0; j < kSinkEpi; ++j)
-            if (sj[j] > -INFINITY) {
-              psink[j] = exp2f((sj[j] - m_new) * scale2);
-              l += psink[j];
-            }
-          m_used = m_new;
-        }
-        any_sink = __any_sync(0xffffffffu, smax > -INFINITY);
-      }
       if (have_o) {
         bool w_ok = mbar_wait(&o_done[i], no & 1, abort_flag, p.wait_limit_ns);
         w_ok = __all_sync(0xffffffffu, w_ok);
@@ -1443,43 +1369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the L1 processes) against 16-byte ones.
         auto store32 = [&](const uint32_t* o, int c) {
           uint32_t wv[16];
-          if (kSinkE && any_sink) {
-            // (O o_mul + sum_j psink_j V_j) / l for this chunk's 32 columns
-            float ov[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __uint_as_float(o[e]) * o_mul;
-#pragma unroll 1
-            for (int j = 0; j < p.n_sink && j < kSinkEpi; ++j) {
-              const uint4* vr = reinterpret_cast<const uint4*>(
-                  p.v + w.bseq * p.v_sb + static_cast<long long>(w.k_base + j) * p.v_ss +
-                  static_cast<long long>(w.hk) * p.v_sh + 32 * c);
-              float pj = 0.f;
-#pragma unroll
-              for (int jj = 0; jj < kSinkEpi; ++jj)
-                if (jj == j) pj = psink[jj];
-#pragma unroll
-              for (int x = 0; x < 4; ++x) {
-                const uint4 vv = vr[x];
-                const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  ov[8 * x + 2 * e] = fmaf(pj, __uint_as_float(vw[e] << 16), ov[8 * x + 2 * e]);
-                  ov[8 * x + 2 * e + 1] =
-                      fmaf(pj, __uint_as_float(vw[e] & 0xffff0000u), ov[8 * x + 2 * e + 1]);
-                }
-              }
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              wv[e] = seen ? pack_bf16x2(ov[2 * e] * inv, ov[2 * e + 1] * inv) : 0u;
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              float a0, a1;
-              f2_split(f2_mul(f2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2),
-                       a0, a1);
-              wv[e] = seen ? pack_bf16x2(a0, a1) : 0u;
-            }
+          for (int e = 0; e < 16; ++e) {
+            float a0, a1;
+            f2_split(f2_mul(f2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2), a0,
+                     a1);
+            wv[e] = seen ? pack_bf16x2(a0, a1) : 0u;
           }
           if (valid) {
             if (p.o_v8) {
@@ -1582,9 +1477,8 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    for (auto fn : {attn_fwd_kernel<D, false, false, false>, attn_fwd_kernel<D, true, false, false>,
-                    attn_fwd_kernel<D, false, true, false>, attn_fwd_kernel<D, true, true, false>,
-                    attn_fwd_kernel<D, false, false, true>, attn_fwd_kernel<D, false, true, true>}) {
+    for (auto fn : {attn_fwd_kernel<D, false, false>, attn_fwd_kernel<D, true, false>,
+                    attn_fwd_kernel<D, false, true>, attn_fwd_kernel<D, true, true>}) {
       attr_err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       C::kSmemBytes);
       if (attr_err != cudaSuccess) return;
@@ -1629,20 +1523,6 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   p.causal = a.causal;
   p.window = a.window;
   p.n_sink = a.n_sink;
-  p.q = static_cast<const __nv_bfloat16*>(a.q);
-  p.k = static_cast<const __nv_bfloat16*>(a.k);
-  p.v = static_cast<const __nv_bfloat16*>(a.v);
-  p.q_sb = a.q_sb;
-  p.q_ss = a.q_ss;
-  p.q_sh = a.q_sh;
-  p.k_sb = a.k_sb;
-  p.k_ss = a.k_ss;
-  p.k_sh = a.k_sh;
-  p.v_sb = a.v_sb;
-  p.v_ss = a.v_ss;
-  p.v_sh = a.v_sh;
-  p.sink_epi = a.window > 0 && a.n_sink > 0 && a.n_sink <= kSinkEpi &&
-               a.page_table == nullptr && a.q != nullptr && a.k != nullptr && a.v != nullptr;
   p.wait_limit_ns = kWaitLimitNs;
   p.status = a.status;
   const long long items = static_cast<long long>(p.num_qpairs) * a.B * a.Hq;
@@ -1658,28 +1538,19 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t stream) {
   // instantiation that builds and walks it.
   const bool table = a.cu_q != nullptr && a.causal && a.B <= kTabMaxSeq &&
                      p.num_qpairs <= kTabMaxLev;
-  // Sink keys merged in the epilogue: instantiations of their own, so that
-  // the other calls' epilogue code stays as it is.
   if (a.page_table != nullptr) {
     if (table)
-      attn_fwd_kernel<D, true, true, false><<<grid, kThreads, C::kSmemBytes, stream>>>(
-          a.tmQ, a.tmK, a.tmV, p);
+      attn_fwd_kernel<D, true, true><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK,
+                                                                              a.tmV, p);
     else
-      attn_fwd_kernel<D, true, false, false><<<grid, kThreads, C::kSmemBytes, stream>>>(
-          a.tmQ, a.tmK, a.tmV, p);
-  } else if (p.sink_epi) {
-    if (table)
-      attn_fwd_kernel<D, false, true, true><<<grid, kThreads, C::kSmemBytes, stream>>>(
-          a.tmQ, a.tmK, a.tmV, p);
-    else
-      attn_fwd_kernel<D, false, false, true><<<grid, kThreads, C::kSmemBytes, stream>>>(
-          a.tmQ, a.tmK, a.tmV, p);
+      attn_fwd_kernel<D, true, false><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK,
+                                                                               a.tmV, p);
   } else if (table) {
-    attn_fwd_kernel<D, false, true, false><<<grid, kThreads, C::kSmemBytes, stream>>>(
-        a.tmQ, a.tmK, a.tmV, p);
+    attn_fwd_kernel<D, false, true><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK,
+                                                                             a.tmV, p);
   } else {
-    attn_fwd_kernel<D, false, false, false><<<grid, kThreads, C::kSmemBytes, stream>>>(
-        a.tmQ, a.tmK, a.tmV, p);
+    attn_fwd_kernel<D, false, false><<<grid, kThreads, C::kSmemBytes, stream>>>(a.tmQ, a.tmK,
+                                                                              a.tmV, p);
   }
   return cudaGetLastError();
 }

@@ -22,10 +22,6 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 struct FwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmO;  // 4-D maps (d, H, S, B) with 64 x 1 x 128 x 1 boxes
   void* o;                    // bf16 output
-  const void* q;              // bf16 inputs, for the sink keys scored in the epilogue (or null)
-  const void* k;
-  const void* v;
-  long long q_sb, q_ss, q_sh, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh;  // their strides (elements)
   float* lse;                 // fp32 log-sum-exp, may be null
   const float* sink;          // fp32 logit sink per query head [Hq], may be null
   const int* cu_q;            // null: dense layout
