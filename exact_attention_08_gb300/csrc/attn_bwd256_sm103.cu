@@ -173,14 +173,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr bool kDQ = kMode == kModeDQ;
   constexpr bool kHasDP = kMode != kModeDV;
   extern __shared__ uint8_t smem[];
+  chain_allow_next();
   // The layout fills shared memory with no room to round the window up to
   // the swizzle atom: a window off the boundary is reported, not used.
   if (smem_addr(smem) & 1023u) {
     if (threadIdx.x == 0) atomicOr(p.status, kStatusLayout);
+    chain_join_prev();
     return;
   }
   Work256 w;
-  if (!work256<kMode>(p, static_cast<int>(blockIdx.x), w)) return;
+  if (!work256<kMode>(p, static_cast<int>(blockIdx.x), w)) {
+    chain_join_prev();
+    return;
+  }
   const int G = p.Hq / p.Hkv;
   const int nt = w.nt;
   uint8_t* sR1 = smem + kOffR1;
@@ -525,11 +530,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   if (warp == 0) tmem_dealloc(tmem, 512);
+  chain_join_prev();
 }
 
+// chained: launched as the programmatic dependent of the gradient kernel
+// before it (never of the row statistics, which every mode reads).
 template <int kMode>
-cudaError_t launch_mode(const BwdParams& p, const BwdLaunch& a, long long items,
+cudaError_t launch_mode(const BwdParams& p, const BwdLaunch& a, long long items, bool chained,
                         cudaStream_t stream) {
+  if (chained)
+    return launch_chained(attn_bwd256_kernel<kMode>, static_cast<unsigned>(items), kSmem256,
+                          stream, a.tmQ, a.tmK, a.tmV, a.tmDO, p);
   attn_bwd256_kernel<kMode><<<static_cast<unsigned>(items), kBwdThreads, kSmem256, stream>>>(
       a.tmQ, a.tmK, a.tmV, a.tmDO, p);
   return cudaGetLastError();
@@ -554,11 +565,11 @@ cudaError_t launch_bwd256(const BwdParams& p, const BwdLaunch& a, cudaStream_t s
   cudaError_t e;
   if (a.Skv > 0) {
     const long long n1 = static_cast<long long>((a.Skv + kB - 1) / kB) * a.Hkv * a.B;
-    if ((e = launch_mode<kModeDV>(p, a, n1, stream)) != cudaSuccess) return e;
-    if ((e = launch_mode<kModeDK>(p, a, n1, stream)) != cudaSuccess) return e;
+    if ((e = launch_mode<kModeDV>(p, a, n1, false, stream)) != cudaSuccess) return e;
+    if ((e = launch_mode<kModeDK>(p, a, n1, true, stream)) != cudaSuccess) return e;
   }
   const long long n2 = static_cast<long long>(p.Sqp / kB) * a.Hq * a.B;
-  return launch_mode<kModeDQ>(p, a, n2, stream);
+  return launch_mode<kModeDQ>(p, a, n2, a.Skv > 0, stream);
 }
 
 }  // namespace attn

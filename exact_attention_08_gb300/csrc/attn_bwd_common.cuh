@@ -34,7 +34,7 @@ struct BwdParams {
   int* status;
 };
 
-// The d = 256 gradient kernels (dQ, then dK and dV in two passes), launched
+// The d = 256 gradient kernels (dV, dK, then dQ, one launch each), launched
 // after the row statistics of attn_bwd_sm103.cu have filled p.lse2 / p.dvec.
 cudaError_t launch_bwd256(const BwdParams& p, const BwdLaunch& a, cudaStream_t stream);
 
@@ -188,6 +188,38 @@ __device__ __forceinline__ int bwd_item_at(int n, int num_items) {
   const int pos = (n & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
   const long long k = static_cast<long long>(n) * G + pos;
   return k < num_items ? static_cast<int>(k) : -1;
+}
+
+// The gradient kernels of one call form a programmatic launch chain.  They
+// read the inputs and the row statistics, never one another's outputs, so a
+// kernel may start on the SMs its predecessor frees.  Every CTA allows its
+// dependents as it starts, and before it exits it waits for its
+// predecessor's grid to complete, so that the last kernel's completion
+// still implies every earlier one's.  In a kernel launched without the
+// programmatic attribute both return at once.
+__device__ __forceinline__ void chain_allow_next() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void chain_join_prev() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch of a gradient kernel as the programmatic dependent of the kernel
+// before it on the stream.
+template <typename Kernel, typename... Args>
+cudaError_t launch_chained(Kernel kernel, unsigned grid, size_t smem, cudaStream_t stream,
+                           Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kBwdThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace

@@ -249,10 +249,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          const __grid_constant__ CUtensorMap tmDO, BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
+  chain_allow_next();
   // The layout fills shared memory with no room to round the window up to
   // the swizzle atom: a window off the boundary is reported, not used.
   if (smem_addr(smem_raw) & 1023u) {
     if (threadIdx.x == 0) atomicOr(p.status, kStatusLayout);
+    chain_join_prev();
     return;
   }
   uint8_t* smem = smem_raw;
@@ -650,6 +652,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   if (warp == 0) tmem_dealloc(tmem, 512);
+  chain_join_prev();
 }
 
 // One query tile of the dQ kernel: which, and the key tiles its rows see.
@@ -716,6 +719,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tmDO, BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
+  chain_allow_next();
   uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sDO = smem + C::kOffDO;
@@ -1072,6 +1076,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   if (warp == 0) tmem_dealloc(tmem, 512);
+  chain_join_prev();
 }
 
 // The dK/dV and dQ kernels of head dimension 64 or 128.
@@ -1094,7 +1099,12 @@ cudaError_t launch_bwd_grads(const BwdParams& p, const BwdLaunch& a, cudaStream_
         a.tmQ, a.tmK, a.tmV, a.tmDO, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  // dQ as the programmatic dependent of dK/dV (never of the row statistics,
+  // which it reads): its CTAs take the SMs that dK/dV CTAs leave.
   const long long n2 = static_cast<long long>(p.Sqp / kB) * a.Hq * a.B;
+  if (a.Skv > 0)
+    return launch_chained(attn_bwd_dq_kernel<D>, grid_of(n2), C::kLaunchQ, stream, a.tmQ, a.tmK,
+                          a.tmV, a.tmDO, p);
   attn_bwd_dq_kernel<D><<<grid_of(n2), kBwdThreads, C::kLaunchQ, stream>>>(a.tmQ, a.tmK, a.tmV,
                                                                           a.tmDO, p);
   return cudaGetLastError();
