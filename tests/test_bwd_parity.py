@@ -374,3 +374,26 @@ def test_persistent_items(ea, case):
         first_seen = Skv - Sq - window + 1  # the first window key of query 0
         assert torch.count_nonzero(dk[:, n_sink:first_seen]) == 0
         assert torch.count_nonzero(dv[:, n_sink:first_seen]) == 0
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_stream_order_after_launch_chain(ea, d):
+    """Work queued on the stream after attn_bwd sees every gradient complete.
+    The gradient kernels run as a programmatic launch chain (each may start
+    while the one before it drains), so the last kernel's completion has to
+    imply the earlier ones': copies taken on the same stream, with no host
+    synchronisation in between, must equal the gradients."""
+    x = workloads.dense_inputs(113, 4, 16, 16, 2048, 2048, d, False)
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    g = workloads.grad_output(163, x.q.shape).cuda()
+    o, lse = ea.attn_fwd_ex(q, k, v, scale=x.scale)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dq, dk, dv = ea.attn_bwd(q, k, v, o, lse, g, scale=x.scale, stream=s)
+        copies = [t.clone() for t in (dv, dk, dq)]
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    for c, t in zip(copies, (dv, dk, dq)):
+        assert torch.equal(c.view(torch.int16), t.view(torch.int16))
+    assert torch.count_nonzero(dv) > 0
