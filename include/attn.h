@@ -214,6 +214,9 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Sq);
  *   get dq = 0 and contribute nothing).  workspace: device buffer of at least
  *   attn_bwd_workspace_size(B, Hq, Sq) bytes, overwritten.  Sq == 0 zeroes
  *   dk and dv; Skv == 0 zeroes dq.  d must be 64, 128 or 256.
+ * The gradient kernels may overlap one another on the stream (each starts
+ * on the SMs the one before it frees); work queued on the stream after the
+ * call still starts only once all three gradients are written.
  */
 ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o,
                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
