@@ -504,7 +504,8 @@ def main():
     pairs_total = sum(c[3] for c in pre)
     kv_bytes = decode_kv_bytes(dx.seqlens.tolist(), Hkv_d, d_d)
     n_calls = len(calls) + 1
-    launches_per_step = len(calls) + 2  # four forward launches, decode split + merge
+    # the four forward launches, and the decode's request order, split and merge
+    launches_per_step = len(calls) + 3
 
     def step(ev):
         with torch.cuda.stream(stream):
